@@ -1,0 +1,152 @@
+"""Thin ctypes binding over ``libbgattn.so`` (the C ABI in include/bg_attn.h).
+
+Argument marshalling only: every function passes device pointers, sizes and
+the current CUDA stream straight to the library; all of the work runs in the
+library's CUDA kernels.  There is no CPU fallback: if the library is missing
+or fails to load, every call raises.
+
+The functions carry the C names.  Tensor arguments are torch CUDA tensors
+(torch is used for device memory and streams only); ``raw`` exposes the
+ctypes functions themselves for callers that manage pointers directly.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libbgattn.so")
+
+BG_OK, BG_ERR_INVALID_ARG, BG_ERR_UNSUPPORTED, BG_ERR_DEVICE_DATA, BG_ERR_CUDA = 0, 1, 2, 3, 4
+BG_DEVSTAT_CU_SEQLENS = 0x01
+BG_DEVSTAT_SEQ_TOO_LONG = 0x02
+BG_DEVSTAT_PARENT = 0x04
+BG_DEVSTAT_CU_PROMPT = 0x08
+BG_DEVSTAT_EMPTY_ROW = 0x10
+BG_DEVSTAT_TIMEOUT = 0x100
+BG_MAX_SUFFIX = 16
+BG_MAX_SEQLEN = 65536
+
+# Every symbol include/bg_attn.h declares, with its ctypes signature.
+_P, _I32, _F32, _SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float, ctypes.c_size_t
+SIGNATURES = {
+    "bg_status_string": ([ctypes.c_int], ctypes.c_char_p),
+    "bg_packed_prefill_workspace_size": ([_I32] * 6, _SZ),
+    "bg_packed_prefill_attn": ([_P, _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32, _F32, _P, _P, _P, _SZ, _P, _P],
+                               ctypes.c_int),
+    "bg_beam_decode_attn": ([_P, _P, _P, _P, _I32, _I32, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _F32, _P,
+                             _P, _P], ctypes.c_int),
+    "bg_beam_suffix_reorder": ([_P, _P, _P, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32, _P, _P],
+                               ctypes.c_int),
+}
+
+
+class BgError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn} failed: {status_string(status)} ({status})")
+
+
+_lib = None
+
+
+def load(path: Optional[str] = None):
+    """Load the library (once).  Raises if it is not built."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(f"{p} is missing: build it with attention_packed_varlen_causal_gb300.build.build() "
+                           "(there is no fallback implementation)")
+    lib = ctypes.CDLL(p)
+    for name, (args, res) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    if path is None:
+        _lib = lib
+    return lib
+
+
+class _Raw:
+    def __getattr__(self, name):
+        return getattr(load(), name)
+
+
+raw = _Raw()
+
+
+def status_string(status: int) -> str:
+    return load().bg_status_string(int(status)).decode()
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else int(t.data_ptr())
+
+
+def _stream(stream) -> Optional[int]:
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return int(s.cuda_stream)
+
+
+def _check(fn: str, status: int):
+    if status != BG_OK:
+        raise BgError(fn, status)
+
+
+def bg_packed_prefill_workspace_size(num_seqs: int, total_tokens: int, max_seqlen: int, Hq: int, Hkv: int,
+                                     head_dim: int) -> int:
+    return int(load().bg_packed_prefill_workspace_size(num_seqs, total_tokens, max_seqlen, Hq, Hkv, head_dim))
+
+
+def bg_packed_prefill_attn(q, k, v, cu_seqlens, max_seqlen: int, out, *, lse=None, scale: Optional[float] = None,
+                           workspace=None, dev_status=None, stream=None):
+    """q [T,Hq,d], k/v [T,Hkv,d] bf16 CUDA tensors; cu_seqlens int32 [B+1] CUDA;
+    out bf16 [T,Hq,d] (written); lse fp32 [T,Hq] or None; workspace a uint8
+    CUDA tensor of at least bg_packed_prefill_workspace_size bytes."""
+    T, Hq, d = q.shape
+    Hkv = k.shape[1]
+    B = cu_seqlens.numel() - 1
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    need = bg_packed_prefill_workspace_size(B, T, max_seqlen, Hq, Hkv, d)
+    if workspace is None:
+        raise ValueError(f"workspace of {need} bytes required (the library never allocates)")
+    st = load().bg_packed_prefill_attn(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), B, T, int(max_seqlen), Hq, Hkv, d,
+                                       float(scale), _ptr(out), _ptr(lse), _ptr(workspace),
+                                       workspace.numel() * workspace.element_size(), _ptr(dev_status),
+                                       _stream(stream))
+    _check("bg_packed_prefill_attn", st)
+    return out
+
+
+def bg_beam_decode_attn(q, prompt_k, prompt_v, cu_prompt, max_prompt_len: int, suffix_k, suffix_v, suffix_len: int,
+                        out, *, scale: Optional[float] = None, dev_status=None, stream=None):
+    """q [R,W,Hq,d]; prompt_k/v [sumP,Hkv,d]; cu_prompt int32 [R+1];
+    suffix_k/v [R,W,S_max,Hkv,d]; out [R,W,Hq,d] (written)."""
+    R, W, Hq, d = q.shape
+    Hkv = prompt_k.shape[1]
+    S_max = suffix_k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    st = load().bg_beam_decode_attn(_ptr(q), _ptr(prompt_k), _ptr(prompt_v), _ptr(cu_prompt), prompt_k.shape[0],
+                                    int(max_prompt_len), _ptr(suffix_k), _ptr(suffix_v), int(suffix_len), S_max, R, W,
+                                    Hq, Hkv, d, float(scale), _ptr(out), _ptr(dev_status), _stream(stream))
+    _check("bg_beam_decode_attn", st)
+    return out
+
+
+def bg_beam_suffix_reorder(src_k, src_v, dst_k, dst_v, parent_idx, n_tokens: int, *, new_k=None, new_v=None,
+                           dev_status=None, stream=None):
+    """src/dst [R,W,S_max,Hkv,d] bf16; parent_idx int32 [R,W]; new_k/new_v
+    [R,W,Hkv,d] or None.  dst[r,b,:n] = src[r,parent[r,b],:n], dst[r,b,n] = new[r,b]."""
+    R, W, S_max, Hkv, d = src_k.shape
+    st = load().bg_beam_suffix_reorder(_ptr(src_k), _ptr(src_v), _ptr(dst_k), _ptr(dst_v), _ptr(parent_idx),
+                                       _ptr(new_k), _ptr(new_v), R, W, S_max, int(n_tokens), Hkv, d,
+                                       _ptr(dev_status), _stream(stream))
+    _check("bg_beam_suffix_reorder", st)
+    return dst_k, dst_v

@@ -1,0 +1,303 @@
+// abi.cu -- the C ABI (include/bg_attn.h): host-side argument checks, TMA
+// tensor-map encoding and kernel launches.  No allocation, no stream
+// synchronisation; every call only enqueues work on the caller's stream.
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "bg_attn.h"
+#include "bg_attn_kernel.cuh"
+#include "bg_internal.h"
+
+using namespace bg;
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder()
+{
+    std::call_once(g_encode_once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    return g_encode;
+}
+
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_sm_count[kMaxDevices];
+
+int sm_count()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
+    if (dev < kMaxDevices) {
+        const int cached = g_sm_count[dev].load(std::memory_order_relaxed);
+        if (cached > 0) return cached;
+    }
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    if (dev < kMaxDevices) g_sm_count[dev].store(n, std::memory_order_relaxed);
+    return n;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+bool overlap(const void *a, size_t na, const void *b, size_t nb)
+{
+    if (!a || !b || na == 0 || nb == 0) return false;
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+}
+
+// bf16 tiled map, 128-byte swizzle, box inner extent 64 elements (128 bytes).
+bool encode_map(CUtensorMap *m, const void *base, int rank, const uint64_t *dims, const uint64_t *strides_bytes,
+                const uint32_t *box)
+{
+    auto fn = encoder();
+    if (!fn) return false;
+    cuuint64_t gdim[5], gstr[4];
+    cuuint32_t bdim[5], estr[5];
+    for (int i = 0; i < rank; ++i) {
+        gdim[i] = dims[i];
+        bdim[i] = box[i];
+        estr[i] = 1;
+    }
+    for (int i = 0; i < rank - 1; ++i) gstr[i] = strides_bytes[i];
+    std::memset(m, 0, sizeof(*m));
+    const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<cuuint32_t>(rank), const_cast<void *>(base),
+                          gdim, gstr, bdim, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+bool supported_head_dim(int32_t d) { return d == 64 || d == 128; }
+
+size_t prefill_entries_bound(int64_t num_seqs, int64_t total_tokens)
+{
+    return static_cast<size_t>(total_tokens / kPrefillTileRows + num_seqs + 1);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *bg_status_string(bg_status_t s)
+{
+    switch (s) {
+    case BG_OK: return "BG_OK";
+    case BG_ERR_INVALID_ARG: return "BG_ERR_INVALID_ARG";
+    case BG_ERR_UNSUPPORTED: return "BG_ERR_UNSUPPORTED";
+    case BG_ERR_DEVICE_DATA: return "BG_ERR_DEVICE_DATA";
+    case BG_ERR_CUDA: return "BG_ERR_CUDA";
+    }
+    return "BG_ERR_UNKNOWN";
+}
+
+size_t bg_packed_prefill_workspace_size(int32_t num_seqs, int32_t total_tokens, int32_t max_seqlen, int32_t Hq,
+                                        int32_t Hkv, int32_t head_dim)
+{
+    (void)max_seqlen;
+    (void)Hq;
+    (void)Hkv;
+    (void)head_dim;
+    if (num_seqs < 0 || total_tokens < 0) return 0;
+    const size_t bytes = kWorkHeaderBytes + sizeof(int2) * prefill_entries_bound(num_seqs, total_tokens);
+    return (bytes + 255) & ~size_t(255);
+}
+
+bg_status_t bg_packed_prefill_attn(const void *q, const void *k, const void *v, const int32_t *cu_seqlens,
+                                   int32_t num_seqs, int32_t total_tokens, int32_t max_seqlen, int32_t Hq,
+                                   int32_t Hkv, int32_t head_dim, float scale, void *out, float *lse, void *workspace,
+                                   size_t workspace_bytes, int32_t *dev_status, cudaStream_t stream)
+{
+    if (num_seqs < 0 || total_tokens < 0 || max_seqlen < 0 || Hq <= 0 || Hkv <= 0 || head_dim <= 0)
+        return BG_ERR_INVALID_ARG;
+    if (Hq % Hkv != 0) return BG_ERR_INVALID_ARG;
+    if (!std::isfinite(scale)) return BG_ERR_INVALID_ARG;
+    if (!supported_head_dim(head_dim) || max_seqlen > BG_MAX_SEQLEN) return BG_ERR_UNSUPPORTED;
+    if (num_seqs == 0 || total_tokens == 0) return BG_OK;
+    if (!q || !k || !v || !cu_seqlens || !out || !workspace) return BG_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) || !aligned(cu_seqlens, 4) ||
+        !aligned(workspace, 256) || (lse && !aligned(lse, 4)) || (dev_status && !aligned(dev_status, 4)))
+        return BG_ERR_INVALID_ARG;
+    if (workspace_bytes < bg_packed_prefill_workspace_size(num_seqs, total_tokens, max_seqlen, Hq, Hkv, head_dim))
+        return BG_ERR_INVALID_ARG;
+    const size_t qbytes = static_cast<size_t>(total_tokens) * Hq * head_dim * 2;
+    const size_t kvbytes = static_cast<size_t>(total_tokens) * Hkv * head_dim * 2;
+    const size_t lsebytes = lse ? static_cast<size_t>(total_tokens) * Hq * 4 : 0;
+    if (overlap(out, qbytes, q, qbytes) || overlap(out, qbytes, k, kvbytes) || overlap(out, qbytes, v, kvbytes) ||
+        overlap(out, qbytes, workspace, workspace_bytes) || overlap(lse, lsebytes, out, qbytes) ||
+        overlap(lse, lsebytes, q, qbytes) || overlap(lse, lsebytes, k, kvbytes) ||
+        overlap(lse, lsebytes, v, kvbytes) || overlap(lse, lsebytes, workspace, workspace_bytes))
+        return BG_ERR_INVALID_ARG;
+
+    const int32_t g = Hq / Hkv;
+    const int nh = prefill_heads_per_cta();
+    const int32_t groups_per_kv = (g + nh - 1) / nh;
+    const int64_t items_bound = static_cast<int64_t>(prefill_entries_bound(num_seqs, total_tokens)) * Hkv * groups_per_kv;
+    if (items_bound >= (int64_t(1) << 31)) return BG_ERR_UNSUPPORTED;
+
+    const int nsm = sm_count();
+    if (nsm <= 0) return BG_ERR_CUDA;
+
+    CUtensorMap tm_q, tm_k, tm_v;
+    const uint64_t D = static_cast<uint64_t>(head_dim);
+    const uint64_t dq[3] = {D, static_cast<uint64_t>(Hq), static_cast<uint64_t>(total_tokens)};
+    const uint64_t sq[2] = {D * 2, static_cast<uint64_t>(Hq) * D * 2};
+    const uint64_t dkv[3] = {D, static_cast<uint64_t>(Hkv), static_cast<uint64_t>(total_tokens)};
+    const uint64_t skv[2] = {D * 2, static_cast<uint64_t>(Hkv) * D * 2};
+    const uint32_t box[3] = {64, 1, 128};
+    if (!encode_map(&tm_q, q, 3, dq, sq, box) || !encode_map(&tm_k, k, 3, dkv, skv, box) ||
+        !encode_map(&tm_v, v, 3, dkv, skv, box))
+        return BG_ERR_CUDA;
+
+    int32_t *hdr = static_cast<int32_t *>(workspace);
+    int2 *work = reinterpret_cast<int2 *>(static_cast<uint8_t *>(workspace) + kWorkHeaderBytes);
+    if (launch_prefill_worklist(cu_seqlens, num_seqs, total_tokens, max_seqlen, hdr, work, dev_status, stream) !=
+        cudaSuccess)
+        return BG_ERR_CUDA;
+
+    AttnParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.g = g;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.out = static_cast<__nv_bfloat16 *>(out);
+    p.dev_status = dev_status;
+    p.err_word = hdr + 2;
+    p.cu_seqlens = cu_seqlens;
+    p.work = work;
+    p.work_hdr = hdr;
+    p.groups_per_kv = groups_per_kv;
+    p.n_head_groups = Hkv * groups_per_kv;
+    p.lse = lse;
+    const int grid = static_cast<int>(items_bound < nsm ? items_bound : nsm);
+    if (launch_prefill_attn(head_dim, tm_q, tm_k, tm_v, p, grid, stream) != cudaSuccess) return BG_ERR_CUDA;
+    return BG_OK;
+}
+
+bg_status_t bg_beam_decode_attn(const void *q, const void *prompt_k, const void *prompt_v, const int32_t *cu_prompt,
+                                int32_t total_prompt_tokens, int32_t max_prompt_len, const void *suffix_k,
+                                const void *suffix_v, int32_t suffix_len, int32_t suffix_max, int32_t R, int32_t W,
+                                int32_t Hq, int32_t Hkv, int32_t head_dim, float scale, void *out,
+                                int32_t *dev_status, cudaStream_t stream)
+{
+    if (R < 0 || W <= 0 || Hq <= 0 || Hkv <= 0 || head_dim <= 0 || total_prompt_tokens < 0 || max_prompt_len < 0 ||
+        suffix_len < 0 || suffix_max < 0 || suffix_len > suffix_max)
+        return BG_ERR_INVALID_ARG;
+    if (Hq % Hkv != 0 || !std::isfinite(scale)) return BG_ERR_INVALID_ARG;
+    const int32_t g = Hq / Hkv;
+    if (!supported_head_dim(head_dim) || g > 128 || suffix_max > BG_MAX_SUFFIX) return BG_ERR_UNSUPPORTED;
+    if (max_prompt_len == 0 && suffix_len == 0) return BG_ERR_INVALID_ARG;   // every softmax would be empty
+    if (R == 0) return BG_OK;
+    if (static_cast<int64_t>(R) * W >= (int64_t(1) << 31)) return BG_ERR_UNSUPPORTED;
+    if (!q || !out || !cu_prompt) return BG_ERR_INVALID_ARG;
+    if (total_prompt_tokens > 0 && (!prompt_k || !prompt_v)) return BG_ERR_INVALID_ARG;
+    if (suffix_len > 0 && (!suffix_k || !suffix_v)) return BG_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(out, 16) || !aligned(cu_prompt, 4) || (prompt_k && !aligned(prompt_k, 16)) ||
+        (prompt_v && !aligned(prompt_v, 16)) || (suffix_k && !aligned(suffix_k, 16)) ||
+        (suffix_v && !aligned(suffix_v, 16)) || (dev_status && !aligned(dev_status, 4)))
+        return BG_ERR_INVALID_ARG;
+    const size_t qbytes = static_cast<size_t>(R) * W * Hq * head_dim * 2;
+    const size_t pbytes = static_cast<size_t>(total_prompt_tokens) * Hkv * head_dim * 2;
+    const size_t sbytes = static_cast<size_t>(R) * W * suffix_max * Hkv * head_dim * 2;
+    if (overlap(out, qbytes, q, qbytes) || overlap(out, qbytes, prompt_k, pbytes) ||
+        overlap(out, qbytes, prompt_v, pbytes) || (suffix_len > 0 && (overlap(out, qbytes, suffix_k, sbytes) ||
+                                                                      overlap(out, qbytes, suffix_v, sbytes))))
+        return BG_ERR_INVALID_ARG;
+
+    const int nsm = sm_count();
+    if (nsm <= 0) return BG_ERR_CUDA;
+
+    const int nh = decode_tiles_per_cta();
+    const int32_t BT = 128 / g;
+    const int32_t beam_tiles = (W + BT - 1) / BT;
+    const int32_t pairs = (beam_tiles + nh - 1) / nh;
+    const int64_t items = static_cast<int64_t>(R) * Hkv * pairs;
+    if (items >= (int64_t(1) << 31)) return BG_ERR_UNSUPPORTED;
+
+    CUtensorMap tm_q, tm_k, tm_v;
+    const uint64_t D = static_cast<uint64_t>(head_dim);
+    const uint64_t dq[4] = {D, static_cast<uint64_t>(g), static_cast<uint64_t>(Hkv), static_cast<uint64_t>(R) * W};
+    const uint64_t sq[3] = {D * 2, static_cast<uint64_t>(g) * D * 2, static_cast<uint64_t>(Hq) * D * 2};
+    const uint32_t boxq[4] = {64, static_cast<uint32_t>(g), 1, static_cast<uint32_t>(BT)};
+    const uint64_t np = total_prompt_tokens > 0 ? static_cast<uint64_t>(total_prompt_tokens) : 1;
+    const uint64_t dkv[3] = {D, static_cast<uint64_t>(Hkv), np};
+    const uint64_t skv[2] = {D * 2, static_cast<uint64_t>(Hkv) * D * 2};
+    const uint32_t boxkv[3] = {64, 1, 128};
+    // With no prompt tokens no K/V tile is ever loaded; the maps only need a valid base.
+    const void *kbase = total_prompt_tokens > 0 ? prompt_k : q;
+    const void *vbase = total_prompt_tokens > 0 ? prompt_v : q;
+    if (!encode_map(&tm_q, q, 4, dq, sq, boxq) || !encode_map(&tm_k, kbase, 3, dkv, skv, boxkv) ||
+        !encode_map(&tm_v, vbase, 3, dkv, skv, boxkv))
+        return BG_ERR_CUDA;
+
+    AttnParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.g = g;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.out = static_cast<__nv_bfloat16 *>(out);
+    p.dev_status = dev_status;
+    p.err_word = nullptr;
+    p.cu_prompt = cu_prompt;
+    p.R = R;
+    p.W = W;
+    p.BT = BT;
+    p.pairs_per_rk = pairs;
+    p.max_prompt_len = max_prompt_len;
+    p.total_prompt = total_prompt_tokens;
+    p.q = static_cast<const __nv_bfloat16 *>(q);
+    p.suffix_k = static_cast<const __nv_bfloat16 *>(suffix_k);
+    p.suffix_v = static_cast<const __nv_bfloat16 *>(suffix_v);
+    p.suffix_len = suffix_len;
+    p.suffix_max = suffix_max;
+    p.n_items_decode = static_cast<int32_t>(items);
+    const int grid = static_cast<int>(items < nsm ? items : nsm);
+    if (launch_decode_attn(head_dim, tm_q, tm_k, tm_v, p, grid, stream) != cudaSuccess) return BG_ERR_CUDA;
+    return BG_OK;
+}
+
+bg_status_t bg_beam_suffix_reorder(const void *src_k, const void *src_v, void *dst_k, void *dst_v,
+                                   const int32_t *parent_idx, const void *new_k, const void *new_v, int32_t R,
+                                   int32_t W, int32_t suffix_max, int32_t n_tokens, int32_t Hkv, int32_t head_dim,
+                                   int32_t *dev_status, cudaStream_t stream)
+{
+    if (R < 0 || W <= 0 || suffix_max <= 0 || n_tokens < 0 || Hkv <= 0 || head_dim <= 0) return BG_ERR_INVALID_ARG;
+    if (!supported_head_dim(head_dim)) return BG_ERR_UNSUPPORTED;
+    const bool append = new_k != nullptr || new_v != nullptr;
+    if (append && (!new_k || !new_v)) return BG_ERR_INVALID_ARG;
+    if (n_tokens + (append ? 1 : 0) > suffix_max) return BG_ERR_INVALID_ARG;
+    if (R == 0) return BG_OK;
+    if (!src_k || !src_v || !dst_k || !dst_v || !parent_idx) return BG_ERR_INVALID_ARG;
+    if (!aligned(src_k, 16) || !aligned(src_v, 16) || !aligned(dst_k, 16) || !aligned(dst_v, 16) ||
+        !aligned(parent_idx, 4) || (new_k && !aligned(new_k, 16)) || (new_v && !aligned(new_v, 16)) ||
+        (dev_status && !aligned(dev_status, 4)))
+        return BG_ERR_INVALID_ARG;
+    const size_t bytes = static_cast<size_t>(R) * W * suffix_max * Hkv * head_dim * 2;
+    const size_t nbytes = static_cast<size_t>(R) * W * Hkv * head_dim * 2;
+    if (overlap(dst_k, bytes, src_k, bytes) || overlap(dst_k, bytes, src_v, bytes) ||
+        overlap(dst_v, bytes, src_k, bytes) || overlap(dst_v, bytes, src_v, bytes) ||
+        overlap(dst_k, bytes, dst_v, bytes) || overlap(dst_k, bytes, new_k, nbytes) ||
+        overlap(dst_k, bytes, new_v, nbytes) || overlap(dst_v, bytes, new_k, nbytes) ||
+        overlap(dst_v, bytes, new_v, nbytes))
+        return BG_ERR_INVALID_ARG;
+    if (launch_suffix_reorder(src_k, src_v, dst_k, dst_v, parent_idx, new_k, new_v, R, W, suffix_max, n_tokens, Hkv,
+                              head_dim, dev_status, stream) != cudaSuccess)
+        return BG_ERR_CUDA;
+    return BG_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,56 @@
+// bg_internal.h -- launchers shared between the C-ABI layer and the kernel
+// translation units (not part of the public interface).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <atomic>
+
+#include "bg_attn.h"
+
+namespace bg {
+
+struct AttnParams;
+
+// Prefill: work-list pre-pass + attention kernel.  Maps are built by the
+// caller.  Returns cudaSuccess or the launch error.
+cudaError_t launch_prefill_worklist(const int32_t *cu_seqlens, int32_t num_seqs, int32_t total_tokens,
+                                    int32_t max_seqlen, int32_t *work_hdr, int2 *work, int32_t *dev_status,
+                                    cudaStream_t stream);
+cudaError_t launch_prefill_attn(int head_dim, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
+                                const CUtensorMap &tm_v, const AttnParams &p, int grid, cudaStream_t stream);
+int prefill_heads_per_cta();
+
+cudaError_t launch_decode_attn(int head_dim, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
+                               const CUtensorMap &tm_v, const AttnParams &p, int grid, cudaStream_t stream);
+int decode_tiles_per_cta();
+
+cudaError_t launch_suffix_reorder(const void *src_k, const void *src_v, void *dst_k, void *dst_v,
+                                  const int32_t *parent_idx, const void *new_k, const void *new_v, int32_t R,
+                                  int32_t W, int32_t suffix_max, int32_t n_tokens, int32_t Hkv, int32_t head_dim,
+                                  int32_t *dev_status, cudaStream_t stream);
+
+// Raises the dynamic shared-memory limit of `kern` once per device (bit d of
+// `done`), so later launches -- including ones inside a CUDA-graph capture --
+// make no attribute call.
+template <typename Kern>
+cudaError_t ensure_smem_attribute(Kern kern, int bytes, std::atomic<uint64_t> &done)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
+    if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
+    return e;
+}
+
+// Work-list layout inside the caller's workspace.
+constexpr size_t kWorkHeaderBytes = 256;
+constexpr int kPrefillTileRows = 128;
+constexpr int kMaxTilesPerSeq = BG_MAX_SEQLEN / kPrefillTileRows;
+
+}  // namespace bg

@@ -1,0 +1,121 @@
+// prefill.cu -- packed variable-length causal GQA prefill attention.
+//
+// "SLM 生成式高并发推理引擎：延迟约束下的有效吞吐优化", abstract (Packed
+// Prefill) and section 1.2: each sequence keeps its valid length and only its
+// valid tokens are computed, so no work depends on the longest sequence.
+//
+// Two launches on the caller's stream:
+//   1. worklist_kernel (one CTA): checks cu_seqlens on the device and writes
+//      the list of (sequence, query tile) entries, sequences with more tiles
+//      first and, within a sequence, later (costlier) query tiles first.
+//      Only tiles of valid tokens exist: a sequence of length L has
+//      ceil(L/128) query tiles and tile t streams key tiles 0..t.
+//   2. attn_kernel<Prefill>: persistent CTAs walk the list round-robin.
+#include "bg_attn_kernel.cuh"
+#include "bg_internal.h"
+
+#include <atomic>
+
+namespace bg {
+
+__global__ void __launch_bounds__(1024) worklist_kernel(const int32_t *__restrict__ cu, int32_t B, int32_t T,
+                                                        int32_t max_seqlen, int32_t *__restrict__ hdr,
+                                                        int2 *__restrict__ work, int32_t *dev_status)
+{
+    __shared__ int s_err;
+    __shared__ int s_count[kMaxTilesPerSeq + 1];   // sequences per tile count
+    __shared__ int s_off[kMaxTilesPerSeq + 2];     // first entry of each tile-count bucket
+    const int tid = threadIdx.x;
+    if (tid == 0) s_err = 0;
+    for (int i = tid; i <= kMaxTilesPerSeq; i += blockDim.x) s_count[i] = 0;
+    __syncthreads();
+
+    int err = 0;
+    if (B > 0 && tid == 0 && cu[0] != 0) err |= BG_DEVSTAT_CU_SEQLENS;
+    for (int i = tid; i < B; i += blockDim.x) {
+        const int a = cu[i], b = cu[i + 1];
+        if (b < a || a < 0 || b > T) {
+            err |= BG_DEVSTAT_CU_SEQLENS;
+            continue;
+        }
+        if (i == B - 1 && b != T) err |= BG_DEVSTAT_CU_SEQLENS;
+        if (b - a > max_seqlen) {
+            err |= BG_DEVSTAT_SEQ_TOO_LONG;
+            continue;
+        }
+        const int nt = (b - a + kPrefillTileRows - 1) / kPrefillTileRows;
+        if (nt > 0) atomicAdd(&s_count[nt], 1);
+    }
+    if (err) atomicOr(&s_err, err);
+    __syncthreads();
+    if (s_err) {
+        if (tid == 0) {
+            hdr[0] = s_err;
+            hdr[1] = 0;
+            if (dev_status) atomicOr(dev_status, s_err);
+        }
+        return;
+    }
+    if (tid == 0) {
+        // buckets in decreasing tile count; a sequence with nt tiles owns nt entries
+        int off = 0;
+        for (int nt = kMaxTilesPerSeq; nt >= 1; --nt) {
+            s_off[nt] = off;
+            off += s_count[nt] * nt;
+        }
+        hdr[1] = off;
+        hdr[0] = 0;
+    }
+    __syncthreads();
+    for (int i = tid; i < B; i += blockDim.x) {
+        const int L = cu[i + 1] - cu[i];
+        const int nt = (L + kPrefillTileRows - 1) / kPrefillTileRows;
+        if (nt == 0) continue;
+        const int pos = atomicAdd(&s_off[nt], nt);
+        for (int t = 0; t < nt; ++t) work[pos + t] = make_int2(i, nt - 1 - t);
+    }
+}
+
+cudaError_t launch_prefill_worklist(const int32_t *cu_seqlens, int32_t num_seqs, int32_t total_tokens,
+                                    int32_t max_seqlen, int32_t *work_hdr, int2 *work, int32_t *dev_status,
+                                    cudaStream_t stream)
+{
+    worklist_kernel<<<1, 1024, 0, stream>>>(cu_seqlens, num_seqs, total_tokens, max_seqlen, work_hdr, work,
+                                            dev_status);
+    return cudaGetLastError();
+}
+
+namespace {
+constexpr int kNH = 2;   // query heads of one kv head per CTA (share every K/V tile)
+
+template <int D, int NSTAGE>
+std::atomic<uint64_t> &smem_attr_done()
+{
+    static std::atomic<uint64_t> mask{0};
+    return mask;
+}
+
+template <int D, int NSTAGE>
+cudaError_t launch_one(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
+                       const AttnParams &p, int grid, cudaStream_t stream)
+{
+    using C = AttnCfg<D, kNH, NSTAGE>;
+    auto kern = attn_kernel<Mode::Prefill, D, kNH, NSTAGE>;
+    cudaError_t e = ensure_smem_attribute(kern, C::kSmemBytes, smem_attr_done<D, NSTAGE>());
+    if (e != cudaSuccess) return e;
+    kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(tm_q, tm_k, tm_v, p);
+    return cudaGetLastError();
+}
+}  // namespace
+
+int prefill_heads_per_cta() { return kNH; }
+
+cudaError_t launch_prefill_attn(int head_dim, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
+                                const CUtensorMap &tm_v, const AttnParams &p, int grid, cudaStream_t stream)
+{
+    if (head_dim == 128) return launch_one<128, 2>(tm_q, tm_k, tm_v, p, grid, stream);
+    if (head_dim == 64) return launch_one<64, 4>(tm_q, tm_k, tm_v, p, grid, stream);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace bg

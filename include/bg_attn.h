@@ -1,0 +1,192 @@
+/*
+ * bg_attn.h -- C ABI of the GB300 (sm_103a) attention hot path of a
+ * bounded-generation SLM inference engine.
+ *
+ * The method is described in "SLM 生成式高并发推理引擎：延迟约束下的有效吞吐优化"
+ * (163.com):
+ *   - abstract: Packed Prefill and a request-internal shared-prefix K/V layout
+ *     are two of the custom pieces embedded in the engine;
+ *   - section 1.1 (two execution forms): Prefill-Only runs one prefill; Beam
+ *     Search runs one prefill plus a fixed number of decode steps at a fixed
+ *     beam width, keeping candidates, cumulative scores and a parent index;
+ *   - section 1.2 (input/state bounds): only valid tokens of each sequence are
+ *     processed (no padding); the beams of one request share one prompt K/V
+ *     and each beam keeps its own short suffix K/V; all capacity is planned
+ *     and preallocated at load time.
+ *
+ * Conventions shared by every entry point
+ *   - Tensor pointers are DEVICE pointers, owned by the caller, contiguous
+ *     row-major, 16-byte aligned.  bf16 tensors are passed as void*.
+ *   - The library never allocates or frees memory and never synchronises the
+ *     stream: every call only enqueues work on `stream` (0 = legacy default
+ *     stream) and returns.
+ *   - Host-checkable faults (NULL pointers, bad sizes, unsupported shapes,
+ *     misalignment, aliasing) return an error before anything is enqueued.
+ *   - Device-data faults (bad cu_seqlens / cu_prompt / parent_idx contents)
+ *     cannot be seen by the host without a synchronisation, so the kernels
+ *     check them on the device: offending work is skipped (never executed
+ *     with bad indices, never trapped) and, when `dev_status` is non-NULL,
+ *     the BG_DEVSTAT_* bits below are OR-ed into that device int32.  The
+ *     library never clears it; zero it before the calls you want to watch.
+ *   - Every internal wait of a kernel is bounded (about one second); if a
+ *     wait runs out the kernel gives up, sets BG_DEVSTAT_TIMEOUT and returns.
+ *   - Launch failures return BG_ERR_CUDA.
+ *   - Query head h uses kv head h / (Hq / Hkv) (contiguous groups).
+ */
+#ifndef BG_ATTN_H
+#define BG_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    BG_OK = 0,
+    BG_ERR_INVALID_ARG = 1,   /* bad pointer, size, alignment or aliasing      */
+    BG_ERR_UNSUPPORTED = 2,   /* valid but outside what the kernels implement  */
+    BG_ERR_DEVICE_DATA = 3,   /* reserved: device-data faults go to dev_status */
+    BG_ERR_CUDA = 4           /* a CUDA runtime call or launch failed          */
+} bg_status_t;
+
+/* Bits OR-ed into *dev_status by the kernels. */
+#define BG_DEVSTAT_CU_SEQLENS   0x01  /* cu_seqlens[0]!=0, decreasing, or cu[B]!=T  */
+#define BG_DEVSTAT_SEQ_TOO_LONG 0x02  /* a sequence is longer than max_seqlen       */
+#define BG_DEVSTAT_PARENT       0x04  /* a parent index is outside [0, W)           */
+#define BG_DEVSTAT_CU_PROMPT    0x08  /* cu_prompt invalid or prompt > max_prompt   */
+#define BG_DEVSTAT_EMPTY_ROW    0x10  /* prompt length 0 with suffix_len 0          */
+#define BG_DEVSTAT_TIMEOUT      0x100 /* an internal pipeline wait ran out          */
+
+/* Supported shapes: head_dim in {64, 128}; Hq % Hkv == 0; for decode
+ * Hq/Hkv <= 128; suffix_max <= BG_MAX_SUFFIX; max_seqlen <= BG_MAX_SEQLEN. */
+#define BG_MAX_SUFFIX 16
+#define BG_MAX_SEQLEN 65536
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char *bg_status_string(bg_status_t status);
+
+/*
+ * Bytes of device workspace bg_packed_prefill_attn needs for these sizes (an
+ * upper bound that depends only on host-known sizes).  The workspace holds
+ * the per-call work list the kernels build from cu_seqlens; it may be reused
+ * across calls on the same stream but not by calls that overlap in time.
+ */
+size_t bg_packed_prefill_workspace_size(int32_t num_seqs, int32_t total_tokens,
+                                        int32_t max_seqlen, int32_t Hq, int32_t Hkv,
+                                        int32_t head_dim);
+
+/*
+ * Packed variable-length causal GQA prefill attention.
+ * Source: abstract (Packed Prefill) and section 1.2 (valid tokens only, no
+ * padding) of the page above.  For every sequence i (packed rows
+ * cu_seqlens[i] .. cu_seqlens[i+1]-1), query head h and position p:
+ *     out[row p, h] = sum_{j<=p} softmax_j(scale * q[p,h] . k[j,kvh]) v[j,kvh]
+ * with kvh = h / (Hq/Hkv).  The softmax runs in fp32; Q.K^T and P.V run on
+ * the tensor cores with bf16 operands and fp32 accumulation.
+ *
+ *   q            bf16 [total_tokens, Hq,  head_dim]
+ *   k, v         bf16 [total_tokens, Hkv, head_dim]
+ *   cu_seqlens   int32 [num_seqs+1], device; cu[0]=0, non-decreasing,
+ *                cu[num_seqs]=total_tokens; zero-length sequences allowed
+ *   max_seqlen   host upper bound of every sequence length (checked on device)
+ *   scale        softmax scale (1/sqrt(head_dim) for standard attention)
+ *   out          bf16 [total_tokens, Hq, head_dim]; rows of every valid token
+ *                are written, nothing else is touched
+ *   lse          fp32 [total_tokens, Hq] natural-log sum-exp of the scaled
+ *                logits of each row, or NULL
+ *   workspace    device buffer of at least
+ *                bg_packed_prefill_workspace_size(...) bytes, 256-B aligned
+ *   dev_status   device int32 or NULL (see conventions)
+ * Errors: BG_ERR_INVALID_ARG for NULL/misaligned pointers, negative sizes,
+ * Hq % Hkv != 0, a too-small workspace, or out aliasing an input;
+ * BG_ERR_UNSUPPORTED for head_dim not in {64,128} or max_seqlen > BG_MAX_SEQLEN.
+ * total_tokens == 0 or num_seqs == 0 is a valid no-op.
+ */
+bg_status_t bg_packed_prefill_attn(const void *q, const void *k, const void *v,
+                                   const int32_t *cu_seqlens, int32_t num_seqs,
+                                   int32_t total_tokens, int32_t max_seqlen,
+                                   int32_t Hq, int32_t Hkv, int32_t head_dim, float scale,
+                                   void *out, float *lse,
+                                   void *workspace, size_t workspace_bytes,
+                                   int32_t *dev_status, cudaStream_t stream);
+
+/*
+ * Beam-search decode attention over a shared prompt K/V plus each beam's own
+ * suffix K/V.
+ * Source: section 1.2 (the beams of a request share one prompt K/V, each
+ * beam keeps a short suffix K/V) and section 1.1 (fixed beam width, fixed
+ * number of decode steps) of the page above.  For request r, beam b, query
+ * head h (kvh = h / (Hq/Hkv)):
+ *     keys   = [prompt_k rows of r ; suffix_k[r, b, 0:suffix_len, kvh]]
+ *     out[r,b,h] = sum_j softmax_j(scale * q[r,b,h] . key_j) value_j
+ * The query is the newest position, so nothing is masked.  The prompt part
+ * is computed as one dense tensor-core tile of all beams x group heads of a
+ * request against the prompt K/V; the suffix part and the merge run in fp32.
+ *
+ *   q                     bf16 [R, W, Hq, head_dim]
+ *   prompt_k, prompt_v    bf16 [total_prompt_tokens, Hkv, head_dim], request r
+ *                         at rows cu_prompt[r] .. cu_prompt[r+1]-1
+ *   cu_prompt             int32 [R+1], device; cu[0]=0, non-decreasing,
+ *                         cu[R]=total_prompt_tokens
+ *   max_prompt_len        host upper bound of every prompt length
+ *   suffix_k, suffix_v    bf16 [R, W, suffix_max, Hkv, head_dim]; slots
+ *                         0..suffix_len-1 of each beam are read (already in
+ *                         this step's beam order, see bg_beam_suffix_reorder)
+ *   suffix_len            0 .. suffix_max (0: prompt only)
+ *   out                   bf16 [R, W, Hq, head_dim]
+ * A request with prompt length 0 and suffix_len 0 has an empty softmax: its
+ * rows are skipped and BG_DEVSTAT_EMPTY_ROW is raised.
+ * Errors: BG_ERR_INVALID_ARG for NULL/misaligned pointers, bad sizes,
+ * suffix_len > suffix_max, Hq % Hkv != 0, out aliasing an input;
+ * BG_ERR_UNSUPPORTED for head_dim not in {64,128}, Hq/Hkv > 128 or
+ * suffix_max > BG_MAX_SUFFIX.
+ */
+bg_status_t bg_beam_decode_attn(const void *q, const void *prompt_k, const void *prompt_v,
+                                const int32_t *cu_prompt, int32_t total_prompt_tokens,
+                                int32_t max_prompt_len,
+                                const void *suffix_k, const void *suffix_v,
+                                int32_t suffix_len, int32_t suffix_max,
+                                int32_t R, int32_t W, int32_t Hq, int32_t Hkv, int32_t head_dim,
+                                float scale, void *out, int32_t *dev_status,
+                                cudaStream_t stream);
+
+/*
+ * Reorder of the per-beam suffix K/V by the beam parent index, with the
+ * optional append of this step's new token.
+ * Source: section 1.1 (beam selection yields a parent index per surviving
+ * beam) and section 1.2 (each beam keeps its own suffix K/V) of the page
+ * above; the page does not spell out the mechanism, the plain reading is
+ * that each surviving beam inherits its parent's suffix:
+ *     dst[r, b, s] = src[r, parent_idx[r, b], s]   for s < n_tokens
+ *     dst[r, b, n_tokens] = new[r, b]              if new_k/new_v non-NULL
+ * for K and V.  A pure copy of bf16 bit patterns: bit-exact.
+ *
+ *   src_k, src_v, dst_k, dst_v   bf16 [R, W, suffix_max, Hkv, head_dim]; dst
+ *                                must not overlap src (ping-pong buffers)
+ *   parent_idx                   int32 [R, W], device, each in [0, W);
+ *                                repeats allowed (one parent, many children)
+ *   new_k, new_v                 bf16 [R, W, Hkv, head_dim] or both NULL
+ *   n_tokens                     slots moved, 0 .. suffix_max (suffix_max-1
+ *                                when appending)
+ * Beams whose parent index is out of range are left untouched in dst and
+ * raise BG_DEVSTAT_PARENT.
+ * Errors: BG_ERR_INVALID_ARG for NULL/misaligned pointers, bad sizes,
+ * overlapping src/dst, only one of new_k/new_v given, no room to append;
+ * BG_ERR_UNSUPPORTED for head_dim not in {64,128}.
+ */
+bg_status_t bg_beam_suffix_reorder(const void *src_k, const void *src_v,
+                                   void *dst_k, void *dst_v,
+                                   const int32_t *parent_idx,
+                                   const void *new_k, const void *new_v,
+                                   int32_t R, int32_t W, int32_t suffix_max, int32_t n_tokens,
+                                   int32_t Hkv, int32_t head_dim,
+                                   int32_t *dev_status, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BG_ATTN_H */

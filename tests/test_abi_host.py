@@ -1,0 +1,109 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports
+every symbol include/bg_attn.h declares, and rejects bad arguments before
+enqueuing anything."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from attention_packed_varlen_causal_gb300 import binding, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.load()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "bg_attn.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(bg_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("bg_packed_prefill_attn", "bg_beam_decode_attn", "bg_beam_suffix_reorder",
+              "bg_packed_prefill_workspace_size", "bg_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for n in declared_functions():
+        assert hasattr(lib, n), f"{n} declared in bg_attn.h but not exported"
+        assert n in binding.SIGNATURES, f"{n} has no binding signature"
+
+
+def test_status_strings(lib):
+    assert binding.status_string(0) == "BG_OK"
+    assert binding.status_string(1) == "BG_ERR_INVALID_ARG"
+    assert binding.status_string(99) == "BG_ERR_UNKNOWN"
+
+
+def test_workspace_size(lib):
+    ws = lib.bg_packed_prefill_workspace_size(240, 70375, 500, 16, 8, 128)
+    assert ws % 256 == 0 and ws >= 256 + 8 * (70375 // 128 + 240)
+    assert lib.bg_packed_prefill_workspace_size(-1, 5, 5, 1, 1, 64) == 0
+
+
+FAKE = 0x10000          # 16-byte aligned, never dereferenced: every call below fails validation first
+
+
+def prefill(lib, **kw):
+    a = dict(q=FAKE, k=FAKE * 2, v=FAKE * 3, cu=FAKE * 4, B=2, T=10, maxlen=8, Hq=4, Hkv=2, d=64, scale=0.125,
+             out=FAKE * 5, lse=None, ws=FAKE * 6, wsb=1 << 20, st=None, stream=None)
+    a.update(kw)
+    return lib.bg_packed_prefill_attn(a["q"], a["k"], a["v"], a["cu"], a["B"], a["T"], a["maxlen"], a["Hq"],
+                                      a["Hkv"], a["d"], a["scale"], a["out"], a["lse"], a["ws"], a["wsb"], a["st"],
+                                      a["stream"])
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(q=None), 1), (dict(cu=None), 1), (dict(out=None), 1), (dict(ws=None), 1),
+    (dict(Hq=6, Hkv=4), 1), (dict(d=96), 2), (dict(d=256), 2), (dict(maxlen=70000), 2),
+    (dict(B=-1), 1), (dict(q=FAKE + 8), 1), (dict(ws=FAKE * 6 + 16), 1), (dict(wsb=64), 1),
+    (dict(out=FAKE * 1 + 64), 1),            # out overlaps q
+    (dict(scale=float("nan")), 1),
+    (dict(B=0, q=None), 0), (dict(T=0, q=None), 0),   # empty problems are a no-op
+])
+def test_prefill_host_validation(lib, kw, expect):
+    assert prefill(lib, **kw) == expect
+
+
+def decode(lib, **kw):
+    a = dict(q=FAKE, pk=FAKE * 2, pv=FAKE * 3, cu=FAKE * 4, P=100, maxP=60, sk=FAKE * 8, sv=FAKE * 16, t=2, S=4,
+             R=2, W=5, Hq=14, Hkv=2, d=64, scale=0.125, out=FAKE * 32, st=None, stream=None)
+    a.update(kw)
+    return lib.bg_beam_decode_attn(a["q"], a["pk"], a["pv"], a["cu"], a["P"], a["maxP"], a["sk"], a["sv"], a["t"],
+                                   a["S"], a["R"], a["W"], a["Hq"], a["Hkv"], a["d"], a["scale"], a["out"], a["st"],
+                                   a["stream"])
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(q=None), 1), (dict(out=None), 1), (dict(cu=None), 1), (dict(t=5), 1), (dict(t=-1), 1),
+    (dict(pk=None), 1), (dict(sk=None), 1), (dict(Hq=15), 1), (dict(d=80), 2), (dict(S=17, t=2), 2),
+    (dict(Hq=258, Hkv=2), 2), (dict(maxP=0, t=0), 1), (dict(W=0), 1), (dict(out=FAKE + 16), 1),
+    (dict(R=0, q=None), 0),
+])
+def test_decode_host_validation(lib, kw, expect):
+    assert decode(lib, **kw) == expect
+
+
+def reorder(lib, **kw):
+    a = dict(sk=FAKE, sv=FAKE * 2, dk=FAKE * 4, dv=FAKE * 8, par=FAKE * 16, nk=None, nv=None, R=2, W=3, S=4, n=2,
+             Hkv=2, d=64, st=None, stream=None)
+    a.update(kw)
+    return lib.bg_beam_suffix_reorder(a["sk"], a["sv"], a["dk"], a["dv"], a["par"], a["nk"], a["nv"], a["R"],
+                                      a["W"], a["S"], a["n"], a["Hkv"], a["d"], a["st"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(sk=None), 1), (dict(par=None), 1), (dict(n=5), 1), (dict(n=4, nk=FAKE * 32, nv=FAKE * 64), 1),
+    (dict(nk=FAKE * 32), 1), (dict(dk=FAKE), 1), (dict(dk=FAKE * 2 + 256), 1), (dict(d=32), 2),
+    (dict(sk=FAKE + 4), 1), (dict(W=0), 1), (dict(R=0, sk=None), 0),
+])
+def test_reorder_host_validation(lib, kw, expect):
+    assert reorder(lib, **kw) == expect
