@@ -1,0 +1,84 @@
+"""Runs one hot-path call on a named workload a few times, for profilers.
+
+    python -m attention_packed_varlen_causal_gb300.profile_case prefill_only --iters 3
+    python -m attention_packed_varlen_causal_gb300.profile_case beam_long --iters 2
+
+Prefill workloads (tiny, prefill_only, skewed) call bg_packed_prefill_attn
+``iters`` times on one layer of inputs; decode workloads (beam_short,
+beam_long) run ``iters`` complete beam searches of one layer (per step: the
+suffix reorder + append, then the decode attention).  Inputs are drawn on the
+device with a seeded generator, shaped as in ``workloads``.  Nothing is
+timed here: use ncu (or bench.py for timings).
+"""
+from __future__ import annotations
+
+import argparse
+import os
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+def main(argv=None):
+    import numpy as np
+    import torch
+
+    from attention_packed_varlen_causal_gb300 import binding as bg
+    from attention_packed_varlen_causal_gb300 import build
+    from attention_packed_varlen_causal_gb300 import workloads as wl
+
+    ap = argparse.ArgumentParser()
+    ap.add_argument("workload", choices=sorted(list(wl.PREFILL_CONFIGS) + list(wl.DECODE_CONFIGS)))
+    ap.add_argument("--iters", type=int, default=3)
+    args = ap.parse_args(argv)
+    build.build()
+    bg.load()
+    dev = torch.device("cuda:0")
+    g = torch.Generator(device=dev)
+    g.manual_seed(1234)
+    bf = torch.bfloat16
+    if args.workload in wl.PREFILL_CONFIGS:
+        cfg = wl.PREFILL_CONFIGS[args.workload]
+        lengths = wl.prefill_lengths(cfg)
+        cu_np = wl.cu_from_lengths(lengths)
+        T = int(cu_np[-1])
+        q = torch.randn((T, cfg.Hq, cfg.head_dim), generator=g, device=dev).to(bf)
+        k = torch.randn((T, cfg.Hkv, cfg.head_dim), generator=g, device=dev).to(bf)
+        v = torch.randn((T, cfg.Hkv, cfg.head_dim), generator=g, device=dev).to(bf)
+        out = torch.empty_like(q)
+        cu = torch.from_numpy(cu_np).to(dev)
+        ws = torch.empty(bg.bg_packed_prefill_workspace_size(len(lengths), T, max(lengths), cfg.Hq, cfg.Hkv,
+                                                             cfg.head_dim), dtype=torch.uint8, device=dev)
+        for _ in range(args.iters):
+            bg.bg_packed_prefill_attn(q, k, v, cu, max(lengths), out, workspace=ws)
+    else:
+        cfg = wl.DECODE_CONFIGS[args.workload]
+        plen = wl.decode_prompt_lengths(cfg)
+        cu_np = wl.cu_from_lengths(plen)
+        P = int(cu_np[-1])
+        R, W, Hq, Hkv, d, S = cfg.R, cfg.W, cfg.Hq, cfg.Hkv, cfg.head_dim, cfg.steps
+        pk = torch.randn((P, Hkv, d), generator=g, device=dev).to(bf)
+        pv = torch.randn((P, Hkv, d), generator=g, device=dev).to(bf)
+        cu = torch.from_numpy(cu_np).to(dev)
+        qs = [torch.randn((R, W, Hq, d), generator=g, device=dev).to(bf) for _ in range(S)]
+        nk = [torch.randn((R, W, Hkv, d), generator=g, device=dev).to(bf) for _ in range(S)]
+        nv = [torch.randn((R, W, Hkv, d), generator=g, device=dev).to(bf) for _ in range(S)]
+        parents = [torch.from_numpy(np.random.default_rng(wl.SEED_PARENT + s).integers(0, W, size=(R, W))
+                                    .astype(np.int32)).to(dev) for s in range(S)]
+        sk = [torch.zeros((R, W, S, Hkv, d), dtype=bf, device=dev) for _ in range(2)]
+        sv = [torch.zeros((R, W, S, Hkv, d), dtype=bf, device=dev) for _ in range(2)]
+        out = torch.empty_like(qs[0])
+        for _ in range(args.iters):
+            for s in range(S):
+                src, dst = s % 2, 1 - s % 2
+                bg.bg_beam_suffix_reorder(sk[src], sv[src], sk[dst], sv[dst], parents[s], s, new_k=nk[s],
+                                          new_v=nv[s])
+                bg.bg_beam_decode_attn(qs[s], pk, pv, cu, max(plen), sk[dst], sv[dst], s + 1, out)
+    torch.cuda.synchronize()
+    print(f"profile_case {args.workload}: {args.iters} iteration(s) done")
+
+
+if __name__ == "__main__":
+    main()
