@@ -28,6 +28,7 @@ BG_DEVSTAT_EMPTY_ROW = 0x10
 BG_DEVSTAT_TIMEOUT = 0x100
 BG_MAX_SUFFIX = 16
 BG_MAX_SEQLEN = 65536
+BG_NOALLOC_SCRATCH_BYTES = 1 << 20
 
 # Every symbol include/bg_attn.h declares, with its ctypes signature.
 _P, _I32, _F32, _SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float, ctypes.c_size_t
@@ -36,6 +37,8 @@ SIGNATURES = {
     "bg_packed_prefill_workspace_size": ([_I32] * 6, _SZ),
     "bg_packed_prefill_attn": ([_P, _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32, _F32, _P, _P, _P, _SZ, _P, _P],
                                ctypes.c_int),
+    "bg_packed_prefill_attn_noalloc": ([_P, _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32, _F32, _P, _P, _P, _P],
+                                       ctypes.c_int),
     "bg_beam_decode_attn": ([_P, _P, _P, _P, _I32, _I32, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _F32, _P,
                              _P, _P], ctypes.c_int),
     "bg_beam_suffix_reorder": ([_P, _P, _P, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32, _P, _P],
@@ -121,6 +124,25 @@ def bg_packed_prefill_attn(q, k, v, cu_seqlens, max_seqlen: int, out, *, lse=Non
                                        workspace.numel() * workspace.element_size(), _ptr(dev_status),
                                        _stream(stream))
     _check("bg_packed_prefill_attn", st)
+    return out
+
+
+def bg_packed_prefill_attn_noalloc(q, k, v, cu_seqlens, max_seqlen: int, out, *, lse=None,
+                                   scale: Optional[float] = None, dev_status=None, stream=None):
+    """As bg_packed_prefill_attn, for callers that cannot allocate: the work
+    list lives in the library's own fixed device array (no workspace
+    argument).  Calls on one device share that array, so calls that can
+    overlap on the GPU must be serialised; the first call on a device should
+    precede any stream capture."""
+    T, Hq, d = q.shape
+    Hkv = k.shape[1]
+    B = cu_seqlens.numel() - 1
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    st = load().bg_packed_prefill_attn_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), B, T, int(max_seqlen), Hq,
+                                               Hkv, d, float(scale), _ptr(out), _ptr(lse), _ptr(dev_status),
+                                               _stream(stream))
+    _check("bg_packed_prefill_attn_noalloc", st)
     return out
 
 

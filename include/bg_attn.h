@@ -185,6 +185,38 @@ bg_status_t bg_beam_suffix_reorder(const void *src_k, const void *src_v,
                                    int32_t Hkv, int32_t head_dim,
                                    int32_t *dev_status, cudaStream_t stream);
 
+/*
+ * Allocation-free variant of bg_packed_prefill_attn.  The paper has no
+ * counterpart to this entry point; it exists for callers that cannot
+ * allocate device memory or hold a workspace of their own -- for example a
+ * node inside a runtime that owns every device buffer and passes a kernel
+ * call only its inputs and outputs, or a latency-bound serving loop that
+ * must not call cudaMalloc.
+ *
+ * Same arguments, semantics and errors as bg_packed_prefill_attn, minus the
+ * workspace.  The work list lives in a fixed array of
+ * BG_NOALLOC_SCRATCH_BYTES in the library's own device memory, which every
+ * GPU that loads the library keeps until the process exits.  Limits and
+ * rules:
+ *   - problems with bg_packed_prefill_workspace_size(...) larger than
+ *     BG_NOALLOC_SCRATCH_BYTES (total_tokens/128 + num_seqs + 1 > 131040)
+ *     return BG_ERR_UNSUPPORTED and enqueue nothing;
+ *   - all calls on a device share that array: calls that can overlap on the
+ *     GPU (different streams, concurrent graphs) race and must be
+ *     serialised by the caller;
+ *   - the first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current) and caches it; make
+ *     that first call before any stream capture.
+ * It never calls cudaMalloc, cudaFree or any allocating routine.
+ */
+#define BG_NOALLOC_SCRATCH_BYTES (1u << 20)
+bg_status_t bg_packed_prefill_attn_noalloc(const void *q, const void *k, const void *v,
+                                           const int32_t *cu_seqlens, int32_t num_seqs,
+                                           int32_t total_tokens, int32_t max_seqlen,
+                                           int32_t Hq, int32_t Hkv, int32_t head_dim, float scale,
+                                           void *out, float *lse,
+                                           int32_t *dev_status, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
