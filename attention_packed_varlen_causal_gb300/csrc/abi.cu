@@ -111,7 +111,7 @@ size_t bg_packed_prefill_workspace_size(int32_t num_seqs, int32_t total_tokens, 
     (void)Hkv;
     (void)head_dim;
     if (num_seqs < 0 || total_tokens < 0) return 0;
-    const size_t bytes = kWorkHeaderBytes + sizeof(int2) * prefill_entries_bound(num_seqs, total_tokens);
+    const size_t bytes = kWorkHeaderBytes + sizeof(int4) * prefill_entries_bound(num_seqs, total_tokens);
     return (bytes + 255) & ~size_t(255);
 }
 
@@ -156,13 +156,15 @@ bg_status_t bg_packed_prefill_attn(const void *q, const void *k, const void *v, 
     const uint64_t sq[2] = {D * 2, static_cast<uint64_t>(Hq) * D * 2};
     const uint64_t dkv[3] = {D, static_cast<uint64_t>(Hkv), static_cast<uint64_t>(total_tokens)};
     const uint64_t skv[2] = {D * 2, static_cast<uint64_t>(Hkv) * D * 2};
-    const uint32_t box[3] = {64, 1, 128};
-    if (!encode_map(&tm_q, q, 3, dq, sq, box) || !encode_map(&tm_k, k, 3, dkv, skv, box) ||
-        !encode_map(&tm_v, v, 3, dkv, skv, box))
+    // boxes: 64 columns (one 128-byte swizzle span) x one head x the kernel's tile height
+    const uint32_t boxq[3] = {64, 1, static_cast<uint32_t>(bg::kRows)};
+    const uint32_t boxkv[3] = {64, 1, static_cast<uint32_t>(bg::kKeys)};
+    if (!encode_map(&tm_q, q, 3, dq, sq, boxq) || !encode_map(&tm_k, k, 3, dkv, skv, boxkv) ||
+        !encode_map(&tm_v, v, 3, dkv, skv, boxkv))
         return BG_ERR_CUDA;
 
     int32_t *hdr = static_cast<int32_t *>(workspace);
-    int2 *work = reinterpret_cast<int2 *>(static_cast<uint8_t *>(workspace) + kWorkHeaderBytes);
+    int4 *work = reinterpret_cast<int4 *>(static_cast<uint8_t *>(workspace) + kWorkHeaderBytes);
     if (launch_prefill_worklist(cu_seqlens, num_seqs, total_tokens, max_seqlen, hdr, work, dev_status, stream) !=
         cudaSuccess)
         return BG_ERR_CUDA;
@@ -235,7 +237,7 @@ bg_status_t bg_beam_decode_attn(const void *q, const void *prompt_k, const void 
     const uint64_t np = total_prompt_tokens > 0 ? static_cast<uint64_t>(total_prompt_tokens) : 1;
     const uint64_t dkv[3] = {D, static_cast<uint64_t>(Hkv), np};
     const uint64_t skv[2] = {D * 2, static_cast<uint64_t>(Hkv) * D * 2};
-    const uint32_t boxkv[3] = {64, 1, 128};
+    const uint32_t boxkv[3] = {64, 1, static_cast<uint32_t>(bg::kKeys)};
     // With no prompt tokens no K/V tile is ever loaded; the maps only need a valid base.
     const void *kbase = total_prompt_tokens > 0 ? prompt_k : q;
     const void *vbase = total_prompt_tokens > 0 ? prompt_v : q;

@@ -4,26 +4,45 @@
 // generation engine ("SLM 生成式高并发推理引擎：延迟约束下的有效吞吐优化",
 // abstract and section 1.2):
 //   * Prefill: packed variable-length causal GQA attention.  A work item is
-//     (sequence, 128-row query tile, NH query heads of one kv head); its key
-//     tiles are 0..qtile (causal), the last one masked on the diagonal.
+//     (sequence, 128-row query tile, NH query heads of one kv head); it
+//     streams the 64-key tiles up to its diagonal (only valid tokens).
 //   * Decode (shared-prompt phase): a work item is (request, kv head, NH
-//     tiles of beams x group heads); every tile is a dense 128-row block of
-//     queries of several beams against the one prompt K/V of the request,
-//     followed in the epilogue by each beam's own suffix keys and the merge.
+//     tiles of beams x group heads); each tile is a dense 128-row block of
+//     queries of several beams against the request's one prompt K/V; the
+//     epilogue folds in each beam's own suffix keys and merges.
 //
 // Per CTA (persistent, one per SM, static round-robin over items):
-//   warp 0      TMA producer: Q tiles of the item, then K/V tiles through an
-//               NSTAGE ring (one K and one V slot per stage)
-//   warp 1      TMEM allocator + single-thread tcgen05.mma issuer:
-//               S_h = Q_h K^T (SMEM x SMEM), then O_h += P_h V (P_h read from
-//               TMEM, where the softmax warps wrote it over S_h)
-//   warps 2-3   idle
-//   warps 4..   NH softmax warpgroups; thread t of group h owns query row t
-//               of tile h (TMEM lane t): online softmax in fp32 with the
-//               exponent in base 2, lazy rescaling of O (only when the row
-//               maximum grows by more than 2^8), epilogue normalisation and
-//               bf16 store.
-// TMEM: S_h at columns [128h, 128h+128), O_h at [128 NH + D h, ... + D).
+//   warp 0      TMA producer of Q and K: Q tiles of each item into one of two Q
+//               buffers (the next item's Q loads while the current one
+//               computes), K tiles of 64 keys through an NK-stage ring.  A K
+//               stage is released as soon as its QK completes, a Q buffer
+//               after the item's last QK.
+//   warp 2      TMA producer of V: V tiles through an NV-stage ring, released
+//               after their P.V (separate from K so neither stream waits on
+//               the other's consumer).
+//   warp 1      TMEM allocator + single-thread tcgen05.mma issuer.  For every
+//               key tile t it issues S_h(t) = Q_h K(t)^T into one of TWO S
+//               buffers per query tile, one tile ahead of O_h += P_h(t-1) V,
+//               so the tensor cores compute the next scores while the softmax
+//               warps work on the current ones; the lookahead also crosses
+//               item boundaries.  P is read from TMEM (written there by the
+//               softmax warps over their S buffer).
+//   warp 3      idle
+//   warps 4..   NH softmax warpgroups; thread t of group h owns query row t of
+//               tile h (TMEM lane t): masked running max in base-2 units,
+//               lazy rescaling of O (only when the max grows by > 2^8),
+//               exp2 on the SFU, bf16 P back to TMEM; epilogue normalisation
+//               (decode: after merging the suffix keys), 32 columns at a time
+//               through a 2 KB per-warp staging area, so that each bf16 store
+//               instruction writes 64-byte row segments of 8 rows.
+//               Warps whose 32 rows are all masked for a key tile skip it.
+// TMEM columns: S(h,b) at 64*(2h+b), O_h at 128*NH + D*h.
+// Ordering: the MMA warp issues ... QK(t+1), PV(t), QK(t+2), PV(t+1) ... from
+// one thread, and tcgen05.mma executes in issue order, so QK(t+2) may be
+// issued right after PV(t) although it overwrites the S buffer PV(t) reads P
+// from.  The commit after QK(t) therefore also tells the softmax warps that
+// PV(t-2) and everything before it has completed, which keeps every parity
+// wait on pv_done unambiguous.
 // Every wait is bounded (bg::mbar_wait); on a time-out every role leaves its
 // loop, in-flight copies and MMAs are drained, TMEM is freed and the kernel
 // reports BG_DEVSTAT_TIMEOUT.
@@ -35,9 +54,10 @@
 namespace bg {
 
 constexpr int kRows = 128;                 // query rows per tile = TMEM lanes
-constexpr int kKeys = 128;                 // keys per K/V tile
-constexpr int kBoxBytes = 128 * 128;       // 128 rows x 64 bf16 (one swizzle-128B column block)
-constexpr float kRescaleLog2 = 8.0f;       // rescale O only if the max grew by > 2^8
+constexpr int kKeys = 64;                  // keys per K/V tile
+constexpr int kQBox = 128 * 128;           // 128 rows x 64 bf16 (one 128-byte-swizzled column block)
+constexpr int kKVBox = 64 * 128;           // 64 rows x 64 bf16
+constexpr float kRescaleLog2 = 8.0f;       // rescale O only if the max grew by more than 2^8
 constexpr int kMaxSuffix = 16;
 
 enum class Mode : int { Prefill = 0, Decode = 1 };
@@ -50,7 +70,7 @@ struct AttnParams {
     int32_t *err_word;             // extra device word that receives timeouts, or null
     // prefill
     const int32_t *cu_seqlens;
-    const int2 *work;              // (sequence, query tile) entries, longest sequences first
+    const int4 *work;              // (sequence start, length, query tile, sequence) entries
     const int32_t *work_hdr;       // [0] status, [1] number of entries
     int32_t n_head_groups;         // items per entry = Hkv * groups_per_kv
     int32_t groups_per_kv;         // ceil(g / NH)
@@ -66,58 +86,75 @@ struct AttnParams {
     int32_t n_items_decode;
 };
 
-template <int D, int NH, int NSTAGE>
+template <int D, int NH, int NK, int NV>
 struct AttnCfg {
     static constexpr int NB = D / 64;                       // 128-byte column blocks per row
-    static constexpr int kQBytes = NH * NB * kBoxBytes;
-    static constexpr int kTileBytes = NB * kBoxBytes;       // one K or V tile
-    static constexpr int kOffQ = 0;
-    static constexpr int kOffK = kOffQ + kQBytes;
-    static constexpr int kOffV = kOffK + NSTAGE * kTileBytes;
-    static constexpr int kOffBar = kOffV + NSTAGE * kTileBytes;
-    // q_full, q_empty, mma_final, k_full[NS], v_full[NS], kv_empty[NS], s_full[NH], p_full[NH], pv_done[NH]
-    static constexpr int kNumBars = 3 + 3 * NSTAGE + 3 * NH;
+    static constexpr int kQBytes = NH * NB * kQBox;         // one Q buffer (NH tiles)
+    static constexpr int kTileBytes = NB * kKVBox;          // one K or V tile
+    static constexpr int kOffQ = 0;                         // two Q buffers
+    static constexpr int kOffK = kOffQ + 2 * kQBytes;
+    static constexpr int kOffV = kOffK + NK * kTileBytes;
+    static constexpr int kOffStage = kOffV + NV * kTileBytes;     // 2 KB per softmax warp
+    static constexpr int kStageBytes = 32 * 64;
+    static constexpr int kOffBar = kOffStage + 4 * NH * kStageBytes;
+    // q_full[2] q_empty[2] mma_final k_full[NK] k_empty[NK] v_full[NV] v_empty[NV]
+    // s_full[NH][2] p_full[NH][2] pv_done[NH][2]
+    static constexpr int kNumBars = 5 + 2 * NK + 2 * NV + 6 * NH;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + slack for 1024-byte alignment
     static constexpr int kThreads = 128 * (1 + NH);
-    static constexpr int kColS = 0;
     static constexpr int kColO = 128 * NH;
     static constexpr int kColsUsed = 128 * NH + D * NH;
-    static constexpr int kTmemCols = kColsUsed <= 32 ? 32 : kColsUsed <= 64 ? 64 : kColsUsed <= 128 ? 128
-                                   : kColsUsed <= 256 ? 256 : 512;
+    static constexpr int kTmemCols = kColsUsed <= 128 ? 128 : kColsUsed <= 256 ? 256 : 512;
     static_assert(kColsUsed <= 512, "TMEM overflow");
     static_assert(kSmemBytes <= 232448, "shared memory overflow");
+    static_assert(NK >= 2 && NV >= 2, "the K and V rings need two stages for the one-tile lookahead");
 };
+
+__host__ __device__ constexpr uint32_t col_s(int h, int b) { return static_cast<uint32_t>(64 * (2 * h + b)); }
 
 // Everything every role needs to know about one work item.
 struct Item {
     int valid;       // 0: skip entirely (bad device data)
-    int n_tiles;     // K/V tiles to stream (may be 0 in decode)
+    int n_tiles;     // 64-key K/V tiles to stream (may be 0 in decode)
     int kh;          // kv head
     int kv_row0;     // first packed K/V row of the sequence / prompt
     int kv_len;      // sequence length (prefill) or prompt length (decode)
-    // prefill
-    int seq_start, qt, head0;
-    // decode
-    int r, bt0;
+    int seq_start, qt, head0;   // prefill
+    int r, bt0;                 // decode
 };
 
+// The raw descriptor of item `it` in global memory (one 16-byte work entry in
+// prefill, the two prompt offsets in decode).  Fetched one item ahead, so the
+// load latency hides behind the current item.
+template <Mode MODE>
+__device__ __forceinline__ int4 fetch_raw(const AttnParams &p, int it)
+{
+    if constexpr (MODE == Mode::Prefill) {
+        return p.work[it / p.n_head_groups];
+    } else {
+        const int r = it / (p.Hkv * p.pairs_per_rk);
+        return make_int4(p.cu_prompt[r], p.cu_prompt[r + 1], 0, 0);
+    }
+}
+
 template <Mode MODE, int NH>
-__device__ __forceinline__ Item load_item(const AttnParams &p, int it)
+__device__ __forceinline__ Item make_item(const AttnParams &p, int it, int4 raw)
 {
     Item I;
     if constexpr (MODE == Mode::Prefill) {
-        const int e = it / p.n_head_groups;
-        const int hg = it - e * p.n_head_groups;
-        const int2 ent = p.work[e];
+        const int hg = it % p.n_head_groups;
         I.kh = hg / p.groups_per_kv;
         const int hp = hg - I.kh * p.groups_per_kv;
         I.head0 = I.kh * p.g + hp * NH;
-        I.seq_start = p.cu_seqlens[ent.x];
-        I.kv_len = p.cu_seqlens[ent.x + 1] - I.seq_start;
-        I.qt = ent.y;
+        I.seq_start = raw.x;
+        I.kv_len = raw.y;
+        I.qt = raw.z;
         I.kv_row0 = I.seq_start;
-        I.n_tiles = ent.y + 1;
+        // keys up to the tile's last row, and never past the sequence end
+        const int causal_tiles = 2 * raw.z + 2;
+        const int len_tiles = (I.kv_len + kKeys - 1) / kKeys;
+        I.n_tiles = causal_tiles < len_tiles ? causal_tiles : len_tiles;
         I.valid = 1;
         I.r = 0;
         I.bt0 = 0;
@@ -127,8 +164,8 @@ __device__ __forceinline__ Item load_item(const AttnParams &p, int it)
         const int rem = it - I.r * per_r;
         I.kh = rem / p.pairs_per_rk;
         I.bt0 = (rem - I.kh * p.pairs_per_rk) * NH;
-        const int a = p.cu_prompt[I.r];
-        const int b = p.cu_prompt[I.r + 1];
+        const int a = raw.x;
+        const int b = raw.y;
         const bool ok = a >= 0 && b >= a && b <= p.total_prompt && (b - a) <= p.max_prompt_len &&
                         (b - a) + p.suffix_len > 0;
         I.valid = ok ? 1 : 0;
@@ -142,6 +179,52 @@ __device__ __forceinline__ Item load_item(const AttnParams &p, int it)
     return I;
 }
 
+// Walks the (item, key tile) sequence of one CTA, skipping items without
+// tiles.  Every role walks the same sequence, so all agree on global tile
+// numbers (which pick K/V stages, S buffers and barrier phases).
+template <Mode MODE, int NH>
+struct TileWalker {
+    int it, j;           // current item index and tile within it
+    int n_items;
+    Item I;
+    int4 nxt_raw;        // raw descriptor of item it + gridDim.x (prefetched)
+    int n_q;             // items with tiles entered so far (selects the Q buffer)
+    bool valid;
+
+    __device__ void first(const AttnParams &p, int n_items_)
+    {
+        n_items = n_items_;
+        n_q = 0;
+        it = static_cast<int>(blockIdx.x) - static_cast<int>(gridDim.x);
+        j = 0;
+        valid = false;
+        nxt_raw = make_int4(0, 0, 0, 0);
+        if (static_cast<int>(blockIdx.x) < n_items) nxt_raw = fetch_raw<MODE>(p, blockIdx.x);
+        next_item(p);
+    }
+    __device__ void next_item(const AttnParams &p)
+    {
+        for (it += gridDim.x; it < n_items; it += gridDim.x) {
+            const int4 raw = nxt_raw;
+            if (it + static_cast<int>(gridDim.x) < n_items) nxt_raw = fetch_raw<MODE>(p, it + gridDim.x);
+            I = make_item<MODE, NH>(p, it, raw);
+            if (I.valid && I.n_tiles > 0) {
+                j = 0;
+                valid = true;
+                ++n_q;
+                return;
+            }
+        }
+        valid = false;
+    }
+    __device__ void advance(const AttnParams &p)
+    {
+        if (++j >= I.n_tiles) next_item(p);
+    }
+    __device__ int qbuf() const { return (n_q - 1) & 1; }
+    __device__ uint32_t quse() const { return static_cast<uint32_t>((n_q - 1) >> 1); }
+};
+
 // Lane 0 waits, the result is broadcast: the whole warp leaves together.
 __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort)
 {
@@ -151,25 +234,30 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volati
     return ok != 0;
 }
 
-template <Mode MODE, int D, int NH, int NSTAGE>
+template <Mode MODE, int D, int NH, int NK, int NV>
 __global__ void __launch_bounds__(128 * (1 + NH), 1)
     attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const AttnParams p)
 {
-    using C = AttnCfg<D, NH, NSTAGE>;
+    using C = AttnCfg<D, NH, NK, NV>;
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte alignment of the shared-window offset (swizzle-128B atoms need it)
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kOffBar);
-    uint64_t *q_full = bars + 0;
-    uint64_t *q_empty = bars + 1;
-    uint64_t *mma_final = bars + 2;
-    uint64_t *k_full = bars + 3;
-    uint64_t *v_full = k_full + NSTAGE;
-    uint64_t *kv_empty = v_full + NSTAGE;
-    uint64_t *s_full = kv_empty + NSTAGE;
-    uint64_t *p_full = s_full + NH;
-    uint64_t *pv_done = p_full + NH;
+    uint64_t *q_full = bars + 0;         // [2]
+    uint64_t *q_empty = bars + 2;        // [2]
+    uint64_t *mma_final = bars + 4;
+    uint64_t *k_full = bars + 5;            // [NK]
+    uint64_t *k_empty = k_full + NK;        // [NK]
+    uint64_t *v_full = k_empty + NK;        // [NV]
+    uint64_t *v_empty = v_full + NV;        // [NV]
+    uint64_t *s_full = v_empty + NV;        // [NH][2]
+    uint64_t *p_full = s_full + 2 * NH;     // [NH][2]
+    // pv_done[h][b] completes when P.V of a tile stored in S buffer b is done.
+    // One barrier per buffer (not per head): every wait on it is then for
+    // the phase right after the last one its waiter already saw complete,
+    // which is what makes a parity wait unambiguous.
+    uint64_t *pv_done = p_full + 2 * NH;    // [NH][2]
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
 
@@ -184,18 +272,23 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
     }
 
     if (threadIdx.x == 0) {
-        mbar_init(q_full, 1);
-        mbar_init(q_empty, 1);
-        mbar_init(mma_final, 1);
-        for (int s = 0; s < NSTAGE; ++s) {
-            mbar_init(&k_full[s], 1);
-            mbar_init(&v_full[s], 1);
-            mbar_init(&kv_empty[s], 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&q_full[b], 1);
+            mbar_init(&q_empty[b], 1);
         }
-        for (int h = 0; h < NH; ++h) {
-            mbar_init(&s_full[h], 1);
-            mbar_init(&p_full[h], 128);
-            mbar_init(&pv_done[h], 1);
+        mbar_init(mma_final, 1);
+        for (int s = 0; s < NK; ++s) {
+            mbar_init(&k_full[s], 1);
+            mbar_init(&k_empty[s], 1);
+        }
+        for (int s = 0; s < NV; ++s) {
+            mbar_init(&v_full[s], 1);
+            mbar_init(&v_empty[s], 1);
+        }
+        for (int i = 0; i < 2 * NH; ++i) {
+            mbar_init(&s_full[i], 1);
+            mbar_init(&p_full[i], 128);
+            mbar_init(&pv_done[i], 1);
         }
         *abort_flag = 0;
         fence_barrier_init();
@@ -203,7 +296,7 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
     if constexpr (MODE == Mode::Decode) {
         // Decode query tiles fill only BT*g <= 128 rows; keep the rest zero.
         uint4 *q4 = reinterpret_cast<uint4 *>(smem + C::kOffQ);
-        for (int i = threadIdx.x; i < C::kQBytes / 16; i += blockDim.x) q4[i] = make_uint4(0, 0, 0, 0);
+        for (int i = threadIdx.x; i < 2 * C::kQBytes / 16; i += blockDim.x) q4[i] = make_uint4(0, 0, 0, 0);
         fence_proxy_async_smem();
     }
     if (warp == 1) {
@@ -222,125 +315,171 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
 
     if (warp == 0) {
         // =============================================================== producer
-        if (lane == 0) {
-            const uint64_t pol_q = l2_policy_evict_first();
-            const uint64_t pol_kv = l2_policy_evict_last();
-            uint32_t n_q = 0;          // Q loads issued
-            uint32_t n_kv = 0;         // K/V tiles issued
-            bool ok = true;
-            for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
-                const Item I = load_item<MODE, NH>(p, it);
-                if (!I.valid || I.n_tiles == 0) continue;
-                if (n_q > 0 && !mbar_wait(q_empty, (n_q - 1) & 1, abort_flag)) { ok = false; break; }
+        // The whole warp runs the loop (warp-uniform control flow and operands); lane 0
+        // issues each copy.
+        const uint64_t pol_q = l2_policy_evict_first();
+        const uint64_t pol_kv = l2_policy_evict_last();
+        TileWalker<MODE, NH> w;
+        w.first(p, n_items);
+        uint32_t n_kv = 0;                 // K/V tiles issued (global tile number)
+        while (w.valid) {
+            if (w.j == 0) {
+                const int qb = w.qbuf();
+                const uint32_t use = w.quse();
+                if (use > 0 && !warp_wait(&q_empty[qb], (use - 1) & 1, abort_flag)) break;
+                uint8_t *qdst = smem + C::kOffQ + qb * C::kQBytes;
                 if constexpr (MODE == Mode::Prefill) {
-                    mbar_arrive_expect_tx(q_full, NH * C::NB * kBoxBytes);
-                    const int row = I.seq_start + I.qt * kRows;
+                    mbar_arrive_expect_tx_w(&q_full[qb], NH * C::NB * kQBox);
+                    const int row = w.I.seq_start + w.I.qt * kRows;
+#pragma unroll
                     for (int h = 0; h < NH; ++h)
+#pragma unroll
                         for (int b = 0; b < C::NB; ++b)
-                            tma_load_3d(smem + C::kOffQ + (h * C::NB + b) * kBoxBytes, &tm_q, q_full, b * 64,
-                                        I.head0 + h, row, pol_q);
+                            tma_load_3d_w(qdst + (h * C::NB + b) * kQBox, &tm_q, &q_full[qb], b * 64, w.I.head0 + h,
+                                          row, pol_q);
                 } else {
                     const uint32_t box = static_cast<uint32_t>(p.BT * p.g * 128);
-                    mbar_arrive_expect_tx(q_full, NH * C::NB * box);
+                    mbar_arrive_expect_tx_w(&q_full[qb], NH * C::NB * box);
+#pragma unroll
                     for (int h = 0; h < NH; ++h)
+#pragma unroll
                         for (int b = 0; b < C::NB; ++b)
-                            tma_load_4d(smem + C::kOffQ + (h * C::NB + b) * kBoxBytes, &tm_q, q_full, b * 64, 0,
-                                        I.kh, I.r * p.W + (I.bt0 + h) * p.BT, pol_q);
-                }
-                ++n_q;
-                for (int j = 0; j < I.n_tiles; ++j) {
-                    const int st = n_kv % NSTAGE;
-                    const uint32_t use = n_kv / NSTAGE;
-                    if (use > 0 && !mbar_wait(&kv_empty[st], (use - 1) & 1, abort_flag)) { ok = false; break; }
-                    const int row = I.kv_row0 + j * kKeys;
-                    mbar_arrive_expect_tx(&k_full[st], C::kTileBytes);
-                    for (int b = 0; b < C::NB; ++b)
-                        tma_load_3d(smem + C::kOffK + st * C::kTileBytes + b * kBoxBytes, &tm_k, &k_full[st],
-                                    b * 64, I.kh, row, pol_kv);
-                    mbar_arrive_expect_tx(&v_full[st], C::kTileBytes);
-                    for (int b = 0; b < C::NB; ++b)
-                        tma_load_3d(smem + C::kOffV + st * C::kTileBytes + b * kBoxBytes, &tm_v, &v_full[st],
-                                    b * 64, I.kh, row, pol_kv);
-                    ++n_kv;
+                            tma_load_4d_w(qdst + (h * C::NB + b) * kQBox, &tm_q, &q_full[qb], b * 64, 0, w.I.kh,
+                                          w.I.r * p.W + (w.I.bt0 + h) * p.BT, pol_q);
                 }
             }
-            // Let every copy this thread started land before the CTA exits.
-            if (n_q > 0) mbar_wait_drain(q_full, (n_q - 1) & 1);
-            for (int st = 0; st < NSTAGE; ++st) {
-                const uint32_t uses = n_kv / NSTAGE + (st < static_cast<int>(n_kv % NSTAGE) ? 1u : 0u);
-                if (uses > 0) {
-                    mbar_wait_drain(&k_full[st], (uses - 1) & 1);
-                    mbar_wait_drain(&v_full[st], (uses - 1) & 1);
-                }
+            const int st = n_kv % NK;
+            const uint32_t use = n_kv / NK;
+            if (use > 0 && !warp_wait(&k_empty[st], (use - 1) & 1, abort_flag)) break;
+            const int row = w.I.kv_row0 + w.j * kKeys;
+            mbar_arrive_expect_tx_w(&k_full[st], C::kTileBytes);
+#pragma unroll
+            for (int b = 0; b < C::NB; ++b)
+                tma_load_3d_w(smem + C::kOffK + st * C::kTileBytes + b * kKVBox, &tm_k, &k_full[st], b * 64, w.I.kh,
+                              row, pol_kv);
+            ++n_kv;
+            w.advance(p);
+        }
+        // Let every copy this warp started land before the CTA exits.
+        if (lane == 0) {
+            for (int qb = 0; qb < 2; ++qb) {
+                const int uses = (w.n_q - qb + 1) / 2;
+                if (uses > 0) mbar_wait_drain(&q_full[qb], (uses - 1) & 1);
+            }
+            for (int st = 0; st < NK; ++st) {
+                const uint32_t uses = n_kv / NK + (st < static_cast<int>(n_kv % NK) ? 1u : 0u);
+                if (uses > 0) mbar_wait_drain(&k_full[st], (uses - 1) & 1);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 2) {
+        // =============================================================== V producer
+        const uint64_t pol_kv = l2_policy_evict_last();
+        TileWalker<MODE, NH> w;
+        w.first(p, n_items);
+        uint32_t n_v = 0;
+        while (w.valid) {
+            const int st = n_v % NV;
+            const uint32_t use = n_v / NV;
+            if (use > 0 && !warp_wait(&v_empty[st], (use - 1) & 1, abort_flag)) break;
+            const int row = w.I.kv_row0 + w.j * kKeys;
+            mbar_arrive_expect_tx_w(&v_full[st], C::kTileBytes);
+#pragma unroll
+            for (int b = 0; b < C::NB; ++b)
+                tma_load_3d_w(smem + C::kOffV + st * C::kTileBytes + b * kKVBox, &tm_v, &v_full[st], b * 64, w.I.kh,
+                              row, pol_kv);
+            ++n_v;
+            w.advance(p);
+        }
+        if (lane == 0) {
+            for (int st = 0; st < NV; ++st) {
+                const uint32_t uses = n_v / NV + (st < static_cast<int>(n_v % NV) ? 1u : 0u);
+                if (uses > 0) mbar_wait_drain(&v_full[st], (uses - 1) & 1);
             }
         }
         __syncwarp();
     } else if (warp == 1) {
         // =============================================================== MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t kIdescQK = idesc_bf16_f32(128, kKeys, 0);
-            constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, 1);
-            const uint32_t sq = smem_u32(smem + C::kOffQ);
-            const uint32_t sk = smem_u32(smem + C::kOffK);
-            const uint32_t sv = smem_u32(smem + C::kOffV);
-            uint32_t n_q = 0, n_kv = 0;
-            uint32_t n_pv[NH];
+        // Warp-converged like the producer; lane 0 issues every tcgen05.mma and commit.
+        constexpr uint32_t kIdescQK = idesc_bf16_f32(128, kKeys, 0);
+        constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, 1);
+        // Base descriptors, built once; an operand at byte offset `off` from a base is the
+        // base plus off / 16 (the start-address field, no carry: shared memory < 256 KB).
+        const uint64_t dq0 = sdesc_sw128(smem_u32(smem + C::kOffQ), 16, 1024);
+        const uint64_t dk0 = sdesc_sw128(smem_u32(smem + C::kOffK), 16, 1024);
+        const uint64_t dv0 = sdesc_sw128(smem_u32(smem + C::kOffV), kKVBox, 1024);
+        // `b` walks the tiles whose S is computed next, `a` (one behind) the tiles whose
+        // P.V is accumulated next.
+        TileWalker<MODE, NH> b, a;
+        b.first(p, n_items);
+        a = b;
+        uint32_t gb = 0, ga = 0;           // global tile numbers of b and a
+        bool ok = true;
+
+        auto issue_qk = [&](const TileWalker<MODE, NH> &t, uint32_t g) -> bool {
+            if (t.j == 0 && !warp_wait(&q_full[t.qbuf()], t.quse() & 1, abort_flag)) return false;
+            const int st = g % NK;
+            if (!warp_wait(&k_full[st], (g / NK) & 1, abort_flag)) return false;
+            const uint64_t dqb = dq0 + static_cast<uint64_t>((t.qbuf() * C::kQBytes) >> 4);
+            const uint64_t dks = dk0 + static_cast<uint64_t>((st * C::kTileBytes) >> 4);
 #pragma unroll
-            for (int h = 0; h < NH; ++h) n_pv[h] = 0;
-            bool ok = true;
-            for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
-                const Item I = load_item<MODE, NH>(p, it);
-                if (!I.valid || I.n_tiles == 0) continue;
-                if (!mbar_wait(q_full, n_q & 1, abort_flag)) { ok = false; break; }
-                ++n_q;
-                for (int j = 0; j < I.n_tiles; ++j) {
-                    const int st = n_kv % NSTAGE;
-                    const uint32_t par = (n_kv / NSTAGE) & 1;
-                    if (!mbar_wait(&k_full[st], par, abort_flag)) { ok = false; break; }
-                    tc_fence_after();
-                    for (int h = 0; h < NH; ++h) {
-                        // S_h is free once the previous P_h (stored over it) has been consumed.
-                        if (n_pv[h] > 0 && !mbar_wait(&pv_done[h], (n_pv[h] - 1) & 1, abort_flag)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        const uint32_t d_s = tmem + C::kColS + 128 * h;
+            for (int h = 0; h < NH; ++h) {
+                // S(h, g%2) holds P of tile g-2, read by the P.V issued just before this QK.
+                // tcgen05.mma operations issued by one thread execute in issue order, so this
+                // QK cannot overwrite P before that P.V has read it: no wait for its completion.
+                tc_fence_after();
+                const uint32_t d_s = tmem + col_s(h, g & 1);
+                const uint64_t dqh = dqb + static_cast<uint64_t>((h * C::NB * kQBox) >> 4);
 #pragma unroll
-                        for (int kk = 0; kk < D / 16; ++kk) {
-                            const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
-                            const uint64_t a = sdesc_sw128(sq + h * C::NB * kBoxBytes + off, 16, 1024);
-                            const uint64_t b = sdesc_sw128(sk + st * C::kTileBytes + off, 16, 1024);
-                            mma_ss(d_s, a, b, kIdescQK, kk > 0 ? 1u : 0u);
-                        }
-                        mma_commit(&s_full[h]);
-                    }
-                    if (!ok) break;
-                    if (j == I.n_tiles - 1) mma_commit(q_empty);   // Q of this item no longer needed
-                    if (!mbar_wait(&v_full[st], par, abort_flag)) { ok = false; break; }
-                    for (int h = 0; h < NH; ++h) {
-                        if (!mbar_wait(&p_full[h], n_pv[h] & 1, abort_flag)) { ok = false; break; }
-                        tc_fence_after();
-                        const uint32_t d_o = tmem + C::kColO + D * h;
-                        const uint32_t a_p = tmem + C::kColS + 128 * h;
-#pragma unroll
-                        for (int kk = 0; kk < kKeys / 16; ++kk) {
-                            // V tile: 128 key rows of 128 bytes per column block; K = 16 rows per step.
-                            const uint64_t b = sdesc_sw128(sv + st * C::kTileBytes + kk * 16 * 128, kBoxBytes, 1024);
-                            mma_ts(d_o, a_p + kk * 8, b, kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
-                        }
-                        mma_commit(&pv_done[h]);
-                        ++n_pv[h];
-                    }
-                    if (!ok) break;
-                    mma_commit(&kv_empty[st]);
-                    ++n_kv;
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    mma_ss_w(d_s, dqh + (((kk >> 2) * kQBox + (kk & 3) * 32) >> 4),
+                             dks + (((kk >> 2) * kKVBox + (kk & 3) * 32) >> 4), kIdescQK, kk > 0 ? 1u : 0u);
                 }
+                mma_commit_w(&s_full[2 * h + (g & 1)]);
             }
-            // Drain: every MMA issued above completes before TMEM is released.
-            mma_commit(mma_final);
-            mbar_wait_drain(mma_final, 0);
+            mma_commit_w(&k_empty[st]);   // K(g) is free once both QKs completed
+            if (t.j == t.I.n_tiles - 1) mma_commit_w(&q_empty[t.qbuf()]);   // and so is Q after the item's last
+            return true;
+        };
+
+        if (b.valid) {
+            ok = issue_qk(b, gb);
+            b.advance(p);
+            ++gb;
         }
+        while (ok && a.valid) {
+            if (b.valid) {
+                if (!issue_qk(b, gb)) break;
+                b.advance(p);
+                ++gb;
+            }
+            const int st = ga % NV;
+            if (!warp_wait(&v_full[st], (ga / NV) & 1, abort_flag)) break;
+            const uint64_t dvs = dv0 + static_cast<uint64_t>((st * C::kTileBytes) >> 4);
+#pragma unroll
+            for (int h = 0; h < NH; ++h) {
+                if (!warp_wait(&p_full[2 * h + (ga & 1)], (ga >> 1) & 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_o = tmem + C::kColO + D * h;
+                const uint32_t a_p = tmem + col_s(h, ga & 1);
+#pragma unroll
+                for (int kk = 0; kk < kKeys / 16; ++kk) {
+                    // V tile: 64 key rows of 128 bytes per column block; K = 16 rows per step.
+                    mma_ts_w(d_o, a_p + kk * 8, dvs + ((kk * 16 * 128) >> 4), kIdescPV, (a.j > 0 || kk > 0) ? 1u : 0u);
+                }
+                mma_commit_w(&pv_done[2 * h + (ga & 1)]);
+            }
+            if (!ok) break;
+            mma_commit_w(&v_empty[st]);
+            a.advance(p);
+            ++ga;
+        }
+        // Drain: every MMA issued above completes before TMEM is released.
+        mma_commit_w(mma_final);
+        if (lane == 0) mbar_wait_drain(mma_final, 0);
         __syncwarp();
     } else if (warp >= 4) {
         // =============================================================== softmax + epilogue
@@ -348,18 +487,22 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
         const int quad = warp & 3;
         const int row = quad * 32 + lane;
         const uint32_t lane_addr = static_cast<uint32_t>(quad * 32) << 16;
-        const uint32_t tS = tmem + lane_addr + C::kColS + 128 * h;
         const uint32_t tO = tmem + lane_addr + C::kColO + D * h;
         const float sl2 = p.scale_log2;
-        uint32_t n_s = 0;     // S tiles consumed by this thread
+        uint32_t g = 0;       // global tile number (same sequence as the MMA issuer)
         bool ok = true;
+        int4 nxt_raw = make_int4(0, 0, 0, 0);
+        if (static_cast<int>(blockIdx.x) < n_items) nxt_raw = fetch_raw<MODE>(p, blockIdx.x);
         for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
-            const Item I = load_item<MODE, NH>(p, it);
+            const int4 raw = nxt_raw;
+            if (it + static_cast<int>(gridDim.x) < n_items) nxt_raw = fetch_raw<MODE>(p, it + gridDim.x);
+            const Item I = make_item<MODE, NH>(p, it, raw);
             if (!I.valid) {
                 if constexpr (MODE == Mode::Decode) {
                     if (h == 0 && row == 0 && p.dev_status) {
-                        const int a = p.cu_prompt[I.r], b = p.cu_prompt[I.r + 1];
-                        const bool bad_cu = !(a >= 0 && b >= a && b <= p.total_prompt && (b - a) <= p.max_prompt_len);
+                        const int a = raw.x, b = raw.y;
+                        const bool bad_cu =
+                            !(a >= 0 && b >= a && b <= p.total_prompt && (b - a) <= p.max_prompt_len);
                         atomicOr(p.dev_status, bad_cu ? BG_DEVSTAT_CU_PROMPT : BG_DEVSTAT_EMPTY_ROW);
                     }
                 }
@@ -367,93 +510,147 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
             }
             float m = -INFINITY;   // running max of scaled logits (base-2 units)
             float l = 0.f;         // running sum of exp2(logit - m)
-            for (int j = 0; j < I.n_tiles; ++j) {
-                if (!warp_wait(&s_full[h], n_s & 1, abort_flag)) { ok = false; break; }
-                ++n_s;
+            for (int j = 0; j < I.n_tiles; ++j, ++g) {
+                const uint32_t tS = tmem + lane_addr + col_s(h, g & 1);
+                // valid key columns of this tile: for this row (lim) and the warp's rows (lim_lo..lim_hi)
+                int lim, lim_lo, lim_hi;
+                if constexpr (MODE == Mode::Prefill) {
+                    lim_lo = I.qt * kRows + quad * 32 - j * kKeys + 1;
+                    lim = lim_lo + lane;
+                    lim_hi = lim_lo + 31;
+                } else {
+                    lim_lo = I.kv_len - j * kKeys;
+                    lim = lim_lo;
+                    lim_hi = lim_lo;
+                }
+                if (!warp_wait(&s_full[2 * h + (g & 1)], (g >> 1) & 1, abort_flag)) { ok = false; break; }
                 tc_fence_after();
-                float s[kKeys];
+                if (lim_hi <= 0) {
+                    // every row of this warp is masked for this tile: P = 0
+                    uint32_t zr[16];
 #pragma unroll
-                for (int c = 0; c < kKeys / 32; ++c) tmem_ld32(tS + 32 * c, s + 32 * c);
-                int lim = kKeys;   // columns < lim are valid keys for this row
-                if (j == I.n_tiles - 1) {
-                    if constexpr (MODE == Mode::Prefill) lim = row + 1;          // causal diagonal
-                    else lim = I.kv_len - j * kKeys;                             // prompt tail
-                }
-                float mx = -INFINITY;
+                    for (int i = 0; i < 16; ++i) zr[i] = 0u;
+                    tmem_st16(tS, zr);
+                    tmem_st16(tS + 16, zr);
+                } else {
+                    float s[kKeys];
+                    tmem_ld32(tS, s);
+                    tmem_ld32(tS + 32, s + 32);
+                    if (lim_lo < kKeys) {
 #pragma unroll
-                for (int c = 0; c < kKeys; ++c) {
-                    if (c >= lim) s[c] = -INFINITY;
-                    mx = fmaxf(mx, s[c]);
-                }
-                const float m_new = fmaxf(m, mx * sl2);
-                const bool grow = (j > 0) && (m_new > m + kRescaleLog2);
-                if (j == 0) m = m_new;
-                if (__any_sync(0xffffffffu, grow)) {
-                    // O holds the sum of the previous tiles: wait for the last P.V, rescale in place.
-                    if (!warp_wait(&pv_done[h], (n_s - 2) & 1, abort_flag)) { ok = false; break; }
-                    tc_fence_after();
-                    const float alpha = ex2(m - m_new);
-                    m = m_new;
-                    l *= alpha;
-#pragma unroll
-                    for (int c = 0; c < D / 32; ++c) {
-                        float o[32];
-                        tmem_ld32(tO + 32 * c, o);
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) o[i] *= alpha;
-                        tmem_st32f(tO + 32 * c, o);
+                        for (int c = 0; c < kKeys; ++c)
+                            if (c >= lim) s[c] = -INFINITY;
                     }
-                    tmem_st_wait();
-                }
-                float rs = 0.f;
+                    float mx = s[0];
 #pragma unroll
-                for (int c = 0; c < kKeys / 32; ++c) {
-                    uint32_t pk[16];
+                    for (int c = 1; c < kKeys; ++c) mx = fmaxf(mx, s[c]);
+                    const float m_new = fmaxf(m, mx * sl2);
+                    const bool grow = (j > 0) && (m_new > m + kRescaleLog2);
+                    if (j == 0) m = m_new;
+                    if (__any_sync(0xffffffffu, grow)) {
+                        // O holds the previous tiles: wait for their last P.V, rescale in place.
+                        if (!warp_wait(&pv_done[2 * h + ((g - 1) & 1)], ((g - 1) >> 1) & 1, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const float alpha = ex2(m - m_new);
+                        m = m_new;
+                        l *= alpha;
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const float a = ex2(fmaf(s[32 * c + 2 * i], sl2, -m));
-                        const float b = ex2(fmaf(s[32 * c + 2 * i + 1], sl2, -m));
-                        rs += a + b;
-                        pk[i] = pack_bf16x2(a, b);
+                        for (int c = 0; c < D / 32; ++c) {
+                            float o[32];
+                            tmem_ld32(tO + 32 * c, o);
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) o[i] *= alpha;
+                            tmem_st32f(tO + 32 * c, o);
+                        }
                     }
-                    tmem_st16(tS + 16 * c, pk);   // P (bf16 pairs) over the first 64 columns of S
+                    float rs = 0.f;
+#pragma unroll
+                    for (int c = 0; c < kKeys / 32; ++c) {
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const float e0 = ex2(fmaf(s[32 * c + 2 * i], sl2, -m));
+                            const float e1 = ex2(fmaf(s[32 * c + 2 * i + 1], sl2, -m));
+                            rs += e0 + e1;
+                            pk[i] = pack_bf16x2(e0, e1);
+                        }
+                        tmem_st16(tS + 16 * c, pk);   // P (bf16 pairs) over the first 32 columns of S
+                    }
+                    l += rs;
                 }
                 tmem_st_wait();
-                l += rs;
                 tc_fence_before();
-                mbar_arrive(&p_full[h]);
+                mbar_arrive(&p_full[2 * h + (g & 1)]);
             }
             if (!ok) break;
 
             // ------------------------------------------------------- epilogue
             if (I.n_tiles > 0) {
-                if (!warp_wait(&pv_done[h], (n_s - 1) & 1, abort_flag)) { ok = false; break; }
+                // the commit after the item's last P.V covers every earlier MMA too
+                if (!warp_wait(&pv_done[2 * h + ((g - 1) & 1)], ((g - 1) >> 1) & 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
                 tc_fence_after();
             }
+            // destination of tile row r, or nullptr when the row is not a valid output row
+            auto row_dst = [&](int r) -> __nv_bfloat16 * {
+                if constexpr (MODE == Mode::Prefill) {
+                    const int qrow = I.qt * kRows + r;
+                    const int head = I.head0 + h;
+                    if (qrow >= I.kv_len || head - I.kh * p.g >= p.g) return nullptr;
+                    return p.out + (static_cast<int64_t>(I.seq_start + qrow) * p.Hq + head) * D;
+                } else {
+                    const int lb = r / p.g;
+                    const int hh = r - lb * p.g;
+                    const int beam = (I.bt0 + h) * p.BT + lb;
+                    if (lb >= p.BT || beam >= p.W) return nullptr;
+                    return p.out + ((static_cast<int64_t>(I.r) * p.W + beam) * p.Hq + I.kh * p.g + hh) * D;
+                }
+            };
+            // Each warp stores its 32 rows chunk by chunk: a row's 64-byte chunk goes to the warp's
+            // staging area (slot c ^ ((r >> 1) & 3): conflict-free both ways), then every lane
+            // stores 16 bytes of rows lane/4 + 8i, so a store instruction covers 8 whole 64-byte
+            // segments.  dst[i] is this lane's destination row for pass i.
+            uint8_t *stage = smem + C::kOffStage + (warp - 4) * C::kStageBytes;
+            __nv_bfloat16 *dst[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) dst[i] = row_dst(quad * 32 + i * 8 + (lane >> 2));
+            auto put_chunk = [&](int c, const float *o, float inv_l) {
+                uint4 wv[4];
+                uint32_t *wp = reinterpret_cast<uint32_t *>(wv);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) wp[i] = pack_bf16x2(o[2 * i] * inv_l, o[2 * i + 1] * inv_l);
+                __syncwarp();                       // the previous chunk's reads are done
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    *reinterpret_cast<uint4 *>(stage + lane * 64 + ((u ^ ((lane >> 1) & 3)) * 16)) = wv[u];
+                __syncwarp();
+                const int cc = lane & 3;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int rr = i * 8 + (lane >> 2);
+                    const uint4 val = *reinterpret_cast<const uint4 *>(stage + rr * 64 + ((cc ^ ((rr >> 1) & 3)) * 16));
+                    if (dst[i]) reinterpret_cast<uint4 *>(dst[i] + 32 * c)[cc] = val;
+                }
+            };
             if constexpr (MODE == Mode::Prefill) {
-                const int qrow = I.qt * kRows + row;
-                const int head = I.head0 + h;
-                const bool valid = qrow < I.kv_len && (head - I.kh * p.g) < p.g;
                 const float inv_l = 1.f / l;
-                __nv_bfloat16 *dst = p.out + (static_cast<int64_t>(I.seq_start + qrow) * p.Hq + head) * D;
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
                     float o[32];
                     tmem_ld32(tO + 32 * c, o);
-                    if (valid) {
-                        uint4 w[4];
-                        uint32_t *wp = reinterpret_cast<uint32_t *>(w);
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) wp[i] = pack_bf16x2(o[2 * i] * inv_l, o[2 * i + 1] * inv_l);
-                        uint4 *d4 = reinterpret_cast<uint4 *>(dst + 32 * c);
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) d4[i] = w[i];
-                    }
+                    put_chunk(c, o, inv_l);
                 }
-                if (valid && p.lse) {
-                    // natural-log sum-exp: (m + log2 l) * ln 2
-                    p.lse[static_cast<int64_t>(I.seq_start + qrow) * p.Hq + head] =
-                        (m + __log2f(l)) * 0.69314718055994530942f;
+                if (p.lse) {
+                    if (row_dst(row)) {
+                        // natural-log sum-exp: (m + log2 l) * ln 2
+                        p.lse[static_cast<int64_t>(I.seq_start + I.qt * kRows + row) * p.Hq + I.head0 + h] =
+                            (m + __log2f(l)) * 0.69314718055994530942f;
+                    }
                 }
             } else {
                 const int local_beam = row / p.g;
@@ -462,21 +659,31 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
                 const bool valid = local_beam < p.BT && beam < p.W;
                 const int head = I.kh * p.g + hh;
                 const int64_t rb = static_cast<int64_t>(I.r) * p.W + beam;
-                // suffix logits
+                const int ns = valid ? p.suffix_len : 0;
+                // this row's query, kept in registers for the suffix dot products
+                uint4 qv[D / 8];
+#pragma unroll
+                for (int c = 0; c < D / 8; ++c) qv[c] = make_uint4(0, 0, 0, 0);
+                if (ns > 0) {
+                    const uint4 *qp = reinterpret_cast<const uint4 *>(p.q + (rb * p.Hq + head) * D);
+#pragma unroll
+                    for (int c = 0; c < D / 8; ++c) qv[c] = qp[c];
+                }
+                const __nv_bfloat16 *kbase = p.suffix_k + (rb * p.suffix_max * p.Hkv + I.kh) * D;
+                const __nv_bfloat16 *vbase = p.suffix_v + (rb * p.suffix_max * p.Hkv + I.kh) * D;
+                const int64_t sstride = static_cast<int64_t>(p.Hkv) * D;   // between suffix slots
                 float z[kMaxSuffix];
                 float m2 = m;
 #pragma unroll
                 for (int s = 0; s < kMaxSuffix; ++s) {
                     z[s] = -INFINITY;
-                    if (valid && s < p.suffix_len) {
-                        const uint4 *qp = reinterpret_cast<const uint4 *>(p.q + (rb * p.Hq + head) * D);
-                        const uint4 *kp = reinterpret_cast<const uint4 *>(
-                            p.suffix_k + ((rb * p.suffix_max + s) * p.Hkv + I.kh) * D);
+                    if (s < ns) {
+                        const uint4 *kp = reinterpret_cast<const uint4 *>(kbase + s * sstride);
                         float acc = 0.f;
 #pragma unroll
                         for (int c = 0; c < D / 8; ++c) {
-                            const uint4 qa = qp[c], ka = kp[c];
-                            const __nv_bfloat162 *q2 = reinterpret_cast<const __nv_bfloat162 *>(&qa);
+                            const uint4 ka = kp[c];
+                            const __nv_bfloat162 *q2 = reinterpret_cast<const __nv_bfloat162 *>(&qv[c]);
                             const __nv_bfloat162 *k2 = reinterpret_cast<const __nv_bfloat162 *>(&ka);
 #pragma unroll
                             for (int e = 0; e < 4; ++e) {
@@ -492,14 +699,12 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
                 }
                 const float alpha = (I.n_tiles > 0) ? ex2(m - m2) : 0.f;
                 float l2 = l * alpha;
-                float ps[kMaxSuffix];
 #pragma unroll
                 for (int s = 0; s < kMaxSuffix; ++s) {
-                    ps[s] = (s < p.suffix_len && valid) ? ex2(z[s] - m2) : 0.f;
-                    l2 += ps[s];
+                    z[s] = (s < ns) ? ex2(z[s] - m2) : 0.f;   // z now holds the suffix weights
+                    l2 += z[s];
                 }
                 const float inv_l = valid ? 1.f / l2 : 0.f;
-                __nv_bfloat16 *dst = p.out + (rb * p.Hq + head) * D;
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
                     float o[32];
@@ -509,12 +714,12 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
 #pragma unroll
                         for (int i = 0; i < 32; ++i) o[i] = 0.f;
                     }
-                    if (valid) {
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) o[i] *= alpha;
-                        for (int s = 0; s < p.suffix_len; ++s) {
-                            const uint4 *vp = reinterpret_cast<const uint4 *>(
-                                p.suffix_v + ((rb * p.suffix_max + s) * p.Hkv + I.kh) * D + 32 * c);
+                    for (int i = 0; i < 32; ++i) o[i] *= alpha;
+#pragma unroll
+                    for (int s = 0; s < kMaxSuffix; ++s) {
+                        if (s < ns) {
+                            const uint4 *vp = reinterpret_cast<const uint4 *>(vbase + s * sstride + 32 * c);
 #pragma unroll
                             for (int u = 0; u < 4; ++u) {
                                 const uint4 va = vp[u];
@@ -522,19 +727,13 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
 #pragma unroll
                                 for (int e = 0; e < 4; ++e) {
                                     const float2 vf = __bfloat1622float2(v2[e]);
-                                    o[8 * u + 2 * e] = fmaf(ps[s], vf.x, o[8 * u + 2 * e]);
-                                    o[8 * u + 2 * e + 1] = fmaf(ps[s], vf.y, o[8 * u + 2 * e + 1]);
+                                    o[8 * u + 2 * e] = fmaf(z[s], vf.x, o[8 * u + 2 * e]);
+                                    o[8 * u + 2 * e + 1] = fmaf(z[s], vf.y, o[8 * u + 2 * e + 1]);
                                 }
                             }
                         }
-                        uint4 w[4];
-                        uint32_t *wp = reinterpret_cast<uint32_t *>(w);
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) wp[i] = pack_bf16x2(o[2 * i] * inv_l, o[2 * i + 1] * inv_l);
-                        uint4 *d4 = reinterpret_cast<uint4 *>(dst + 32 * c);
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) d4[i] = w[i];
                     }
+                    put_chunk(c, o, inv_l);
                 }
             }
         }

@@ -17,7 +17,7 @@ struct AttnParams;
 // Prefill: work-list pre-pass + attention kernel.  Maps are built by the
 // caller.  Returns cudaSuccess or the launch error.
 cudaError_t launch_prefill_worklist(const int32_t *cu_seqlens, int32_t num_seqs, int32_t total_tokens,
-                                    int32_t max_seqlen, int32_t *work_hdr, int2 *work, int32_t *dev_status,
+                                    int32_t max_seqlen, int32_t *work_hdr, int4 *work, int32_t *dev_status,
                                     cudaStream_t stream);
 cudaError_t launch_prefill_attn(int head_dim, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
                                 const CUtensorMap &tm_v, const AttnParams &p, int grid, cudaStream_t stream);

@@ -207,6 +207,75 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar)
                  : "memory");
 }
 
+// ---- warp-converged issue: every lane executes the call with the same
+// (warp-uniform) operands and lane 0 issues it.  Keeping the issuing warp
+// converged lets the operands stay warp-uniform, which is what makes
+// back-to-back tcgen05.mma / TMA issue cheap.  Always lane 0, so the lane that
+// commits is the lane that issued the MMAs the commit tracks.
+__device__ __forceinline__ void mma_ss_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t"
+        "{ .reg .b32 l; mov.u32 l, %%laneid; setp.eq.u32 e, l, 0; }\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void mma_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t"
+        "{ .reg .b32 l; mov.u32 l, %%laneid; setp.eq.u32 e, l, 0; }\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void mma_commit_w(uint64_t *bar)
+{
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "{ .reg .b32 l; mov.u32 l, %%laneid; setp.eq.u32 e, l, 0; }\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+            smem_u32(bar))
+        : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx_w(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "{ .reg .b32 l; mov.u32 l, %%laneid; setp.eq.u32 e, l, 0; }\n\t"
+        "@e mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;\n\t}" ::"r"(smem_u32(bar)),
+        "r"(bytes)
+        : "memory");
+}
+__device__ __forceinline__ void tma_load_3d_w(void *dst, const CUtensorMap *map, uint64_t *bar, int32_t c0,
+                                              int32_t c1, int32_t c2, uint64_t policy)
+{
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "{ .reg .b32 l; mov.u32 l, %%laneid; setp.eq.u32 e, l, 0; }\n\t"
+        "@e cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4, %5}], [%2], %6;\n\t}" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "l"(policy)
+        : "memory");
+}
+__device__ __forceinline__ void tma_load_4d_w(void *dst, const CUtensorMap *map, uint64_t *bar, int32_t c0,
+                                              int32_t c1, int32_t c2, int32_t c3, uint64_t policy)
+{
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "{ .reg .b32 l; mov.u32 l, %%laneid; setp.eq.u32 e, l, 0; }\n\t"
+        "@e cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2], %7;\n\t}" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
+        "l"(policy)
+        : "memory");
+}
+
 // 32 consecutive fp32 columns of this thread's TMEM lane; the wait is inside
 // the same asm statement so no register is read before it is valid.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float *v)

@@ -17,20 +17,20 @@ namespace bg {
 namespace {
 constexpr int kNH = 2;   // query tiles (of the same request and kv head) per CTA
 
-template <int D, int NSTAGE>
+template <int D, int NK, int NV>
 std::atomic<uint64_t> &smem_attr_done()
 {
     static std::atomic<uint64_t> mask{0};
     return mask;
 }
 
-template <int D, int NSTAGE>
+template <int D, int NK, int NV>
 cudaError_t launch_one(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
                        const AttnParams &p, int grid, cudaStream_t stream)
 {
-    using C = AttnCfg<D, kNH, NSTAGE>;
-    auto kern = attn_kernel<Mode::Decode, D, kNH, NSTAGE>;
-    cudaError_t e = ensure_smem_attribute(kern, C::kSmemBytes, smem_attr_done<D, NSTAGE>());
+    using C = AttnCfg<D, kNH, NK, NV>;
+    auto kern = attn_kernel<Mode::Decode, D, kNH, NK, NV>;
+    cudaError_t e = ensure_smem_attribute(kern, C::kSmemBytes, smem_attr_done<D, NK, NV>());
     if (e != cudaSuccess) return e;
     kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(tm_q, tm_k, tm_v, p);
     return cudaGetLastError();
@@ -42,8 +42,8 @@ int decode_tiles_per_cta() { return kNH; }
 cudaError_t launch_decode_attn(int head_dim, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
                                const CUtensorMap &tm_v, const AttnParams &p, int grid, cudaStream_t stream)
 {
-    if (head_dim == 64) return launch_one<64, 4>(tm_q, tm_k, tm_v, p, grid, stream);
-    if (head_dim == 128) return launch_one<128, 2>(tm_q, tm_k, tm_v, p, grid, stream);
+    if (head_dim == 64) return launch_one<64, 8, 8>(tm_q, tm_k, tm_v, p, grid, stream);
+    if (head_dim == 128) return launch_one<128, 3, 2>(tm_q, tm_k, tm_v, p, grid, stream);
     return cudaErrorInvalidValue;
 }
 

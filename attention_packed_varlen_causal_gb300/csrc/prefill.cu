@@ -6,7 +6,7 @@
 //
 // Two launches on the caller's stream:
 //   1. worklist_kernel (one CTA): checks cu_seqlens on the device and writes
-//      the list of (sequence, query tile) entries, sequences with more tiles
+//      the list of (sequence start, length, query tile) entries, sequences with more tiles
 //      first and, within a sequence, later (costlier) query tiles first.
 //      Only tiles of valid tokens exist: a sequence of length L has
 //      ceil(L/128) query tiles and tile t streams key tiles 0..t.
@@ -20,7 +20,7 @@ namespace bg {
 
 __global__ void __launch_bounds__(1024) worklist_kernel(const int32_t *__restrict__ cu, int32_t B, int32_t T,
                                                         int32_t max_seqlen, int32_t *__restrict__ hdr,
-                                                        int2 *__restrict__ work, int32_t *dev_status)
+                                                        int4 *__restrict__ work, int32_t *dev_status)
 {
     __shared__ int s_err;
     __shared__ int s_count[kMaxTilesPerSeq + 1];   // sequences per tile count
@@ -58,8 +58,9 @@ __global__ void __launch_bounds__(1024) worklist_kernel(const int32_t *__restric
     }
     if (tid == 0) {
         // buckets in decreasing tile count; a sequence with nt tiles owns nt entries
+        const int max_nt = (max_seqlen + kPrefillTileRows - 1) / kPrefillTileRows;
         int off = 0;
-        for (int nt = kMaxTilesPerSeq; nt >= 1; --nt) {
+        for (int nt = max_nt; nt >= 1; --nt) {
             s_off[nt] = off;
             off += s_count[nt] * nt;
         }
@@ -72,12 +73,13 @@ __global__ void __launch_bounds__(1024) worklist_kernel(const int32_t *__restric
         const int nt = (L + kPrefillTileRows - 1) / kPrefillTileRows;
         if (nt == 0) continue;
         const int pos = atomicAdd(&s_off[nt], nt);
-        for (int t = 0; t < nt; ++t) work[pos + t] = make_int2(i, nt - 1 - t);
+        // complete item descriptors (start, length, query tile), so readers need one load
+        for (int t = 0; t < nt; ++t) work[pos + t] = make_int4(cu[i], L, nt - 1 - t, i);
     }
 }
 
 cudaError_t launch_prefill_worklist(const int32_t *cu_seqlens, int32_t num_seqs, int32_t total_tokens,
-                                    int32_t max_seqlen, int32_t *work_hdr, int2 *work, int32_t *dev_status,
+                                    int32_t max_seqlen, int32_t *work_hdr, int4 *work, int32_t *dev_status,
                                     cudaStream_t stream)
 {
     worklist_kernel<<<1, 1024, 0, stream>>>(cu_seqlens, num_seqs, total_tokens, max_seqlen, work_hdr, work,
@@ -88,20 +90,20 @@ cudaError_t launch_prefill_worklist(const int32_t *cu_seqlens, int32_t num_seqs,
 namespace {
 constexpr int kNH = 2;   // query heads of one kv head per CTA (share every K/V tile)
 
-template <int D, int NSTAGE>
+template <int D, int NK, int NV>
 std::atomic<uint64_t> &smem_attr_done()
 {
     static std::atomic<uint64_t> mask{0};
     return mask;
 }
 
-template <int D, int NSTAGE>
+template <int D, int NK, int NV>
 cudaError_t launch_one(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
                        const AttnParams &p, int grid, cudaStream_t stream)
 {
-    using C = AttnCfg<D, kNH, NSTAGE>;
-    auto kern = attn_kernel<Mode::Prefill, D, kNH, NSTAGE>;
-    cudaError_t e = ensure_smem_attribute(kern, C::kSmemBytes, smem_attr_done<D, NSTAGE>());
+    using C = AttnCfg<D, kNH, NK, NV>;
+    auto kern = attn_kernel<Mode::Prefill, D, kNH, NK, NV>;
+    cudaError_t e = ensure_smem_attribute(kern, C::kSmemBytes, smem_attr_done<D, NK, NV>());
     if (e != cudaSuccess) return e;
     kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(tm_q, tm_k, tm_v, p);
     return cudaGetLastError();
@@ -113,8 +115,8 @@ int prefill_heads_per_cta() { return kNH; }
 cudaError_t launch_prefill_attn(int head_dim, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
                                 const CUtensorMap &tm_v, const AttnParams &p, int grid, cudaStream_t stream)
 {
-    if (head_dim == 128) return launch_one<128, 2>(tm_q, tm_k, tm_v, p, grid, stream);
-    if (head_dim == 64) return launch_one<64, 4>(tm_q, tm_k, tm_v, p, grid, stream);
+    if (head_dim == 128) return launch_one<128, 3, 2>(tm_q, tm_k, tm_v, p, grid, stream);
+    if (head_dim == 64) return launch_one<64, 8, 8>(tm_q, tm_k, tm_v, p, grid, stream);
     return cudaErrorInvalidValue;
 }
 

@@ -199,7 +199,7 @@ bg_status_t bg_beam_suffix_reorder(const void *src_k, const void *src_v,
  * GPU that loads the library keeps until the process exits.  Limits and
  * rules:
  *   - problems with bg_packed_prefill_workspace_size(...) larger than
- *     BG_NOALLOC_SCRATCH_BYTES (total_tokens/128 + num_seqs + 1 > 131040)
+ *     BG_NOALLOC_SCRATCH_BYTES (total_tokens/128 + num_seqs + 1 > 65520)
  *     return BG_ERR_UNSUPPORTED and enqueue nothing;
  *   - all calls on a device share that array: calls that can overlap on the
  *     GPU (different streams, concurrent graphs) race and must be

@@ -45,7 +45,7 @@ def test_status_strings(lib):
 
 def test_workspace_size(lib):
     ws = lib.bg_packed_prefill_workspace_size(240, 70375, 500, 16, 8, 128)
-    assert ws % 256 == 0 and ws >= 256 + 8 * (70375 // 128 + 240)
+    assert ws % 256 == 0 and ws >= 256 + 16 * (70375 // 128 + 240)
     assert lib.bg_packed_prefill_workspace_size(-1, 5, 5, 1, 1, 64) == 0
 
 
