@@ -20,14 +20,14 @@
 //   warp 2      TMA producer of V: V tiles through an NV-stage ring, released
 //               after their P.V (separate from K so neither stream waits on
 //               the other's consumer).
-//   warp 1      TMEM allocator + single-thread tcgen05.mma issuer.  For every
-//               key tile t it issues S_h(t) = Q_h K(t)^T into one of TWO S
-//               buffers per query tile, one tile ahead of O_h += P_h(t-1) V,
+//   warps 1, 3  tcgen05.mma issuers, one per query tile h (warp 1 also
+//               allocates TMEM).  For every key tile t the warp of tile h
+//               issues S_h(t) = Q_h K(t)^T into one of TWO S buffers of
+//               tile h, one tile ahead of O_h += P_h(t-1) V,
 //               so the tensor cores compute the next scores while the softmax
 //               warps work on the current ones; the lookahead also crosses
 //               item boundaries.  P is read from TMEM (written there by the
 //               softmax warps over their S buffer).
-//   warp 3      idle
 //   warps 4..   NH softmax warpgroups; thread t of group h owns query row t of
 //               tile h (TMEM lane t): masked running max in base-2 units,
 //               lazy rescaling of O (only when the max grows by > 2^8),
@@ -274,16 +274,16 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
     if (threadIdx.x == 0) {
         for (int b = 0; b < 2; ++b) {
             mbar_init(&q_full[b], 1);
-            mbar_init(&q_empty[b], 1);
+            mbar_init(&q_empty[b], NH);   // one commit per MMA warp
         }
-        mbar_init(mma_final, 1);
+        mbar_init(mma_final, NH);
         for (int s = 0; s < NK; ++s) {
             mbar_init(&k_full[s], 1);
-            mbar_init(&k_empty[s], 1);
+            mbar_init(&k_empty[s], NH);   // one commit per MMA warp
         }
         for (int s = 0; s < NV; ++s) {
             mbar_init(&v_full[s], 1);
-            mbar_init(&v_empty[s], 1);
+            mbar_init(&v_empty[s], NH);
         }
         for (int i = 0; i < 2 * NH; ++i) {
             mbar_init(&s_full[i], 1);
@@ -398,9 +398,12 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
             }
         }
         __syncwarp();
-    } else if (warp == 1) {
-        // =============================================================== MMA issuer
-        // Warp-converged like the producer; lane 0 issues every tcgen05.mma and commit.
+    } else if (warp == 1 || (NH == 2 && warp == 3)) {
+        // =============================================================== MMA issuers
+        // One warp per query tile (warp 1: tile 0, warp 3: tile 1), so the two tiles'
+        // QK -> softmax -> P.V chains do not wait for each other.  Warp-converged like the
+        // producer; lane 0 issues every tcgen05.mma and commit.
+        const int h = (warp == 1) ? 0 : 1;
         constexpr uint32_t kIdescQK = idesc_bf16_f32(128, kKeys, 0);
         constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, 1);
         // Base descriptors, built once; an operand at byte offset `off` from a base is the
@@ -422,22 +425,19 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
             if (!warp_wait(&k_full[st], (g / NK) & 1, abort_flag)) return false;
             const uint64_t dqb = dq0 + static_cast<uint64_t>((t.qbuf() * C::kQBytes) >> 4);
             const uint64_t dks = dk0 + static_cast<uint64_t>((st * C::kTileBytes) >> 4);
+            // S(h, g%2) holds P of tile g-2, read by the P.V this warp issued just before this
+            // QK.  tcgen05.mma operations issued by one thread execute in issue order, so this
+            // QK cannot overwrite P before that P.V has read it: no wait for its completion.
+            tc_fence_after();
+            const uint32_t d_s = tmem + col_s(h, g & 1);
+            const uint64_t dqh = dqb + static_cast<uint64_t>((h * C::NB * kQBox) >> 4);
 #pragma unroll
-            for (int h = 0; h < NH; ++h) {
-                // S(h, g%2) holds P of tile g-2, read by the P.V issued just before this QK.
-                // tcgen05.mma operations issued by one thread execute in issue order, so this
-                // QK cannot overwrite P before that P.V has read it: no wait for its completion.
-                tc_fence_after();
-                const uint32_t d_s = tmem + col_s(h, g & 1);
-                const uint64_t dqh = dqb + static_cast<uint64_t>((h * C::NB * kQBox) >> 4);
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    mma_ss_w(d_s, dqh + (((kk >> 2) * kQBox + (kk & 3) * 32) >> 4),
-                             dks + (((kk >> 2) * kKVBox + (kk & 3) * 32) >> 4), kIdescQK, kk > 0 ? 1u : 0u);
-                }
-                mma_commit_w(&s_full[2 * h + (g & 1)]);
+            for (int kk = 0; kk < D / 16; ++kk) {
+                mma_ss_w(d_s, dqh + (((kk >> 2) * kQBox + (kk & 3) * 32) >> 4),
+                         dks + (((kk >> 2) * kKVBox + (kk & 3) * 32) >> 4), kIdescQK, kk > 0 ? 1u : 0u);
             }
-            mma_commit_w(&k_empty[st]);   // K(g) is free once both QKs completed
+            mma_commit_w(&s_full[2 * h + (g & 1)]);
+            mma_commit_w(&k_empty[st]);   // K(g) is free once every tile's QK completed (count NH)
             if (t.j == t.I.n_tiles - 1) mma_commit_w(&q_empty[t.qbuf()]);   // and so is Q after the item's last
             return true;
         };
@@ -456,24 +456,17 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
             const int st = ga % NV;
             if (!warp_wait(&v_full[st], (ga / NV) & 1, abort_flag)) break;
             const uint64_t dvs = dv0 + static_cast<uint64_t>((st * C::kTileBytes) >> 4);
+            if (!warp_wait(&p_full[2 * h + (ga & 1)], (ga >> 1) & 1, abort_flag)) break;
+            tc_fence_after();
+            const uint32_t d_o = tmem + C::kColO + D * h;
+            const uint32_t a_p = tmem + col_s(h, ga & 1);
 #pragma unroll
-            for (int h = 0; h < NH; ++h) {
-                if (!warp_wait(&p_full[2 * h + (ga & 1)], (ga >> 1) & 1, abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t d_o = tmem + C::kColO + D * h;
-                const uint32_t a_p = tmem + col_s(h, ga & 1);
-#pragma unroll
-                for (int kk = 0; kk < kKeys / 16; ++kk) {
-                    // V tile: 64 key rows of 128 bytes per column block; K = 16 rows per step.
-                    mma_ts_w(d_o, a_p + kk * 8, dvs + ((kk * 16 * 128) >> 4), kIdescPV, (a.j > 0 || kk > 0) ? 1u : 0u);
-                }
-                mma_commit_w(&pv_done[2 * h + (ga & 1)]);
+            for (int kk = 0; kk < kKeys / 16; ++kk) {
+                // V tile: 64 key rows of 128 bytes per column block; K = 16 rows per step.
+                mma_ts_w(d_o, a_p + kk * 8, dvs + ((kk * 16 * 128) >> 4), kIdescPV, (a.j > 0 || kk > 0) ? 1u : 0u);
             }
-            if (!ok) break;
-            mma_commit_w(&v_empty[st]);
+            mma_commit_w(&pv_done[2 * h + (ga & 1)]);
+            mma_commit_w(&v_empty[st]);   // count NH
             a.advance(p);
             ++ga;
         }
@@ -493,6 +486,162 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
         bool ok = true;
         int4 nxt_raw = make_int4(0, 0, 0, 0);
         if (static_cast<int>(blockIdx.x) < n_items) nxt_raw = fetch_raw<MODE>(p, blockIdx.x);
+        // Epilogue of one finished item: wait for its last P.V (the commit covers all earlier
+        // MMAs too), normalise O and store it.  It runs after the NEXT item's first tile has
+        // been turned into P (which reads no O), so the wait for the last P.V overlaps that
+        // work; the next item's first P.V, which overwrites O, is released only after this.
+        auto epilogue = [&](const Item &I, float m, float l, uint32_t g_last) -> bool {
+                if (I.n_tiles > 0) {
+                    // the commit after the item's last P.V covers every earlier MMA too
+                    if (!warp_wait(&pv_done[2 * h + (g_last & 1)], (g_last >> 1) & 1, abort_flag)) return false;
+                    tc_fence_after();
+                }
+                // destination of tile row r, or nullptr when the row is not a valid output row
+                auto row_dst = [&](int r) -> __nv_bfloat16 * {
+                    if constexpr (MODE == Mode::Prefill) {
+                        const int qrow = I.qt * kRows + r;
+                        const int head = I.head0 + h;
+                        if (qrow >= I.kv_len || head - I.kh * p.g >= p.g) return nullptr;
+                        return p.out + (static_cast<int64_t>(I.seq_start + qrow) * p.Hq + head) * D;
+                    } else {
+                        const int lb = r / p.g;
+                        const int hh = r - lb * p.g;
+                        const int beam = (I.bt0 + h) * p.BT + lb;
+                        if (lb >= p.BT || beam >= p.W) return nullptr;
+                        return p.out + ((static_cast<int64_t>(I.r) * p.W + beam) * p.Hq + I.kh * p.g + hh) * D;
+                    }
+                };
+                // Each warp stores its 32 rows chunk by chunk: a row's 64-byte chunk goes to the warp's
+                // staging area (slot c ^ ((r >> 1) & 3): conflict-free both ways), then every lane
+                // stores 16 bytes of rows lane/4 + 8i, so a store instruction covers 8 whole 64-byte
+                // segments.  dst[i] is this lane's destination row for pass i.
+                uint8_t *stage = smem + C::kOffStage + (warp - 4) * C::kStageBytes;
+                __nv_bfloat16 *dst[4];
+    #pragma unroll
+                for (int i = 0; i < 4; ++i) dst[i] = row_dst(quad * 32 + i * 8 + (lane >> 2));
+                auto put_chunk = [&](int c, const float *o, float inv_l) {
+                    uint4 wv[4];
+                    uint32_t *wp = reinterpret_cast<uint32_t *>(wv);
+    #pragma unroll
+                    for (int i = 0; i < 16; ++i) wp[i] = pack_bf16x2(o[2 * i] * inv_l, o[2 * i + 1] * inv_l);
+                    __syncwarp();                       // the previous chunk's reads are done
+    #pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        *reinterpret_cast<uint4 *>(stage + lane * 64 + ((u ^ ((lane >> 1) & 3)) * 16)) = wv[u];
+                    __syncwarp();
+                    const int cc = lane & 3;
+    #pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int rr = i * 8 + (lane >> 2);
+                        const uint4 val = *reinterpret_cast<const uint4 *>(stage + rr * 64 + ((cc ^ ((rr >> 1) & 3)) * 16));
+                        if (dst[i]) reinterpret_cast<uint4 *>(dst[i] + 32 * c)[cc] = val;
+                    }
+                };
+                if constexpr (MODE == Mode::Prefill) {
+                    const float inv_l = 1.f / l;
+    #pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        float o[32];
+                        tmem_ld32(tO + 32 * c, o);
+                        put_chunk(c, o, inv_l);
+                    }
+                    if (p.lse) {
+                        if (row_dst(row)) {
+                            // natural-log sum-exp: (m + log2 l) * ln 2
+                            p.lse[static_cast<int64_t>(I.seq_start + I.qt * kRows + row) * p.Hq + I.head0 + h] =
+                                (m + __log2f(l)) * 0.69314718055994530942f;
+                        }
+                    }
+                } else {
+                    const int local_beam = row / p.g;
+                    const int hh = row - local_beam * p.g;
+                    const int beam = (I.bt0 + h) * p.BT + local_beam;
+                    const bool valid = local_beam < p.BT && beam < p.W;
+                    const int head = I.kh * p.g + hh;
+                    const int64_t rb = static_cast<int64_t>(I.r) * p.W + beam;
+                    const int ns = valid ? p.suffix_len : 0;
+                    // this row's query, kept in registers for the suffix dot products
+                    uint4 qv[D / 8];
+    #pragma unroll
+                    for (int c = 0; c < D / 8; ++c) qv[c] = make_uint4(0, 0, 0, 0);
+                    if (ns > 0) {
+                        const uint4 *qp = reinterpret_cast<const uint4 *>(p.q + (rb * p.Hq + head) * D);
+    #pragma unroll
+                        for (int c = 0; c < D / 8; ++c) qv[c] = qp[c];
+                    }
+                    const __nv_bfloat16 *kbase = p.suffix_k + (rb * p.suffix_max * p.Hkv + I.kh) * D;
+                    const __nv_bfloat16 *vbase = p.suffix_v + (rb * p.suffix_max * p.Hkv + I.kh) * D;
+                    const int64_t sstride = static_cast<int64_t>(p.Hkv) * D;   // between suffix slots
+                    float z[kMaxSuffix];
+                    float m2 = m;
+    #pragma unroll
+                    for (int s = 0; s < kMaxSuffix; ++s) {
+                        z[s] = -INFINITY;
+                        if (s < ns) {
+                            const uint4 *kp = reinterpret_cast<const uint4 *>(kbase + s * sstride);
+                            float acc = 0.f;
+    #pragma unroll
+                            for (int c = 0; c < D / 8; ++c) {
+                                const uint4 ka = kp[c];
+                                const __nv_bfloat162 *q2 = reinterpret_cast<const __nv_bfloat162 *>(&qv[c]);
+                                const __nv_bfloat162 *k2 = reinterpret_cast<const __nv_bfloat162 *>(&ka);
+    #pragma unroll
+                                for (int e = 0; e < 4; ++e) {
+                                    const float2 qf = __bfloat1622float2(q2[e]);
+                                    const float2 kf = __bfloat1622float2(k2[e]);
+                                    acc = fmaf(qf.x, kf.x, acc);
+                                    acc = fmaf(qf.y, kf.y, acc);
+                                }
+                            }
+                            z[s] = acc * sl2;
+                            m2 = fmaxf(m2, z[s]);
+                        }
+                    }
+                    const float alpha = (I.n_tiles > 0) ? ex2(m - m2) : 0.f;
+                    float l2 = l * alpha;
+    #pragma unroll
+                    for (int s = 0; s < kMaxSuffix; ++s) {
+                        z[s] = (s < ns) ? ex2(z[s] - m2) : 0.f;   // z now holds the suffix weights
+                        l2 += z[s];
+                    }
+                    const float inv_l = valid ? 1.f / l2 : 0.f;
+    #pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        float o[32];
+                        if (I.n_tiles > 0) {
+                            tmem_ld32(tO + 32 * c, o);
+                        } else {
+    #pragma unroll
+                            for (int i = 0; i < 32; ++i) o[i] = 0.f;
+                        }
+    #pragma unroll
+                        for (int i = 0; i < 32; ++i) o[i] *= alpha;
+    #pragma unroll
+                        for (int s = 0; s < kMaxSuffix; ++s) {
+                            if (s < ns) {
+                                const uint4 *vp = reinterpret_cast<const uint4 *>(vbase + s * sstride + 32 * c);
+    #pragma unroll
+                                for (int u = 0; u < 4; ++u) {
+                                    const uint4 va = vp[u];
+                                    const __nv_bfloat162 *v2 = reinterpret_cast<const __nv_bfloat162 *>(&va);
+    #pragma unroll
+                                    for (int e = 0; e < 4; ++e) {
+                                        const float2 vf = __bfloat1622float2(v2[e]);
+                                        o[8 * u + 2 * e] = fmaf(z[s], vf.x, o[8 * u + 2 * e]);
+                                        o[8 * u + 2 * e + 1] = fmaf(z[s], vf.y, o[8 * u + 2 * e + 1]);
+                                    }
+                                }
+                            }
+                        }
+                        put_chunk(c, o, inv_l);
+                    }
+                }
+            return true;
+        };
+        bool pend = false;    // an item whose epilogue still has to run
+        Item Ip;
+        float mp = 0.f, lp = 0.f;
+        uint32_t gp = 0;
         for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
             const int4 raw = nxt_raw;
             if (it + static_cast<int>(gridDim.x) < n_items) nxt_raw = fetch_raw<MODE>(p, it + gridDim.x);
@@ -583,160 +732,31 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
                 }
                 tmem_st_wait();
                 tc_fence_before();
+                if (j == 0 && pend) {
+                    if (!epilogue(Ip, mp, lp, gp)) { ok = false; break; }
+                    pend = false;
+                    tc_fence_before();
+                }
                 mbar_arrive(&p_full[2 * h + (g & 1)]);
             }
             if (!ok) break;
-
-            // ------------------------------------------------------- epilogue
-            if (I.n_tiles > 0) {
-                // the commit after the item's last P.V covers every earlier MMA too
-                if (!warp_wait(&pv_done[2 * h + ((g - 1) & 1)], ((g - 1) >> 1) & 1, abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
+            if (pend) {                          // an item without tiles followed
+                if (!epilogue(Ip, mp, lp, gp)) { ok = false; break; }
+                pend = false;
             }
-            // destination of tile row r, or nullptr when the row is not a valid output row
-            auto row_dst = [&](int r) -> __nv_bfloat16 * {
-                if constexpr (MODE == Mode::Prefill) {
-                    const int qrow = I.qt * kRows + r;
-                    const int head = I.head0 + h;
-                    if (qrow >= I.kv_len || head - I.kh * p.g >= p.g) return nullptr;
-                    return p.out + (static_cast<int64_t>(I.seq_start + qrow) * p.Hq + head) * D;
-                } else {
-                    const int lb = r / p.g;
-                    const int hh = r - lb * p.g;
-                    const int beam = (I.bt0 + h) * p.BT + lb;
-                    if (lb >= p.BT || beam >= p.W) return nullptr;
-                    return p.out + ((static_cast<int64_t>(I.r) * p.W + beam) * p.Hq + I.kh * p.g + hh) * D;
-                }
-            };
-            // Each warp stores its 32 rows chunk by chunk: a row's 64-byte chunk goes to the warp's
-            // staging area (slot c ^ ((r >> 1) & 3): conflict-free both ways), then every lane
-            // stores 16 bytes of rows lane/4 + 8i, so a store instruction covers 8 whole 64-byte
-            // segments.  dst[i] is this lane's destination row for pass i.
-            uint8_t *stage = smem + C::kOffStage + (warp - 4) * C::kStageBytes;
-            __nv_bfloat16 *dst[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) dst[i] = row_dst(quad * 32 + i * 8 + (lane >> 2));
-            auto put_chunk = [&](int c, const float *o, float inv_l) {
-                uint4 wv[4];
-                uint32_t *wp = reinterpret_cast<uint32_t *>(wv);
-#pragma unroll
-                for (int i = 0; i < 16; ++i) wp[i] = pack_bf16x2(o[2 * i] * inv_l, o[2 * i + 1] * inv_l);
-                __syncwarp();                       // the previous chunk's reads are done
-#pragma unroll
-                for (int u = 0; u < 4; ++u)
-                    *reinterpret_cast<uint4 *>(stage + lane * 64 + ((u ^ ((lane >> 1) & 3)) * 16)) = wv[u];
-                __syncwarp();
-                const int cc = lane & 3;
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int rr = i * 8 + (lane >> 2);
-                    const uint4 val = *reinterpret_cast<const uint4 *>(stage + rr * 64 + ((cc ^ ((rr >> 1) & 3)) * 16));
-                    if (dst[i]) reinterpret_cast<uint4 *>(dst[i] + 32 * c)[cc] = val;
-                }
-            };
-            if constexpr (MODE == Mode::Prefill) {
-                const float inv_l = 1.f / l;
-#pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    float o[32];
-                    tmem_ld32(tO + 32 * c, o);
-                    put_chunk(c, o, inv_l);
-                }
-                if (p.lse) {
-                    if (row_dst(row)) {
-                        // natural-log sum-exp: (m + log2 l) * ln 2
-                        p.lse[static_cast<int64_t>(I.seq_start + I.qt * kRows + row) * p.Hq + I.head0 + h] =
-                            (m + __log2f(l)) * 0.69314718055994530942f;
-                    }
-                }
-            } else {
-                const int local_beam = row / p.g;
-                const int hh = row - local_beam * p.g;
-                const int beam = (I.bt0 + h) * p.BT + local_beam;
-                const bool valid = local_beam < p.BT && beam < p.W;
-                const int head = I.kh * p.g + hh;
-                const int64_t rb = static_cast<int64_t>(I.r) * p.W + beam;
-                const int ns = valid ? p.suffix_len : 0;
-                // this row's query, kept in registers for the suffix dot products
-                uint4 qv[D / 8];
-#pragma unroll
-                for (int c = 0; c < D / 8; ++c) qv[c] = make_uint4(0, 0, 0, 0);
-                if (ns > 0) {
-                    const uint4 *qp = reinterpret_cast<const uint4 *>(p.q + (rb * p.Hq + head) * D);
-#pragma unroll
-                    for (int c = 0; c < D / 8; ++c) qv[c] = qp[c];
-                }
-                const __nv_bfloat16 *kbase = p.suffix_k + (rb * p.suffix_max * p.Hkv + I.kh) * D;
-                const __nv_bfloat16 *vbase = p.suffix_v + (rb * p.suffix_max * p.Hkv + I.kh) * D;
-                const int64_t sstride = static_cast<int64_t>(p.Hkv) * D;   // between suffix slots
-                float z[kMaxSuffix];
-                float m2 = m;
-#pragma unroll
-                for (int s = 0; s < kMaxSuffix; ++s) {
-                    z[s] = -INFINITY;
-                    if (s < ns) {
-                        const uint4 *kp = reinterpret_cast<const uint4 *>(kbase + s * sstride);
-                        float acc = 0.f;
-#pragma unroll
-                        for (int c = 0; c < D / 8; ++c) {
-                            const uint4 ka = kp[c];
-                            const __nv_bfloat162 *q2 = reinterpret_cast<const __nv_bfloat162 *>(&qv[c]);
-                            const __nv_bfloat162 *k2 = reinterpret_cast<const __nv_bfloat162 *>(&ka);
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const float2 qf = __bfloat1622float2(q2[e]);
-                                const float2 kf = __bfloat1622float2(k2[e]);
-                                acc = fmaf(qf.x, kf.x, acc);
-                                acc = fmaf(qf.y, kf.y, acc);
-                            }
-                        }
-                        z[s] = acc * sl2;
-                        m2 = fmaxf(m2, z[s]);
-                    }
-                }
-                const float alpha = (I.n_tiles > 0) ? ex2(m - m2) : 0.f;
-                float l2 = l * alpha;
-#pragma unroll
-                for (int s = 0; s < kMaxSuffix; ++s) {
-                    z[s] = (s < ns) ? ex2(z[s] - m2) : 0.f;   // z now holds the suffix weights
-                    l2 += z[s];
-                }
-                const float inv_l = valid ? 1.f / l2 : 0.f;
-#pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    float o[32];
-                    if (I.n_tiles > 0) {
-                        tmem_ld32(tO + 32 * c, o);
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) o[i] = 0.f;
-                    }
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) o[i] *= alpha;
-#pragma unroll
-                    for (int s = 0; s < kMaxSuffix; ++s) {
-                        if (s < ns) {
-                            const uint4 *vp = reinterpret_cast<const uint4 *>(vbase + s * sstride + 32 * c);
-#pragma unroll
-                            for (int u = 0; u < 4; ++u) {
-                                const uint4 va = vp[u];
-                                const __nv_bfloat162 *v2 = reinterpret_cast<const __nv_bfloat162 *>(&va);
-#pragma unroll
-                                for (int e = 0; e < 4; ++e) {
-                                    const float2 vf = __bfloat1622float2(v2[e]);
-                                    o[8 * u + 2 * e] = fmaf(z[s], vf.x, o[8 * u + 2 * e]);
-                                    o[8 * u + 2 * e + 1] = fmaf(z[s], vf.y, o[8 * u + 2 * e + 1]);
-                                }
-                            }
-                        }
-                    }
-                    put_chunk(c, o, inv_l);
-                }
+            if (I.n_tiles > 0) {
+                pend = true;
+                Ip = I;
+                mp = m;
+                lp = l;
+                gp = g - 1;
+            } else if (!epilogue(I, m, l, 0)) {
+                ok = false;
+                break;
             }
         }
+        if (ok && pend) ok = epilogue(Ip, mp, lp, gp);
+
         (void)ok;
     }
 
