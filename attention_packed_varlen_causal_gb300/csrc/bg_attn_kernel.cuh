@@ -317,6 +317,7 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
         // =============================================================== producer
         // The whole warp runs the loop (warp-uniform control flow and operands); lane 0
         // issues each copy.
+        const uint32_t leader = (lane == 0) ? 1u : 0u;
         const uint64_t pol_q = l2_policy_evict_first();
         const uint64_t pol_kv = l2_policy_evict_last();
         TileWalker<MODE, NH> w;
@@ -329,22 +330,22 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
                 if (use > 0 && !warp_wait(&q_empty[qb], (use - 1) & 1, abort_flag)) break;
                 uint8_t *qdst = smem + C::kOffQ + qb * C::kQBytes;
                 if constexpr (MODE == Mode::Prefill) {
-                    mbar_arrive_expect_tx_w(&q_full[qb], NH * C::NB * kQBox);
+                    mbar_arrive_expect_tx_w(leader, &q_full[qb], NH * C::NB * kQBox);
                     const int row = w.I.seq_start + w.I.qt * kRows;
 #pragma unroll
                     for (int h = 0; h < NH; ++h)
 #pragma unroll
                         for (int b = 0; b < C::NB; ++b)
-                            tma_load_3d_w(qdst + (h * C::NB + b) * kQBox, &tm_q, &q_full[qb], b * 64, w.I.head0 + h,
+                            tma_load_3d_w(leader, qdst + (h * C::NB + b) * kQBox, &tm_q, &q_full[qb], b * 64, w.I.head0 + h,
                                           row, pol_q);
                 } else {
                     const uint32_t box = static_cast<uint32_t>(p.BT * p.g * 128);
-                    mbar_arrive_expect_tx_w(&q_full[qb], NH * C::NB * box);
+                    mbar_arrive_expect_tx_w(leader, &q_full[qb], NH * C::NB * box);
 #pragma unroll
                     for (int h = 0; h < NH; ++h)
 #pragma unroll
                         for (int b = 0; b < C::NB; ++b)
-                            tma_load_4d_w(qdst + (h * C::NB + b) * kQBox, &tm_q, &q_full[qb], b * 64, 0, w.I.kh,
+                            tma_load_4d_w(leader, qdst + (h * C::NB + b) * kQBox, &tm_q, &q_full[qb], b * 64, 0, w.I.kh,
                                           w.I.r * p.W + (w.I.bt0 + h) * p.BT, pol_q);
                 }
             }
@@ -352,10 +353,10 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
             const uint32_t use = n_kv / NK;
             if (use > 0 && !warp_wait(&k_empty[st], (use - 1) & 1, abort_flag)) break;
             const int row = w.I.kv_row0 + w.j * kKeys;
-            mbar_arrive_expect_tx_w(&k_full[st], C::kTileBytes);
+            mbar_arrive_expect_tx_w(leader, &k_full[st], C::kTileBytes);
 #pragma unroll
             for (int b = 0; b < C::NB; ++b)
-                tma_load_3d_w(smem + C::kOffK + st * C::kTileBytes + b * kKVBox, &tm_k, &k_full[st], b * 64, w.I.kh,
+                tma_load_3d_w(leader, smem + C::kOffK + st * C::kTileBytes + b * kKVBox, &tm_k, &k_full[st], b * 64, w.I.kh,
                               row, pol_kv);
             ++n_kv;
             w.advance(p);
@@ -374,6 +375,7 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
         __syncwarp();
     } else if (warp == 2) {
         // =============================================================== V producer
+        const uint32_t leader = (lane == 0) ? 1u : 0u;
         const uint64_t pol_kv = l2_policy_evict_last();
         TileWalker<MODE, NH> w;
         w.first(p, n_items);
@@ -383,10 +385,10 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
             const uint32_t use = n_v / NV;
             if (use > 0 && !warp_wait(&v_empty[st], (use - 1) & 1, abort_flag)) break;
             const int row = w.I.kv_row0 + w.j * kKeys;
-            mbar_arrive_expect_tx_w(&v_full[st], C::kTileBytes);
+            mbar_arrive_expect_tx_w(leader, &v_full[st], C::kTileBytes);
 #pragma unroll
             for (int b = 0; b < C::NB; ++b)
-                tma_load_3d_w(smem + C::kOffV + st * C::kTileBytes + b * kKVBox, &tm_v, &v_full[st], b * 64, w.I.kh,
+                tma_load_3d_w(leader, smem + C::kOffV + st * C::kTileBytes + b * kKVBox, &tm_v, &v_full[st], b * 64, w.I.kh,
                               row, pol_kv);
             ++n_v;
             w.advance(p);
@@ -404,6 +406,7 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
         // QK -> softmax -> P.V chains do not wait for each other.  Warp-converged like the
         // producer; lane 0 issues every tcgen05.mma and commit.
         const int h = (warp == 1) ? 0 : 1;
+        const uint32_t leader = (lane == 0) ? 1u : 0u;
         constexpr uint32_t kIdescQK = idesc_bf16_f32(128, kKeys, 0);
         constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, 1);
         // Base descriptors, built once; an operand at byte offset `off` from a base is the
@@ -429,16 +432,11 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
             // QK.  tcgen05.mma operations issued by one thread execute in issue order, so this
             // QK cannot overwrite P before that P.V has read it: no wait for its completion.
             tc_fence_after();
-            const uint32_t d_s = tmem + col_s(h, g & 1);
             const uint64_t dqh = dqb + static_cast<uint64_t>((h * C::NB * kQBox) >> 4);
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-                mma_ss_w(d_s, dqh + (((kk >> 2) * kQBox + (kk & 3) * 32) >> 4),
-                         dks + (((kk >> 2) * kKVBox + (kk & 3) * 32) >> 4), kIdescQK, kk > 0 ? 1u : 0u);
-            }
-            mma_commit_w(&s_full[2 * h + (g & 1)]);
-            mma_commit_w(&k_empty[st]);   // K(g) is free once every tile's QK completed (count NH)
-            if (t.j == t.I.n_tiles - 1) mma_commit_w(&q_empty[t.qbuf()]);   // and so is Q after the item's last
+            static_assert(kQBox == 16384 && kKVBox == 8192, "mma_qk_tile hard-codes the column-block strides");
+            mma_qk_tile<C::NB>(leader, tmem + col_s(h, g & 1), dqh, dks, kIdescQK, &s_full[2 * h + (g & 1)]);
+            mma_commit_l(leader, &k_empty[st]);   // K(g) is free once every tile's QK completed (count NH)
+            if (t.j == t.I.n_tiles - 1) mma_commit_l(leader, &q_empty[t.qbuf()]);   // Q after the item's last
             return true;
         };
 
@@ -458,20 +456,16 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
             const uint64_t dvs = dv0 + static_cast<uint64_t>((st * C::kTileBytes) >> 4);
             if (!warp_wait(&p_full[2 * h + (ga & 1)], (ga >> 1) & 1, abort_flag)) break;
             tc_fence_after();
-            const uint32_t d_o = tmem + C::kColO + D * h;
-            const uint32_t a_p = tmem + col_s(h, ga & 1);
-#pragma unroll
-            for (int kk = 0; kk < kKeys / 16; ++kk) {
-                // V tile: 64 key rows of 128 bytes per column block; K = 16 rows per step.
-                mma_ts_w(d_o, a_p + kk * 8, dvs + ((kk * 16 * 128) >> 4), kIdescPV, (a.j > 0 || kk > 0) ? 1u : 0u);
-            }
-            mma_commit_w(&pv_done[2 * h + (ga & 1)]);
-            mma_commit_w(&v_empty[st]);   // count NH
+            // V tile: 64 key rows of 128 bytes per column block; K = 16 rows per step.
+            static_assert(kKeys == 64, "mma_pv_tile issues four 16-key steps");
+            mma_pv_tile(leader, tmem + C::kColO + D * h, tmem + col_s(h, ga & 1), dvs, kIdescPV, a.j > 0 ? 1u : 0u,
+                        &pv_done[2 * h + (ga & 1)]);
+            mma_commit_l(leader, &v_empty[st]);   // count NH
             a.advance(p);
             ++ga;
         }
         // Drain: every MMA issued above completes before TMEM is released.
-        mma_commit_w(mma_final);
+        mma_commit_l(leader, mma_final);
         if (lane == 0) mbar_wait_drain(mma_final, 0);
         __syncwarp();
     } else if (warp >= 4) {
@@ -517,20 +511,24 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
                 // segments.  dst[i] is this lane's destination row for pass i.
                 uint8_t *stage = smem + C::kOffStage + (warp - 4) * C::kStageBytes;
                 __nv_bfloat16 *dst[4];
-    #pragma unroll
+#pragma unroll
                 for (int i = 0; i < 4; ++i) dst[i] = row_dst(quad * 32 + i * 8 + (lane >> 2));
                 auto put_chunk = [&](int c, const float *o, float inv_l) {
                     uint4 wv[4];
                     uint32_t *wp = reinterpret_cast<uint32_t *>(wv);
-    #pragma unroll
-                    for (int i = 0; i < 16; ++i) wp[i] = pack_bf16x2(o[2 * i] * inv_l, o[2 * i + 1] * inv_l);
+                    const float2 il = make_float2(inv_l, inv_l);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const float2 x = fmul2(make_float2(o[2 * i], o[2 * i + 1]), il);
+                        wp[i] = pack_bf16x2(x.x, x.y);
+                    }
                     __syncwarp();                       // the previous chunk's reads are done
-    #pragma unroll
+#pragma unroll
                     for (int u = 0; u < 4; ++u)
                         *reinterpret_cast<uint4 *>(stage + lane * 64 + ((u ^ ((lane >> 1) & 3)) * 16)) = wv[u];
                     __syncwarp();
                     const int cc = lane & 3;
-    #pragma unroll
+#pragma unroll
                     for (int i = 0; i < 4; ++i) {
                         const int rr = i * 8 + (lane >> 2);
                         const uint4 val = *reinterpret_cast<const uint4 *>(stage + rr * 64 + ((cc ^ ((rr >> 1) & 3)) * 16));
@@ -539,7 +537,7 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
                 };
                 if constexpr (MODE == Mode::Prefill) {
                     const float inv_l = 1.f / l;
-    #pragma unroll
+#pragma unroll
                     for (int c = 0; c < D / 32; ++c) {
                         float o[32];
                         tmem_ld32(tO + 32 * c, o);
@@ -562,11 +560,11 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
                     const int ns = valid ? p.suffix_len : 0;
                     // this row's query, kept in registers for the suffix dot products
                     uint4 qv[D / 8];
-    #pragma unroll
+#pragma unroll
                     for (int c = 0; c < D / 8; ++c) qv[c] = make_uint4(0, 0, 0, 0);
                     if (ns > 0) {
                         const uint4 *qp = reinterpret_cast<const uint4 *>(p.q + (rb * p.Hq + head) * D);
-    #pragma unroll
+#pragma unroll
                         for (int c = 0; c < D / 8; ++c) qv[c] = qp[c];
                     }
                     const __nv_bfloat16 *kbase = p.suffix_k + (rb * p.suffix_max * p.Hkv + I.kh) * D;
@@ -574,18 +572,18 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
                     const int64_t sstride = static_cast<int64_t>(p.Hkv) * D;   // between suffix slots
                     float z[kMaxSuffix];
                     float m2 = m;
-    #pragma unroll
+#pragma unroll
                     for (int s = 0; s < kMaxSuffix; ++s) {
                         z[s] = -INFINITY;
                         if (s < ns) {
                             const uint4 *kp = reinterpret_cast<const uint4 *>(kbase + s * sstride);
                             float acc = 0.f;
-    #pragma unroll
+#pragma unroll
                             for (int c = 0; c < D / 8; ++c) {
                                 const uint4 ka = kp[c];
                                 const __nv_bfloat162 *q2 = reinterpret_cast<const __nv_bfloat162 *>(&qv[c]);
                                 const __nv_bfloat162 *k2 = reinterpret_cast<const __nv_bfloat162 *>(&ka);
-    #pragma unroll
+#pragma unroll
                                 for (int e = 0; e < 4; ++e) {
                                     const float2 qf = __bfloat1622float2(q2[e]);
                                     const float2 kf = __bfloat1622float2(k2[e]);
@@ -599,32 +597,32 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
                     }
                     const float alpha = (I.n_tiles > 0) ? ex2(m - m2) : 0.f;
                     float l2 = l * alpha;
-    #pragma unroll
+#pragma unroll
                     for (int s = 0; s < kMaxSuffix; ++s) {
                         z[s] = (s < ns) ? ex2(z[s] - m2) : 0.f;   // z now holds the suffix weights
                         l2 += z[s];
                     }
                     const float inv_l = valid ? 1.f / l2 : 0.f;
-    #pragma unroll
+#pragma unroll
                     for (int c = 0; c < D / 32; ++c) {
                         float o[32];
                         if (I.n_tiles > 0) {
                             tmem_ld32(tO + 32 * c, o);
                         } else {
-    #pragma unroll
+#pragma unroll
                             for (int i = 0; i < 32; ++i) o[i] = 0.f;
                         }
-    #pragma unroll
+#pragma unroll
                         for (int i = 0; i < 32; ++i) o[i] *= alpha;
-    #pragma unroll
+#pragma unroll
                         for (int s = 0; s < kMaxSuffix; ++s) {
                             if (s < ns) {
                                 const uint4 *vp = reinterpret_cast<const uint4 *>(vbase + s * sstride + 32 * c);
-    #pragma unroll
+#pragma unroll
                                 for (int u = 0; u < 4; ++u) {
                                     const uint4 va = vp[u];
                                     const __nv_bfloat162 *v2 = reinterpret_cast<const __nv_bfloat162 *>(&va);
-    #pragma unroll
+#pragma unroll
                                     for (int e = 0; e < 4; ++e) {
                                         const float2 vf = __bfloat1622float2(v2[e]);
                                         o[8 * u + 2 * e] = fmaf(z[s], vf.x, o[8 * u + 2 * e]);
@@ -690,9 +688,9 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
                         for (int c = 0; c < kKeys; ++c)
                             if (c >= lim) s[c] = -INFINITY;
                     }
-                    float mx = s[0];
+                    float mx = fmaxf(s[0], s[1]);
 #pragma unroll
-                    for (int c = 1; c < kKeys; ++c) mx = fmaxf(mx, s[c]);
+                    for (int c = 2; c < kKeys; c += 2) mx = fmax3f(mx, s[c], s[c + 1]);
                     const float m_new = fmaxf(m, mx * sl2);
                     const bool grow = (j > 0) && (m_new > m + kRescaleLog2);
                     if (j == 0) m = m_new;
@@ -715,20 +713,23 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
                             tmem_st32f(tO + 32 * c, o);
                         }
                     }
-                    float rs = 0.f;
+                    // p = 2^(s * scale * log2e - m), two columns per packed FMA; row sum in pairs
+                    float2 rs = make_float2(0.f, 0.f);
+                    const float2 sl2x2 = make_float2(sl2, sl2);
+                    const float2 negm = make_float2(-m, -m);
 #pragma unroll
                     for (int c = 0; c < kKeys / 32; ++c) {
                         uint32_t pk[16];
 #pragma unroll
                         for (int i = 0; i < 16; ++i) {
-                            const float e0 = ex2(fmaf(s[32 * c + 2 * i], sl2, -m));
-                            const float e1 = ex2(fmaf(s[32 * c + 2 * i + 1], sl2, -m));
-                            rs += e0 + e1;
-                            pk[i] = pack_bf16x2(e0, e1);
+                            const float2 x = ffma2(make_float2(s[32 * c + 2 * i], s[32 * c + 2 * i + 1]), sl2x2, negm);
+                            const float2 e = make_float2(ex2(x.x), ex2(x.y));
+                            rs = fadd2(rs, e);
+                            pk[i] = pack_bf16x2(e.x, e.y);
                         }
                         tmem_st16(tS + 16 * c, pk);   // P (bf16 pairs) over the first 32 columns of S
                     }
-                    l += rs;
+                    l += rs.x + rs.y;
                 }
                 tmem_st_wait();
                 tc_fence_before();

@@ -207,72 +207,164 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar)
                  : "memory");
 }
 
+// ---- packed fp32 pairs (two lanes of work per instruction on sm_100+)
+// d = a * b + c, element-wise on (x, y)
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c)
+{
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+        "fma.rn.ftz.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b)
+{
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "add.rn.ftz.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b)
+{
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "mul.rn.ftz.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+// max of three (one instruction on sm_100+)
+__device__ __forceinline__ float fmax3f(float a, float b, float c)
+{
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 // ---- warp-converged issue: every lane executes the call with the same
-// (warp-uniform) operands and lane 0 issues it.  Keeping the issuing warp
-// converged lets the operands stay warp-uniform, which is what makes
-// back-to-back tcgen05.mma / TMA issue cheap.  Always lane 0, so the lane that
+// (warp-uniform) operands and the lane whose `leader` flag is set (lane 0,
+// computed once by the caller) issues it.  Keeping the issuing warp converged
+// lets the operands stay warp-uniform, which is what makes back-to-back
+// tcgen05.mma / TMA issue cheap; always the same lane, so the lane that
 // commits is the lane that issued the MMAs the commit tracks.
-__device__ __forceinline__ void mma_ss_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                         uint32_t accumulate)
+__device__ __forceinline__ void mbar_arrive_expect_tx_w(uint32_t leader, uint64_t *bar, uint32_t bytes)
 {
     asm volatile(
-        "{\n\t.reg .pred p, e;\n\t"
-        "{ .reg .b32 l; mov.u32 l, %%laneid; setp.eq.u32 e, l, 0; }\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        "{\n\t.reg .pred e;\n\tsetp.ne.b32 e, %0, 0;\n\t"
+        "@e mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%1], %2;\n\t}" ::"r"(leader),
+        "r"(smem_u32(bar)), "r"(bytes)
         : "memory");
 }
-__device__ __forceinline__ void mma_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                         uint32_t accumulate)
+__device__ __forceinline__ void tma_load_3d_w(uint32_t leader, void *dst, const CUtensorMap *map, uint64_t *bar,
+                                              int32_t c0, int32_t c1, int32_t c2, uint64_t policy)
 {
     asm volatile(
-        "{\n\t.reg .pred p, e;\n\t"
-        "{ .reg .b32 l; mov.u32 l, %%laneid; setp.eq.u32 e, l, 0; }\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-__device__ __forceinline__ void mma_commit_w(uint64_t *bar)
-{
-    asm volatile(
-        "{\n\t.reg .pred e;\n\t"
-        "{ .reg .b32 l; mov.u32 l, %%laneid; setp.eq.u32 e, l, 0; }\n\t"
-        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
-            smem_u32(bar))
-        : "memory");
-}
-__device__ __forceinline__ void mbar_arrive_expect_tx_w(uint64_t *bar, uint32_t bytes)
-{
-    asm volatile(
-        "{\n\t.reg .pred e;\n\t"
-        "{ .reg .b32 l; mov.u32 l, %%laneid; setp.eq.u32 e, l, 0; }\n\t"
-        "@e mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;\n\t}" ::"r"(smem_u32(bar)),
-        "r"(bytes)
-        : "memory");
-}
-__device__ __forceinline__ void tma_load_3d_w(void *dst, const CUtensorMap *map, uint64_t *bar, int32_t c0,
-                                              int32_t c1, int32_t c2, uint64_t policy)
-{
-    asm volatile(
-        "{\n\t.reg .pred e;\n\t"
-        "{ .reg .b32 l; mov.u32 l, %%laneid; setp.eq.u32 e, l, 0; }\n\t"
+        "{\n\t.reg .pred e;\n\tsetp.ne.b32 e, %0, 0;\n\t"
         "@e cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1, {%3, %4, %5}], [%2], %6;\n\t}" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "l"(policy)
+        " [%1], [%2, {%4, %5, %6}], [%3], %7;\n\t}" ::"r"(leader),
+        "r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2),
+        "l"(policy)
         : "memory");
 }
-__device__ __forceinline__ void tma_load_4d_w(void *dst, const CUtensorMap *map, uint64_t *bar, int32_t c0,
-                                              int32_t c1, int32_t c2, int32_t c3, uint64_t policy)
+__device__ __forceinline__ void tma_load_4d_w(uint32_t leader, void *dst, const CUtensorMap *map, uint64_t *bar,
+                                              int32_t c0, int32_t c1, int32_t c2, int32_t c3, uint64_t policy)
 {
     asm volatile(
-        "{\n\t.reg .pred e;\n\t"
-        "{ .reg .b32 l; mov.u32 l, %%laneid; setp.eq.u32 e, l, 0; }\n\t"
+        "{\n\t.reg .pred e;\n\tsetp.ne.b32 e, %0, 0;\n\t"
         "@e cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1, {%3, %4, %5, %6}], [%2], %7;\n\t}" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
-        "l"(policy)
+        " [%1], [%2, {%4, %5, %6, %7}], [%3], %8;\n\t}" ::"r"(leader),
+        "r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2),
+        "r"(c3), "l"(policy)
+        : "memory");
+}
+
+// ---- batched issue for the attention kernel: one asm statement per tile and
+// operand group, `leader` predicates every instruction, descriptor offsets are
+// immediates.
+//
+// S = Q K^T over K = 64 * NB (NB 128-byte column blocks): 4 MMAs per block, A
+// and B advance 32 bytes (2 descriptor units) per 16-element step, Q column
+// blocks are 16 KB (1024 units) and K column blocks 8 KB (512 units) apart;
+// then a commit to `bar`.
+template <int NB>
+__device__ __forceinline__ void mma_qk_tile(uint32_t leader, uint32_t d_tmem, uint64_t dq, uint64_t dk,
+                                            uint32_t idesc, uint64_t *bar);
+
+template <>
+__device__ __forceinline__ void mma_qk_tile<1>(uint32_t leader, uint32_t d_tmem, uint64_t dq, uint64_t dk,
+                                               uint32_t idesc, uint64_t *bar)
+{
+    asm volatile(
+        "{\n\t.reg .pred e, pf, pt;\n\t.reg .b64 a1, a2, a3, b1, b2, b3;\n\t"
+        "setp.ne.b32 e, %0, 0;\n\tsetp.ne.b32 pf, 0, 0;\n\tsetp.eq.b32 pt, 0, 0;\n\t"
+        "add.s64 a1, %2, 2;\n\tadd.s64 a2, %2, 4;\n\tadd.s64 a3, %2, 6;\n\t"
+        "add.s64 b1, %3, 2;\n\tadd.s64 b2, %3, 4;\n\tadd.s64 b3, %3, 6;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%1], %2, %3, %4, pf;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%1], a1, b1, %4, pt;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%1], a2, b2, %4, pt;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%1], a3, b3, %4, pt;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%5];\n\t}" ::"r"(leader),
+        "r"(d_tmem), "l"(dq), "l"(dk), "r"(idesc), "r"(smem_u32(bar))
+        : "memory");
+}
+
+template <>
+__device__ __forceinline__ void mma_qk_tile<2>(uint32_t leader, uint32_t d_tmem, uint64_t dq, uint64_t dk,
+                                               uint32_t idesc, uint64_t *bar)
+{
+    asm volatile(
+        "{\n\t.reg .pred e, pf, pt;\n\t.reg .b64 a1, a2, a3, a4, a5, a6, a7, b1, b2, b3, b4, b5, b6, b7;\n\t"
+        "setp.ne.b32 e, %0, 0;\n\tsetp.ne.b32 pf, 0, 0;\n\tsetp.eq.b32 pt, 0, 0;\n\t"
+        "add.s64 a1, %2, 2;\n\tadd.s64 a2, %2, 4;\n\tadd.s64 a3, %2, 6;\n\t"
+        "add.s64 a4, %2, 1024;\n\tadd.s64 a5, %2, 1026;\n\tadd.s64 a6, %2, 1028;\n\tadd.s64 a7, %2, 1030;\n\t"
+        "add.s64 b1, %3, 2;\n\tadd.s64 b2, %3, 4;\n\tadd.s64 b3, %3, 6;\n\t"
+        "add.s64 b4, %3, 512;\n\tadd.s64 b5, %3, 514;\n\tadd.s64 b6, %3, 516;\n\tadd.s64 b7, %3, 518;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%1], %2, %3, %4, pf;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%1], a1, b1, %4, pt;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%1], a2, b2, %4, pt;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%1], a3, b3, %4, pt;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%1], a4, b4, %4, pt;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%1], a5, b5, %4, pt;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%1], a6, b6, %4, pt;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%1], a7, b7, %4, pt;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%5];\n\t}" ::"r"(leader),
+        "r"(d_tmem), "l"(dq), "l"(dk), "r"(idesc), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// O (+)= P V over 64 keys: A = P in TMEM (8 columns per 16 keys), B = V (MN-major,
+// 16 key rows = 2048 bytes = 128 units per step); the first MMA accumulates only
+// if `acc`; then a commit to `bar`.
+__device__ __forceinline__ void mma_pv_tile(uint32_t leader, uint32_t d_tmem, uint32_t a_tmem, uint64_t dv,
+                                            uint32_t idesc, uint32_t acc, uint64_t *bar)
+{
+    asm volatile(
+        "{\n\t.reg .pred e, p0, pt;\n\t.reg .b64 b1, b2, b3;\n\t.reg .b32 t1, t2, t3;\n\t"
+        "setp.ne.b32 e, %0, 0;\n\tsetp.ne.b32 p0, %5, 0;\n\tsetp.eq.b32 pt, 0, 0;\n\t"
+        "add.s64 b1, %3, 128;\n\tadd.s64 b2, %3, 256;\n\tadd.s64 b3, %3, 384;\n\t"
+        "add.u32 t1, %2, 8;\n\tadd.u32 t2, %2, 16;\n\tadd.u32 t3, %2, 24;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%1], [%2], %3, %4, p0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%1], [t1], b1, %4, pt;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%1], [t2], b2, %4, pt;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%1], [t3], b3, %4, pt;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%6];\n\t}" ::"r"(leader),
+        "r"(d_tmem), "r"(a_tmem), "l"(dv), "r"(idesc), "r"(acc), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// commit predicated by the leader flag
+__device__ __forceinline__ void mma_commit_l(uint32_t leader, uint64_t *bar)
+{
+    asm volatile(
+        "{\n\t.reg .pred e;\n\tsetp.ne.b32 e, %0, 0;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%1];\n\t}" ::"r"(leader),
+        "r"(smem_u32(bar))
         : "memory");
 }
 
