@@ -14,12 +14,14 @@
 // Per CTA (persistent, one per SM, static round-robin over items):
 //   warp 0      TMA producer of Q and K: Q tiles of each item into one of two Q
 //               buffers (the next item's Q loads while the current one
-//               computes), K tiles of 64 keys through an NK-stage ring.  A K
-//               stage is released as soon as its QK completes, a Q buffer
-//               after the item's last QK.
-//   warp 2      TMA producer of V: V tiles through an NV-stage ring, released
-//               after their P.V (separate from K so neither stream waits on
-//               the other's consumer).
+//               computes), K tiles of 64 keys through a two-stage ring.  A K
+//               stage is reloaded once its QK completed for every query tile
+//               (seen on the S barriers themselves: no separate release
+//               commit), a Q buffer after the item's last QK.
+//   warp 2      TMA producer of V: V tiles through a two-stage ring, reloaded
+//               once their P.V completed (seen on the P.V barriers).  Each
+//               extra tcgen05.commit costs the MMA warps ~160 cycles, so
+//               stage release piggybacks on barriers that exist anyway.
 //   warps 1, 3  tcgen05.mma issuers, one per query tile h (warp 1 also
 //               allocates TMEM).  For every key tile t the warp of tile h
 //               issues S_h(t) = Q_h K(t)^T into one of TWO S buffers of
@@ -97,9 +99,8 @@ struct AttnCfg {
     static constexpr int kOffStage = kOffV + NV * kTileBytes;     // 2 KB per softmax warp
     static constexpr int kStageBytes = 32 * 64;
     static constexpr int kOffBar = kOffStage + 4 * NH * kStageBytes;
-    // q_full[2] q_empty[2] mma_final k_full[NK] k_empty[NK] v_full[NV] v_empty[NV]
-    // s_full[NH][2] p_full[NH][2] pv_done[NH][2]
-    static constexpr int kNumBars = 5 + 2 * NK + 2 * NV + 6 * NH;
+    // q_full[2] q_empty[2] mma_final k_full[NK] v_full[NV] s_full[NH][2] p_full[NH][2] pv_done[NH][2]
+    static constexpr int kNumBars = 5 + NK + NV + 6 * NH;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + slack for 1024-byte alignment
     static constexpr int kThreads = 128 * (1 + NH);
@@ -108,7 +109,10 @@ struct AttnCfg {
     static constexpr int kTmemCols = kColsUsed <= 128 ? 128 : kColsUsed <= 256 ? 256 : 512;
     static_assert(kColsUsed <= 512, "TMEM overflow");
     static_assert(kSmemBytes <= 232448, "shared memory overflow");
-    static_assert(NK >= 2 && NV >= 2, "the K and V rings need two stages for the one-tile lookahead");
+    // Two stages exactly: a stage is released by the completion of the tile two back on a
+    // two-buffer barrier (S or P.V), and only with two stages is that parity wait unambiguous
+    // (the completion after it needs the very load that is waiting).
+    static_assert(NK == 2 && NV == 2, "K and V rings have exactly two stages");
 };
 
 __host__ __device__ constexpr uint32_t col_s(int h, int b) { return static_cast<uint32_t>(64 * (2 * h + b)); }
@@ -248,10 +252,8 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
     uint64_t *q_empty = bars + 2;        // [2]
     uint64_t *mma_final = bars + 4;
     uint64_t *k_full = bars + 5;            // [NK]
-    uint64_t *k_empty = k_full + NK;        // [NK]
-    uint64_t *v_full = k_empty + NK;        // [NV]
-    uint64_t *v_empty = v_full + NV;        // [NV]
-    uint64_t *s_full = v_empty + NV;        // [NH][2]
+    uint64_t *v_full = k_full + NK;         // [NV]
+    uint64_t *s_full = v_full + NV;         // [NH][2]
     uint64_t *p_full = s_full + 2 * NH;     // [NH][2]
     // pv_done[h][b] completes when P.V of a tile stored in S buffer b is done.
     // One barrier per buffer (not per head): every wait on it is then for
@@ -277,14 +279,8 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
             mbar_init(&q_empty[b], NH);   // one commit per MMA warp
         }
         mbar_init(mma_final, NH);
-        for (int s = 0; s < NK; ++s) {
-            mbar_init(&k_full[s], 1);
-            mbar_init(&k_empty[s], NH);   // one commit per MMA warp
-        }
-        for (int s = 0; s < NV; ++s) {
-            mbar_init(&v_full[s], 1);
-            mbar_init(&v_empty[s], NH);
-        }
+        for (int s = 0; s < NK; ++s) mbar_init(&k_full[s], 1);
+        for (int s = 0; s < NV; ++s) mbar_init(&v_full[s], 1);
         for (int i = 0; i < 2 * NH; ++i) {
             mbar_init(&s_full[i], 1);
             mbar_init(&p_full[i], 128);
@@ -350,8 +346,15 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
                 }
             }
             const int st = n_kv % NK;
-            const uint32_t use = n_kv / NK;
-            if (use > 0 && !warp_wait(&k_empty[st], (use - 1) & 1, abort_flag)) break;
+            if (n_kv >= NK) {
+                // stage st held K of tile n_kv - 2: free once that tile's QK completed for every
+                // query tile, i.e. on completion (n_kv - 2) / 2 of each tile's S barrier st
+                bool free_ok = true;
+#pragma unroll
+                for (int h = 0; h < NH; ++h)
+                    if (free_ok && !warp_wait(&s_full[2 * h + st], ((n_kv - 2) >> 1) & 1, abort_flag)) free_ok = false;
+                if (!free_ok) break;
+            }
             const int row = w.I.kv_row0 + w.j * kKeys;
             mbar_arrive_expect_tx_w(leader, &k_full[st], C::kTileBytes);
 #pragma unroll
@@ -382,8 +385,14 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
         uint32_t n_v = 0;
         while (w.valid) {
             const int st = n_v % NV;
-            const uint32_t use = n_v / NV;
-            if (use > 0 && !warp_wait(&v_empty[st], (use - 1) & 1, abort_flag)) break;
+            if (n_v >= NV) {
+                // stage st held V of tile n_v - 2: free once that tile's P.V completed everywhere
+                bool free_ok = true;
+#pragma unroll
+                for (int h = 0; h < NH; ++h)
+                    if (free_ok && !warp_wait(&pv_done[2 * h + st], ((n_v - 2) >> 1) & 1, abort_flag)) free_ok = false;
+                if (!free_ok) break;
+            }
             const int row = w.I.kv_row0 + w.j * kKeys;
             mbar_arrive_expect_tx_w(leader, &v_full[st], C::kTileBytes);
 #pragma unroll
@@ -435,7 +444,6 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
             const uint64_t dqh = dqb + static_cast<uint64_t>((h * C::NB * kQBox) >> 4);
             static_assert(kQBox == 16384 && kKVBox == 8192, "mma_qk_tile hard-codes the column-block strides");
             mma_qk_tile<C::NB>(leader, tmem + col_s(h, g & 1), dqh, dks, kIdescQK, &s_full[2 * h + (g & 1)]);
-            mma_commit_l(leader, &k_empty[st]);   // K(g) is free once every tile's QK completed (count NH)
             if (t.j == t.I.n_tiles - 1) mma_commit_l(leader, &q_empty[t.qbuf()]);   // Q after the item's last
             return true;
         };
@@ -460,7 +468,6 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
             static_assert(kKeys == 64, "mma_pv_tile issues four 16-key steps");
             mma_pv_tile(leader, tmem + C::kColO + D * h, tmem + col_s(h, ga & 1), dvs, kIdescPV, a.j > 0 ? 1u : 0u,
                         &pv_done[2 * h + (ga & 1)]);
-            mma_commit_l(leader, &v_empty[st]);   // count NH
             a.advance(p);
             ++ga;
         }
@@ -538,10 +545,11 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
                 if constexpr (MODE == Mode::Prefill) {
                     const float inv_l = 1.f / l;
 #pragma unroll
-                    for (int c = 0; c < D / 32; ++c) {
-                        float o[32];
-                        tmem_ld32(tO + 32 * c, o);
-                        put_chunk(c, o, inv_l);
+                    for (int c = 0; c < D / 64; ++c) {
+                        float o[64];
+                        tmem_ld64(tO + 64 * c, o);
+                        put_chunk(2 * c, o, inv_l);
+                        put_chunk(2 * c + 1, o + 32, inv_l);
                     }
                     if (p.lse) {
                         if (row_dst(row)) {
@@ -681,16 +689,22 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
                     tmem_st16(tS + 16, zr);
                 } else {
                     float s[kKeys];
-                    tmem_ld32(tS, s);
-                    tmem_ld32(tS + 32, s + 32);
+                    static_assert(kKeys == 64, "one tmem_ld64 per S tile");
+                    tmem_ld64(tS, s);
                     if (lim_lo < kKeys) {
 #pragma unroll
                         for (int c = 0; c < kKeys; ++c)
                             if (c >= lim) s[c] = -INFINITY;
                     }
-                    float mx = fmaxf(s[0], s[1]);
+                    // row max: four independent 3-input-max chains (short dependency chains)
+                    float mq[4];
 #pragma unroll
-                    for (int c = 2; c < kKeys; c += 2) mx = fmax3f(mx, s[c], s[c + 1]);
+                    for (int q = 0; q < 4; ++q) mq[q] = fmaxf(s[16 * q], s[16 * q + 1]);
+#pragma unroll
+                    for (int c = 2; c < 16; c += 2)
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) mq[q] = fmax3f(mq[q], s[16 * q + c], s[16 * q + c + 1]);
+                    const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
                     const float m_new = fmaxf(m, mx * sl2);
                     const bool grow = (j > 0) && (m_new > m + kRescaleLog2);
                     if (j == 0) m = m_new;
@@ -713,8 +727,11 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
                             tmem_st32f(tO + 32 * c, o);
                         }
                     }
-                    // p = 2^(s * scale * log2e - m), two columns per packed FMA; row sum in pairs
-                    float2 rs = make_float2(0.f, 0.f);
+                    // p = 2^(s * scale * log2e - m), two columns per packed FMA; row sum in four
+                    // independent pair accumulators
+                    float2 rs[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) rs[q] = make_float2(0.f, 0.f);
                     const float2 sl2x2 = make_float2(sl2, sl2);
                     const float2 negm = make_float2(-m, -m);
 #pragma unroll
@@ -724,12 +741,13 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
                         for (int i = 0; i < 16; ++i) {
                             const float2 x = ffma2(make_float2(s[32 * c + 2 * i], s[32 * c + 2 * i + 1]), sl2x2, negm);
                             const float2 e = make_float2(ex2(x.x), ex2(x.y));
-                            rs = fadd2(rs, e);
+                            rs[i & 3] = fadd2(rs[i & 3], e);
                             pk[i] = pack_bf16x2(e.x, e.y);
                         }
                         tmem_st16(tS + 16 * c, pk);   // P (bf16 pairs) over the first 32 columns of S
                     }
-                    l += rs.x + rs.y;
+                    const float2 r01 = fadd2(rs[0], rs[1]), r23 = fadd2(rs[2], rs[3]);
+                    l += (r01.x + r23.x) + (r01.y + r23.y);
                 }
                 tmem_st_wait();
                 tc_fence_before();
