@@ -14,10 +14,11 @@
 // Per CTA (persistent, one per SM, static round-robin over items):
 //   warp 0      TMA producer of Q and K: Q tiles of each item into one of two Q
 //               buffers (the next item's Q loads while the current one
-//               computes), K tiles of 64 keys through a two-stage ring.  A K
-//               stage is reloaded once its QK completed for every query tile
-//               (seen on the S barriers themselves: no separate release
-//               commit), a Q buffer after the item's last QK.
+//               computes), K tiles of 64 keys through an NK-stage ring.  A K
+//               stage is released by a plain arrive of each softmax
+//               warpgroup once it has seen its S of that tile (so the QK
+//               that read the stage has completed; no extra tcgen05.commit),
+//               a Q buffer after the item's last QK.
 //   warp 2      TMA producer of V: V tiles through a two-stage ring, reloaded
 //               once their P.V completed (seen on the P.V barriers).  Each
 //               extra tcgen05.commit costs the MMA warps ~160 cycles, so
@@ -99,8 +100,9 @@ struct AttnCfg {
     static constexpr int kOffStage = kOffV + NV * kTileBytes;     // 2 KB per softmax warp
     static constexpr int kStageBytes = 32 * 64;
     static constexpr int kOffBar = kOffStage + 4 * NH * kStageBytes;
-    // q_full[2] q_empty[2] mma_final k_full[NK] v_full[NV] s_full[NH][2] p_full[NH][2] pv_done[NH][2]
-    static constexpr int kNumBars = 5 + NK + NV + 6 * NH;
+    // q_full[2] q_empty[2] mma_final k_full[NK] k_empty[NK] v_full[NV] s_full[NH][2] p_full[NH][2]
+    // pv_done[NH][2]
+    static constexpr int kNumBars = 5 + 2 * NK + NV + 6 * NH;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + slack for 1024-byte alignment
     static constexpr int kThreads = 128 * (1 + NH);
@@ -109,10 +111,10 @@ struct AttnCfg {
     static constexpr int kTmemCols = kColsUsed <= 128 ? 128 : kColsUsed <= 256 ? 256 : 512;
     static_assert(kColsUsed <= 512, "TMEM overflow");
     static_assert(kSmemBytes <= 232448, "shared memory overflow");
-    // Two stages exactly: a stage is released by the completion of the tile two back on a
-    // two-buffer barrier (S or P.V), and only with two stages is that parity wait unambiguous
-    // (the completion after it needs the very load that is waiting).
-    static_assert(NK == 2 && NV == 2, "K and V rings have exactly two stages");
+    // V: two stages exactly.  A V stage is released by the completion of the P.V two tiles
+    // back on the two-buffer P.V barrier, and only with two stages is that parity wait
+    // unambiguous (the completion after it needs the very load that is waiting).
+    static_assert(NK >= 2 && NV == 2, "K ring needs two or more stages, the V ring exactly two");
 };
 
 __host__ __device__ constexpr uint32_t col_s(int h, int b) { return static_cast<uint32_t>(64 * (2 * h + b)); }
@@ -252,7 +254,8 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
     uint64_t *q_empty = bars + 2;        // [2]
     uint64_t *mma_final = bars + 4;
     uint64_t *k_full = bars + 5;            // [NK]
-    uint64_t *v_full = k_full + NK;         // [NV]
+    uint64_t *k_empty = k_full + NK;        // [NK]
+    uint64_t *v_full = k_empty + NK;        // [NV]
     uint64_t *s_full = v_full + NV;         // [NH][2]
     uint64_t *p_full = s_full + 2 * NH;     // [NH][2]
     // pv_done[h][b] completes when P.V of a tile stored in S buffer b is done.
@@ -279,7 +282,10 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
             mbar_init(&q_empty[b], NH);   // one commit per MMA warp
         }
         mbar_init(mma_final, NH);
-        for (int s = 0; s < NK; ++s) mbar_init(&k_full[s], 1);
+        for (int s = 0; s < NK; ++s) {
+            mbar_init(&k_full[s], 1);
+            mbar_init(&k_empty[s], NH);   // one arrive per softmax warpgroup
+        }
         for (int s = 0; s < NV; ++s) mbar_init(&v_full[s], 1);
         for (int i = 0; i < 2 * NH; ++i) {
             mbar_init(&s_full[i], 1);
@@ -346,15 +352,8 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
                 }
             }
             const int st = n_kv % NK;
-            if (n_kv >= NK) {
-                // stage st held K of tile n_kv - 2: free once that tile's QK completed for every
-                // query tile, i.e. on completion (n_kv - 2) / 2 of each tile's S barrier st
-                bool free_ok = true;
-#pragma unroll
-                for (int h = 0; h < NH; ++h)
-                    if (free_ok && !warp_wait(&s_full[2 * h + st], ((n_kv - 2) >> 1) & 1, abort_flag)) free_ok = false;
-                if (!free_ok) break;
-            }
+            const uint32_t use = n_kv / NK;
+            if (use > 0 && !warp_wait(&k_empty[st], (use - 1) & 1, abort_flag)) break;
             const int row = w.I.kv_row0 + w.j * kKeys;
             mbar_arrive_expect_tx_w(leader, &k_full[st], C::kTileBytes);
 #pragma unroll
@@ -680,6 +679,8 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
                 }
                 if (!warp_wait(&s_full[2 * h + (g & 1)], (g >> 1) & 1, abort_flag)) { ok = false; break; }
                 tc_fence_after();
+                // this tile's QK has completed: its K stage can be reloaded (one arrive per warpgroup)
+                if (quad == 0 && lane == 0) mbar_arrive(&k_empty[g % NK]);
                 if (lim_hi <= 0) {
                     // every row of this warp is masked for this tile: P = 0
                     uint32_t zr[16];
