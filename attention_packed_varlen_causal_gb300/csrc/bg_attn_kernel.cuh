@@ -565,80 +565,81 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
                     const int head = I.kh * p.g + hh;
                     const int64_t rb = static_cast<int64_t>(I.r) * p.W + beam;
                     const int ns = valid ? p.suffix_len : 0;
-                    // this row's query, kept in registers for the suffix dot products
-                    uint4 qv[D / 8];
-#pragma unroll
-                    for (int c = 0; c < D / 8; ++c) qv[c] = make_uint4(0, 0, 0, 0);
-                    if (ns > 0) {
-                        const uint4 *qp = reinterpret_cast<const uint4 *>(p.q + (rb * p.Hq + head) * D);
-#pragma unroll
-                        for (int c = 0; c < D / 8; ++c) qv[c] = qp[c];
-                    }
                     const __nv_bfloat16 *kbase = p.suffix_k + (rb * p.suffix_max * p.Hkv + I.kh) * D;
                     const __nv_bfloat16 *vbase = p.suffix_v + (rb * p.suffix_max * p.Hkv + I.kh) * D;
                     const int64_t sstride = static_cast<int64_t>(p.Hkv) * D;   // between suffix slots
-                    float z[kMaxSuffix];
+                    // The beam's suffix keys join the prompt softmax: first their logits and the
+                    // merged max and sum, then O rescaled and the weighted suffix values added, 64
+                    // columns at a time.  Runtime loops keep the code small; the weights sit in a
+                    // small per-thread array.
+                    float w[kMaxSuffix];
                     float m2 = m;
+                    if (ns > 0) {
+                        uint4 qv[D / 8];
+                        const uint4 *qp = reinterpret_cast<const uint4 *>(p.q + (rb * p.Hq + head) * D);
 #pragma unroll
-                    for (int s = 0; s < kMaxSuffix; ++s) {
-                        z[s] = -INFINITY;
-                        if (s < ns) {
+                        for (int c = 0; c < D / 8; ++c) qv[c] = qp[c];
+#pragma unroll 1
+                        for (int s = 0; s < ns; ++s) {
                             const uint4 *kp = reinterpret_cast<const uint4 *>(kbase + s * sstride);
-                            float acc = 0.f;
+                            float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
                             for (int c = 0; c < D / 8; ++c) {
                                 const uint4 ka = kp[c];
                                 const __nv_bfloat162 *q2 = reinterpret_cast<const __nv_bfloat162 *>(&qv[c]);
                                 const __nv_bfloat162 *k2 = reinterpret_cast<const __nv_bfloat162 *>(&ka);
 #pragma unroll
-                                for (int e = 0; e < 4; ++e) {
-                                    const float2 qf = __bfloat1622float2(q2[e]);
-                                    const float2 kf = __bfloat1622float2(k2[e]);
-                                    acc = fmaf(qf.x, kf.x, acc);
-                                    acc = fmaf(qf.y, kf.y, acc);
-                                }
+                                for (int e = 0; e < 4; ++e)
+                                    acc = ffma2(__bfloat1622float2(q2[e]), __bfloat1622float2(k2[e]), acc);
                             }
-                            z[s] = acc * sl2;
-                            m2 = fmaxf(m2, z[s]);
+                            w[s] = (acc.x + acc.y) * sl2;
+                            m2 = fmaxf(m2, w[s]);
                         }
                     }
+                    // no prompt keys: m is -inf and l is 0, so the prompt part drops out
                     const float alpha = (I.n_tiles > 0) ? ex2(m - m2) : 0.f;
                     float l2 = l * alpha;
-#pragma unroll
-                    for (int s = 0; s < kMaxSuffix; ++s) {
-                        z[s] = (s < ns) ? ex2(z[s] - m2) : 0.f;   // z now holds the suffix weights
-                        l2 += z[s];
+#pragma unroll 1
+                    for (int s = 0; s < ns; ++s) {
+                        w[s] = ex2(w[s] - m2);
+                        l2 += w[s];
                     }
                     const float inv_l = valid ? 1.f / l2 : 0.f;
-#pragma unroll
-                    for (int c = 0; c < D / 32; ++c) {
-                        float o[32];
+                    const float2 a2 = make_float2(alpha, alpha);
+#pragma unroll 1
+                    for (int hc = 0; hc < D / 64; ++hc) {
+                        float o[64];
                         if (I.n_tiles > 0) {
-                            tmem_ld32(tO + 32 * c, o);
+                            tmem_ld64(tO + 64 * hc, o);
                         } else {
 #pragma unroll
-                            for (int i = 0; i < 32; ++i) o[i] = 0.f;
+                            for (int i = 0; i < 64; ++i) o[i] = 0.f;
                         }
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) o[i] *= alpha;
+                        for (int i = 0; i < 64; i += 2) {
+                            const float2 x = fmul2(make_float2(o[i], o[i + 1]), a2);
+                            o[i] = x.x;
+                            o[i + 1] = x.y;
+                        }
+#pragma unroll 1
+                        for (int s = 0; s < ns; ++s) {
+                            const float2 p2 = make_float2(w[s], w[s]);
+                            const uint4 *vp = reinterpret_cast<const uint4 *>(vbase + s * sstride + 64 * hc);
 #pragma unroll
-                        for (int s = 0; s < kMaxSuffix; ++s) {
-                            if (s < ns) {
-                                const uint4 *vp = reinterpret_cast<const uint4 *>(vbase + s * sstride + 32 * c);
+                            for (int u = 0; u < 8; ++u) {
+                                const uint4 va = vp[u];
+                                const __nv_bfloat162 *v2 = reinterpret_cast<const __nv_bfloat162 *>(&va);
 #pragma unroll
-                                for (int u = 0; u < 4; ++u) {
-                                    const uint4 va = vp[u];
-                                    const __nv_bfloat162 *v2 = reinterpret_cast<const __nv_bfloat162 *>(&va);
-#pragma unroll
-                                    for (int e = 0; e < 4; ++e) {
-                                        const float2 vf = __bfloat1622float2(v2[e]);
-                                        o[8 * u + 2 * e] = fmaf(z[s], vf.x, o[8 * u + 2 * e]);
-                                        o[8 * u + 2 * e + 1] = fmaf(z[s], vf.y, o[8 * u + 2 * e + 1]);
-                                    }
+                                for (int e = 0; e < 4; ++e) {
+                                    const float2 x = ffma2(p2, __bfloat1622float2(v2[e]),
+                                                           make_float2(o[8 * u + 2 * e], o[8 * u + 2 * e + 1]));
+                                    o[8 * u + 2 * e] = x.x;
+                                    o[8 * u + 2 * e + 1] = x.y;
                                 }
                             }
                         }
-                        put_chunk(c, o, inv_l);
+                        put_chunk(2 * hc, o, inv_l);
+                        put_chunk(2 * hc + 1, o + 32, inv_l);
                     }
                 }
             return true;
