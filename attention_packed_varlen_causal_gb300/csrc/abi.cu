@@ -123,7 +123,7 @@ bg_status_t bg_packed_prefill_attn(const void *q, const void *k, const void *v, 
     if (num_seqs < 0 || total_tokens < 0 || max_seqlen < 0 || Hq <= 0 || Hkv <= 0 || head_dim <= 0)
         return BG_ERR_INVALID_ARG;
     if (Hq % Hkv != 0) return BG_ERR_INVALID_ARG;
-    if (!std::isfinite(scale)) return BG_ERR_INVALID_ARG;
+    if (!std::isfinite(scale) || !(scale > 0.f)) return BG_ERR_INVALID_ARG;   // masked logits are -inf
     if (!supported_head_dim(head_dim) || max_seqlen > BG_MAX_SEQLEN) return BG_ERR_UNSUPPORTED;
     if (num_seqs == 0 || total_tokens == 0) return BG_OK;
     if (!q || !k || !v || !cu_seqlens || !out || !workspace) return BG_ERR_INVALID_ARG;
@@ -198,7 +198,7 @@ bg_status_t bg_beam_decode_attn(const void *q, const void *prompt_k, const void 
     if (R < 0 || W <= 0 || Hq <= 0 || Hkv <= 0 || head_dim <= 0 || total_prompt_tokens < 0 || max_prompt_len < 0 ||
         suffix_len < 0 || suffix_max < 0 || suffix_len > suffix_max)
         return BG_ERR_INVALID_ARG;
-    if (Hq % Hkv != 0 || !std::isfinite(scale)) return BG_ERR_INVALID_ARG;
+    if (Hq % Hkv != 0 || !std::isfinite(scale) || !(scale > 0.f)) return BG_ERR_INVALID_ARG;
     const int32_t g = Hq / Hkv;
     if (!supported_head_dim(head_dim) || g > 128 || suffix_max > BG_MAX_SUFFIX) return BG_ERR_UNSUPPORTED;
     if (max_prompt_len == 0 && suffix_len == 0) return BG_ERR_INVALID_ARG;   // every softmax would be empty
@@ -229,7 +229,7 @@ bg_status_t bg_beam_decode_attn(const void *q, const void *prompt_k, const void 
     const int64_t items = static_cast<int64_t>(R) * Hkv * pairs;
     if (items >= (int64_t(1) << 31)) return BG_ERR_UNSUPPORTED;
 
-    CUtensorMap tm_q, tm_k, tm_v;
+    CUtensorMap tm_q, tm_k, tm_v, tm_sk, tm_sv;
     const uint64_t D = static_cast<uint64_t>(head_dim);
     const uint64_t dq[4] = {D, static_cast<uint64_t>(g), static_cast<uint64_t>(Hkv), static_cast<uint64_t>(R) * W};
     const uint64_t sq[3] = {D * 2, static_cast<uint64_t>(g) * D * 2, static_cast<uint64_t>(Hq) * D * 2};
@@ -243,6 +243,20 @@ bg_status_t bg_beam_decode_attn(const void *q, const void *prompt_k, const void 
     const void *vbase = total_prompt_tokens > 0 ? prompt_v : q;
     if (!encode_map(&tm_q, q, 4, dq, sq, boxq) || !encode_map(&tm_k, kbase, 3, dkv, skv, boxkv) ||
         !encode_map(&tm_v, vbase, 3, dkv, skv, boxkv))
+        return BG_ERR_CUDA;
+    // Suffix key tiles: slots 0..t-1 of suf_bpt consecutive beams per tile (beam-major rows),
+    // over [R*W beams][suffix_max slots][Hkv][d]; beams past R*W read as zeros.
+    const int32_t t_suf = suffix_len > 0 ? suffix_len : 1;
+    int32_t bpt = bg::kKeys / t_suf;
+    if (bpt > nh * BT) bpt = nh * BT;
+    const uint64_t ds[4] = {D, static_cast<uint64_t>(Hkv), static_cast<uint64_t>(suffix_max > 0 ? suffix_max : 1),
+                            static_cast<uint64_t>(R) * W};
+    const uint64_t ss[3] = {D * 2, static_cast<uint64_t>(Hkv) * D * 2,
+                            static_cast<uint64_t>(suffix_max > 0 ? suffix_max : 1) * Hkv * D * 2};
+    const uint32_t boxs[4] = {64, 1, static_cast<uint32_t>(t_suf), static_cast<uint32_t>(bpt)};
+    const void *skbase = suffix_len > 0 ? suffix_k : q;
+    const void *svbase = suffix_len > 0 ? suffix_v : q;
+    if (!encode_map(&tm_sk, skbase, 4, ds, ss, boxs) || !encode_map(&tm_sv, svbase, 4, ds, ss, boxs))
         return BG_ERR_CUDA;
 
     AttnParams p;
@@ -261,14 +275,12 @@ bg_status_t bg_beam_decode_attn(const void *q, const void *prompt_k, const void 
     p.pairs_per_rk = pairs;
     p.max_prompt_len = max_prompt_len;
     p.total_prompt = total_prompt_tokens;
-    p.q = static_cast<const __nv_bfloat16 *>(q);
-    p.suffix_k = static_cast<const __nv_bfloat16 *>(suffix_k);
-    p.suffix_v = static_cast<const __nv_bfloat16 *>(suffix_v);
     p.suffix_len = suffix_len;
-    p.suffix_max = suffix_max;
+    p.suf_bpt = bpt;
+    p.suf_tx = (head_dim / 64) * 128 * t_suf * bpt;
     p.n_items_decode = static_cast<int32_t>(items);
     const int grid = static_cast<int>(items < nsm ? items : nsm);
-    if (launch_decode_attn(head_dim, tm_q, tm_k, tm_v, p, grid, stream) != cudaSuccess) return BG_ERR_CUDA;
+    if (launch_decode_attn(head_dim, tm_q, tm_k, tm_v, tm_sk, tm_sv, p, grid, stream) != cudaSuccess) return BG_ERR_CUDA;
     return BG_OK;
 }
 

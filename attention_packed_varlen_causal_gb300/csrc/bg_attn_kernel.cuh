@@ -6,10 +6,12 @@
 //   * Prefill: packed variable-length causal GQA attention.  A work item is
 //     (sequence, 128-row query tile, NH query heads of one kv head); it
 //     streams the 64-key tiles up to its diagonal (only valid tokens).
-//   * Decode (shared-prompt phase): a work item is (request, kv head, NH
-//     tiles of beams x group heads); each tile is a dense 128-row block of
-//     queries of several beams against the request's one prompt K/V; the
-//     epilogue folds in each beam's own suffix keys and merges.
+//   * Decode: a work item is (request, kv head, NH tiles of beams x group
+//     heads); each tile is a dense 128-row block of queries of several beams
+//     against the request's one prompt K/V.  The beams' own suffix keys follow
+//     as a few more 64-key tiles of the same item: each holds the suffix slots
+//     of a run of consecutive beams (TMA-gathered, beam-major), and every query
+//     row keeps only the columns of its own beam.
 //
 // Per CTA (persistent, one per SM, static round-robin over items):
 //   warp 0      TMA producer of Q and K: Q tiles of each item into one of two Q
@@ -34,8 +36,8 @@
 //   warps 4..   NH softmax warpgroups; thread t of group h owns query row t of
 //               tile h (TMEM lane t): masked running max in base-2 units,
 //               lazy rescaling of O (only when the max grows by > 2^8),
-//               exp2 on the SFU, bf16 P back to TMEM; epilogue normalisation
-//               (decode: after merging the suffix keys), 32 columns at a time
+//               exp2 on the SFU, bf16 P back to TMEM; epilogue normalisation,
+//               32 columns at a time
 //               through a 2 KB per-warp staging area, so that each bf16 store
 //               instruction writes 64-byte row segments of 8 rows.
 //               Warps whose 32 rows are all masked for a key tile skip it.
@@ -61,7 +63,6 @@ constexpr int kKeys = 64;                  // keys per K/V tile
 constexpr int kQBox = 128 * 128;           // 128 rows x 64 bf16 (one 128-byte-swizzled column block)
 constexpr int kKVBox = 64 * 128;           // 64 rows x 64 bf16
 constexpr float kRescaleLog2 = 8.0f;       // rescale O only if the max grew by more than 2^8
-constexpr int kMaxSuffix = 16;
 
 enum class Mode : int { Prefill = 0, Decode = 1 };
 
@@ -83,13 +84,13 @@ struct AttnParams {
     int32_t R, W, BT;              // BT = beams per query tile = 128 / g
     int32_t pairs_per_rk;          // ceil(ceil(W / BT) / NH)
     int32_t max_prompt_len, total_prompt;
-    const __nv_bfloat16 *q;        // decode queries (for the suffix dot products)
-    const __nv_bfloat16 *suffix_k, *suffix_v;
-    int32_t suffix_len, suffix_max;
+    int32_t suffix_len;            // suffix slots per beam (t)
+    int32_t suf_bpt;               // beams per suffix key tile (suf_bpt * t <= 64)
+    int32_t suf_tx;                // bytes one suffix key tile brings (all column blocks)
     int32_t n_items_decode;
 };
 
-template <int D, int NH, int NK, int NV>
+template <int D, int NH, int NK, int NV, int NS>
 struct AttnCfg {
     static constexpr int NB = D / 64;                       // 128-byte column blocks per row
     static constexpr int kQBytes = NH * NB * kQBox;         // one Q buffer (NH tiles)
@@ -100,29 +101,30 @@ struct AttnCfg {
     static constexpr int kOffStage = kOffV + NV * kTileBytes;     // 2 KB per softmax warp
     static constexpr int kStageBytes = 32 * 64;
     static constexpr int kOffBar = kOffStage + 4 * NH * kStageBytes;
-    // q_full[2] q_empty[2] mma_final k_full[NK] k_empty[NK] v_full[NV] s_full[NH][2] p_full[NH][2]
-    // pv_done[NH][2]
-    static constexpr int kNumBars = 5 + 2 * NK + NV + 6 * NH;
+    // q_full[2] q_empty[2] mma_final k_full[NK] k_empty[NK] v_full[NV] s_full[NH][NS] p_full[NH][NS]
+    // pv_done[NH][NS]
+    static constexpr int kNumBars = 5 + 2 * NK + NV + 3 * NS * NH;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + slack for 1024-byte alignment
     static constexpr int kThreads = 128 * (1 + NH);
-    static constexpr int kColO = 128 * NH;
-    static constexpr int kColsUsed = 128 * NH + D * NH;
+    static constexpr int kColO = 64 * NS * NH;
+    static constexpr int kColsUsed = 64 * NS * NH + D * NH;
     static constexpr int kTmemCols = kColsUsed <= 128 ? 128 : kColsUsed <= 256 ? 256 : 512;
     static_assert(kColsUsed <= 512, "TMEM overflow");
     static_assert(kSmemBytes <= 232448, "shared memory overflow");
-    // V: two stages exactly.  A V stage is released by the completion of the P.V two tiles
-    // back on the two-buffer P.V barrier, and only with two stages is that parity wait
-    // unambiguous (the completion after it needs the very load that is waiting).
-    static_assert(NK >= 2 && NV == 2, "K ring needs two or more stages, the V ring exactly two");
+    // V: two stages.  A V stage is released by the completion of the P.V two tiles back on
+    // the per-S-buffer P.V barrier; that parity wait is unambiguous while NS >= NV (the
+    // completion after it on the same barrier needs a V tile this producer has not loaded).
+    static_assert(NK >= 2 && NV == 2 && NS >= NV && NS <= 3, "ring / buffer counts");
+    // TMEM column of S buffer b of query tile h
+    static __device__ __forceinline__ uint32_t col_s(int h, int b) { return static_cast<uint32_t>(64 * (NS * h + b)); }
 };
-
-__host__ __device__ constexpr uint32_t col_s(int h, int b) { return static_cast<uint32_t>(64 * (2 * h + b)); }
 
 // Everything every role needs to know about one work item.
 struct Item {
     int valid;       // 0: skip entirely (bad device data)
-    int n_tiles;     // 64-key K/V tiles to stream (may be 0 in decode)
+    int n_tiles;     // 64-key K/V tiles to stream
+    int n_prompt;    // of which from the sequence / prompt; decode: the rest hold suffix keys
     int kh;          // kv head
     int kv_row0;     // first packed K/V row of the sequence / prompt
     int kv_len;      // sequence length (prefill) or prompt length (decode)
@@ -161,6 +163,7 @@ __device__ __forceinline__ Item make_item(const AttnParams &p, int it, int4 raw)
         const int causal_tiles = 2 * raw.z + 2;
         const int len_tiles = (I.kv_len + kKeys - 1) / kKeys;
         I.n_tiles = causal_tiles < len_tiles ? causal_tiles : len_tiles;
+        I.n_prompt = I.n_tiles;
         I.valid = 1;
         I.r = 0;
         I.bt0 = 0;
@@ -177,7 +180,12 @@ __device__ __forceinline__ Item make_item(const AttnParams &p, int it, int4 raw)
         I.valid = ok ? 1 : 0;
         I.kv_row0 = a;
         I.kv_len = ok ? b - a : 0;
-        I.n_tiles = ok ? (b - a + kKeys - 1) / kKeys : 0;
+        I.n_prompt = ok ? (b - a + kKeys - 1) / kKeys : 0;
+        // suffix tiles: the item's beams (NH tiles of BT, cut at W), suf_bpt per tile
+        int nb = p.W - I.bt0 * p.BT;
+        if (nb > NH * p.BT) nb = NH * p.BT;
+        const int n_suf = (ok && p.suffix_len > 0) ? (nb + p.suf_bpt - 1) / p.suf_bpt : 0;
+        I.n_tiles = I.n_prompt + n_suf;
         I.seq_start = 0;
         I.qt = 0;
         I.head0 = 0;
@@ -240,12 +248,13 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volati
     return ok != 0;
 }
 
-template <Mode MODE, int D, int NH, int NK, int NV>
+template <Mode MODE, int D, int NH, int NK, int NV, int NS>
 __global__ void __launch_bounds__(128 * (1 + NH), 1)
     attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                const __grid_constant__ CUtensorMap tm_v, const AttnParams p)
+                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_sk,
+                const __grid_constant__ CUtensorMap tm_sv, const AttnParams p)
 {
-    using C = AttnCfg<D, NH, NK, NV>;
+    using C = AttnCfg<D, NH, NK, NV, NS>;
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte alignment of the shared-window offset (swizzle-128B atoms need it)
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -256,13 +265,13 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
     uint64_t *k_full = bars + 5;            // [NK]
     uint64_t *k_empty = k_full + NK;        // [NK]
     uint64_t *v_full = k_empty + NK;        // [NV]
-    uint64_t *s_full = v_full + NV;         // [NH][2]
-    uint64_t *p_full = s_full + 2 * NH;     // [NH][2]
+    uint64_t *s_full = v_full + NV;         // [NH][NS]
+    uint64_t *p_full = s_full + NS * NH;    // [NH][NS]
     // pv_done[h][b] completes when P.V of a tile stored in S buffer b is done.
     // One barrier per buffer (not per head): every wait on it is then for
     // the phase right after the last one its waiter already saw complete,
     // which is what makes a parity wait unambiguous.
-    uint64_t *pv_done = p_full + 2 * NH;    // [NH][2]
+    uint64_t *pv_done = p_full + NS * NH;   // [NH][NS]
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
 
@@ -287,7 +296,7 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
             mbar_init(&k_empty[s], NH);   // one arrive per softmax warpgroup
         }
         for (int s = 0; s < NV; ++s) mbar_init(&v_full[s], 1);
-        for (int i = 0; i < 2 * NH; ++i) {
+        for (int i = 0; i < NS * NH; ++i) {
             mbar_init(&s_full[i], 1);
             mbar_init(&p_full[i], 128);
             mbar_init(&pv_done[i], 1);
@@ -296,9 +305,11 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
         fence_barrier_init();
     }
     if constexpr (MODE == Mode::Decode) {
-        // Decode query tiles fill only BT*g <= 128 rows; keep the rest zero.
-        uint4 *q4 = reinterpret_cast<uint4 *>(smem + C::kOffQ);
-        for (int i = threadIdx.x; i < 2 * C::kQBytes / 16; i += blockDim.x) q4[i] = make_uint4(0, 0, 0, 0);
+        // Decode query tiles fill only BT*g <= 128 rows and suffix key tiles only suf_bpt*t
+        // <= 64 rows; the rows past them keep what an earlier tile left (finite) or these
+        // zeros, so the masked columns they feed multiply finite values only.
+        uint4 *z4 = reinterpret_cast<uint4 *>(smem + C::kOffQ);
+        for (int i = threadIdx.x; i < C::kOffStage / 16; i += blockDim.x) z4[i] = make_uint4(0, 0, 0, 0);
         fence_proxy_async_smem();
     }
     if (warp == 1) {
@@ -309,6 +320,10 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
         tma_prefetch_desc(&tm_q);
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
+        if constexpr (MODE == Mode::Decode) {
+            tma_prefetch_desc(&tm_sk);
+            tma_prefetch_desc(&tm_sv);
+        }
     }
     tc_fence_before();
     __syncthreads();
@@ -354,12 +369,21 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
             const int st = n_kv % NK;
             const uint32_t use = n_kv / NK;
             if (use > 0 && !warp_wait(&k_empty[st], (use - 1) & 1, abort_flag)) break;
-            const int row = w.I.kv_row0 + w.j * kKeys;
-            mbar_arrive_expect_tx_w(leader, &k_full[st], C::kTileBytes);
+            uint8_t *kdst = smem + C::kOffK + st * C::kTileBytes;
+            if (MODE == Mode::Prefill || w.j < w.I.n_prompt) {
+                const int row = w.I.kv_row0 + w.j * kKeys;
+                mbar_arrive_expect_tx_w(leader, &k_full[st], C::kTileBytes);
 #pragma unroll
-            for (int b = 0; b < C::NB; ++b)
-                tma_load_3d_w(leader, smem + C::kOffK + st * C::kTileBytes + b * kKVBox, &tm_k, &k_full[st], b * 64, w.I.kh,
-                              row, pol_kv);
+                for (int b = 0; b < C::NB; ++b)
+                    tma_load_3d_w(leader, kdst + b * kKVBox, &tm_k, &k_full[st], b * 64, w.I.kh, row, pol_kv);
+            } else {
+                // suffix slots 0..t-1 of suf_bpt consecutive beams: rows beam-major
+                const int beam = w.I.r * p.W + w.I.bt0 * p.BT + (w.j - w.I.n_prompt) * p.suf_bpt;
+                mbar_arrive_expect_tx_w(leader, &k_full[st], p.suf_tx);
+#pragma unroll
+                for (int b = 0; b < C::NB; ++b)
+                    tma_load_4d_w(leader, kdst + b * kKVBox, &tm_sk, &k_full[st], b * 64, w.I.kh, 0, beam, pol_q);
+            }
             ++n_kv;
             w.advance(p);
         }
@@ -379,6 +403,7 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
         // =============================================================== V producer
         const uint32_t leader = (lane == 0) ? 1u : 0u;
         const uint64_t pol_kv = l2_policy_evict_last();
+        const uint64_t pol_q = l2_policy_evict_first();
         TileWalker<MODE, NH> w;
         w.first(p, n_items);
         uint32_t n_v = 0;
@@ -389,15 +414,24 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
                 bool free_ok = true;
 #pragma unroll
                 for (int h = 0; h < NH; ++h)
-                    if (free_ok && !warp_wait(&pv_done[2 * h + st], ((n_v - 2) >> 1) & 1, abort_flag)) free_ok = false;
+                    if (free_ok && !warp_wait(&pv_done[NS * h + (n_v - NV) % NS], ((n_v - NV) / NS) & 1, abort_flag))
+                        free_ok = false;
                 if (!free_ok) break;
             }
-            const int row = w.I.kv_row0 + w.j * kKeys;
-            mbar_arrive_expect_tx_w(leader, &v_full[st], C::kTileBytes);
+            uint8_t *vdst = smem + C::kOffV + st * C::kTileBytes;
+            if (MODE == Mode::Prefill || w.j < w.I.n_prompt) {
+                const int row = w.I.kv_row0 + w.j * kKeys;
+                mbar_arrive_expect_tx_w(leader, &v_full[st], C::kTileBytes);
 #pragma unroll
-            for (int b = 0; b < C::NB; ++b)
-                tma_load_3d_w(leader, smem + C::kOffV + st * C::kTileBytes + b * kKVBox, &tm_v, &v_full[st], b * 64, w.I.kh,
-                              row, pol_kv);
+                for (int b = 0; b < C::NB; ++b)
+                    tma_load_3d_w(leader, vdst + b * kKVBox, &tm_v, &v_full[st], b * 64, w.I.kh, row, pol_kv);
+            } else {
+                const int beam = w.I.r * p.W + w.I.bt0 * p.BT + (w.j - w.I.n_prompt) * p.suf_bpt;
+                mbar_arrive_expect_tx_w(leader, &v_full[st], p.suf_tx);
+#pragma unroll
+                for (int b = 0; b < C::NB; ++b)
+                    tma_load_4d_w(leader, vdst + b * kKVBox, &tm_sv, &v_full[st], b * 64, w.I.kh, 0, beam, pol_q);
+            }
             ++n_v;
             w.advance(p);
         }
@@ -442,12 +476,14 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
             tc_fence_after();
             const uint64_t dqh = dqb + static_cast<uint64_t>((h * C::NB * kQBox) >> 4);
             static_assert(kQBox == 16384 && kKVBox == 8192, "mma_qk_tile hard-codes the column-block strides");
-            mma_qk_tile<C::NB>(leader, tmem + col_s(h, g & 1), dqh, dks, kIdescQK, &s_full[2 * h + (g & 1)]);
+            mma_qk_tile<C::NB>(leader, tmem + C::col_s(h, g % NS), dqh, dks, kIdescQK, &s_full[NS * h + g % NS]);
             if (t.j == t.I.n_tiles - 1) mma_commit_l(leader, &q_empty[t.qbuf()]);   // Q after the item's last
             return true;
         };
 
-        if (b.valid) {
+        // QK runs NS-1 tiles ahead of P.V: QK(t + NS - 1) reuses the S buffer of P(t - 1),
+        // whose P.V was issued before it.
+        for (int i = 0; i < NS - 1 && ok && b.valid; ++i) {
             ok = issue_qk(b, gb);
             b.advance(p);
             ++gb;
@@ -461,12 +497,12 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
             const int st = ga % NV;
             if (!warp_wait(&v_full[st], (ga / NV) & 1, abort_flag)) break;
             const uint64_t dvs = dv0 + static_cast<uint64_t>((st * C::kTileBytes) >> 4);
-            if (!warp_wait(&p_full[2 * h + (ga & 1)], (ga >> 1) & 1, abort_flag)) break;
+            if (!warp_wait(&p_full[NS * h + ga % NS], (ga / NS) & 1, abort_flag)) break;
             tc_fence_after();
             // V tile: 64 key rows of 128 bytes per column block; K = 16 rows per step.
             static_assert(kKeys == 64, "mma_pv_tile issues four 16-key steps");
-            mma_pv_tile(leader, tmem + C::kColO + D * h, tmem + col_s(h, ga & 1), dvs, kIdescPV, a.j > 0 ? 1u : 0u,
-                        &pv_done[2 * h + (ga & 1)]);
+            mma_pv_tile(leader, tmem + C::kColO + D * h, tmem + C::col_s(h, ga % NS), dvs, kIdescPV, a.j > 0 ? 1u : 0u,
+                        &pv_done[NS * h + ga % NS]);
             a.advance(p);
             ++ga;
         }
@@ -491,9 +527,11 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
         // been turned into P (which reads no O), so the wait for the last P.V overlaps that
         // work; the next item's first P.V, which overwrites O, is released only after this.
         auto epilogue = [&](const Item &I, float m, float l, uint32_t g_last) -> bool {
+                // The commit after the item's last P.V covers every earlier MMA too.  (Items always
+                // have tiles here; the test stays because ptxas allocates the prefill kernel's
+                // registers with fewer spills with it: 235 vs 297 us on the Prefill-Only batch.)
                 if (I.n_tiles > 0) {
-                    // the commit after the item's last P.V covers every earlier MMA too
-                    if (!warp_wait(&pv_done[2 * h + (g_last & 1)], (g_last >> 1) & 1, abort_flag)) return false;
+                    if (!warp_wait(&pv_done[NS * h + g_last % NS], (g_last / NS) & 1, abort_flag)) return false;
                     tc_fence_after();
                 }
                 // destination of tile row r, or nullptr when the row is not a valid output row
@@ -541,105 +579,21 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
                         if (dst[i]) reinterpret_cast<uint4 *>(dst[i] + 32 * c)[cc] = val;
                     }
                 };
-                if constexpr (MODE == Mode::Prefill) {
-                    const float inv_l = 1.f / l;
+                const float inv_l = 1.f / l;
 #pragma unroll
-                    for (int c = 0; c < D / 64; ++c) {
-                        float o[64];
-                        tmem_ld64(tO + 64 * c, o);
-                        put_chunk(2 * c, o, inv_l);
-                        put_chunk(2 * c + 1, o + 32, inv_l);
-                    }
+                for (int c = 0; c < D / 64; ++c) {
+                    float o[64];
+                    tmem_ld64(tO + 64 * c, o);
+                    put_chunk(2 * c, o, inv_l);
+                    put_chunk(2 * c + 1, o + 32, inv_l);
+                }
+                if constexpr (MODE == Mode::Prefill) {
                     if (p.lse) {
                         if (row_dst(row)) {
                             // natural-log sum-exp: (m + log2 l) * ln 2
                             p.lse[static_cast<int64_t>(I.seq_start + I.qt * kRows + row) * p.Hq + I.head0 + h] =
                                 (m + __log2f(l)) * 0.69314718055994530942f;
                         }
-                    }
-                } else {
-                    const int local_beam = row / p.g;
-                    const int hh = row - local_beam * p.g;
-                    const int beam = (I.bt0 + h) * p.BT + local_beam;
-                    const bool valid = local_beam < p.BT && beam < p.W;
-                    const int head = I.kh * p.g + hh;
-                    const int64_t rb = static_cast<int64_t>(I.r) * p.W + beam;
-                    const int ns = valid ? p.suffix_len : 0;
-                    const __nv_bfloat16 *kbase = p.suffix_k + (rb * p.suffix_max * p.Hkv + I.kh) * D;
-                    const __nv_bfloat16 *vbase = p.suffix_v + (rb * p.suffix_max * p.Hkv + I.kh) * D;
-                    const int64_t sstride = static_cast<int64_t>(p.Hkv) * D;   // between suffix slots
-                    // The beam's suffix keys join the prompt softmax: first their logits and the
-                    // merged max and sum, then O rescaled and the weighted suffix values added, 64
-                    // columns at a time.  Runtime loops keep the code small; the weights sit in a
-                    // small per-thread array.
-                    float w[kMaxSuffix];
-                    float m2 = m;
-                    if (ns > 0) {
-                        uint4 qv[D / 8];
-                        const uint4 *qp = reinterpret_cast<const uint4 *>(p.q + (rb * p.Hq + head) * D);
-#pragma unroll
-                        for (int c = 0; c < D / 8; ++c) qv[c] = qp[c];
-#pragma unroll 1
-                        for (int s = 0; s < ns; ++s) {
-                            const uint4 *kp = reinterpret_cast<const uint4 *>(kbase + s * sstride);
-                            float2 acc = make_float2(0.f, 0.f);
-#pragma unroll
-                            for (int c = 0; c < D / 8; ++c) {
-                                const uint4 ka = kp[c];
-                                const __nv_bfloat162 *q2 = reinterpret_cast<const __nv_bfloat162 *>(&qv[c]);
-                                const __nv_bfloat162 *k2 = reinterpret_cast<const __nv_bfloat162 *>(&ka);
-#pragma unroll
-                                for (int e = 0; e < 4; ++e)
-                                    acc = ffma2(__bfloat1622float2(q2[e]), __bfloat1622float2(k2[e]), acc);
-                            }
-                            w[s] = (acc.x + acc.y) * sl2;
-                            m2 = fmaxf(m2, w[s]);
-                        }
-                    }
-                    // no prompt keys: m is -inf and l is 0, so the prompt part drops out
-                    const float alpha = (I.n_tiles > 0) ? ex2(m - m2) : 0.f;
-                    float l2 = l * alpha;
-#pragma unroll 1
-                    for (int s = 0; s < ns; ++s) {
-                        w[s] = ex2(w[s] - m2);
-                        l2 += w[s];
-                    }
-                    const float inv_l = valid ? 1.f / l2 : 0.f;
-                    const float2 a2 = make_float2(alpha, alpha);
-#pragma unroll 1
-                    for (int hc = 0; hc < D / 64; ++hc) {
-                        float o[64];
-                        if (I.n_tiles > 0) {
-                            tmem_ld64(tO + 64 * hc, o);
-                        } else {
-#pragma unroll
-                            for (int i = 0; i < 64; ++i) o[i] = 0.f;
-                        }
-#pragma unroll
-                        for (int i = 0; i < 64; i += 2) {
-                            const float2 x = fmul2(make_float2(o[i], o[i + 1]), a2);
-                            o[i] = x.x;
-                            o[i + 1] = x.y;
-                        }
-#pragma unroll 1
-                        for (int s = 0; s < ns; ++s) {
-                            const float2 p2 = make_float2(w[s], w[s]);
-                            const uint4 *vp = reinterpret_cast<const uint4 *>(vbase + s * sstride + 64 * hc);
-#pragma unroll
-                            for (int u = 0; u < 8; ++u) {
-                                const uint4 va = vp[u];
-                                const __nv_bfloat162 *v2 = reinterpret_cast<const __nv_bfloat162 *>(&va);
-#pragma unroll
-                                for (int e = 0; e < 4; ++e) {
-                                    const float2 x = ffma2(p2, __bfloat1622float2(v2[e]),
-                                                           make_float2(o[8 * u + 2 * e], o[8 * u + 2 * e + 1]));
-                                    o[8 * u + 2 * e] = x.x;
-                                    o[8 * u + 2 * e + 1] = x.y;
-                                }
-                            }
-                        }
-                        put_chunk(2 * hc, o, inv_l);
-                        put_chunk(2 * hc + 1, o + 32, inv_l);
                     }
                 }
             return true;
@@ -663,12 +617,16 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
                 }
                 continue;
             }
+            if (I.n_tiles == 0) continue;   // not produced by make_item for a valid item; skipped by every role
             float m = -INFINITY;   // running max of scaled logits (base-2 units)
             float l = 0.f;         // running sum of exp2(logit - m)
             for (int j = 0; j < I.n_tiles; ++j, ++g) {
-                const uint32_t tS = tmem + lane_addr + col_s(h, g & 1);
-                // valid key columns of this tile: for this row (lim) and the warp's rows (lim_lo..lim_hi)
+                const uint32_t tS = tmem + lane_addr + C::col_s(h, g % NS);
+                // valid key columns of this tile: c < lim for this row (lim_lo..lim_hi over the
+                // warp's rows); a decode suffix tile keeps c in [c0, c0 + nsuf) instead
                 int lim, lim_lo, lim_hi;
+                bool suf = false;
+                int c0 = 0, nsuf = 0;
                 if constexpr (MODE == Mode::Prefill) {
                     lim_lo = I.qt * kRows + quad * 32 - j * kKeys + 1;
                     lim = lim_lo + lane;
@@ -677,8 +635,18 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
                     lim_lo = I.kv_len - j * kKeys;
                     lim = lim_lo;
                     lim_hi = lim_lo;
+                    if (j >= I.n_prompt) {
+                        // this row's beam, counted from the item's first beam, and its place in the tile
+                        suf = true;
+                        const int lb = row / p.g;
+                        const int pos = h * p.BT + lb - (j - I.n_prompt) * p.suf_bpt;
+                        const bool mine = lb < p.BT && (I.bt0 + h) * p.BT + lb < p.W && pos >= 0 && pos < p.suf_bpt;
+                        c0 = pos * p.suffix_len;
+                        nsuf = mine ? p.suffix_len : 0;
+                        lim_hi = __any_sync(0xffffffffu, nsuf > 0) ? 1 : 0;
+                    }
                 }
-                if (!warp_wait(&s_full[2 * h + (g & 1)], (g >> 1) & 1, abort_flag)) { ok = false; break; }
+                if (!warp_wait(&s_full[NS * h + g % NS], (g / NS) & 1, abort_flag)) { ok = false; break; }
                 tc_fence_after();
                 // this tile's QK has completed: its K stage can be reloaded (one arrive per warpgroup)
                 if (quad == 0 && lane == 0) mbar_arrive(&k_empty[g % NK]);
@@ -693,7 +661,11 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
                     float s[kKeys];
                     static_assert(kKeys == 64, "one tmem_ld64 per S tile");
                     tmem_ld64(tS, s);
-                    if (lim_lo < kKeys) {
+                    if (suf) {
+#pragma unroll
+                        for (int c = 0; c < kKeys; ++c)
+                            if (static_cast<unsigned>(c - c0) >= static_cast<unsigned>(nsuf)) s[c] = -INFINITY;
+                    } else if (lim_lo < kKeys) {
 #pragma unroll
                         for (int c = 0; c < kKeys; ++c)
                             if (c >= lim) s[c] = -INFINITY;
@@ -712,12 +684,14 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
                     if (j == 0) m = m_new;
                     if (__any_sync(0xffffffffu, grow)) {
                         // O holds the previous tiles: wait for their last P.V, rescale in place.
-                        if (!warp_wait(&pv_done[2 * h + ((g - 1) & 1)], ((g - 1) >> 1) & 1, abort_flag)) {
+                        if (!warp_wait(&pv_done[NS * h + (g - 1) % NS], ((g - 1) / NS) & 1, abort_flag)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
-                        const float alpha = ex2(m - m_new);
+                        // decode: a row with no valid key so far has O = 0 and l = 0 (alpha 0, not
+                        // the NaN of -inf - -inf when its max is still -inf)
+                        const float alpha = (MODE == Mode::Decode && m == -INFINITY) ? 0.f : ex2(m - m_new);
                         m = m_new;
                         l *= alpha;
 #pragma unroll
@@ -735,7 +709,10 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
 #pragma unroll
                     for (int q = 0; q < 4; ++q) rs[q] = make_float2(0.f, 0.f);
                     const float2 sl2x2 = make_float2(sl2, sl2);
-                    const float2 negm = make_float2(-m, -m);
+                    // decode: a row that has seen no valid key yet (max -inf) gets p = 0, not NaN;
+                    // a prefill row always has key 0 in its first tile
+                    const float mu = (MODE == Mode::Decode && m == -INFINITY) ? 0.f : m;
+                    const float2 negm = make_float2(-mu, -mu);
 #pragma unroll
                     for (int c = 0; c < kKeys / 32; ++c) {
                         uint32_t pk[16];
@@ -758,23 +735,14 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
                     pend = false;
                     tc_fence_before();
                 }
-                mbar_arrive(&p_full[2 * h + (g & 1)]);
+                mbar_arrive(&p_full[NS * h + g % NS]);
             }
             if (!ok) break;
-            if (pend) {                          // an item without tiles followed
-                if (!epilogue(Ip, mp, lp, gp)) { ok = false; break; }
-                pend = false;
-            }
-            if (I.n_tiles > 0) {
-                pend = true;
-                Ip = I;
-                mp = m;
-                lp = l;
-                gp = g - 1;
-            } else if (!epilogue(I, m, l, 0)) {
-                ok = false;
-                break;
-            }
+            pend = true;
+            Ip = I;
+            mp = m;
+            lp = l;
+            gp = g - 1;
         }
         if (ok && pend) ok = epilogue(Ip, mp, lp, gp);
 

@@ -24,7 +24,8 @@ cudaError_t launch_prefill_attn(int head_dim, const CUtensorMap &tm_q, const CUt
 int prefill_heads_per_cta();
 
 cudaError_t launch_decode_attn(int head_dim, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
-                               const CUtensorMap &tm_v, const AttnParams &p, int grid, cudaStream_t stream);
+                               const CUtensorMap &tm_v, const CUtensorMap &tm_sk, const CUtensorMap &tm_sv,
+                               const AttnParams &p, int grid, cudaStream_t stream);
 int decode_tiles_per_cta();
 
 cudaError_t launch_suffix_reorder(const void *src_k, const void *src_v, void *dst_k, void *dst_v,

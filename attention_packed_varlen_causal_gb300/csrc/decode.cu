@@ -5,8 +5,8 @@
 // suffix K/V.  The shared prompt is what makes the decode step dense: the
 // queries of all beams x group heads of one kv head form 128-row tiles that
 // run on the tensor cores against the prompt K/V, read once per tile pair
-// (and from L2 for the sibling tiles).  The few suffix keys of each beam are
-// folded in by the epilogue of attn_kernel<Decode>.
+// (and from L2 for the sibling tiles).  The few suffix keys of each beam
+// follow as extra key tiles of the same item (see attn_kernel<Decode>).
 #include "bg_attn_kernel.cuh"
 #include "bg_internal.h"
 
@@ -17,22 +17,23 @@ namespace bg {
 namespace {
 constexpr int kNH = 2;   // query tiles (of the same request and kv head) per CTA
 
-template <int D, int NK, int NV>
+template <int D, int NK, int NV, int NS>
 std::atomic<uint64_t> &smem_attr_done()
 {
     static std::atomic<uint64_t> mask{0};
     return mask;
 }
 
-template <int D, int NK, int NV>
+template <int D, int NK, int NV, int NS>
 cudaError_t launch_one(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
-                       const AttnParams &p, int grid, cudaStream_t stream)
+                       const CUtensorMap &tm_sk, const CUtensorMap &tm_sv, const AttnParams &p, int grid,
+                       cudaStream_t stream)
 {
-    using C = AttnCfg<D, kNH, NK, NV>;
-    auto kern = attn_kernel<Mode::Decode, D, kNH, NK, NV>;
-    cudaError_t e = ensure_smem_attribute(kern, C::kSmemBytes, smem_attr_done<D, NK, NV>());
+    using C = AttnCfg<D, kNH, NK, NV, NS>;
+    auto kern = attn_kernel<Mode::Decode, D, kNH, NK, NV, NS>;
+    cudaError_t e = ensure_smem_attribute(kern, C::kSmemBytes, smem_attr_done<D, NK, NV, NS>());
     if (e != cudaSuccess) return e;
-    kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(tm_q, tm_k, tm_v, p);
+    kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(tm_q, tm_k, tm_v, tm_sk, tm_sv, p);
     return cudaGetLastError();
 }
 }  // namespace
@@ -40,10 +41,11 @@ cudaError_t launch_one(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const C
 int decode_tiles_per_cta() { return kNH; }
 
 cudaError_t launch_decode_attn(int head_dim, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
-                               const CUtensorMap &tm_v, const AttnParams &p, int grid, cudaStream_t stream)
+                               const CUtensorMap &tm_v, const CUtensorMap &tm_sk, const CUtensorMap &tm_sv,
+                               const AttnParams &p, int grid, cudaStream_t stream)
 {
-    if (head_dim == 64) return launch_one<64, 4, 2>(tm_q, tm_k, tm_v, p, grid, stream);
-    if (head_dim == 128) return launch_one<128, 3, 2>(tm_q, tm_k, tm_v, p, grid, stream);
+    if (head_dim == 64) return launch_one<64, 4, 2, 3>(tm_q, tm_k, tm_v, tm_sk, tm_sv, p, grid, stream);
+    if (head_dim == 128) return launch_one<128, 3, 2, 2>(tm_q, tm_k, tm_v, tm_sk, tm_sv, p, grid, stream);
     return cudaErrorInvalidValue;
 }
 

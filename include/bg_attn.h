@@ -92,7 +92,8 @@ size_t bg_packed_prefill_workspace_size(int32_t num_seqs, int32_t total_tokens,
  *   cu_seqlens   int32 [num_seqs+1], device; cu[0]=0, non-decreasing,
  *                cu[num_seqs]=total_tokens; zero-length sequences allowed
  *   max_seqlen   host upper bound of every sequence length (checked on device)
- *   scale        softmax scale (1/sqrt(head_dim) for standard attention)
+ *   scale        softmax scale, finite and > 0 (1/sqrt(head_dim) for standard
+ *                attention); anything else gives BG_ERR_INVALID_ARG
  *   out          bf16 [total_tokens, Hq, head_dim]; rows of every valid token
  *                are written, nothing else is touched
  *   lse          fp32 [total_tokens, Hq] natural-log sum-exp of the scaled
@@ -122,9 +123,11 @@ bg_status_t bg_packed_prefill_attn(const void *q, const void *k, const void *v,
  * head h (kvh = h / (Hq/Hkv)):
  *     keys   = [prompt_k rows of r ; suffix_k[r, b, 0:suffix_len, kvh]]
  *     out[r,b,h] = sum_j softmax_j(scale * q[r,b,h] . key_j) value_j
- * The query is the newest position, so nothing is masked.  The prompt part
- * is computed as one dense tensor-core tile of all beams x group heads of a
- * request against the prompt K/V; the suffix part and the merge run in fp32.
+ * The query is the newest position, so nothing is masked.  The queries of
+ * all beams x group heads of a request form dense 128-row tensor-core tiles
+ * against the prompt K/V; the suffix slots of runs of consecutive beams
+ * follow as extra 64-key tiles in which each row keeps only its own beam's
+ * columns, all in one online softmax (fp32).
  *
  *   q                     bf16 [R, W, Hq, head_dim]
  *   prompt_k, prompt_v    bf16 [total_prompt_tokens, Hkv, head_dim], request r
@@ -139,8 +142,10 @@ bg_status_t bg_packed_prefill_attn(const void *q, const void *k, const void *v,
  *   out                   bf16 [R, W, Hq, head_dim]
  * A request with prompt length 0 and suffix_len 0 has an empty softmax: its
  * rows are skipped and BG_DEVSTAT_EMPTY_ROW is raised.
+ *   scale                 softmax scale, finite and > 0
  * Errors: BG_ERR_INVALID_ARG for NULL/misaligned pointers, bad sizes,
- * suffix_len > suffix_max, Hq % Hkv != 0, out aliasing an input;
+ * suffix_len > suffix_max, Hq % Hkv != 0, scale not finite and > 0, out
+ * aliasing an input;
  * BG_ERR_UNSUPPORTED for head_dim not in {64,128}, Hq/Hkv > 128 or
  * suffix_max > BG_MAX_SUFFIX.
  */

@@ -66,7 +66,7 @@ def prefill(lib, **kw):
     (dict(Hq=6, Hkv=4), 1), (dict(d=96), 2), (dict(d=256), 2), (dict(maxlen=70000), 2),
     (dict(B=-1), 1), (dict(q=FAKE + 8), 1), (dict(ws=FAKE * 6 + 16), 1), (dict(wsb=64), 1),
     (dict(out=FAKE * 1 + 64), 1),            # out overlaps q
-    (dict(scale=float("nan")), 1),
+    (dict(scale=float("nan")), 1), (dict(scale=0.0), 1), (dict(scale=-0.125), 1),
     (dict(B=0, q=None), 0), (dict(T=0, q=None), 0),   # empty problems are a no-op
 ])
 def test_prefill_host_validation(lib, kw, expect):
@@ -86,6 +86,7 @@ def decode(lib, **kw):
     (dict(q=None), 1), (dict(out=None), 1), (dict(cu=None), 1), (dict(t=5), 1), (dict(t=-1), 1),
     (dict(pk=None), 1), (dict(sk=None), 1), (dict(Hq=15), 1), (dict(d=80), 2), (dict(S=17, t=2), 2),
     (dict(Hq=258, Hkv=2), 2), (dict(maxP=0, t=0), 1), (dict(W=0), 1), (dict(out=FAKE + 16), 1),
+    (dict(scale=0.0), 1), (dict(scale=-1.0), 1), (dict(scale=float("inf")), 1),
     (dict(R=0, q=None), 0),
 ])
 def test_decode_host_validation(lib, kw, expect):
