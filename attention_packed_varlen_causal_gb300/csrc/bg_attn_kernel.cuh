@@ -101,9 +101,9 @@ struct AttnCfg {
     static constexpr int kOffStage = kOffV + NV * kTileBytes;     // 2 KB per softmax warp
     static constexpr int kStageBytes = 32 * 64;
     static constexpr int kOffBar = kOffStage + 4 * NH * kStageBytes;
-    // q_full[2] q_empty[2] mma_final k_full[NK] k_empty[NK] v_full[NV] s_full[NH][NS] p_full[NH][NS]
-    // pv_done[NH][NS]
-    static constexpr int kNumBars = 5 + 2 * NK + NV + 3 * NS * NH;
+    // q_full[2] q_empty[2] mma_final k_full[NK] k_empty[NK] v_full[NV] v_empty[NV] s_full[NH][NS]
+    // p_full[NH][NS] pv_done[NH][NS]
+    static constexpr int kNumBars = 5 + 2 * NK + 2 * NV + 3 * NS * NH;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + slack for 1024-byte alignment
     static constexpr int kThreads = 128 * (1 + NH);
@@ -112,10 +112,7 @@ struct AttnCfg {
     static constexpr int kTmemCols = kColsUsed <= 128 ? 128 : kColsUsed <= 256 ? 256 : 512;
     static_assert(kColsUsed <= 512, "TMEM overflow");
     static_assert(kSmemBytes <= 232448, "shared memory overflow");
-    // V: two stages.  A V stage is released by the completion of the P.V two tiles back on
-    // the per-S-buffer P.V barrier; that parity wait is unambiguous while NS >= NV (the
-    // completion after it on the same barrier needs a V tile this producer has not loaded).
-    static_assert(NK >= 2 && NV == 2 && NS >= NV && NS <= 3, "ring / buffer counts");
+    static_assert(NK >= 2 && NV >= 2 && NS >= 2 && NS <= 3, "ring / buffer counts");
     // TMEM column of S buffer b of query tile h
     static __device__ __forceinline__ uint32_t col_s(int h, int b) { return static_cast<uint32_t>(64 * (NS * h + b)); }
 };
@@ -265,7 +262,8 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
     uint64_t *k_full = bars + 5;            // [NK]
     uint64_t *k_empty = k_full + NK;        // [NK]
     uint64_t *v_full = k_empty + NK;        // [NV]
-    uint64_t *s_full = v_full + NV;         // [NH][NS]
+    uint64_t *v_empty = v_full + NV;        // [NV]
+    uint64_t *s_full = v_empty + NV;        // [NH][NS]
     uint64_t *p_full = s_full + NS * NH;    // [NH][NS]
     // pv_done[h][b] completes when P.V of a tile stored in S buffer b is done.
     // One barrier per buffer (not per head): every wait on it is then for
@@ -295,7 +293,10 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
             mbar_init(&k_full[s], 1);
             mbar_init(&k_empty[s], NH);   // one arrive per softmax warpgroup
         }
-        for (int s = 0; s < NV; ++s) mbar_init(&v_full[s], 1);
+        for (int s = 0; s < NV; ++s) {
+            mbar_init(&v_full[s], 1);
+            mbar_init(&v_empty[s], NH);   // one arrive per softmax warpgroup
+        }
         for (int i = 0; i < NS * NH; ++i) {
             mbar_init(&s_full[i], 1);
             mbar_init(&p_full[i], 128);
@@ -409,15 +410,8 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
         uint32_t n_v = 0;
         while (w.valid) {
             const int st = n_v % NV;
-            if (n_v >= NV) {
-                // stage st held V of tile n_v - 2: free once that tile's P.V completed everywhere
-                bool free_ok = true;
-#pragma unroll
-                for (int h = 0; h < NH; ++h)
-                    if (free_ok && !warp_wait(&pv_done[NS * h + (n_v - NV) % NS], ((n_v - NV) / NS) & 1, abort_flag))
-                        free_ok = false;
-                if (!free_ok) break;
-            }
+            const uint32_t use = n_v / NV;
+            if (use > 0 && !warp_wait(&v_empty[st], (use - 1) & 1, abort_flag)) break;
             uint8_t *vdst = smem + C::kOffV + st * C::kTileBytes;
             if (MODE == Mode::Prefill || w.j < w.I.n_prompt) {
                 const int row = w.I.kv_row0 + w.j * kKeys;
@@ -649,7 +643,12 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
                 if (!warp_wait(&s_full[NS * h + g % NS], (g / NS) & 1, abort_flag)) { ok = false; break; }
                 tc_fence_after();
                 // this tile's QK has completed: its K stage can be reloaded (one arrive per warpgroup)
-                if (quad == 0 && lane == 0) mbar_arrive(&k_empty[g % NK]);
+                // ... and so has every MMA its warp issued before that QK, which includes the P.V of
+                // tile g - NS: that V stage can be reloaded too
+                if (quad == 0 && lane == 0) {
+                    mbar_arrive(&k_empty[g % NK]);
+                    if (g >= NS) mbar_arrive(&v_empty[(g - NS) % NV]);
+                }
                 if (lim_hi <= 0) {
                     // every row of this warp is masked for this tile: P = 0
                     uint32_t zr[16];

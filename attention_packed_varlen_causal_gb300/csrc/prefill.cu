@@ -115,8 +115,8 @@ int prefill_heads_per_cta() { return kNH; }
 cudaError_t launch_prefill_attn(int head_dim, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
                                 const CUtensorMap &tm_v, const AttnParams &p, int grid, cudaStream_t stream)
 {
-    if (head_dim == 128) return launch_one<128, 3, 2, 2>(tm_q, tm_k, tm_v, p, grid, stream);
-    if (head_dim == 64) return launch_one<64, 4, 2, 3>(tm_q, tm_k, tm_v, p, grid, stream);
+    if (head_dim == 128) return launch_one<128, 2, 3, 2>(tm_q, tm_k, tm_v, p, grid, stream);
+    if (head_dim == 64) return launch_one<64, 4, 4, 3>(tm_q, tm_k, tm_v, p, grid, stream);
     return cudaErrorInvalidValue;
 }
 
