@@ -42,6 +42,26 @@ from attention_packed_varlen_causal_gb300 import workloads as wl  # noqa: E402
 METRIC = "packed-prefill attn TFLOP/s (% bf16 peak); beam-decode attn µs/step (% roofline)"
 LAYERS = 28
 
+# DRAM bytes of one attn_kernel<Prefill,128> launch on one layer of the Prefill-Only batch
+# (dram__bytes_read.sum + dram__bytes_write.sum from one ncu capture, written up in
+# profiles/attn_kernel_prefill_prefill_only.md).  It holds only for the kernel sources it was
+# taken on, identified by `sources`; for any other sources the bench reports null.
+PREFILL_TRAFFIC = {"sources": "a396f4cb82619a53", "bytes": 650542080 + 249124352}
+
+
+def kernel_sources_hash():
+    import glob
+    import hashlib
+    pkg = os.path.join(ROOT, "attention_packed_varlen_causal_gb300")
+    files = sorted(glob.glob(os.path.join(pkg, "csrc", "*.cu")) + glob.glob(os.path.join(pkg, "csrc", "*.cuh")) +
+                   glob.glob(os.path.join(pkg, "csrc", "*.h")) + glob.glob(os.path.join(ROOT, "include", "*.h")))
+    h = hashlib.sha256()
+    for f in files:
+        h.update(os.path.basename(f).encode())
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
 
 # --------------------------------------------------------------------------- work accounting
 def prefill_flops(lengths, Hq, d):
@@ -378,8 +398,12 @@ def run_ours(args):
                "seconds": round(dt, 2)}
 
     achieved = pre.bytes / avg_call_s / 1e9
+    traffic = args.traffic
+    if traffic is None and kernel_sources_hash() == PREFILL_TRAFFIC["sources"]:
+        traffic = PREFILL_TRAFFIC["bytes"]
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": args.traffic,
+                "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
+                "algorithmic_bytes_per_launch": pre.bytes,
                 "kernel": "bg_packed_prefill_attn (work-list pre-pass + attn_kernel<Prefill,128>)",
                 "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs, burst copy)",
                 "tensor_frac_of_bf16_peak": round(pre.flops / avg_call_s / 1e12 / peaks["bf16_tflops"], 4)}
