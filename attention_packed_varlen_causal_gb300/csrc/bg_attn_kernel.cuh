@@ -570,7 +570,7 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
                     for (int i = 0; i < 4; ++i) {
                         const int rr = i * 8 + (lane >> 2);
                         const uint4 val = *reinterpret_cast<const uint4 *>(stage + rr * 64 + ((cc ^ ((rr >> 1) & 3)) * 16));
-                        if (dst[i]) reinterpret_cast<uint4 *>(dst[i] + 32 * c)[cc] = val;
+                        if (dst[i]) __stcs(reinterpret_cast<uint4 *>(dst[i] + 32 * c) + cc, val);   // streamed: never re-read
                     }
                 };
                 const float inv_l = 1.f / l;
