@@ -520,7 +520,9 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
         // MMAs too), normalise O and store it.  It runs after the NEXT item's first tile has
         // been turned into P (which reads no O), so the wait for the last P.V overlaps that
         // work; the next item's first P.V, which overwrites O, is released only after this.
-        auto epilogue = [&](const Item &I, float m, float l, uint32_t g_last) -> bool {
+        // `release` runs once O is in registers: the caller lets the next P.V overwrite O from
+        // then on, while the stores below still run.
+        auto epilogue = [&](const Item &I, float m, float l, uint32_t g_last, auto &&release) -> bool {
                 // The commit after the item's last P.V covers every earlier MMA too.  (Items always
                 // have tiles here; the test stays because ptxas allocates the prefill kernel's
                 // registers with fewer spills with it: 235 vs 297 us on the Prefill-Only batch.)
@@ -574,12 +576,23 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
                     }
                 };
                 const float inv_l = 1.f / l;
+                if constexpr (D <= 64) {
+                    // all of O fits in registers: hand O back before the stores
+                    float o[D];
+                    tmem_ld64(tO, o);
+                    release();
 #pragma unroll
-                for (int c = 0; c < D / 64; ++c) {
-                    float o[64];
-                    tmem_ld64(tO + 64 * c, o);
-                    put_chunk(2 * c, o, inv_l);
-                    put_chunk(2 * c + 1, o + 32, inv_l);
+                    for (int c = 0; c < D / 32; ++c) put_chunk(c, o + 32 * c, inv_l);
+                } else {
+                    // 64 columns at a time (register budget), O handed back at the end
+#pragma unroll
+                    for (int c = 0; c < D / 64; ++c) {
+                        float o[64];
+                        tmem_ld64(tO + 64 * c, o);
+                        put_chunk(2 * c, o, inv_l);
+                        put_chunk(2 * c + 1, o + 32, inv_l);
+                    }
+                    release();
                 }
                 if constexpr (MODE == Mode::Prefill) {
                     if (p.lse) {
@@ -730,11 +743,18 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
                 tmem_st_wait();
                 tc_fence_before();
                 if (j == 0 && pend) {
-                    if (!epilogue(Ip, mp, lp, gp)) { ok = false; break; }
+                    // the previous item's O is read before this tile's P.V may overwrite it
+                    if (!epilogue(Ip, mp, lp, gp, [&]() {
+                            tc_fence_before();
+                            mbar_arrive(&p_full[NS * h + g % NS]);
+                        })) {
+                        ok = false;
+                        break;
+                    }
                     pend = false;
-                    tc_fence_before();
+                } else {
+                    mbar_arrive(&p_full[NS * h + g % NS]);
                 }
-                mbar_arrive(&p_full[NS * h + g % NS]);
             }
             if (!ok) break;
             pend = true;
@@ -743,7 +763,7 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
             lp = l;
             gp = g - 1;
         }
-        if (ok && pend) ok = epilogue(Ip, mp, lp, gp);
+        if (ok && pend) ok = epilogue(Ip, mp, lp, gp, []() {});
 
         (void)ok;
     }
