@@ -553,19 +553,13 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
                 __nv_bfloat16 *dst[4];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) dst[i] = row_dst(quad * 32 + i * 8 + (lane >> 2));
-                auto put_chunk = [&](int c, const float *o, float inv_l) {
-                    uint4 wv[4];
-                    uint32_t *wp = reinterpret_cast<uint32_t *>(wv);
-                    const float2 il = make_float2(inv_l, inv_l);
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const float2 x = fmul2(make_float2(o[2 * i], o[2 * i + 1]), il);
-                        wp[i] = pack_bf16x2(x.x, x.y);
-                    }
+                // row's 32 bf16 of chunk c (16 packed pairs) -> staging -> coalesced stores
+                auto put_chunk = [&](int c, const uint32_t *wp) {
                     __syncwarp();                       // the previous chunk's reads are done
 #pragma unroll
                     for (int u = 0; u < 4; ++u)
-                        *reinterpret_cast<uint4 *>(stage + lane * 64 + ((u ^ ((lane >> 1) & 3)) * 16)) = wv[u];
+                        *reinterpret_cast<uint4 *>(stage + lane * 64 + ((u ^ ((lane >> 1) & 3)) * 16)) =
+                            make_uint4(wp[4 * u], wp[4 * u + 1], wp[4 * u + 2], wp[4 * u + 3]);
                     __syncwarp();
                     const int cc = lane & 3;
 #pragma unroll
@@ -575,25 +569,24 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
                         if (dst[i]) __stcs(reinterpret_cast<uint4 *>(dst[i] + 32 * c) + cc, val);   // streamed: never re-read
                     }
                 };
+                // O is read 64 columns at a time, normalised and packed to bf16 pairs (half the
+                // registers), and handed back to the next item's P.V before the stores
                 const float inv_l = 1.f / l;
-                if constexpr (D <= 64) {
-                    // all of O fits in registers: hand O back before the stores
-                    float o[D];
-                    tmem_ld64(tO, o);
-                    release();
+                const float2 il = make_float2(inv_l, inv_l);
+                uint32_t pk[D / 2];
 #pragma unroll
-                    for (int c = 0; c < D / 32; ++c) put_chunk(c, o + 32 * c, inv_l);
-                } else {
-                    // 64 columns at a time (register budget), O handed back at the end
+                for (int c2 = 0; c2 < D / 64; ++c2) {
+                    float o[64];
+                    tmem_ld64(tO + 64 * c2, o);
 #pragma unroll
-                    for (int c = 0; c < D / 64; ++c) {
-                        float o[64];
-                        tmem_ld64(tO + 64 * c, o);
-                        put_chunk(2 * c, o, inv_l);
-                        put_chunk(2 * c + 1, o + 32, inv_l);
+                    for (int i = 0; i < 32; ++i) {
+                        const float2 x = fmul2(make_float2(o[2 * i], o[2 * i + 1]), il);
+                        pk[32 * c2 + i] = pack_bf16x2(x.x, x.y);
                     }
-                    release();
                 }
+                release();
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) put_chunk(c, pk + 16 * c);
                 if constexpr (MODE == Mode::Prefill) {
                     if (p.lse) {
                         if (row_dst(row)) {
