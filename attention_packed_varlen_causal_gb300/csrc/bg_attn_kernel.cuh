@@ -21,14 +21,16 @@
 //               warpgroup once it has seen its S of that tile (so the QK
 //               that read the stage has completed; no extra tcgen05.commit),
 //               a Q buffer after the item's last QK.
-//   warp 2      TMA producer of V: V tiles through a two-stage ring, reloaded
-//               once their P.V completed (seen on the P.V barriers).  Each
-//               extra tcgen05.commit costs the MMA warps ~160 cycles, so
-//               stage release piggybacks on barriers that exist anyway.
+//   warp 2      TMA producer of V: V tiles through an NV-stage ring.  A V stage
+//               is released by the softmax warpgroups' same arrive, NS tiles
+//               later: S of tile t complete implies every MMA issued before
+//               that QK, the P.V of tile t-NS included, has completed.  Each
+//               extra tcgen05.commit costs the MMA warps ~160 cycles, so stage
+//               release piggybacks on barriers that exist anyway.
 //   warps 1, 3  tcgen05.mma issuers, one per query tile h (warp 1 also
 //               allocates TMEM).  For every key tile t the warp of tile h
-//               issues S_h(t) = Q_h K(t)^T into one of TWO S buffers of
-//               tile h, one tile ahead of O_h += P_h(t-1) V,
+//               issues S_h(t) = Q_h K(t)^T into one of NS S buffers of
+//               tile h, NS-1 tiles ahead of O_h += P_h(t-NS+1) V,
 //               so the tensor cores compute the next scores while the softmax
 //               warps work on the current ones; the lookahead also crosses
 //               item boundaries.  P is read from TMEM (written there by the
@@ -36,12 +38,14 @@
 //   warps 4..   NH softmax warpgroups; thread t of group h owns query row t of
 //               tile h (TMEM lane t): masked running max in base-2 units,
 //               lazy rescaling of O (only when the max grows by > 2^8),
-//               exp2 on the SFU, bf16 P back to TMEM; epilogue normalisation,
-//               32 columns at a time
-//               through a 2 KB per-warp staging area, so that each bf16 store
-//               instruction writes 64-byte row segments of 8 rows.
+//               exp2 on the SFU, bf16 P back to TMEM.  Epilogue (deferred to
+//               after the next item's first tile): O read from TMEM,
+//               normalised and packed to bf16 in registers, the buffer handed
+//               back to the next P.V, then stored 32 columns at a time through a
+//               2 KB per-warp staging area, so that each store instruction
+//               writes 64-byte row segments of 8 rows.
 //               Warps whose 32 rows are all masked for a key tile skip it.
-// TMEM columns: S(h,b) at 64*(2h+b), O_h at 128*NH + D*h.
+// TMEM columns: S(h,b) at 64*(NS*h+b), O_h at 64*NS*NH + D*h.
 // Ordering: the MMA warp issues ... QK(t+1), PV(t), QK(t+2), PV(t+1) ... from
 // one thread, and tcgen05.mma executes in issue order, so QK(t+2) may be
 // issued right after PV(t) although it overwrites the S buffer PV(t) reads P

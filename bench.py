@@ -46,7 +46,7 @@ LAYERS = 28
 # (dram__bytes_read.sum + dram__bytes_write.sum from one ncu capture, written up in
 # profiles/attn_kernel_prefill_prefill_only.md).  It holds only for the kernel sources it was
 # taken on, identified by `sources`; for any other sources the bench reports null.
-PREFILL_TRAFFIC = {"sources": "997b0a29465c2a28", "bytes": 649622528 + 244686080}
+PREFILL_TRAFFIC = {"sources": "e7f2b68cff50cf36", "bytes": 649622528 + 244686080}
 
 
 def kernel_sources_hash():
