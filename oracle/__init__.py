@@ -71,6 +71,8 @@ def _load():
             i32 = ctypes.c_int32
             lib.oracle_prefill.argtypes = [P, P, P, P, i32, i32, i32, i32, ctypes.c_double, P, P]
             lib.oracle_prefill.restype = ctypes.c_int
+            lib.oracle_last_token.argtypes = [P, P, P, P, i32, i32, i32, i32, ctypes.c_double, P, P]
+            lib.oracle_last_token.restype = ctypes.c_int
             lib.oracle_decode.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i32, i32,
                                           ctypes.c_double, P, P]
             lib.oracle_decode.restype = ctypes.c_int
@@ -112,6 +114,27 @@ def prefill(q, k, v, cu_seqlens, scale: float, want_lse: bool = False):
                                 float(scale), _ptr(out), _ptr(lse))
     if rc != 0:
         raise ValueError(f"oracle_prefill rejected its arguments (rc={rc})")
+    return (out, lse) if want_lse else out
+
+
+def last_token(q, k, v, cu_seqlens, scale: float, want_lse: bool = False):
+    """Attention of each sequence's last valid token over its own keys, in fp64.
+
+    q: uint16 [B,Hq,d] (the last row of each sequence); k, v: uint16 [T,Hkv,d];
+    cu_seqlens: int32 [B+1].  Returns float64 [B,Hq,d] (rows of zero-length
+    sequences stay 0) and lse float64 [B,Hq] if want_lse."""
+    q, k, v = _u16(q), _u16(k), _u16(v)
+    cu = np.ascontiguousarray(cu_seqlens, dtype=np.int32)
+    B, Hq, d = q.shape
+    T, Hkv = k.shape[0], k.shape[1]
+    if len(cu) != B + 1 or k.shape != (T, Hkv, d) or v.shape != (T, Hkv, d) or int(cu[-1]) != T:
+        raise ValueError("shape mismatch")
+    out = np.zeros((B, Hq, d), dtype=np.float64)
+    lse = np.zeros((B, Hq), dtype=np.float64) if want_lse else None
+    rc = _load().oracle_last_token(_ptr(q), _ptr(k), _ptr(v), _ptr(cu), B, Hq, Hkv, d, float(scale), _ptr(out),
+                                   _ptr(lse))
+    if rc != 0:
+        raise ValueError(f"oracle_last_token rejected its arguments (rc={rc})")
     return (out, lse) if want_lse else out
 
 

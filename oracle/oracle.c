@@ -142,6 +142,66 @@ int oracle_prefill(const uint16_t *q, const uint16_t *k, const uint16_t *v,
 }
 
 /*
+ * Attention of each sequence's last valid token only (abstract and section
+ * 1.1: a Prefill-Only request needs the next-token logits at the last valid
+ * position of each sequence, so the last layer's attention is needed for that
+ * one row): for sequence i of length L >= 1 and query head h,
+ *   out[i, h] = softmax(scale q[i, h] . k_j) v_j  over the sequence's L keys,
+ * i.e. row L-1 of the causal prefill.  Zero-length sequences write nothing.
+ *
+ *   q   : bf16 [B, Hq, d]   the last row of each sequence
+ *   k, v: bf16 [T, Hkv, d]  packed by cu (int32 [B+1], cu[0] = 0, non-decreasing)
+ *   out : double [B, Hq, d]  lse : double [B, Hq] or NULL
+ */
+int oracle_last_token(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                      const int32_t *cu, int32_t B, int32_t Hq, int32_t Hkv,
+                      int32_t d, double scale, double *out, double *lse)
+{
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || Hq % Hkv != 0) return -1;
+    if (B > 0 && cu[0] != 0) return -1;
+    int64_t maxlen = 0;
+    for (int32_t i = 0; i < B; ++i) {
+        if (cu[i + 1] < cu[i]) return -1;
+        if (cu[i + 1] - cu[i] > maxlen) maxlen = cu[i + 1] - cu[i];
+    }
+    const int32_t g = Hq / Hkv;
+    const int64_t pairs = (int64_t)B * Hq;
+    int err = 0;
+
+#pragma omp parallel
+    {
+        const size_t n = (size_t)(maxlen > 0 ? maxlen : 1);
+        double *z = (double *)malloc(sizeof(double) * n);
+        const uint16_t **keys = (const uint16_t **)malloc(sizeof(void *) * n);
+        const uint16_t **vals = (const uint16_t **)malloc(sizeof(void *) * n);
+        if (!z || !keys || !vals) {
+#pragma omp atomic write
+            err = 1;
+        } else {
+#pragma omp for schedule(dynamic, 1)
+            for (int64_t w = 0; w < pairs; ++w) {
+                const int32_t i = (int32_t)(w / Hq);
+                const int32_t h = (int32_t)(w % Hq);
+                const int32_t kh = h / g;
+                const int64_t s0 = cu[i];
+                const int64_t L = (int64_t)cu[i + 1] - s0;
+                if (L == 0) continue;
+                for (int64_t j = 0; j < L; ++j) {
+                    keys[j] = k + ((s0 + j) * Hkv + kh) * d;
+                    vals[j] = v + ((s0 + j) * Hkv + kh) * d;
+                }
+                attend_row(q + ((int64_t)i * Hq + h) * d, keys, vals, L, d, scale, z,
+                           out + ((int64_t)i * Hq + h) * d, lse ? lse + (int64_t)i * Hq + h : NULL);
+            }
+        }
+        free(z);
+        free((void *)keys);
+        free((void *)vals);
+    }
+    return err ? -2 : 0;
+}
+
+/*
  * Beam-search decode attention over a shared prompt K/V and per-beam
  * suffixes (section 1.2: the beams of one request share a single prompt
  * K/V, each beam keeps its own short suffix K/V).

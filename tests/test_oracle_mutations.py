@@ -21,6 +21,9 @@ MUTATIONS = [
     ("sequence offset ignored", "const int64_t s0 = cu[i];", "const int64_t s0 = cu[i] > 0 ? cu[i] - 1 : 0;"),
     ("decode prompt offset ignored", "keys[j] = pk + ((p0 + j) * Hkv + kh) * d;", "keys[j] = pk + ((j) * Hkv + kh) * d;"),
     ("decode suffix order lost", "keys[P + s] = hk + ((rb * t + s) * Hkv + kh) * d;", "keys[P + s] = hk + ((rb * t + 0) * Hkv + kh) * d;"),
+    ("last token drops its own key", "keys, vals, L, d, scale, z,", "keys, vals, (L > 1 ? L - 1 : 1), d, scale, z,"),
+    ("last token reads the wrong query head", "attend_row(q + ((int64_t)i * Hq + h) * d,",
+     "attend_row(q + ((int64_t)i * Hq + (h ^ 1)) * d,"),
     ("decode prompt dropped", "attend_row(q + (rb * Hq + h) * d, keys, vals, P + t,", "attend_row(q + (rb * Hq + h) * d, keys + P, vals + P, t > 0 ? t : P,"),
 ]
 

@@ -11,6 +11,7 @@ Mistake -> test that catches it
   softmax not normalised ........... test_one_hot_v_weights_log_ratio (rows sum to 1)
   decode ignores prompt / suffix ... test_decode_equals_full_kv, test_decode_equals_last_prefill_row
   reorder gathers the wrong beam ... test_history_follows_parent_chain, test_history_composition
+  last token off by one or head .... test_last_token_equals_last_padded_row, test_last_token_closed_forms
 """
 import json
 import math
@@ -351,3 +352,55 @@ def test_history_identity_and_composition():
         np.testing.assert_array_equal(k2[r], k0[r][comp[r]])
     with pytest.raises(ValueError):
         h.step(np.full((R, W), W))
+
+
+# ---------------------------------------------------------------- last valid token
+def _last_rows(q_full, cu):
+    """The query row of each sequence's last valid token (row 0 for an empty one)."""
+    idx = [max(int(cu[i + 1]) - 1, int(cu[i])) for i in range(len(cu) - 1)]
+    return np.ascontiguousarray(q_full[np.minimum(idx, max(q_full.shape[0] - 1, 0))])
+
+
+def test_last_token_equals_last_padded_row():
+    """The last-token op is the last row of the causal prefill: checked against the
+    independent padded + masked numpy formulation, with an empty sequence in the batch."""
+    lengths = [1, 2, 17, 64, 0, 100, 3]
+    x = rand_prefill(lengths, 4, 2, 32, seed=61)
+    cu = x["cu_seqlens"]
+    scale = 1 / math.sqrt(32)
+    full = oracle_np.prefill_padded(x["q"], x["k"], x["v"], cu, scale)
+    out = oracle.last_token(_last_rows(x["q"], cu), x["k"], x["v"], cu, scale)
+    for i, L in enumerate(lengths):
+        if L == 0:
+            assert np.all(out[i] == 0)               # an empty sequence writes nothing
+        else:
+            assert np.max(np.abs(out[i] - full[int(cu[i + 1]) - 1])) < 1e-12
+
+
+def test_last_token_closed_forms():
+    # one key: the output is that key's value row, per query head through its kv head
+    x = rand_prefill([1, 1], 4, 2, 16, seed=71)
+    out = oracle.last_token(x["q"], x["k"], x["v"], x["cu_seqlens"], 0.25)
+    kv = widen(x["v"])
+    for h in range(4):
+        np.testing.assert_array_equal(out[:, h, :], kv[:, h // 2, :])
+    # two keys: the logistic weight of the larger logit, and its lse
+    fx = json.load(open(os.path.join(GOLDEN, "closed_form_fixtures.json")))["two_keys"]
+    d = fx["head_dim"]
+    scale = 1.0 / math.sqrt(d)
+    q = bits(np.array([[fx["q"]]], dtype=np.float32))
+    k = bits(np.array([[fx["k0"]], [fx["k1"]]], dtype=np.float32))
+    v = bits(np.array([[fx["v0"]], [fx["v1"]]], dtype=np.float32))
+    out, lse = oracle.last_token(q, k, v, np.array([0, 2], np.int32), scale, want_lse=True)
+    z0 = scale * (fx["q"][0] * fx["k0"][0] + fx["q"][1] * fx["k0"][1])
+    z1 = scale * (fx["q"][0] * fx["k1"][0] + fx["q"][1] * fx["k1"][1])
+    w1 = 1.0 / (1.0 + math.exp(z0 - z1))
+    for c in range(d):
+        assert abs(out[0, 0, c] - ((1 - w1) * fx["v0"][c] + w1 * fx["v1"][c])) < 1e-15
+    assert abs(lse[0, 0] - (max(z0, z1) + math.log1p(math.exp(-abs(z0 - z1))))) < 1e-15
+    # constant values: every head returns them
+    y = rand_prefill([5, 9], 4, 2, 8, seed=81)
+    c = np.linspace(-3, 3, 8, dtype=np.float32)
+    out = oracle.last_token(_last_rows(y["q"], y["cu_seqlens"]), y["k"], bits(np.broadcast_to(c, y["v"].shape)),
+                            y["cu_seqlens"], 1 / math.sqrt(8))
+    assert np.max(np.abs(out - widen(bits(c))[None, None, :])) < 1e-14
