@@ -39,6 +39,8 @@ SIGNATURES = {
                                ctypes.c_int),
     "bg_packed_prefill_attn_noalloc": ([_P, _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32, _F32, _P, _P, _P, _P],
                                        ctypes.c_int),
+    "bg_packed_last_token_attn": ([_P, _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32, _F32, _P, _P, _P, _P],
+                                  ctypes.c_int),
     "bg_beam_decode_attn": ([_P, _P, _P, _P, _I32, _I32, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _F32, _P,
                              _P, _P], ctypes.c_int),
     "bg_beam_suffix_reorder": ([_P, _P, _P, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32, _P, _P],
@@ -143,6 +145,21 @@ def bg_packed_prefill_attn_noalloc(q, k, v, cu_seqlens, max_seqlen: int, out, *,
                                                Hkv, d, float(scale), _ptr(out), _ptr(lse), _ptr(dev_status),
                                                _stream(stream))
     _check("bg_packed_prefill_attn_noalloc", st)
+    return out
+
+
+def bg_packed_last_token_attn(q, k, v, cu_seqlens, max_seqlen: int, out, *, lse=None,
+                              scale: Optional[float] = None, dev_status=None, stream=None):
+    """q [B,Hq,d] (each sequence's last valid row); k, v [T,Hkv,d]; cu_seqlens
+    int32 [B+1]; out [B,Hq,d] (written); lse fp32 [B,Hq] or None."""
+    B, Hq, d = q.shape
+    T, Hkv = k.shape[0], k.shape[1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    st = load().bg_packed_last_token_attn(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), B, T, int(max_seqlen), Hq,
+                                          Hkv, d, float(scale), _ptr(out), _ptr(lse), _ptr(dev_status),
+                                          _stream(stream))
+    _check("bg_packed_last_token_attn", st)
     return out
 
 

@@ -189,6 +189,36 @@ bg_status_t bg_packed_prefill_attn(const void *q, const void *k, const void *v, 
     return BG_OK;
 }
 
+bg_status_t bg_packed_last_token_attn(const void *q, const void *k, const void *v, const int32_t *cu_seqlens,
+                                      int32_t num_seqs, int32_t total_tokens, int32_t max_seqlen, int32_t Hq,
+                                      int32_t Hkv, int32_t head_dim, float scale, void *out, float *lse,
+                                      int32_t *dev_status, cudaStream_t stream)
+{
+    if (num_seqs < 0 || total_tokens < 0 || max_seqlen < 0 || Hq <= 0 || Hkv <= 0 || head_dim <= 0)
+        return BG_ERR_INVALID_ARG;
+    if (Hq % Hkv != 0) return BG_ERR_INVALID_ARG;
+    if (!std::isfinite(scale) || !(scale > 0.f)) return BG_ERR_INVALID_ARG;
+    if (!supported_head_dim(head_dim) || max_seqlen > BG_MAX_SEQLEN || Hq / Hkv > last_token_max_group())
+        return BG_ERR_UNSUPPORTED;
+    if (num_seqs == 0) return BG_OK;
+    if (!q || !k || !v || !cu_seqlens || !out) return BG_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) || !aligned(cu_seqlens, 4) ||
+        (lse && !aligned(lse, 4)) || (dev_status && !aligned(dev_status, 4)))
+        return BG_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(num_seqs) * Hkv >= (int64_t(1) << 31)) return BG_ERR_UNSUPPORTED;
+    const size_t obytes = static_cast<size_t>(num_seqs) * Hq * head_dim * 2;
+    const size_t kvbytes = static_cast<size_t>(total_tokens) * Hkv * head_dim * 2;
+    const size_t lsebytes = lse ? static_cast<size_t>(num_seqs) * Hq * 4 : 0;
+    if (overlap(out, obytes, q, obytes) || overlap(out, obytes, k, kvbytes) || overlap(out, obytes, v, kvbytes) ||
+        overlap(lse, lsebytes, out, obytes) || overlap(lse, lsebytes, q, obytes) || overlap(lse, lsebytes, k, kvbytes) ||
+        overlap(lse, lsebytes, v, kvbytes))
+        return BG_ERR_INVALID_ARG;
+    if (launch_last_token_attn(head_dim, q, k, v, cu_seqlens, num_seqs, total_tokens, max_seqlen, Hq, Hkv, scale, out,
+                               lse, dev_status, stream) != cudaSuccess)
+        return BG_ERR_CUDA;
+    return BG_OK;
+}
+
 bg_status_t bg_beam_decode_attn(const void *q, const void *prompt_k, const void *prompt_v, const int32_t *cu_prompt,
                                 int32_t total_prompt_tokens, int32_t max_prompt_len, const void *suffix_k,
                                 const void *suffix_v, int32_t suffix_len, int32_t suffix_max, int32_t R, int32_t W,

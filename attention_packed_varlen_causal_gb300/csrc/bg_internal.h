@@ -28,6 +28,12 @@ cudaError_t launch_decode_attn(int head_dim, const CUtensorMap &tm_q, const CUte
                                const AttnParams &p, int grid, cudaStream_t stream);
 int decode_tiles_per_cta();
 
+// Attention of each sequence's last valid token (one CTA per sequence and kv head).
+cudaError_t launch_last_token_attn(int head_dim, const void *q, const void *k, const void *v, const int32_t *cu,
+                                   int32_t B, int32_t T, int32_t max_seqlen, int32_t Hq, int32_t Hkv, float scale,
+                                   void *out, float *lse, int32_t *dev_status, cudaStream_t stream);
+int last_token_max_group();
+
 cudaError_t launch_suffix_reorder(const void *src_k, const void *src_v, void *dst_k, void *dst_v,
                                   const int32_t *parent_idx, const void *new_k, const void *new_v, int32_t R,
                                   int32_t W, int32_t suffix_max, int32_t n_tokens, int32_t Hkv, int32_t head_dim,

@@ -115,6 +115,35 @@ bg_status_t bg_packed_prefill_attn(const void *q, const void *k, const void *v,
                                    int32_t *dev_status, cudaStream_t stream);
 
 /*
+ * Attention of each packed sequence's last valid token only, for the last
+ * layer of a Prefill-Only request.  Source: abstract and section 1.1 of the
+ * page above (the request is answered from the next-token logits at each
+ * sequence's last valid position).  For sequence i of length L >= 1 and
+ * query head h (kvh = h / (Hq/Hkv)):
+ *     out[i, h] = sum_{j<L} softmax_j(scale * q[i, h] . k[cu[i]+j, kvh]) v[cu[i]+j, kvh]
+ * i.e. row L-1 of bg_packed_prefill_attn, at O(L) instead of O(L^2) cost: it
+ * reads each sequence's K and V once per kv head (bandwidth-bound).
+ *
+ *   q            bf16 [num_seqs, Hq, head_dim]: the last valid row of each
+ *                sequence (any values for zero-length sequences)
+ *   k, v         bf16 [total_tokens, Hkv, head_dim], packed by cu_seqlens
+ *   cu_seqlens   int32 [num_seqs+1], device (as for bg_packed_prefill_attn;
+ *                checked on device, bad sequences skipped with
+ *                BG_DEVSTAT_CU_SEQLENS)
+ *   out          bf16 [num_seqs, Hq, head_dim]; rows of zero-length
+ *                sequences are not written
+ *   lse          fp32 [num_seqs, Hq] natural-log sum-exp, or NULL
+ * Errors: as bg_packed_prefill_attn (no workspace);
+ * BG_ERR_UNSUPPORTED also for Hq/Hkv > 16.
+ */
+bg_status_t bg_packed_last_token_attn(const void *q, const void *k, const void *v,
+                                      const int32_t *cu_seqlens, int32_t num_seqs,
+                                      int32_t total_tokens, int32_t max_seqlen,
+                                      int32_t Hq, int32_t Hkv, int32_t head_dim, float scale,
+                                      void *out, float *lse,
+                                      int32_t *dev_status, cudaStream_t stream);
+
+/*
  * Beam-search decode attention over a shared prompt K/V plus each beam's own
  * suffix K/V.
  * Source: section 1.2 (the beams of a request share one prompt K/V, each

@@ -73,6 +73,24 @@ def test_prefill_host_validation(lib, kw, expect):
     assert prefill(lib, **kw) == expect
 
 
+def last_token(lib, **kw):
+    a = dict(q=FAKE, k=FAKE * 2, v=FAKE * 3, cu=FAKE * 4, B=2, T=10, maxlen=8, Hq=4, Hkv=2, d=64, scale=0.125,
+             out=FAKE * 5, lse=None, st=None, stream=None)
+    a.update(kw)
+    return lib.bg_packed_last_token_attn(a["q"], a["k"], a["v"], a["cu"], a["B"], a["T"], a["maxlen"], a["Hq"],
+                                         a["Hkv"], a["d"], a["scale"], a["out"], a["lse"], a["st"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(q=None), 1), (dict(k=None), 1), (dict(cu=None), 1), (dict(out=None), 1), (dict(Hq=6, Hkv=4), 1),
+    (dict(d=96), 2), (dict(maxlen=70000), 2), (dict(Hq=34, Hkv=2), 2), (dict(q=FAKE + 8), 1),
+    (dict(out=FAKE * 2), 1), (dict(lse=FAKE * 5 + 4), 1), (dict(scale=0.0), 1), (dict(B=-1), 1),
+    (dict(B=0, q=None), 0),
+])
+def test_last_token_host_validation(lib, kw, expect):
+    assert last_token(lib, **kw) == expect
+
+
 def decode(lib, **kw):
     a = dict(q=FAKE, pk=FAKE * 2, pv=FAKE * 3, cu=FAKE * 4, P=100, maxP=60, sk=FAKE * 8, sv=FAKE * 16, t=2, S=4,
              R=2, W=5, Hq=14, Hkv=2, d=64, scale=0.125, out=FAKE * 32, st=None, stream=None)
