@@ -9,20 +9,21 @@
 // so it runs on the CUDA cores, not the tensor cores.
 //
 // One CTA (256 threads, 8 warps) per (sequence, kv head) serves the g query
-// heads of that kv head, over chunks of 256 keys with an online softmax in fp32:
+// heads of that kv head, over chunks of 128 keys with an online softmax in fp32:
+//   stage   the chunk's K and V rows of this kv head are copied into shared
+//           memory with cp.async, 16 bytes per copy, all in flight at once and
+//           costing no registers;
 //   scores  thread t owns 8 columns (16 bytes) of K and every (256/(d/8))-th key
-//           of the chunk, all its loads in flight at once; partial dot products
-//           with its columns of the g scaled queries, summed over the lanes of a
-//           row with shuffles, into shared memory;
+//           of the chunk: partial dot products with its columns of the g scaled
+//           queries, summed over the lanes of a row with shuffles;
 //   softmax warp w takes heads w, w + 8, ...: chunk max, the running max and
 //           rescale, exp2, chunk sum;
-//   values  thread t owns 8 columns (16 bytes) of V and every (256/(d/8))-th key
-//           of the chunk, all its loads in flight at once, accumulated for all
-//           g heads in registers;
+//   values  the same thread mapping over V, accumulated for all g heads in
+//           registers;
 // then the partial outputs are summed (shuffles inside a warp, shared memory
-// across the 8 warps),
-// normalised and stored (bf16), with the LSE if asked for.
+// across the 8 warps), normalised and stored (bf16), with the LSE if asked for.
 #include "bg_internal.h"
+#include "bg_ptx.cuh"
 
 #include <cuda_bf16.h>
 
@@ -33,13 +34,20 @@ namespace bg {
 namespace {
 constexpr int kLtThreads = 256;
 constexpr int kLtWarps = kLtThreads / 32;
-constexpr int kLtChunk = kLtThreads;   // keys per chunk: one per thread in the score pass
+constexpr int kLtChunk = 128;          // keys per chunk
 
-// dynamic shared memory layout (floats): qs[g][D] | sc[g][256] | st[3][g] (m, l, alpha) | part[8][g][D]
-__host__ __device__ constexpr size_t lt_smem_floats(int g, int D)
+// dynamic shared memory: K and V of a chunk (bf16 [128][D] each; after the last chunk the
+// per-warp partial outputs [8][g][D] fp32 reuse this space), then qs[g][D] | sc[g][128] |
+// st[3][g] (m, l, alpha), fp32
+__host__ __device__ constexpr size_t lt_smem_bytes(int g, int D)
 {
-    return static_cast<size_t>(g) * D + static_cast<size_t>(g) * kLtChunk + 3 * static_cast<size_t>(g) +
-           static_cast<size_t>(kLtWarps) * g * D;
+    return 2 * static_cast<size_t>(kLtChunk) * D * 2 +
+           (static_cast<size_t>(g) * D + static_cast<size_t>(g) * kLtChunk + 3 * static_cast<size_t>(g)) * 4;
+}
+
+__device__ __forceinline__ void cp_async16(void *dst, const void *src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
 }
 
 // G: a power of two >= g = Hq / Hkv; the per-thread arrays are sized by it
@@ -50,17 +58,19 @@ __global__ void __launch_bounds__(kLtThreads)
                       int32_t max_seqlen, int32_t Hq, int32_t Hkv, float scale_log2, __nv_bfloat16 *__restrict__ out,
                       float *__restrict__ lse, int32_t *dev_status)
 {
-    extern __shared__ float lt_smem[];
+    extern __shared__ __align__(16) uint8_t lt_smem[];
     const int g = Hq / Hkv;
     const int seq = static_cast<int>(blockIdx.x) / Hkv;
     const int kh = static_cast<int>(blockIdx.x) - seq * Hkv;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    float *qs = lt_smem;                       // [g][D], pre-scaled by scale * log2(e)
-    float *sc = qs + g * D;                    // [g][256]
+    __nv_bfloat16 *ks = reinterpret_cast<__nv_bfloat16 *>(lt_smem);    // [128][D]
+    __nv_bfloat16 *vs = ks + kLtChunk * D;                              // [128][D]
+    float *part = reinterpret_cast<float *>(lt_smem);                   // [8][g][D], after the last chunk
+    float *qs = reinterpret_cast<float *>(vs + kLtChunk * D);          // [g][D], scaled by scale * log2(e)
+    float *sc = qs + g * D;                    // [g][128]
     float *st_m = sc + g * kLtChunk;           // [g] running max (base-2 units)
     float *st_l = st_m + g;                    // [g] running sum
     float *st_a = st_l + g;                    // [g] rescale factor of the current chunk
-    float *part = st_a + g;                    // [8][g][D] per-warp partial outputs
 
     const int a = cu[seq], b = cu[seq + 1];
     const bool bad = a < 0 || b < a || b > T || b - a > max_seqlen || (seq == 0 && a != 0) || (seq == B - 1 && b != T);
@@ -84,7 +94,6 @@ __global__ void __launch_bounds__(kLtThreads)
     constexpr int NCB = D / 8;                 // 16-byte column blocks of a row
     constexpr int KPT = kLtThreads / NCB;      // threads per column block
     constexpr int NM = kLtChunk / KPT;         // keys per thread and chunk
-    constexpr int kMB = NM < 8 ? NM : 8;       // loads in flight per thread
     const int cb = tid % NCB, kr0 = tid / NCB;
     float acc[G][8];                           // g <= G heads x this thread's 8 columns
 #pragma unroll
@@ -104,38 +113,36 @@ __global__ void __launch_bounds__(kLtThreads)
     const __nv_bfloat16 *vb = v + static_cast<int64_t>(a) * row_stride + kh * D;
     for (int c0 = 0; c0 < L; c0 += kLtChunk) {
         const int n = (L - c0 < kLtChunk) ? L - c0 : kLtChunk;
-        // ---- scores: like the values, thread tid reads 16-byte block cb of every KPT-th key
-        // (whole rows per group of NCB lanes, coalesced); the NCB partial dot products of a
-        // key are summed with shuffles
+        // ---- stage K and V rows c0 .. c0 + n - 1 (16-byte blocks, all copies in flight)
+        for (int i = tid; i < n * NCB; i += kLtThreads) {
+            const int r = i / NCB, c = i - r * NCB;
+            cp_async16(ks + r * D + 8 * c, kb + (c0 + r) * row_stride + 8 * c);
+            cp_async16(vs + r * D + 8 * c, vb + (c0 + r) * row_stride + 8 * c);
+        }
+        asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+        __syncthreads();
+        // ---- scores: thread tid reads block cb of keys kr0 + KPT m (a warp reads whole rows,
+        // conflict-free); the NCB partial dot products of a key are summed with shuffles
 #pragma unroll
-        for (int m0 = 0; m0 < NM; m0 += kMB) {
-            uint4 kw[kMB];
+        for (int m = 0; m < NM; ++m) {
+            const int j = kr0 + KPT * m;
+            const uint4 kw = *reinterpret_cast<const uint4 *>(ks + j * D + 8 * cb);
+            const __nv_bfloat162 *w2 = reinterpret_cast<const __nv_bfloat162 *>(&kw);
+            float kf[8];
 #pragma unroll
-            for (int mm = 0; mm < kMB; ++mm) {
-                const int j = kr0 + KPT * (m0 + mm);
-                kw[mm] = (j < n) ? reinterpret_cast<const uint4 *>(kb + (c0 + j) * row_stride)[cb] : make_uint4(0, 0, 0, 0);
+            for (int e = 0; e < 4; ++e) {
+                const float2 f = __bfloat1622float2(w2[e]);
+                kf[2 * e] = f.x;
+                kf[2 * e + 1] = f.y;
             }
 #pragma unroll
-            for (int mm = 0; mm < kMB; ++mm) {
-                const int m = m0 + mm;
-                const int j = kr0 + KPT * m;
-                const __nv_bfloat162 *w2 = reinterpret_cast<const __nv_bfloat162 *>(&kw[mm]);
-                float kf[8];
+            for (int h = 0; h < G; ++h) {
+                float dsum = 0.f;
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float2 f = __bfloat1622float2(w2[e]);
-                    kf[2 * e] = f.x;
-                    kf[2 * e + 1] = f.y;
-                }
+                for (int e = 0; e < 8; ++e) dsum = fmaf(qf[h][e], kf[e], dsum);
 #pragma unroll
-                for (int h = 0; h < G; ++h) {
-                    float dsum = 0.f;
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) dsum = fmaf(qf[h][e], kf[e], dsum);
-#pragma unroll
-                    for (int o = 1; o < NCB; o <<= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, o);
-                    if (h < g && cb == 0 && j < n) sc[h * kLtChunk + j] = dsum;
-                }
+                for (int o = 1; o < NCB; o <<= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, o);
+                if (h < g && cb == 0 && j < n) sc[h * kLtChunk + j] = dsum;
             }
         }
         __syncthreads();
@@ -173,39 +180,31 @@ __global__ void __launch_bounds__(kLtThreads)
                 for (int e = 0; e < 8; ++e) acc[h][e] *= al;
             }
         }
-        // this thread's V blocks are requested kMB at a time before any is used
+        // ---- values: the same mapping over V
 #pragma unroll
-        for (int m0 = 0; m0 < NM; m0 += kMB) {
-            uint4 vw[kMB];
+        for (int m = 0; m < NM; ++m) {
+            const int j = kr0 + KPT * m;
+            if (j < n) {
+                const uint4 vw = *reinterpret_cast<const uint4 *>(vs + j * D + 8 * cb);
+                const __nv_bfloat162 *w2 = reinterpret_cast<const __nv_bfloat162 *>(&vw);
+                float vf[8];
 #pragma unroll
-            for (int mm = 0; mm < kMB; ++mm) {
-                const int j = kr0 + KPT * (m0 + mm);
-                vw[mm] = (j < n) ? reinterpret_cast<const uint4 *>(vb + (c0 + j) * row_stride)[cb] : make_uint4(0, 0, 0, 0);
-            }
+                for (int e = 0; e < 4; ++e) {
+                    const float2 f = __bfloat1622float2(w2[e]);
+                    vf[2 * e] = f.x;
+                    vf[2 * e + 1] = f.y;
+                }
 #pragma unroll
-            for (int mm = 0; mm < kMB; ++mm) {
-                const int j = kr0 + KPT * (m0 + mm);
-                if (j < n) {
-                    const __nv_bfloat162 *w2 = reinterpret_cast<const __nv_bfloat162 *>(&vw[mm]);
-                    float vf[8];
+                for (int h = 0; h < G; ++h) {
+                    if (h < g) {
+                        const float pw = sc[h * kLtChunk + j];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float2 f = __bfloat1622float2(w2[e]);
-                        vf[2 * e] = f.x;
-                        vf[2 * e + 1] = f.y;
-                    }
-#pragma unroll
-                    for (int h = 0; h < G; ++h) {
-                        if (h < g) {
-                            const float pw = sc[h * kLtChunk + j];
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) acc[h][e] = fmaf(pw, vf[e], acc[h][e]);
-                        }
+                        for (int e = 0; e < 8; ++e) acc[h][e] = fmaf(pw, vf[e], acc[h][e]);
                     }
                 }
             }
         }
-        __syncthreads();   // sc is rewritten by the next chunk's scores
+        __syncthreads();   // K, V and sc are rewritten by the next chunk
     }
     // ---- combine the 8 warps' partial outputs, normalise, store
 #pragma unroll
@@ -241,7 +240,7 @@ cudaError_t launch_lt(const void *q, const void *k, const void *v, const int32_t
                       int32_t *dev_status, cudaStream_t stream)
 {
     const int g = Hq / Hkv;
-    const size_t smem = lt_smem_floats(g, D) * sizeof(float);
+    const size_t smem = lt_smem_bytes(g, D);
     auto kern = last_token_kernel<D, G>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;

@@ -389,6 +389,7 @@ def run_ours(args):
     # e2e: one layer per step through the C ABI with host buffers (pinned),
     # H2D of q, k, v, cu_seqlens and D2H of the output inside the timed region
     e2e = run_e2e(pre, device, stream, args)
+    last = run_last_token(pre, stream, peaks)
 
     # oracle CPU baseline (rank 0, N = 1 only)
     cpu = None
@@ -422,11 +423,42 @@ def run_ours(args):
                     "avg_call_us": round(avg_call_s * 1e6, 2), "tokens_per_s": round(world * pre.T * layers * args.steps / (prefill_ms / 1e3), 1)},
         "decode": {"beam_short": dec_report(dec_s, short_ms), "beam_long": dec_report(dec_l, long_ms)},
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk, "gpu_launches": launches,
+        "last_token": last,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+def run_last_token(pre, stream, peaks, reps: int = 5):
+    """The Prefill-Only last-layer variant, timed apart from the step: attention of each
+    sequence's last valid token over the layer's K/V (bg_packed_last_token_attn), on every
+    layer's own K/V, CUDA events on the launching stream."""
+    import torch
+    bg = pre.bg
+    rows = torch.from_numpy(pre.cu_np[1:] - 1).to(pre.q[0].device).long()
+    B = len(pre.lengths)
+    qs = [pre.q[l].index_select(0, rows).contiguous() for l in range(len(pre.q))]
+    out = torch.empty((B, pre.Hq, pre.d), dtype=torch.bfloat16, device=pre.q[0].device)
+    with torch.cuda.stream(stream):
+        for l in range(len(qs)):
+            bg.bg_packed_last_token_attn(qs[l], pre.k[l], pre.v[l], pre.cu, pre.maxlen, out, stream=stream)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            for l in range(len(qs)):
+                bg.bg_packed_last_token_attn(qs[l], pre.k[l], pre.v[l], pre.cu, pre.maxlen, out, stream=stream)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / (reps * len(qs))
+    by = float(pre.T * pre.Hkv * pre.d * 2 * 2 + 2 * B * pre.Hq * pre.d * 2)   # K, V once; q in, out
+    gbs = by / us / 1e3
+    return {"workload": f"Prefill-Only batch, last valid token of each of {B} sequences, {len(qs)} layers",
+            "us_per_layer": round(us, 2), "bytes_per_layer": by, "achieved_gbs": round(gbs, 1),
+            "hbm_frac": round(gbs / peaks["hbm_gbs"], 4), "bound": "hbm",
+            "definition": "bg_packed_last_token_attn per layer, timed apart from the step (not in value)"}
 
 
 def run_e2e(pre, device, stream, args):
