@@ -28,7 +28,8 @@
 //               extra tcgen05.commit costs the MMA warps ~160 cycles, so stage
 //               release piggybacks on barriers that exist anyway.
 //   warps 1, 3  tcgen05.mma issuers, one per query tile h (warp 1 also
-//               allocates TMEM).  For every key tile t the warp of tile h
+//               allocates TMEM); lane 0 alone runs the issue loop.  For every
+//               key tile t the thread of tile h
 //               issues S_h(t) = Q_h K(t)^T into one of NS S buffers of
 //               tile h, NS-1 tiles ahead of O_h += P_h(t-NS+1) V,
 //               so the tensor cores compute the next scores while the softmax
@@ -442,71 +443,74 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
         __syncwarp();
     } else if (warp == 1 || (NH == 2 && warp == 3)) {
         // =============================================================== MMA issuers
-        // One warp per query tile (warp 1: tile 0, warp 3: tile 1), so the two tiles'
-        // QK -> softmax -> P.V chains do not wait for each other.  Warp-converged like the
-        // producer; lane 0 issues every tcgen05.mma and commit.
-        const int h = (warp == 1) ? 0 : 1;
-        const uint32_t leader = (lane == 0) ? 1u : 0u;
-        constexpr uint32_t kIdescQK = idesc_bf16_f32(128, kKeys, 0);
-        constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, 1);
-        // Base descriptors, built once; an operand at byte offset `off` from a base is the
-        // base plus off / 16 (the start-address field, no carry: shared memory < 256 KB).
-        const uint64_t dq0 = sdesc_sw128(smem_u32(smem + C::kOffQ), 16, 1024);
-        const uint64_t dk0 = sdesc_sw128(smem_u32(smem + C::kOffK), 16, 1024);
-        const uint64_t dv0 = sdesc_sw128(smem_u32(smem + C::kOffV), kKVBox, 1024);
-        // `b` walks the tiles whose S is computed next, `a` (one behind) the tiles whose
-        // P.V is accumulated next.
-        TileWalker<MODE, NH> b, a;
-        b.first(p, n_items);
-        a = b;
-        uint32_t gb = 0, ga = 0;           // global tile numbers of b and a
-        bool ok = true;
+        // One thread per query tile (lane 0 of warp 1: tile 0, of warp 3: tile 1), so the two
+        // tiles' QK -> softmax -> P.V chains do not wait for each other.  The thread waits on
+        // the barriers itself and issues every tcgen05.mma and commit of its tile: no
+        // warp-wide broadcast of wait results and no per-instruction predicate on the issue
+        // path (each costs the issuing loop tens of cycles per step).
+        if (lane == 0) {
+            const int h = (warp == 1) ? 0 : 1;
+            constexpr uint32_t kIdescQK = idesc_bf16_f32(128, kKeys, 0);
+            constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, 1);
+            // Base descriptors, built once; an operand at byte offset `off` from a base is the
+            // base plus off / 16 (the start-address field, no carry: shared memory < 256 KB).
+            const uint64_t dq0 = sdesc_sw128(smem_u32(smem + C::kOffQ), 16, 1024);
+            const uint64_t dk0 = sdesc_sw128(smem_u32(smem + C::kOffK), 16, 1024);
+            const uint64_t dv0 = sdesc_sw128(smem_u32(smem + C::kOffV), kKVBox, 1024);
+            // `b` walks the tiles whose S is computed next, `a` (one behind) the tiles whose
+            // P.V is accumulated next.
+            TileWalker<MODE, NH> b, a;
+            b.first(p, n_items);
+            a = b;
+            uint32_t gb = 0, ga = 0;           // global tile numbers of b and a
+            bool ok = true;
 
-        auto issue_qk = [&](const TileWalker<MODE, NH> &t, uint32_t g) -> bool {
-            if (t.j == 0 && !warp_wait(&q_full[t.qbuf()], t.quse() & 1, abort_flag)) return false;
-            const int st = g % NK;
-            if (!warp_wait(&k_full[st], (g / NK) & 1, abort_flag)) return false;
-            const uint64_t dqb = dq0 + static_cast<uint64_t>((t.qbuf() * C::kQBytes) >> 4);
-            const uint64_t dks = dk0 + static_cast<uint64_t>((st * C::kTileBytes) >> 4);
-            // S(h, g%2) holds P of tile g-2, read by the P.V this warp issued just before this
-            // QK.  tcgen05.mma operations issued by one thread execute in issue order, so this
-            // QK cannot overwrite P before that P.V has read it: no wait for its completion.
-            tc_fence_after();
-            const uint64_t dqh = dqb + static_cast<uint64_t>((h * C::NB * kQBox) >> 4);
-            static_assert(kQBox == 16384 && kKVBox == 8192, "mma_qk_tile hard-codes the column-block strides");
-            mma_qk_tile<C::NB>(leader, tmem + C::col_s(h, g % NS), dqh, dks, kIdescQK, &s_full[NS * h + g % NS]);
-            if (t.j == t.I.n_tiles - 1) mma_commit_l(leader, &q_empty[t.qbuf()]);   // Q after the item's last
-            return true;
-        };
+            auto issue_qk = [&](const TileWalker<MODE, NH> &t, uint32_t g) -> bool {
+                if (t.j == 0 && !mbar_wait(&q_full[t.qbuf()], t.quse() & 1, abort_flag)) return false;
+                const int st = g % NK;
+                if (!mbar_wait(&k_full[st], (g / NK) & 1, abort_flag)) return false;
+                const uint64_t dqb = dq0 + static_cast<uint64_t>((t.qbuf() * C::kQBytes) >> 4);
+                const uint64_t dks = dk0 + static_cast<uint64_t>((st * C::kTileBytes) >> 4);
+                // S(h, g%NS) holds P of tile g-NS, read by the P.V this thread issued just before
+                // this QK.  tcgen05.mma operations issued by one thread execute in issue order, so
+                // this QK cannot overwrite P before that P.V has read it: no wait for its completion.
+                tc_fence_after();
+                const uint64_t dqh = dqb + static_cast<uint64_t>((h * C::NB * kQBox) >> 4);
+                static_assert(kQBox == 16384 && kKVBox == 8192, "mma_qk_tile hard-codes the column-block strides");
+                mma_qk_tile<C::NB>(tmem + C::col_s(h, g % NS), dqh, dks, kIdescQK, &s_full[NS * h + g % NS]);
+                if (t.j == t.I.n_tiles - 1) mma_commit(&q_empty[t.qbuf()]);   // Q after the item's last
+                return true;
+            };
 
-        // QK runs NS-1 tiles ahead of P.V: QK(t + NS - 1) reuses the S buffer of P(t - 1),
-        // whose P.V was issued before it.
-        for (int i = 0; i < NS - 1 && ok && b.valid; ++i) {
-            ok = issue_qk(b, gb);
-            b.advance(p);
-            ++gb;
-        }
-        while (ok && a.valid) {
-            if (b.valid) {
-                if (!issue_qk(b, gb)) break;
+            // QK runs NS-1 tiles ahead of P.V: QK(t + NS - 1) reuses the S buffer of P(t - 1),
+            // whose P.V was issued before it.
+            for (int i = 0; i < NS - 1 && ok && b.valid; ++i) {
+                ok = issue_qk(b, gb);
                 b.advance(p);
                 ++gb;
             }
-            const int st = ga % NV;
-            if (!warp_wait(&v_full[st], (ga / NV) & 1, abort_flag)) break;
-            const uint64_t dvs = dv0 + static_cast<uint64_t>((st * C::kTileBytes) >> 4);
-            if (!warp_wait(&p_full[NS * h + ga % NS], (ga / NS) & 1, abort_flag)) break;
-            tc_fence_after();
-            // V tile: 64 key rows of 128 bytes per column block; K = 16 rows per step.
-            static_assert(kKeys == 64, "mma_pv_tile issues four 16-key steps");
-            mma_pv_tile(leader, tmem + C::kColO + D * h, tmem + C::col_s(h, ga % NS), dvs, kIdescPV, a.j > 0 ? 1u : 0u,
-                        &pv_done[NS * h + ga % NS]);
-            a.advance(p);
-            ++ga;
+            while (ok && a.valid) {
+                if (b.valid) {
+                    if (!issue_qk(b, gb)) break;
+                    b.advance(p);
+                    ++gb;
+                }
+                const int st = ga % NV;
+                if (!mbar_wait(&v_full[st], (ga / NV) & 1, abort_flag)) break;
+                const uint64_t dvs = dv0 + static_cast<uint64_t>((st * C::kTileBytes) >> 4);
+                if (!mbar_wait(&p_full[NS * h + ga % NS], (ga / NS) & 1, abort_flag)) break;
+                tc_fence_after();
+                // V tile: 64 key rows of 128 bytes per column block; K = 16 rows per step.
+                static_assert(kKeys == 64, "mma_pv_tile issues four 16-key steps");
+                mma_pv_tile(tmem + C::kColO + D * h, tmem + C::col_s(h, ga % NS), dvs, kIdescPV, a.j > 0 ? 1u : 0u,
+                            &pv_done[NS * h + ga % NS]);
+                a.advance(p);
+                ++ga;
+            }
+            // Drain: every MMA issued above completes before TMEM is released.
+            mma_commit(mma_final);
+            mbar_wait_drain(mma_final, 0);
         }
-        // Drain: every MMA issued above completes before TMEM is released.
-        mma_commit_l(leader, mma_final);
-        if (lane == 0) mbar_wait_drain(mma_final, 0);
         __syncwarp();
     } else if (warp >= 4) {
         // =============================================================== softmax + epilogue

@@ -285,86 +285,74 @@ __device__ __forceinline__ void tma_load_4d_w(uint32_t leader, void *dst, const 
 }
 
 // ---- batched issue for the attention kernel: one asm statement per tile and
-// operand group, `leader` predicates every instruction, descriptor offsets are
-// immediates.
+// operand group, executed by the one thread that issues every tcgen05.mma and
+// commit of its query tile (a commit tracks the MMAs of the thread that
+// executes it).  Descriptor offsets are immediates.
 //
 // S = Q K^T over K = 64 * NB (NB 128-byte column blocks): 4 MMAs per block, A
 // and B advance 32 bytes (2 descriptor units) per 16-element step, Q column
 // blocks are 16 KB (1024 units) and K column blocks 8 KB (512 units) apart;
 // then a commit to `bar`.
 template <int NB>
-__device__ __forceinline__ void mma_qk_tile(uint32_t leader, uint32_t d_tmem, uint64_t dq, uint64_t dk,
-                                            uint32_t idesc, uint64_t *bar);
+__device__ __forceinline__ void mma_qk_tile(uint32_t d_tmem, uint64_t dq, uint64_t dk, uint32_t idesc, uint64_t *bar);
 
 template <>
-__device__ __forceinline__ void mma_qk_tile<1>(uint32_t leader, uint32_t d_tmem, uint64_t dq, uint64_t dk,
-                                               uint32_t idesc, uint64_t *bar)
+__device__ __forceinline__ void mma_qk_tile<1>(uint32_t d_tmem, uint64_t dq, uint64_t dk, uint32_t idesc, uint64_t *bar)
 {
     asm volatile(
-        "{\n\t.reg .pred e, pf, pt;\n\t.reg .b64 a1, a2, a3, b1, b2, b3;\n\t"
-        "setp.ne.b32 e, %0, 0;\n\tsetp.ne.b32 pf, 0, 0;\n\tsetp.eq.b32 pt, 0, 0;\n\t"
-        "add.s64 a1, %2, 2;\n\tadd.s64 a2, %2, 4;\n\tadd.s64 a3, %2, 6;\n\t"
-        "add.s64 b1, %3, 2;\n\tadd.s64 b2, %3, 4;\n\tadd.s64 b3, %3, 6;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%1], %2, %3, %4, pf;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%1], a1, b1, %4, pt;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%1], a2, b2, %4, pt;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%1], a3, b3, %4, pt;\n\t"
-        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%5];\n\t}" ::"r"(leader),
-        "r"(d_tmem), "l"(dq), "l"(dk), "r"(idesc), "r"(smem_u32(bar))
+        "{\n\t.reg .pred pf, pt;\n\t.reg .b64 a1, a2, a3, b1, b2, b3;\n\t"
+        "setp.ne.b32 pf, 0, 0;\n\tsetp.eq.b32 pt, 0, 0;\n\t"
+        "add.s64 a1, %1, 2;\n\tadd.s64 a2, %1, 4;\n\tadd.s64 a3, %1, 6;\n\t"
+        "add.s64 b1, %2, 2;\n\tadd.s64 b2, %2, 4;\n\tadd.s64 b3, %2, 6;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, pf;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, pt;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a2, b2, %3, pt;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a3, b3, %3, pt;\n\t"
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%4];\n\t}" ::"r"(d_tmem),
+        "l"(dq), "l"(dk), "r"(idesc), "r"(smem_u32(bar))
         : "memory");
 }
 
 template <>
-__device__ __forceinline__ void mma_qk_tile<2>(uint32_t leader, uint32_t d_tmem, uint64_t dq, uint64_t dk,
-                                               uint32_t idesc, uint64_t *bar)
+__device__ __forceinline__ void mma_qk_tile<2>(uint32_t d_tmem, uint64_t dq, uint64_t dk, uint32_t idesc, uint64_t *bar)
 {
     asm volatile(
-        "{\n\t.reg .pred e, pf, pt;\n\t.reg .b64 a1, a2, a3, a4, a5, a6, a7, b1, b2, b3, b4, b5, b6, b7;\n\t"
-        "setp.ne.b32 e, %0, 0;\n\tsetp.ne.b32 pf, 0, 0;\n\tsetp.eq.b32 pt, 0, 0;\n\t"
-        "add.s64 a1, %2, 2;\n\tadd.s64 a2, %2, 4;\n\tadd.s64 a3, %2, 6;\n\t"
-        "add.s64 a4, %2, 1024;\n\tadd.s64 a5, %2, 1026;\n\tadd.s64 a6, %2, 1028;\n\tadd.s64 a7, %2, 1030;\n\t"
-        "add.s64 b1, %3, 2;\n\tadd.s64 b2, %3, 4;\n\tadd.s64 b3, %3, 6;\n\t"
-        "add.s64 b4, %3, 512;\n\tadd.s64 b5, %3, 514;\n\tadd.s64 b6, %3, 516;\n\tadd.s64 b7, %3, 518;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%1], %2, %3, %4, pf;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%1], a1, b1, %4, pt;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%1], a2, b2, %4, pt;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%1], a3, b3, %4, pt;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%1], a4, b4, %4, pt;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%1], a5, b5, %4, pt;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%1], a6, b6, %4, pt;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%1], a7, b7, %4, pt;\n\t"
-        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%5];\n\t}" ::"r"(leader),
-        "r"(d_tmem), "l"(dq), "l"(dk), "r"(idesc), "r"(smem_u32(bar))
+        "{\n\t.reg .pred pf, pt;\n\t.reg .b64 a1, a2, a3, a4, a5, a6, a7, b1, b2, b3, b4, b5, b6, b7;\n\t"
+        "setp.ne.b32 pf, 0, 0;\n\tsetp.eq.b32 pt, 0, 0;\n\t"
+        "add.s64 a1, %1, 2;\n\tadd.s64 a2, %1, 4;\n\tadd.s64 a3, %1, 6;\n\t"
+        "add.s64 a4, %1, 1024;\n\tadd.s64 a5, %1, 1026;\n\tadd.s64 a6, %1, 1028;\n\tadd.s64 a7, %1, 1030;\n\t"
+        "add.s64 b1, %2, 2;\n\tadd.s64 b2, %2, 4;\n\tadd.s64 b3, %2, 6;\n\t"
+        "add.s64 b4, %2, 512;\n\tadd.s64 b5, %2, 514;\n\tadd.s64 b6, %2, 516;\n\tadd.s64 b7, %2, 518;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, pf;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, pt;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a2, b2, %3, pt;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a3, b3, %3, pt;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a4, b4, %3, pt;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a5, b5, %3, pt;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a6, b6, %3, pt;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], a7, b7, %3, pt;\n\t"
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%4];\n\t}" ::"r"(d_tmem),
+        "l"(dq), "l"(dk), "r"(idesc), "r"(smem_u32(bar))
         : "memory");
 }
 
 // O (+)= P V over 64 keys: A = P in TMEM (8 columns per 16 keys), B = V (MN-major,
 // 16 key rows = 2048 bytes = 128 units per step); the first MMA accumulates only
 // if `acc`; then a commit to `bar`.
-__device__ __forceinline__ void mma_pv_tile(uint32_t leader, uint32_t d_tmem, uint32_t a_tmem, uint64_t dv,
-                                            uint32_t idesc, uint32_t acc, uint64_t *bar)
+__device__ __forceinline__ void mma_pv_tile(uint32_t d_tmem, uint32_t a_tmem, uint64_t dv, uint32_t idesc,
+                                            uint32_t acc, uint64_t *bar)
 {
     asm volatile(
-        "{\n\t.reg .pred e, p0, pt;\n\t.reg .b64 b1, b2, b3;\n\t.reg .b32 t1, t2, t3;\n\t"
-        "setp.ne.b32 e, %0, 0;\n\tsetp.ne.b32 p0, %5, 0;\n\tsetp.eq.b32 pt, 0, 0;\n\t"
-        "add.s64 b1, %3, 128;\n\tadd.s64 b2, %3, 256;\n\tadd.s64 b3, %3, 384;\n\t"
-        "add.u32 t1, %2, 8;\n\tadd.u32 t2, %2, 16;\n\tadd.u32 t3, %2, 24;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%1], [%2], %3, %4, p0;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%1], [t1], b1, %4, pt;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%1], [t2], b2, %4, pt;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%1], [t3], b3, %4, pt;\n\t"
-        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%6];\n\t}" ::"r"(leader),
-        "r"(d_tmem), "r"(a_tmem), "l"(dv), "r"(idesc), "r"(acc), "r"(smem_u32(bar))
-        : "memory");
-}
-
-// commit predicated by the leader flag
-__device__ __forceinline__ void mma_commit_l(uint32_t leader, uint64_t *bar)
-{
-    asm volatile(
-        "{\n\t.reg .pred e;\n\tsetp.ne.b32 e, %0, 0;\n\t"
-        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%1];\n\t}" ::"r"(leader),
-        "r"(smem_u32(bar))
+        "{\n\t.reg .pred p0, pt;\n\t.reg .b64 b1, b2, b3;\n\t.reg .b32 t1, t2, t3;\n\t"
+        "setp.ne.b32 p0, %4, 0;\n\tsetp.eq.b32 pt, 0, 0;\n\t"
+        "add.s64 b1, %2, 128;\n\tadd.s64 b2, %2, 256;\n\tadd.s64 b3, %2, 384;\n\t"
+        "add.u32 t1, %1, 8;\n\tadd.u32 t2, %1, 16;\n\tadd.u32 t3, %1, 24;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [t1], b1, %3, pt;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [t2], b2, %3, pt;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [t3], b3, %3, pt;\n\t"
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%5];\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(dv), "r"(idesc), "r"(acc), "r"(smem_u32(bar))
         : "memory");
 }
 
