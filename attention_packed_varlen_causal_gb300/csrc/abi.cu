@@ -150,7 +150,7 @@ bg_status_t bg_packed_prefill_attn(const void *q, const void *k, const void *v, 
     const int nsm = sm_count();
     if (nsm <= 0) return BG_ERR_CUDA;
 
-    CUtensorMap tm_q, tm_k, tm_v;
+    CUtensorMap tm_q, tm_k, tm_v, tm_o;
     const uint64_t D = static_cast<uint64_t>(head_dim);
     const uint64_t dq[3] = {D, static_cast<uint64_t>(Hq), static_cast<uint64_t>(total_tokens)};
     const uint64_t sq[2] = {D * 2, static_cast<uint64_t>(Hq) * D * 2};
@@ -159,8 +159,9 @@ bg_status_t bg_packed_prefill_attn(const void *q, const void *k, const void *v, 
     // boxes: 64 columns (one 128-byte swizzle span) x one head x the kernel's tile height
     const uint32_t boxq[3] = {64, 1, static_cast<uint32_t>(bg::kRows)};
     const uint32_t boxkv[3] = {64, 1, static_cast<uint32_t>(bg::kKeys)};
+    // the output has the query's shape: whole 128-row tiles leave through the same box
     if (!encode_map(&tm_q, q, 3, dq, sq, boxq) || !encode_map(&tm_k, k, 3, dkv, skv, boxkv) ||
-        !encode_map(&tm_v, v, 3, dkv, skv, boxkv))
+        !encode_map(&tm_v, v, 3, dkv, skv, boxkv) || !encode_map(&tm_o, out, 3, dq, sq, boxq))
         return BG_ERR_CUDA;
 
     int32_t *hdr = static_cast<int32_t *>(workspace);
@@ -185,7 +186,7 @@ bg_status_t bg_packed_prefill_attn(const void *q, const void *k, const void *v, 
     p.n_head_groups = Hkv * groups_per_kv;
     p.lse = lse;
     const int grid = static_cast<int>(items_bound < nsm ? items_bound : nsm);
-    if (launch_prefill_attn(head_dim, tm_q, tm_k, tm_v, p, grid, stream) != cudaSuccess) return BG_ERR_CUDA;
+    if (launch_prefill_attn(head_dim, tm_q, tm_k, tm_v, tm_o, p, grid, stream) != cudaSuccess) return BG_ERR_CUDA;
     return BG_OK;
 }
 
@@ -259,7 +260,7 @@ bg_status_t bg_beam_decode_attn(const void *q, const void *prompt_k, const void 
     const int64_t items = static_cast<int64_t>(R) * Hkv * pairs;
     if (items >= (int64_t(1) << 31)) return BG_ERR_UNSUPPORTED;
 
-    CUtensorMap tm_q, tm_k, tm_v, tm_sk, tm_sv;
+    CUtensorMap tm_q, tm_k, tm_v, tm_sk, tm_sv, tm_o;
     const uint64_t D = static_cast<uint64_t>(head_dim);
     const uint64_t dq[4] = {D, static_cast<uint64_t>(g), static_cast<uint64_t>(Hkv), static_cast<uint64_t>(R) * W};
     const uint64_t sq[3] = {D * 2, static_cast<uint64_t>(g) * D * 2, static_cast<uint64_t>(Hq) * D * 2};
@@ -271,8 +272,9 @@ bg_status_t bg_beam_decode_attn(const void *q, const void *prompt_k, const void 
     // With no prompt tokens no K/V tile is ever loaded; the maps only need a valid base.
     const void *kbase = total_prompt_tokens > 0 ? prompt_k : q;
     const void *vbase = total_prompt_tokens > 0 ? prompt_v : q;
+    // the output has the query's shape: whole tiles of BT beams leave through the same box
     if (!encode_map(&tm_q, q, 4, dq, sq, boxq) || !encode_map(&tm_k, kbase, 3, dkv, skv, boxkv) ||
-        !encode_map(&tm_v, vbase, 3, dkv, skv, boxkv))
+        !encode_map(&tm_v, vbase, 3, dkv, skv, boxkv) || !encode_map(&tm_o, out, 4, dq, sq, boxq))
         return BG_ERR_CUDA;
     // Suffix key tiles: slots 0..t-1 of suf_bpt consecutive beams per tile (beam-major rows),
     // over [R*W beams][suffix_max slots][Hkv][d]; beams past R*W read as zeros.
@@ -310,7 +312,7 @@ bg_status_t bg_beam_decode_attn(const void *q, const void *prompt_k, const void 
     p.suf_tx = (head_dim / 64) * 128 * t_suf * bpt;
     p.n_items_decode = static_cast<int32_t>(items);
     const int grid = static_cast<int>(items < nsm ? items : nsm);
-    if (launch_decode_attn(head_dim, tm_q, tm_k, tm_v, tm_sk, tm_sv, p, grid, stream) != cudaSuccess) return BG_ERR_CUDA;
+    if (launch_decode_attn(head_dim, tm_q, tm_k, tm_v, tm_sk, tm_sv, tm_o, p, grid, stream) != cudaSuccess) return BG_ERR_CUDA;
     return BG_OK;
 }
 

@@ -195,6 +195,23 @@ __device__ __forceinline__ Item make_item(const AttnParams &p, int it, int4 raw)
     return I;
 }
 
+// Whether query tile h of a decode item is stored through the TMA unit out of its Q buffer
+// (see the epilogue): only when all of its BT beams are beams of the request.  The MMA thread
+// and the softmax warpgroup of h both evaluate it, so they agree on who releases the item's Q
+// buffer: the MMA thread right after the item's last QK (the tile is then stored row by row),
+// or the epilogue once the TMA unit has read the tile out of it.  Prefill tiles always take the
+// row-by-row path: the prefill kernel is at its register limit, and the extra epilogue code made
+// it slower than the store overlap gained.
+template <Mode MODE>
+__device__ __forceinline__ bool tile_store_via_tma(const AttnParams &p, const Item &I, int h)
+{
+    if constexpr (MODE == Mode::Prefill) {
+        return false;
+    } else {
+        return (I.bt0 + h) * p.BT + p.BT <= p.W;
+    }
+}
+
 // Walks the (item, key tile) sequence of one CTA, skipping items without
 // tiles.  Every role walks the same sequence, so all agree on global tile
 // numbers (which pick K/V stages, S buffers and barrier phases).
@@ -254,7 +271,8 @@ template <Mode MODE, int D, int NH, int NK, int NV, int NS>
 __global__ void __launch_bounds__(128 * (1 + NH), 1)
     attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_sk,
-                const __grid_constant__ CUtensorMap tm_sv, const AttnParams p)
+                const __grid_constant__ CUtensorMap tm_sv, const __grid_constant__ CUtensorMap tm_o,
+                const AttnParams p)
 {
     using C = AttnCfg<D, NH, NK, NV, NS>;
     extern __shared__ uint8_t smem_raw[];
@@ -291,7 +309,7 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
     if (threadIdx.x == 0) {
         for (int b = 0; b < 2; ++b) {
             mbar_init(&q_full[b], 1);
-            mbar_init(&q_empty[b], NH);   // one commit per MMA warp
+            mbar_init(&q_empty[b], NH);   // one arrive per softmax warpgroup, from its epilogue
         }
         mbar_init(mma_final, NH);
         for (int s = 0; s < NK; ++s) {
@@ -326,6 +344,7 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
         tma_prefetch_desc(&tm_q);
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
+        tma_prefetch_desc(&tm_o);
         if constexpr (MODE == Mode::Decode) {
             tma_prefetch_desc(&tm_sk);
             tma_prefetch_desc(&tm_sv);
@@ -478,7 +497,10 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
                 const uint64_t dqh = dqb + static_cast<uint64_t>((h * C::NB * kQBox) >> 4);
                 static_assert(kQBox == 16384 && kKVBox == 8192, "mma_qk_tile hard-codes the column-block strides");
                 mma_qk_tile<C::NB>(tmem + C::col_s(h, g % NS), dqh, dks, kIdescQK, &s_full[NS * h + g % NS]);
-                if (t.j == t.I.n_tiles - 1) mma_commit(&q_empty[t.qbuf()]);   // Q after the item's last
+                // the item's Q buffer is free once its last QK has completed, unless the epilogue
+                // stores the output tile out of it
+                if (t.j == t.I.n_tiles - 1 && !tile_store_via_tma<MODE>(p, t.I, h))
+                    mma_commit(&q_empty[t.qbuf()]);
                 return true;
             };
 
@@ -530,7 +552,14 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
         // work; the next item's first P.V, which overwrites O, is released only after this.
         // `release` runs once O is in registers: the caller lets the next P.V overwrite O from
         // then on, while the stores below still run.
-        auto epilogue = [&](const Item &I, float m, float l, uint32_t g_last, auto &&release) -> bool {
+        // A decode tile whose BT beams all belong to the request goes out through the TMA unit:
+        // every thread writes its row into the item's Q buffer (free once the item's last QK has
+        // completed, which its last P.V completing implies; same 128-byte-swizzled layout and box
+        // as the Q load), and one thread issues the tile stores and, once the TMA unit has read the
+        // buffer, hands it back to the Q producer.  The warps do not wait for the global writes.
+        // Other tiles, and every prefill tile, are stored row by row through the staging area.
+        auto epilogue = [&](const Item &I, float m, float l, uint32_t g_last, int qbi, bool via_tma,
+                            auto &&release) -> bool {
                 // The commit after the item's last P.V covers every earlier MMA too.  (Items always
                 // have tiles here; the test stays because ptxas allocates the prefill kernel's
                 // registers with fewer spills with it: 235 vs 297 us on the Prefill-Only batch.)
@@ -593,8 +622,35 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
                     }
                 }
                 release();
+                const bool leader = quad == 0 && lane == 0;
+                if (MODE == Mode::Decode && via_tma) {
+                    // row `row` of column block cb: 16-byte chunk c at (c ^ (row % 8)) in its 128-byte row
+                    uint8_t *tile = smem + C::kOffQ + qbi * C::kQBytes + h * C::NB * kQBox;
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) put_chunk(c, pk + 16 * c);
+                    for (int cb = 0; cb < C::NB; ++cb)
+#pragma unroll
+                        for (int c = 0; c < 8; ++c)
+                            *reinterpret_cast<uint4 *>(tile + cb * kQBox + row * 128 + ((c ^ (row & 7)) << 4)) =
+                                make_uint4(pk[32 * cb + 4 * c], pk[32 * cb + 4 * c + 1], pk[32 * cb + 4 * c + 2],
+                                           pk[32 * cb + 4 * c + 3]);
+                    fence_proxy_async_smem();          // generic-proxy writes -> the TMA unit's reads
+                    named_bar_sync(1 + h, 128);        // the warpgroup's four warps have written their rows
+                    if (leader) {
+#pragma unroll
+                        for (int cb = 0; cb < C::NB; ++cb) {
+                            if constexpr (MODE == Mode::Prefill)
+                                tma_store_3d(&tm_o, tile + cb * kQBox, cb * 64, I.head0 + h, I.seq_start + I.qt * kRows);
+                            else
+                                tma_store_4d(&tm_o, tile + cb * kQBox, cb * 64, 0, I.kh, I.r * p.W + (I.bt0 + h) * p.BT);
+                        }
+                        bulk_commit_group();
+                        bulk_wait_read_all();
+                        mbar_arrive(&q_empty[qbi]);    // the Q producer may refill the buffer
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) put_chunk(c, pk + 16 * c);
+                }
                 if constexpr (MODE == Mode::Prefill) {
                     if (p.lse) {
                         if (row_dst(row)) {
@@ -610,6 +666,8 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
         Item Ip;
         float mp = 0.f, lp = 0.f;
         uint32_t gp = 0;
+        int nq = 0, qbp = 0;  // items with tiles entered so far (selects the Q buffer, as in TileWalker)
+        bool tmap = false;    // the pending item's tile leaves through the TMA unit
         for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
             const int4 raw = nxt_raw;
             if (it + static_cast<int>(gridDim.x) < n_items) nxt_raw = fetch_raw<MODE>(p, it + gridDim.x);
@@ -626,6 +684,8 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
                 continue;
             }
             if (I.n_tiles == 0) continue;   // not produced by make_item for a valid item; skipped by every role
+            ++nq;
+            const bool tma_I = tile_store_via_tma<MODE>(p, I, h);
             float m = -INFINITY;   // running max of scaled logits (base-2 units)
             float l = 0.f;         // running sum of exp2(logit - m)
             for (int j = 0; j < I.n_tiles; ++j, ++g) {
@@ -745,7 +805,7 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
                 tc_fence_before();
                 if (j == 0 && pend) {
                     // the previous item's O is read before this tile's P.V may overwrite it
-                    if (!epilogue(Ip, mp, lp, gp, [&]() {
+                    if (!epilogue(Ip, mp, lp, gp, qbp, tmap, [&]() {
                             tc_fence_before();
                             mbar_arrive(&p_full[NS * h + g % NS]);
                         })) {
@@ -759,12 +819,16 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
             }
             if (!ok) break;
             pend = true;
+            qbp = (nq - 1) & 1;
+            tmap = tma_I;
             Ip = I;
             mp = m;
             lp = l;
             gp = g - 1;
         }
-        if (ok && pend) ok = epilogue(Ip, mp, lp, gp, []() {});
+        if (ok && pend) ok = epilogue(Ip, mp, lp, gp, qbp, tmap, []() {});
+        // every tile store this thread issued has written global memory before the CTA exits
+        if (quad == 0 && lane == 0) bulk_wait_all();
 
         (void)ok;
     }

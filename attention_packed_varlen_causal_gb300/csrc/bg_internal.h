@@ -20,12 +20,13 @@ cudaError_t launch_prefill_worklist(const int32_t *cu_seqlens, int32_t num_seqs,
                                     int32_t max_seqlen, int32_t *work_hdr, int4 *work, int32_t *dev_status,
                                     cudaStream_t stream);
 cudaError_t launch_prefill_attn(int head_dim, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
-                                const CUtensorMap &tm_v, const AttnParams &p, int grid, cudaStream_t stream);
+                                const CUtensorMap &tm_v, const CUtensorMap &tm_o, const AttnParams &p, int grid,
+                                cudaStream_t stream);
 int prefill_heads_per_cta();
 
 cudaError_t launch_decode_attn(int head_dim, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
                                const CUtensorMap &tm_v, const CUtensorMap &tm_sk, const CUtensorMap &tm_sv,
-                               const AttnParams &p, int grid, cudaStream_t stream);
+                               const CUtensorMap &tm_o, const AttnParams &p, int grid, cudaStream_t stream);
 int decode_tiles_per_cta();
 
 // Attention of each sequence's last valid token (one CTA per sequence and kv head).

@@ -26,14 +26,14 @@ std::atomic<uint64_t> &smem_attr_done()
 
 template <int D, int NK, int NV, int NS>
 cudaError_t launch_one(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
-                       const CUtensorMap &tm_sk, const CUtensorMap &tm_sv, const AttnParams &p, int grid,
-                       cudaStream_t stream)
+                       const CUtensorMap &tm_sk, const CUtensorMap &tm_sv, const CUtensorMap &tm_o,
+                       const AttnParams &p, int grid, cudaStream_t stream)
 {
     using C = AttnCfg<D, kNH, NK, NV, NS>;
     auto kern = attn_kernel<Mode::Decode, D, kNH, NK, NV, NS>;
     cudaError_t e = ensure_smem_attribute(kern, C::kSmemBytes, smem_attr_done<D, NK, NV, NS>());
     if (e != cudaSuccess) return e;
-    kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(tm_q, tm_k, tm_v, tm_sk, tm_sv, p);
+    kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(tm_q, tm_k, tm_v, tm_sk, tm_sv, tm_o, p);
     return cudaGetLastError();
 }
 }  // namespace
@@ -42,10 +42,10 @@ int decode_tiles_per_cta() { return kNH; }
 
 cudaError_t launch_decode_attn(int head_dim, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
                                const CUtensorMap &tm_v, const CUtensorMap &tm_sk, const CUtensorMap &tm_sv,
-                               const AttnParams &p, int grid, cudaStream_t stream)
+                               const CUtensorMap &tm_o, const AttnParams &p, int grid, cudaStream_t stream)
 {
-    if (head_dim == 64) return launch_one<64, 4, 4, 3>(tm_q, tm_k, tm_v, tm_sk, tm_sv, p, grid, stream);
-    if (head_dim == 128) return launch_one<128, 3, 2, 2>(tm_q, tm_k, tm_v, tm_sk, tm_sv, p, grid, stream);
+    if (head_dim == 64) return launch_one<64, 4, 4, 3>(tm_q, tm_k, tm_v, tm_sk, tm_sv, tm_o, p, grid, stream);
+    if (head_dim == 128) return launch_one<128, 3, 2, 2>(tm_q, tm_k, tm_v, tm_sk, tm_sv, tm_o, p, grid, stream);
     return cudaErrorInvalidValue;
 }
 
