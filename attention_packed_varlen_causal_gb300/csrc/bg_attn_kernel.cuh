@@ -298,13 +298,7 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-
-    int n_items;
-    if constexpr (MODE == Mode::Prefill) {
-        n_items = (p.work_hdr[0] == 0) ? p.work_hdr[1] * p.n_head_groups : 0;
-    } else {
-        n_items = p.n_items_decode;
-    }
+    grid_dep_launch();   // the next kernel's CTAs may start their prologue (they wait before any global access)
 
     if (threadIdx.x == 0) {
         for (int b = 0; b < 2; ++b) {
@@ -350,10 +344,18 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
             tma_prefetch_desc(&tm_sv);
         }
     }
+    grid_dep_wait();     // the previous kernel of the stream has completed: inputs may be read
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+
+    int n_items;
+    if constexpr (MODE == Mode::Prefill) {
+        n_items = (p.work_hdr[0] == 0) ? p.work_hdr[1] * p.n_head_groups : 0;
+    } else {
+        n_items = p.n_items_decode;
+    }
 
     if (warp == 0) {
         // =============================================================== producer

@@ -7,6 +7,7 @@
 #include <stdint.h>
 
 #include <atomic>
+#include <utility>
 
 #include "bg_attn.h"
 
@@ -39,6 +40,28 @@ cudaError_t launch_suffix_reorder(const void *src_k, const void *src_v, void *ds
                                   const int32_t *parent_idx, const void *new_k, const void *new_v, int32_t R,
                                   int32_t W, int32_t suffix_max, int32_t n_tokens, int32_t Hkv, int32_t head_dim,
                                   int32_t *dev_status, cudaStream_t stream);
+
+// Launches `kern` on `stream` with programmatic stream serialization: its CTAs may
+// start while the previous kernel of the stream still runs (that kernel lets them
+// with griddepcontrol.launch_dependents); every kernel of this library waits
+// (griddepcontrol.wait) before its first global-memory access, so only prologue
+// work overlaps.  Valid inside CUDA-graph stream capture.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                             Args &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 // Raises the dynamic shared-memory limit of `kern` once per device (bit d of
 // `done`), so later launches -- including ones inside a CUDA-graph capture --

@@ -98,6 +98,24 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t *bar, uint32_t parity)
     }
 }
 
+// ------------------------------------------------------------------ dependent launch
+// Programmatic dependent launch (PTX griddepcontrol).  grid_dep_launch lets the
+// next kernel of the stream, when it was launched with programmatic stream
+// serialization, start its CTAs (they run their prologue meanwhile);
+// grid_dep_wait blocks until every grid this one depends on has completed and
+// its memory writes are visible.  Both are no-ops for a kernel launched
+// without that attribute.  Every kernel of this library calls grid_dep_wait in
+// every thread before its first global-memory access, so only prologue work
+// (barrier set-up, TMEM allocation, shared memory) overlaps the previous kernel.
+__device__ __forceinline__ void grid_dep_launch()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dep_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // 2^x on the special-function unit (PTX ex2.approx.ftz.f32).
 __device__ __forceinline__ float ex2(float x)
 {

@@ -33,8 +33,8 @@ cudaError_t launch_one(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const C
     auto kern = attn_kernel<Mode::Decode, D, kNH, NK, NV, NS>;
     cudaError_t e = ensure_smem_attribute(kern, C::kSmemBytes, smem_attr_done<D, NK, NV, NS>());
     if (e != cudaSuccess) return e;
-    kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(tm_q, tm_k, tm_v, tm_sk, tm_sv, tm_o, p);
-    return cudaGetLastError();
+    return launch_dependent(kern, dim3(grid), dim3(C::kThreads), C::kSmemBytes, stream, tm_q, tm_k, tm_v, tm_sk,
+                            tm_sv, tm_o, p);
 }
 }  // namespace
 

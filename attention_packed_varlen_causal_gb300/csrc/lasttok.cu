@@ -63,6 +63,8 @@ __global__ void __launch_bounds__(kLtThreads)
     const int seq = static_cast<int>(blockIdx.x) / Hkv;
     const int kh = static_cast<int>(blockIdx.x) - seq * Hkv;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    grid_dep_launch();
+    grid_dep_wait();     // the previous kernel of the stream has completed
     __nv_bfloat16 *ks = reinterpret_cast<__nv_bfloat16 *>(lt_smem);    // [128][D]
     __nv_bfloat16 *vs = ks + kLtChunk * D;                              // [128][D]
     float *part = reinterpret_cast<float *>(lt_smem);                   // [8][g][D], after the last chunk
@@ -245,11 +247,10 @@ cudaError_t launch_lt(const void *q, const void *k, const void *v, const int32_t
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     const int64_t grid = static_cast<int64_t>(B) * Hkv;
-    kern<<<static_cast<unsigned>(grid), kLtThreads, smem, stream>>>(
-        static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(k),
-        static_cast<const __nv_bfloat16 *>(v), cu, B, T, max_seqlen, Hq, Hkv, scale_log2,
-        static_cast<__nv_bfloat16 *>(out), lse, dev_status);
-    return cudaGetLastError();
+    return launch_dependent(kern, dim3(static_cast<unsigned>(grid)), dim3(kLtThreads), smem, stream,
+                            static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(k),
+                            static_cast<const __nv_bfloat16 *>(v), cu, B, T, max_seqlen, Hq, Hkv, scale_log2,
+                            static_cast<__nv_bfloat16 *>(out), lse, dev_status);
 }
 }  // namespace
 

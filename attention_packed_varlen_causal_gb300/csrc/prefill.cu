@@ -26,8 +26,10 @@ __global__ void __launch_bounds__(1024) worklist_kernel(const int32_t *__restric
     __shared__ int s_count[kMaxTilesPerSeq + 1];   // sequences per tile count
     __shared__ int s_off[kMaxTilesPerSeq + 2];     // first entry of each tile-count bucket
     const int tid = threadIdx.x;
+    grid_dep_launch();
     if (tid == 0) s_err = 0;
     for (int i = tid; i <= kMaxTilesPerSeq; i += blockDim.x) s_count[i] = 0;
+    grid_dep_wait();
     __syncthreads();
 
     int err = 0;
@@ -82,9 +84,8 @@ cudaError_t launch_prefill_worklist(const int32_t *cu_seqlens, int32_t num_seqs,
                                     int32_t max_seqlen, int32_t *work_hdr, int4 *work, int32_t *dev_status,
                                     cudaStream_t stream)
 {
-    worklist_kernel<<<1, 1024, 0, stream>>>(cu_seqlens, num_seqs, total_tokens, max_seqlen, work_hdr, work,
-                                            dev_status);
-    return cudaGetLastError();
+    return launch_dependent(worklist_kernel, dim3(1), dim3(1024), 0, stream, cu_seqlens, num_seqs, total_tokens,
+                            max_seqlen, work_hdr, work, dev_status);
 }
 
 namespace {
@@ -105,8 +106,8 @@ cudaError_t launch_one(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const C
     auto kern = attn_kernel<Mode::Prefill, D, kNH, NK, NV, NS>;
     cudaError_t e = ensure_smem_attribute(kern, C::kSmemBytes, smem_attr_done<D, NK, NV, NS>());
     if (e != cudaSuccess) return e;
-    kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(tm_q, tm_k, tm_v, tm_k, tm_v, tm_o, p);   // no suffix maps
-    return cudaGetLastError();
+    return launch_dependent(kern, dim3(grid), dim3(C::kThreads), C::kSmemBytes, stream, tm_q, tm_k, tm_v, tm_k, tm_v,
+                            tm_o, p);   // no suffix maps
 }
 }  // namespace
 

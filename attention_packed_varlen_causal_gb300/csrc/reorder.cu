@@ -12,6 +12,7 @@
 // warp moves them with coalesced 16-byte loads and stores.  HBM-bound: it
 // reads and writes 2 * n * Hkv * head_dim * 2 bytes per beam (+ the append).
 #include "bg_internal.h"
+#include "bg_ptx.cuh"
 
 namespace bg {
 
@@ -24,6 +25,8 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock)
                    const uint4 *__restrict__ new_v, int32_t R, int32_t W, int32_t suffix_max, int32_t n,
                    int32_t vec_per_tok, int32_t *dev_status)
 {
+    grid_dep_launch();
+    grid_dep_wait();     // the previous kernel of the stream has completed
     const int64_t beam = static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (beam >= static_cast<int64_t>(R) * W) return;
@@ -65,11 +68,11 @@ cudaError_t launch_suffix_reorder(const void *src_k, const void *src_v, void *ds
     if (beams == 0) return cudaSuccess;
     const int32_t vec_per_tok = Hkv * head_dim * 2 / 16;
     const int64_t blocks = (beams + kWarpsPerBlock - 1) / kWarpsPerBlock;
-    reorder_kernel<<<static_cast<unsigned>(blocks), 32 * kWarpsPerBlock, 0, stream>>>(
-        static_cast<const uint4 *>(src_k), static_cast<const uint4 *>(src_v), static_cast<uint4 *>(dst_k),
-        static_cast<uint4 *>(dst_v), parent_idx, static_cast<const uint4 *>(new_k),
-        static_cast<const uint4 *>(new_v), R, W, suffix_max, n_tokens, vec_per_tok, dev_status);
-    return cudaGetLastError();
+    return launch_dependent(reorder_kernel, dim3(static_cast<unsigned>(blocks)), dim3(32 * kWarpsPerBlock), 0, stream,
+                            static_cast<const uint4 *>(src_k), static_cast<const uint4 *>(src_v),
+                            static_cast<uint4 *>(dst_k), static_cast<uint4 *>(dst_v), parent_idx,
+                            static_cast<const uint4 *>(new_k), static_cast<const uint4 *>(new_v), R, W, suffix_max,
+                            n_tokens, vec_per_tok, dev_status);
 }
 
 }  // namespace bg
