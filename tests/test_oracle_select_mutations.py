@@ -19,7 +19,8 @@ MUTATIONS = [
     ("accumulated score subtracted", "s = (c[r][:, None] + lp[r]).reshape(-1)", "s = (lp[r] - c[r][:, None]).reshape(-1)"),
     ("ties: larger index first", "order = np.lexsort((flat_index, -s))", "order = np.lexsort((-flat_index, -s))"),
     ("lowest scores kept", "order = np.lexsort((flat_index, -s))", "order = np.lexsort((flat_index, s))"),
-    ("parent and token swapped", "parent[r] = (keep // V).astype(np.int32)", "parent[r] = (keep % W).astype(np.int32)"),
+    ("parent and token swapped", "parent[r] = (keep // V).astype(np.int32)\n        token[r] = (keep % V).astype(np.int32)",
+     "parent[r] = (keep % V).astype(np.int32)\n        token[r] = (keep // V).astype(np.int32)"),
     ("best candidate dropped", "keep = order[:W]", "keep = order[1:W + 1]"),
     ("per-beam selection without merge", "keep = order[:W]",
      "keep = np.array([b * V + int(np.argmax(s[b * V:(b + 1) * V])) for b in range(W)])"),
