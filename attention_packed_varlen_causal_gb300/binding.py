@@ -29,6 +29,8 @@ BG_DEVSTAT_TIMEOUT = 0x100
 BG_MAX_SUFFIX = 16
 BG_MAX_SEQLEN = 65536
 BG_NOALLOC_SCRATCH_BYTES = 1 << 20
+BG_MAX_BEAM = 512
+BG_MAX_VOCAB = 1 << 22
 
 # Every symbol include/bg_attn.h declares, with its ctypes signature.
 _P, _I32, _F32, _SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float, ctypes.c_size_t
@@ -45,6 +47,8 @@ SIGNATURES = {
                              _P, _P], ctypes.c_int),
     "bg_beam_suffix_reorder": ([_P, _P, _P, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32, _P, _P],
                                ctypes.c_int),
+    "bg_beam_select_workspace_size": ([_I32] * 3, _SZ),
+    "bg_beam_select": ([_P, _P, _I32, _I32, _I32, _P, _P, _P, _P, _SZ, _P], ctypes.c_int),
 }
 
 
@@ -189,3 +193,21 @@ def bg_beam_suffix_reorder(src_k, src_v, dst_k, dst_v, parent_idx, n_tokens: int
                                        _ptr(dev_status), _stream(stream))
     _check("bg_beam_suffix_reorder", st)
     return dst_k, dst_v
+
+
+def bg_beam_select_workspace_size(R: int, W: int, V: int) -> int:
+    return int(load().bg_beam_select_workspace_size(R, W, V))
+
+
+def bg_beam_select(logits, cum, token_out, parent_out, score_out, *, workspace=None, stream=None):
+    """logits fp32 [R,W,V]; cum fp32 [R,W]; token_out/parent_out int32 [R,W] and
+    score_out fp32 [R,W] (written); workspace a uint8 CUDA tensor of at least
+    bg_beam_select_workspace_size bytes."""
+    R, W, V = logits.shape
+    need = bg_beam_select_workspace_size(R, W, V)
+    if workspace is None:
+        raise ValueError(f"workspace of {need} bytes required (the library never allocates)")
+    st = load().bg_beam_select(_ptr(logits), _ptr(cum), R, W, V, _ptr(token_out), _ptr(parent_out), _ptr(score_out),
+                               _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
+    _check("bg_beam_select", st)
+    return token_out, parent_out, score_out

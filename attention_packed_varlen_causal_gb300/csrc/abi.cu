@@ -346,4 +346,50 @@ bg_status_t bg_beam_suffix_reorder(const void *src_k, const void *src_v, void *d
     return BG_OK;
 }
 
+size_t bg_beam_select_workspace_size(int32_t R, int32_t W, int32_t V)
+{
+    (void)V;
+    if (R < 0 || W <= 0) return 0;
+    const size_t cand = static_cast<size_t>(R) * W * W;     // per-beam candidates: value + token
+    const size_t val_bytes = (cand * sizeof(float) + 255) & ~size_t(255);
+    const size_t tok_bytes = (cand * sizeof(int32_t) + 255) & ~size_t(255);
+    const size_t lse_bytes = (static_cast<size_t>(R) * W * sizeof(float) + 255) & ~size_t(255);
+    return val_bytes + tok_bytes + lse_bytes;
+}
+
+bg_status_t bg_beam_select(const float *logits, const float *cum, int32_t R, int32_t W, int32_t V,
+                           int32_t *token_out, int32_t *parent_out, float *score_out, void *workspace,
+                           size_t workspace_bytes, cudaStream_t stream)
+{
+    if (R < 0) return BG_ERR_INVALID_ARG;
+    if (W < 1 || W > BG_MAX_BEAM || V < W || V > BG_MAX_VOCAB) return BG_ERR_UNSUPPORTED;
+    if (R == 0) return BG_OK;
+    if (!logits || !cum || !token_out || !parent_out || !score_out || !workspace) return BG_ERR_INVALID_ARG;
+    if (!aligned(logits, 16) || !aligned(cum, 4) || !aligned(token_out, 4) || !aligned(parent_out, 4) ||
+        !aligned(score_out, 4) || !aligned(workspace, 256))
+        return BG_ERR_INVALID_ARG;
+    if (workspace_bytes < bg_beam_select_workspace_size(R, W, V)) return BG_ERR_INVALID_ARG;
+    const size_t rw = static_cast<size_t>(R) * W;
+    const size_t lbytes = rw * V * sizeof(float);
+    const void *ins[3] = {logits, cum, workspace};
+    const size_t in_bytes[3] = {lbytes, rw * sizeof(float), workspace_bytes};
+    const void *outs[3] = {token_out, parent_out, score_out};
+    for (int o = 0; o < 3; ++o) {
+        for (int i = 0; i < 3; ++i)
+            if (overlap(outs[o], rw * 4, ins[i], in_bytes[i])) return BG_ERR_INVALID_ARG;
+        for (int o2 = o + 1; o2 < 3; ++o2)
+            if (overlap(outs[o], rw * 4, outs[o2], rw * 4)) return BG_ERR_INVALID_ARG;
+    }
+    const size_t cand = rw * W;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    float *cand_val = reinterpret_cast<float *>(ws);
+    int32_t *cand_tok = reinterpret_cast<int32_t *>(ws + ((cand * sizeof(float) + 255) & ~size_t(255)));
+    float *row_lse = reinterpret_cast<float *>(ws + ((cand * sizeof(float) + 255) & ~size_t(255)) +
+                                               ((cand * sizeof(int32_t) + 255) & ~size_t(255)));
+    if (launch_beam_select(logits, cum, R, W, V, token_out, parent_out, score_out, cand_val, cand_tok, row_lse,
+                           stream) != cudaSuccess)
+        return BG_ERR_CUDA;
+    return BG_OK;
+}
+
 }  // extern "C"

@@ -1,0 +1,371 @@
+// select.cu -- beam candidate selection of one decode step.
+//
+// "SLM 生成式高并发推理引擎：延迟约束下的有效吞吐优化", section 1.1: every decode
+// step selects local candidates from each beam's token distribution, merges them
+// with the accumulated scores and keeps a fixed number W of candidate sequences;
+// the candidates, their scores and the parent index come out.  Readings: the
+// distribution is the softmax of the beam's logits, scores add log-probabilities,
+//     score(b, v) = cum[b] + logits[b, v] - logsumexp_u(logits[b, u]),
+// the W best (b, v) of a request are kept, best first, equal scores by the
+// smaller b * V + v.
+//
+// Two launches on the caller's stream:
+//   1. row_select_kernel, one CTA per beam row: one pass over the row from HBM
+//      computes its logsumexp (online max and sum of exponentials) and a
+//      4096-bin histogram of the top 12 bits of an order-preserving integer key
+//      of every logit; a second pass (the row is still in L2) gathers the
+//      logits at or above the bin that holds the W-th largest into shared
+//      memory (two more radix levels narrow the bin when it holds too many), a
+//      bitonic sort orders them, and the beam's W best (value, token) and its
+//      logsumexp go to the workspace.  A beam's W best tokens contain its whole
+//      share of the request's W best candidates.
+//   2. merge_select_kernel, one CTA per request: the same selection over the
+//      W x W local candidates, keyed by their scores.
+// HBM-bound: the logits are read once; everything else stays on chip or in L2.
+#include "bg_internal.h"
+#include "bg_ptx.cuh"
+
+#include <stdint.h>
+
+namespace bg {
+namespace {
+
+constexpr int kSelThreads = 512;
+constexpr int kCap = 2048;          // candidates a CTA can gather and sort
+constexpr int kBins = 4096;         // 12-bit radix digits
+
+// Order-preserving map fp32 -> uint32: a larger float gets a larger key (-inf lowest).
+__device__ __forceinline__ uint32_t f2key(float f)
+{
+    const uint32_t u = __float_as_uint(f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key2f(uint32_t k)
+{
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+struct SelShared {
+    uint32_t hist[kBins];
+    uint32_t ck[kCap];
+    int32_t ci[kCap];
+    float red_m[kSelThreads / 32];
+    float red_s[kSelThreads / 32];
+    uint32_t warp_tot[kSelThreads / 32];
+    int n_cand;
+    uint32_t digit;        // selected bin of the current level
+    uint32_t above;        // keys in higher bins of the current level (plus earlier levels)
+};
+
+// Finds, over hist[0..nbins), the bin d where the count of keys in bins >= d first
+// reaches `need` (counting from the top).  Writes sh.digit = d and adds the count of
+// keys in bins > d to sh.above.  nbins = kBins or 256; all threads call it.
+__device__ void find_digit(SelShared &sh, int nbins, uint32_t need)
+{
+    const int tid = threadIdx.x;
+    const int per = nbins / kSelThreads > 0 ? nbins / kSelThreads : 1;   // bins per thread (8 or 1)
+    const int active = nbins / per;                                      // threads that own bins
+    // thread t owns bins [top - per*(t+1) + 1, top - per*t], counted from the top
+    uint32_t local = 0;
+    if (tid < active)
+        for (int k = 0; k < per; ++k) local += sh.hist[nbins - 1 - (tid * per + k)];
+    // exclusive scan of `local` over threads (descending bin order)
+    const int lane = tid & 31, warp = tid >> 5;
+    uint32_t incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) sh.warp_tot[warp] = incl;
+    __syncthreads();
+    uint32_t before = 0;
+    for (int w = 0; w < warp; ++w) before += sh.warp_tot[w];
+    const uint32_t excl = before + incl - local;
+    __syncthreads();
+    if (tid < active && excl < need && excl + local >= need) {
+        uint32_t acc = excl;
+        for (int k = 0; k < per; ++k) {
+            const int bin = nbins - 1 - (tid * per + k);
+            const uint32_t c = sh.hist[bin];
+            if (acc + c >= need) {
+                sh.digit = static_cast<uint32_t>(bin);
+                sh.above += acc;
+                break;
+            }
+            acc += c;
+        }
+    }
+    __syncthreads();
+}
+
+// Sorts sh.ck/ci[0..n) (padded to a power of two with sentinels) so that higher keys
+// come first and equal keys keep the smaller index first.
+__device__ void sort_candidates(SelShared &sh, int n)
+{
+    int P = 2;
+    while (P < n) P <<= 1;
+    for (int i = n + threadIdx.x; i < P; i += kSelThreads) {
+        sh.ck[i] = 0u;
+        sh.ci[i] = 0x7fffffff;
+    }
+    __syncthreads();
+    for (int k = 2; k <= P; k <<= 1) {
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            for (int i = threadIdx.x; i < P; i += kSelThreads) {
+                const int l = i ^ j;
+                if (l > i) {
+                    const uint32_t ka = sh.ck[i], kb = sh.ck[l];
+                    const int32_t ia = sh.ci[i], ib = sh.ci[l];
+                    const bool a_first = ka > kb || (ka == kb && ia < ib);
+                    const bool first_half = (i & k) == 0;
+                    if (first_half != a_first) {
+                        sh.ck[i] = kb;
+                        sh.ck[l] = ka;
+                        sh.ci[i] = ib;
+                        sh.ci[l] = ia;
+                    }
+                }
+            }
+            __syncthreads();
+        }
+    }
+}
+
+// Selection of the W highest keys of n elements (key(i) for element i; equal keys by
+// smaller i), given the level-1 histogram of key >> 20 in sh.hist.  Leaves the W
+// winners sorted in sh.ck/ci[0..W).  n >= W >= 1.
+template <typename KeyFn>
+__device__ void select_top(SelShared &sh, int n, int W, KeyFn key)
+{
+    const int tid = threadIdx.x;
+    if (tid == 0) {
+        sh.above = 0;
+        sh.n_cand = 0;
+    }
+    __syncthreads();
+    find_digit(sh, kBins, static_cast<uint32_t>(W));
+    const uint32_t d1 = sh.digit;
+    uint32_t lo_key;                    // gather every key >= lo_key (all fit) ...
+    bool exact = false;                 // ... or, at the last level, keys > T and the first equal ones
+    if (sh.above + sh.hist[d1] <= static_cast<uint32_t>(kCap)) {
+        lo_key = d1 << 20;
+    } else {
+        // level 2: bits 19..8 of the keys in bin d1
+        const uint32_t need1 = static_cast<uint32_t>(W) - sh.above;
+        __syncthreads();
+        for (int b = tid; b < kBins; b += kSelThreads) sh.hist[b] = 0u;
+        __syncthreads();
+        for (int i = tid; i < n; i += kSelThreads) {
+            const uint32_t k = key(i);
+            if ((k >> 20) == d1) atomicAdd(&sh.hist[(k >> 8) & 0xfffu], 1u);
+        }
+        __syncthreads();
+        find_digit(sh, kBins, need1);
+        const uint32_t d2 = sh.digit;
+        if (sh.above + sh.hist[d2] <= static_cast<uint32_t>(kCap)) {
+            lo_key = (d1 << 20) | (d2 << 8);
+        } else {
+            // level 3: bits 7..0 give the exact key T of the W-th element
+            const uint32_t need2 = static_cast<uint32_t>(W) - sh.above;
+            const uint32_t pre = (d1 << 12) | d2;
+            __syncthreads();
+            for (int b = tid; b < 256; b += kSelThreads) sh.hist[b] = 0u;
+            __syncthreads();
+            for (int i = tid; i < n; i += kSelThreads) {
+                const uint32_t k = key(i);
+                if ((k >> 8) == pre) atomicAdd(&sh.hist[k & 0xffu], 1u);
+            }
+            __syncthreads();
+            find_digit(sh, 256, need2);
+            lo_key = (pre << 8) | sh.digit;
+            exact = true;
+        }
+    }
+    __syncthreads();
+    if (!exact) {
+        for (int i = tid; i < n; i += kSelThreads) {
+            const uint32_t k = key(i);
+            if (k >= lo_key) {
+                const int pos = atomicAdd(&sh.n_cand, 1);
+                sh.ck[pos] = k;
+                sh.ci[pos] = i;
+            }
+        }
+        __syncthreads();
+    } else {
+        // keys above T (fewer than W), then the first W - above keys equal to T in index order
+        const uint32_t T = lo_key;
+        for (int i = tid; i < n; i += kSelThreads) {
+            const uint32_t k = key(i);
+            if (k > T) {
+                const int pos = atomicAdd(&sh.n_cand, 1);
+                sh.ck[pos] = k;
+                sh.ci[pos] = i;
+            }
+        }
+        __syncthreads();
+        const int base = sh.n_cand;
+        const int need = W - base;
+        int taken = 0;
+        const int lane = tid & 31, warp = tid >> 5;
+        for (int c0 = 0; c0 < n && taken < need; c0 += kSelThreads) {
+            const int i = c0 + tid;
+            const bool eq = i < n && key(i) == T;
+            const uint32_t bal = __ballot_sync(0xffffffffu, eq);
+            if (lane == 0) sh.warp_tot[warp] = __popc(bal);
+            __syncthreads();
+            int before = taken;
+            for (int w = 0; w < warp; ++w) before += static_cast<int>(sh.warp_tot[w]);
+            const int pos = before + __popc(bal & ((1u << lane) - 1u));
+            if (eq && pos < need) {
+                sh.ck[base + pos] = T;
+                sh.ci[base + pos] = i;
+            }
+            int tot = 0;
+            for (int w = 0; w < kSelThreads / 32; ++w) tot += static_cast<int>(sh.warp_tot[w]);
+            taken += tot;
+            __syncthreads();
+        }
+        if (tid == 0) sh.n_cand = W;
+        __syncthreads();
+    }
+    sort_candidates(sh, sh.n_cand);
+}
+
+__global__ void __launch_bounds__(kSelThreads)
+    row_select_kernel(const float *__restrict__ logits, int32_t V, int32_t W, float *__restrict__ cand_val,
+                      int32_t *__restrict__ cand_tok, float *__restrict__ row_lse)
+{
+    __shared__ SelShared sh;
+    grid_dep_launch();
+    const int tid = threadIdx.x;
+    for (int b = tid; b < kBins; b += kSelThreads) sh.hist[b] = 0u;
+    grid_dep_wait();     // the previous kernel of the stream has completed
+    __syncthreads();
+    const int64_t row = blockIdx.x;
+    const float *x = logits + row * static_cast<int64_t>(V);
+    constexpr float kL2E = 1.4426950408889634f;
+    // pass 1: online max / sum of exponentials and the level-1 histogram
+    float m = -INFINITY, s = 0.f;
+    auto add4 = [&](float a, float b, float c, float d) {
+        const float mx = fmaxf(fmaxf(a, b), fmaxf(c, d));
+        const float mn = fmaxf(m, mx);
+        if (mn > -INFINITY) {
+            s = s * ex2((m - mn) * kL2E) + ex2((a - mn) * kL2E) + ex2((b - mn) * kL2E) + ex2((c - mn) * kL2E) +
+                ex2((d - mn) * kL2E);
+            m = mn;
+        }
+        atomicAdd(&sh.hist[f2key(a) >> 20], 1u);
+        atomicAdd(&sh.hist[f2key(b) >> 20], 1u);
+        atomicAdd(&sh.hist[f2key(c) >> 20], 1u);
+        atomicAdd(&sh.hist[f2key(d) >> 20], 1u);
+    };
+    if ((V & 3) == 0) {
+        const float4 *x4 = reinterpret_cast<const float4 *>(x);
+        for (int i = tid; i < V / 4; i += kSelThreads) {
+            const float4 f = __ldcs(x4 + i);   // streamed: read from HBM once
+            add4(f.x, f.y, f.z, f.w);
+        }
+    } else {
+        for (int i = tid; i < V; i += kSelThreads) {
+            const float a = __ldcs(x + i);
+            const float mn = fmaxf(m, a);
+            if (mn > -INFINITY) {
+                s = s * ex2((m - mn) * kL2E) + ex2((a - mn) * kL2E);
+                m = mn;
+            }
+            atomicAdd(&sh.hist[f2key(a) >> 20], 1u);
+        }
+    }
+    // combine (m, s) over the CTA
+    const int lane = tid & 31, warp = tid >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+        const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+        const float mn = fmaxf(m, m2);
+        if (mn > -INFINITY) {
+            s = s * ex2((m - mn) * kL2E) + s2 * ex2((m2 - mn) * kL2E);
+            m = mn;
+        }
+    }
+    if (lane == 0) {
+        sh.red_m[warp] = m;
+        sh.red_s[warp] = s;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        float M = -INFINITY, S = 0.f;
+        for (int w = 0; w < kSelThreads / 32; ++w) {
+            const float mn = fmaxf(M, sh.red_m[w]);
+            if (mn > -INFINITY) {
+                S = S * ex2((M - mn) * kL2E) + sh.red_s[w] * ex2((sh.red_m[w] - mn) * kL2E);
+                M = mn;
+            }
+        }
+        row_lse[row] = M + __logf(S);
+    }
+    // pass 2 onward: the W best logits of the row (the row is still in L2)
+    select_top(sh, V, W, [&](int i) -> uint32_t { return f2key(x[i]); });
+    for (int k = tid; k < W; k += kSelThreads) {
+        cand_val[row * W + k] = key2f(sh.ck[k]);
+        cand_tok[row * W + k] = sh.ci[k];
+    }
+}
+
+__global__ void __launch_bounds__(kSelThreads)
+    merge_select_kernel(const float *__restrict__ cand_val, const int32_t *__restrict__ cand_tok,
+                        const float *__restrict__ row_lse, const float *__restrict__ cum, int32_t W,
+                        int32_t *__restrict__ token_out, int32_t *__restrict__ parent_out,
+                        float *__restrict__ score_out)
+{
+    __shared__ SelShared sh;
+    grid_dep_launch();
+    const int tid = threadIdx.x;
+    for (int b = tid; b < kBins; b += kSelThreads) sh.hist[b] = 0u;
+    grid_dep_wait();     // the row selection has completed
+    __syncthreads();
+    const int64_t r = blockIdx.x;
+    const int n = W * W;
+    const float *val = cand_val + r * n;
+    const float *lse = row_lse + r * W;
+    const float *cr = cum + r * W;
+    // candidate i = b * W + k: the k-th best token of beam b; its score as a key
+    auto key = [&](int i) -> uint32_t {
+        const int b = i / W;
+        return f2key(cr[b] + (val[i] - lse[b]));
+    };
+    for (int i = tid; i < n; i += kSelThreads) atomicAdd(&sh.hist[key(i) >> 20], 1u);
+    __syncthreads();
+    // equal scores: the smaller candidate number is the smaller b * V + v (beams in order,
+    // and a beam's candidates with equal scores have equal logits, kept in token order)
+    select_top(sh, n, W, key);
+    for (int k = tid; k < W; k += kSelThreads) {
+        const int i = sh.ci[k];
+        const int b = i / W;
+        token_out[r * W + k] = cand_tok[r * n + i];
+        parent_out[r * W + k] = b;
+        score_out[r * W + k] = key2f(sh.ck[k]);
+    }
+}
+
+}  // namespace
+
+int beam_select_max_width() { return kCap / 2; }
+
+cudaError_t launch_beam_select(const float *logits, const float *cum, int32_t R, int32_t W, int32_t V,
+                               int32_t *token_out, int32_t *parent_out, float *score_out, float *cand_val,
+                               int32_t *cand_tok, float *row_lse, cudaStream_t stream)
+{
+    const int64_t rows = static_cast<int64_t>(R) * W;
+    if (rows == 0) return cudaSuccess;
+    cudaError_t e = launch_dependent(row_select_kernel, dim3(static_cast<unsigned>(rows)), dim3(kSelThreads), 0,
+                                     stream, logits, V, W, cand_val, cand_tok, row_lse);
+    if (e != cudaSuccess) return e;
+    return launch_dependent(merge_select_kernel, dim3(static_cast<unsigned>(R)), dim3(kSelThreads), 0, stream,
+                            static_cast<const float *>(cand_val), static_cast<const int32_t *>(cand_tok),
+                            static_cast<const float *>(row_lse), cum, W, token_out, parent_out, score_out);
+}
+
+}  // namespace bg

@@ -64,6 +64,10 @@ typedef enum {
  * Hq/Hkv <= 128; suffix_max <= BG_MAX_SUFFIX; max_seqlen <= BG_MAX_SEQLEN. */
 #define BG_MAX_SUFFIX 16
 #define BG_MAX_SEQLEN 65536
+/* Beam width of bg_beam_select: 1 <= W <= BG_MAX_BEAM (the page's configurations
+ * keep at most 400 beams); vocabulary: W <= V <= BG_MAX_VOCAB. */
+#define BG_MAX_BEAM 512
+#define BG_MAX_VOCAB (1 << 22)
 
 /* Human-readable name of a status code (static storage, never NULL). */
 const char *bg_status_string(bg_status_t status);
@@ -218,6 +222,38 @@ bg_status_t bg_beam_suffix_reorder(const void *src_k, const void *src_v,
                                    int32_t R, int32_t W, int32_t suffix_max, int32_t n_tokens,
                                    int32_t Hkv, int32_t head_dim,
                                    int32_t *dev_status, cudaStream_t stream);
+
+/*
+ * Beam candidate selection of one decode step.  Source: section 1.1 of the page
+ * above: each step selects local candidates from every beam's token
+ * distribution, merges them with the accumulated scores and keeps W candidate
+ * sequences; candidates, scores and the parent index come out (the parent
+ * index is what bg_beam_suffix_reorder consumes next).  For request r, beam b
+ * and token v:
+ *     score(b, v) = cum[r, b] + logits[r, b, v] - log sum_u exp(logits[r, b, u])
+ * and the W candidates (b, v) with the highest scores are kept, best first,
+ * equal scores by the smaller b * V + v (all in fp32).  The first step of a
+ * search is the same call with only beam 0 alive (cum = 0, -inf, ..., -inf).
+ *
+ *   logits       fp32 [R, W, V] next-token logits of every beam, 16-byte aligned
+ *   cum          fp32 [R, W] accumulated scores (-inf marks a dead beam)
+ *   token_out    int32 [R, W]  kept candidate k of request r: its token v
+ *   parent_out   int32 [R, W]  ... its parent beam b (in [0, W))
+ *   score_out    fp32  [R, W]  ... its score (the new accumulated score)
+ *   workspace    device scratch of at least bg_beam_select_workspace_size(R, W, V)
+ *                bytes, 256-byte aligned (per-beam candidates between the two
+ *                kernels); contents on entry do not matter
+ * Outputs must not overlap the inputs or the workspace.  Two launches on
+ * `stream`; the logits are read once.
+ * Errors: BG_ERR_INVALID_ARG for NULL/misaligned pointers, R < 0, a too small
+ * workspace or overlaps; BG_ERR_UNSUPPORTED unless 1 <= W <= BG_MAX_BEAM and
+ * W <= V <= BG_MAX_VOCAB.
+ */
+size_t bg_beam_select_workspace_size(int32_t R, int32_t W, int32_t V);
+bg_status_t bg_beam_select(const float *logits, const float *cum,
+                           int32_t R, int32_t W, int32_t V,
+                           int32_t *token_out, int32_t *parent_out, float *score_out,
+                           void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
  * Allocation-free variant of bg_packed_prefill_attn.  The paper has no

@@ -126,3 +126,30 @@ def reorder(lib, **kw):
 ])
 def test_reorder_host_validation(lib, kw, expect):
     assert reorder(lib, **kw) == expect
+
+
+def test_beam_select_host_checks(lib):
+    ws = lib.bg_beam_select_workspace_size(32, 100, 65536)
+    assert ws % 256 == 0 and ws >= 32 * 100 * 100 * 8 + 32 * 100 * 4
+    assert lib.bg_beam_select_workspace_size(-1, 4, 8) == 0
+
+    def sel(**kw):
+        a = dict(logits=FAKE, cum=FAKE * 2, R=2, W=4, V=16, tok=FAKE * 3, par=FAKE * 4, sc=FAKE * 5, ws=FAKE * 6,
+                 wsb=1 << 20)
+        a.update(kw)
+        return lib.bg_beam_select(a["logits"], a["cum"], a["R"], a["W"], a["V"], a["tok"], a["par"], a["sc"],
+                                  a["ws"], a["wsb"], None)
+
+    assert sel(R=0) == binding.BG_OK                         # nothing to do, nothing launched
+    assert sel(R=-1) == binding.BG_ERR_INVALID_ARG
+    assert sel(W=0) == binding.BG_ERR_UNSUPPORTED
+    assert sel(W=binding.BG_MAX_BEAM + 1, V=1 << 20) == binding.BG_ERR_UNSUPPORTED
+    assert sel(V=3) == binding.BG_ERR_UNSUPPORTED            # fewer tokens than beams
+    assert sel(V=binding.BG_MAX_VOCAB + 1) == binding.BG_ERR_UNSUPPORTED
+    assert sel(logits=None) == binding.BG_ERR_INVALID_ARG
+    assert sel(tok=None) == binding.BG_ERR_INVALID_ARG
+    assert sel(logits=FAKE + 4) == binding.BG_ERR_INVALID_ARG   # logits need 16-byte alignment
+    assert sel(ws=FAKE + 16) == binding.BG_ERR_INVALID_ARG     # workspace needs 256-byte alignment
+    assert sel(wsb=16) == binding.BG_ERR_INVALID_ARG
+    assert sel(tok=FAKE * 8 + 64, logits=FAKE * 8) == binding.BG_ERR_INVALID_ARG   # output inside the logits
+    assert sel(par=FAKE * 3) == binding.BG_ERR_INVALID_ARG               # two outputs overlap
