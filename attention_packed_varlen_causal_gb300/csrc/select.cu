@@ -132,6 +132,24 @@ __device__ void sort_candidates(SelShared &sh, int n)
     }
 }
 
+// Calls body(i, key(i)) for every element i < n owned by this thread, loading eight
+// keys before using any, so that eight loads per thread are in flight (the passes
+// over a row are otherwise bound by load latency, not bandwidth).
+template <typename KeyFn, typename Body>
+__device__ __forceinline__ void for_each_key(int n, KeyFn key, Body body)
+{
+    constexpr int U = 8;
+    int i = threadIdx.x;
+    for (; i + (U - 1) * kSelThreads < n; i += U * kSelThreads) {
+        uint32_t k[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) k[u] = key(i + u * kSelThreads);
+#pragma unroll
+        for (int u = 0; u < U; ++u) body(i + u * kSelThreads, k[u]);
+    }
+    for (; i < n; i += kSelThreads) body(i, key(i));
+}
+
 // Selection of the W highest keys of n elements (key(i) for element i; equal keys by
 // smaller i), given the level-1 histogram of key >> 20 in sh.hist.  Leaves the W
 // winners sorted in sh.ck/ci[0..W).  n >= W >= 1.
@@ -156,10 +174,9 @@ __device__ void select_top(SelShared &sh, int n, int W, KeyFn key)
         __syncthreads();
         for (int b = tid; b < kBins; b += kSelThreads) sh.hist[b] = 0u;
         __syncthreads();
-        for (int i = tid; i < n; i += kSelThreads) {
-            const uint32_t k = key(i);
+        for_each_key(n, key, [&](int, uint32_t k) {
             if ((k >> 20) == d1) atomicAdd(&sh.hist[(k >> 8) & 0xfffu], 1u);
-        }
+        });
         __syncthreads();
         find_digit(sh, kBins, need1);
         const uint32_t d2 = sh.digit;
@@ -172,10 +189,9 @@ __device__ void select_top(SelShared &sh, int n, int W, KeyFn key)
             __syncthreads();
             for (int b = tid; b < 256; b += kSelThreads) sh.hist[b] = 0u;
             __syncthreads();
-            for (int i = tid; i < n; i += kSelThreads) {
-                const uint32_t k = key(i);
+            for_each_key(n, key, [&](int, uint32_t k) {
                 if ((k >> 8) == pre) atomicAdd(&sh.hist[k & 0xffu], 1u);
-            }
+            });
             __syncthreads();
             find_digit(sh, 256, need2);
             lo_key = (pre << 8) | sh.digit;
@@ -184,26 +200,24 @@ __device__ void select_top(SelShared &sh, int n, int W, KeyFn key)
     }
     __syncthreads();
     if (!exact) {
-        for (int i = tid; i < n; i += kSelThreads) {
-            const uint32_t k = key(i);
+        for_each_key(n, key, [&](int i, uint32_t k) {
             if (k >= lo_key) {
                 const int pos = atomicAdd(&sh.n_cand, 1);
                 sh.ck[pos] = k;
                 sh.ci[pos] = i;
             }
-        }
+        });
         __syncthreads();
     } else {
         // keys above T (fewer than W), then the first W - above keys equal to T in index order
         const uint32_t T = lo_key;
-        for (int i = tid; i < n; i += kSelThreads) {
-            const uint32_t k = key(i);
+        for_each_key(n, key, [&](int i, uint32_t k) {
             if (k > T) {
                 const int pos = atomicAdd(&sh.n_cand, 1);
                 sh.ck[pos] = k;
                 sh.ci[pos] = i;
             }
-        }
+        });
         __syncthreads();
         const int base = sh.n_cand;
         const int need = W - base;
@@ -263,13 +277,22 @@ __global__ void __launch_bounds__(kSelThreads)
     };
     if ((V & 3) == 0) {
         const float4 *x4 = reinterpret_cast<const float4 *>(x);
-        for (int i = tid; i < V / 4; i += kSelThreads) {
-            const float4 f = __ldcs(x4 + i);   // streamed: read from HBM once
+        const int n4 = V / 4;
+        int i = tid;
+        for (; i + 3 * kSelThreads < n4; i += 4 * kSelThreads) {
+            float4 f[4];   // four loads in flight before any is used
+#pragma unroll
+            for (int u = 0; u < 4; ++u) f[u] = x4[i + u * kSelThreads];   // default caching: read again by the gather
+#pragma unroll
+            for (int u = 0; u < 4; ++u) add4(f[u].x, f[u].y, f[u].z, f[u].w);
+        }
+        for (; i < n4; i += kSelThreads) {
+            const float4 f = x4[i];
             add4(f.x, f.y, f.z, f.w);
         }
     } else {
         for (int i = tid; i < V; i += kSelThreads) {
-            const float a = __ldcs(x + i);
+            const float a = x[i];
             const float mn = fmaxf(m, a);
             if (mn > -INFINITY) {
                 s = s * ex2((m - mn) * kL2E) + ex2((a - mn) * kL2E);
@@ -307,7 +330,8 @@ __global__ void __launch_bounds__(kSelThreads)
         row_lse[row] = M + __logf(S);
     }
     // pass 2 onward: the W best logits of the row (the row is still in L2)
-    select_top(sh, V, W, [&](int i) -> uint32_t { return f2key(x[i]); });
+    // evict-first: the gather pass is the row's last use
+    select_top(sh, V, W, [&](int i) -> uint32_t { return f2key(__ldcs(x + i)); });
     for (int k = tid; k < W; k += kSelThreads) {
         cand_val[row * W + k] = key2f(sh.ck[k]);
         cand_tok[row * W + k] = sh.ci[k];
@@ -336,7 +360,7 @@ __global__ void __launch_bounds__(kSelThreads)
         const int b = i / W;
         return f2key(cr[b] + (val[i] - lse[b]));
     };
-    for (int i = tid; i < n; i += kSelThreads) atomicAdd(&sh.hist[key(i) >> 20], 1u);
+    for_each_key(n, key, [&](int, uint32_t k) { atomicAdd(&sh.hist[k >> 20], 1u); });
     __syncthreads();
     // equal scores: the smaller candidate number is the smaller b * V + v (beams in order,
     // and a beam's candidates with equal scores have equal logits, kept in token order)

@@ -390,6 +390,7 @@ def run_ours(args):
     # H2D of q, k, v, cu_seqlens and D2H of the output inside the timed region
     e2e = run_e2e(pre, device, stream, args)
     last = run_last_token(pre, stream, peaks)
+    select = run_beam_select(device, stream, peaks)
 
     # oracle CPU baseline (rank 0, N = 1 only)
     cpu = None
@@ -423,7 +424,7 @@ def run_ours(args):
                     "avg_call_us": round(avg_call_s * 1e6, 2), "tokens_per_s": round(world * pre.T * layers * args.steps / (prefill_ms / 1e3), 1)},
         "decode": {"beam_short": dec_report(dec_s, short_ms), "beam_long": dec_report(dec_l, long_ms)},
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk, "gpu_launches": launches,
-        "last_token": last,
+        "last_token": last, "beam_select": select,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -459,6 +460,48 @@ def run_last_token(pre, stream, peaks, reps: int = 5):
             "us_per_layer": round(us, 2), "bytes_per_layer": by, "achieved_gbs": round(gbs, 1),
             "hbm_frac": round(gbs / peaks["hbm_gbs"], 4), "bound": "hbm",
             "definition": "bg_packed_last_token_attn per layer, timed apart from the step (not in value)"}
+
+
+SELECT_VOCAB = 65536   # the pages give no vocabulary size; selection cost is linear in it
+
+
+def run_beam_select(device, stream, peaks, reps: int = 5):
+    """Beam candidate selection of one decode step (bg_beam_select) on the two beam
+    configurations' shapes, timed apart from the step: fp32 logits N(0, 3) of every beam
+    over SELECT_VOCAB tokens (0.84 / 1.68 GB, larger than L2), accumulated scores N(-3, 1)."""
+    import torch
+    from attention_packed_varlen_causal_gb300 import binding as bg
+    res = {}
+    g = torch.Generator(device=device)
+    for name in ("beam_short", "beam_long"):
+        cfg = wl.DECODE_CONFIGS[name]
+        R, W, V = cfg.R, cfg.W, SELECT_VOCAB
+        g.manual_seed(4000 + R)
+        logits = torch.randn((R, W, V), generator=g, device=device) * 3.0
+        cum = torch.randn((R, W), generator=g, device=device) - 3.0
+        tok = torch.empty((R, W), dtype=torch.int32, device=device)
+        par = torch.empty((R, W), dtype=torch.int32, device=device)
+        sc = torch.empty((R, W), dtype=torch.float32, device=device)
+        ws = torch.empty(bg.bg_beam_select_workspace_size(R, W, V), dtype=torch.uint8, device=device)
+        with torch.cuda.stream(stream):
+            for _ in range(2):
+                bg.bg_beam_select(logits, cum, tok, par, sc, workspace=ws, stream=stream)
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                bg.bg_beam_select(logits, cum, tok, par, sc, workspace=ws, stream=stream)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / reps
+        by = float(R * W * V * 4 + R * W * 4 * 4)      # logits once; cum in; token, parent, score out
+        gbs = by / us / 1e3
+        res[name] = {"workload": f"R{R} W{W} V{V} fp32 logits", "us_per_call": round(us, 2), "bytes": by,
+                     "achieved_gbs": round(gbs, 1), "hbm_frac": round(gbs / peaks["hbm_gbs"], 4)}
+        del logits
+    res["definition"] = ("bg_beam_select per decode step (per-beam logsumexp + top-W, merged by accumulated score), "
+                         "timed apart from the step (not in value); bound: HBM, logits read once")
+    return res
 
 
 def run_e2e(pre, device, stream, args):
