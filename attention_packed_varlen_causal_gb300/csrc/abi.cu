@@ -351,10 +351,9 @@ size_t bg_beam_select_workspace_size(int32_t R, int32_t W, int32_t V)
     (void)V;
     if (R < 0 || W <= 0) return 0;
     const size_t cand = static_cast<size_t>(R) * W * W;     // per-beam candidates: value + token
-    const size_t val_bytes = (cand * sizeof(float) + 255) & ~size_t(255);
-    const size_t tok_bytes = (cand * sizeof(int32_t) + 255) & ~size_t(255);
-    const size_t lse_bytes = (static_cast<size_t>(R) * W * sizeof(float) + 255) & ~size_t(255);
-    return val_bytes + tok_bytes + lse_bytes;
+    const size_t part = static_cast<size_t>(R) * beam_select_slices(R, W) * W;   // merge level 1: key + index
+    auto al = [](size_t b) { return (b + 255) & ~size_t(255); };
+    return al(cand * 4) + al(cand * 4) + al(static_cast<size_t>(R) * W * 4) + al(part * 4) + al(part * 4);
 }
 
 bg_status_t bg_beam_select(const float *logits, const float *cum, int32_t R, int32_t W, int32_t V,
@@ -381,13 +380,16 @@ bg_status_t bg_beam_select(const float *logits, const float *cum, int32_t R, int
             if (overlap(outs[o], rw * 4, outs[o2], rw * 4)) return BG_ERR_INVALID_ARG;
     }
     const size_t cand = rw * W;
+    const size_t part = static_cast<size_t>(R) * beam_select_slices(R, W) * W;
+    auto al = [](size_t b) { return (b + 255) & ~size_t(255); };
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     float *cand_val = reinterpret_cast<float *>(ws);
-    int32_t *cand_tok = reinterpret_cast<int32_t *>(ws + ((cand * sizeof(float) + 255) & ~size_t(255)));
-    float *row_lse = reinterpret_cast<float *>(ws + ((cand * sizeof(float) + 255) & ~size_t(255)) +
-                                               ((cand * sizeof(int32_t) + 255) & ~size_t(255)));
+    int32_t *cand_tok = reinterpret_cast<int32_t *>(ws + al(cand * 4));
+    float *row_lse = reinterpret_cast<float *>(ws + 2 * al(cand * 4));
+    uint32_t *part_key = reinterpret_cast<uint32_t *>(ws + 2 * al(cand * 4) + al(rw * 4));
+    int32_t *part_idx = reinterpret_cast<int32_t *>(ws + 2 * al(cand * 4) + al(rw * 4) + al(part * 4));
     if (launch_beam_select(logits, cum, R, W, V, token_out, parent_out, score_out, cand_val, cand_tok, row_lse,
-                           stream) != cudaSuccess)
+                           part_key, part_idx, stream) != cudaSuccess)
         return BG_ERR_CUDA;
     return BG_OK;
 }

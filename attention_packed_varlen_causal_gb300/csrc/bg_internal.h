@@ -36,11 +36,13 @@ cudaError_t launch_last_token_attn(int head_dim, const void *q, const void *k, c
                                    void *out, float *lse, int32_t *dev_status, cudaStream_t stream);
 int last_token_max_group();
 
-// Beam candidate selection: per-beam selection into (cand_val, cand_tok, row_lse),
-// then the per-request merge into the outputs.
+// Beam candidate selection: per-beam selection into (cand_val, cand_tok, row_lse), the
+// merge's level 1 into (part_key, part_idx) of R * S * W entries, level 2 into the outputs.
+int beam_select_slices(int32_t R, int32_t W);
 cudaError_t launch_beam_select(const float *logits, const float *cum, int32_t R, int32_t W, int32_t V,
                                int32_t *token_out, int32_t *parent_out, float *score_out, float *cand_val,
-                               int32_t *cand_tok, float *row_lse, cudaStream_t stream);
+                               int32_t *cand_tok, float *row_lse, uint32_t *part_key, int32_t *part_idx,
+                               cudaStream_t stream);
 
 cudaError_t launch_suffix_reorder(const void *src_k, const void *src_v, void *dst_k, void *dst_v,
                                   const int32_t *parent_idx, const void *new_k, const void *new_v, int32_t R,

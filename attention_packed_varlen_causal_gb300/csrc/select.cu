@@ -19,8 +19,10 @@
 //      bitonic sort orders them, and the beam's W best (value, token) and its
 //      logsumexp go to the workspace.  A beam's W best tokens contain its whole
 //      share of the request's W best candidates.
-//   2. merge_select_kernel, one CTA per request: the same selection over the
-//      W x W local candidates, keyed by their scores.
+//   2. the merge, the same selection over the W x W local candidates of a request keyed
+//      by their scores, in two levels so that more than R CTAs share it:
+//      merge_part_kernel selects the W best of each of S slices of beams, and
+//      merge_final_kernel the W best of the S * W survivors of each request.
 // HBM-bound: the logits are read once; everything else stays on chip or in L2.
 #include "bg_internal.h"
 #include "bg_ptx.cuh"
@@ -338,11 +340,13 @@ __global__ void __launch_bounds__(kSelThreads)
     }
 }
 
+// Merge, level 1: CTA (r, s) selects the W best of the local candidates of beams
+// [s*W/S, (s+1)*W/S) of request r and writes their score keys and candidate numbers
+// i = b * W + k (its slice is the contiguous range of i starting at b0 * W).
 __global__ void __launch_bounds__(kSelThreads)
-    merge_select_kernel(const float *__restrict__ cand_val, const int32_t *__restrict__ cand_tok,
-                        const float *__restrict__ row_lse, const float *__restrict__ cum, int32_t W,
-                        int32_t *__restrict__ token_out, int32_t *__restrict__ parent_out,
-                        float *__restrict__ score_out)
+    merge_part_kernel(const float *__restrict__ cand_val, const float *__restrict__ row_lse,
+                      const float *__restrict__ cum, int32_t W, int32_t S, uint32_t *__restrict__ part_key,
+                      int32_t *__restrict__ part_idx)
 {
     __shared__ SelShared sh;
     grid_dep_launch();
@@ -350,13 +354,18 @@ __global__ void __launch_bounds__(kSelThreads)
     for (int b = tid; b < kBins; b += kSelThreads) sh.hist[b] = 0u;
     grid_dep_wait();     // the row selection has completed
     __syncthreads();
-    const int64_t r = blockIdx.x;
-    const int n = W * W;
-    const float *val = cand_val + r * n;
+    const int64_t r = blockIdx.x / S;
+    const int s = static_cast<int>(blockIdx.x - r * S);
+    const int b0 = static_cast<int>((static_cast<int64_t>(s) * W) / S);
+    const int b1 = static_cast<int>((static_cast<int64_t>(s + 1) * W) / S);
+    const int base = b0 * W;
+    const int n = (b1 - b0) * W;                      // >= W: every slice holds at least one beam
+    const float *val = cand_val + r * W * W;
     const float *lse = row_lse + r * W;
     const float *cr = cum + r * W;
-    // candidate i = b * W + k: the k-th best token of beam b; its score as a key
-    auto key = [&](int i) -> uint32_t {
+    // local candidate p = candidate base + p: the k-th best token of beam b; its score as a key
+    auto key = [&](int p) -> uint32_t {
+        const int i = base + p;
         const int b = i / W;
         return f2key(cr[b] + (val[i] - lse[b]));
     };
@@ -365,31 +374,72 @@ __global__ void __launch_bounds__(kSelThreads)
     // equal scores: the smaller candidate number is the smaller b * V + v (beams in order,
     // and a beam's candidates with equal scores have equal logits, kept in token order)
     select_top(sh, n, W, key);
+    const int64_t out = blockIdx.x * static_cast<int64_t>(W);
     for (int k = tid; k < W; k += kSelThreads) {
-        const int i = sh.ci[k];
-        const int b = i / W;
-        token_out[r * W + k] = cand_tok[r * n + i];
-        parent_out[r * W + k] = b;
+        part_key[out + k] = sh.ck[k];
+        part_idx[out + k] = base + sh.ci[k];
+    }
+}
+
+// Merge, level 2: one CTA per request selects the W best of its S * W level-1 survivors.
+// Survivors are stored slice by slice (beams ascending), each slice best first with equal
+// keys by candidate number, so equal keys keep candidate order by their position too.
+__global__ void __launch_bounds__(kSelThreads)
+    merge_final_kernel(const uint32_t *__restrict__ part_key, const int32_t *__restrict__ part_idx,
+                       const int32_t *__restrict__ cand_tok, int32_t W, int32_t S, int32_t *__restrict__ token_out,
+                       int32_t *__restrict__ parent_out, float *__restrict__ score_out)
+{
+    __shared__ SelShared sh;
+    grid_dep_launch();
+    const int tid = threadIdx.x;
+    for (int b = tid; b < kBins; b += kSelThreads) sh.hist[b] = 0u;
+    grid_dep_wait();     // level 1 has completed
+    __syncthreads();
+    const int64_t r = blockIdx.x;
+    const int n = S * W;
+    const uint32_t *pk = part_key + r * n;
+    const int32_t *pi = part_idx + r * n;
+    auto key = [&](int p) -> uint32_t { return pk[p]; };
+    for_each_key(n, key, [&](int, uint32_t k) { atomicAdd(&sh.hist[k >> 20], 1u); });
+    __syncthreads();
+    select_top(sh, n, W, key);
+    for (int k = tid; k < W; k += kSelThreads) {
+        const int i = pi[sh.ci[k]];
+        token_out[r * W + k] = cand_tok[r * W * W + i];
+        parent_out[r * W + k] = i / W;
         score_out[r * W + k] = key2f(sh.ck[k]);
     }
 }
 
 }  // namespace
 
-int beam_select_max_width() { return kCap / 2; }
+int beam_select_slices(int32_t R, int32_t W)
+{
+    // about two level-1 CTAs per SM over the requests; every slice keeps at least one beam
+    int S = static_cast<int>((2 * 152 + R - 1) / (R > 0 ? R : 1));
+    if (S > W) S = W;
+    if (S > 16) S = 16;
+    return S < 1 ? 1 : S;
+}
 
 cudaError_t launch_beam_select(const float *logits, const float *cum, int32_t R, int32_t W, int32_t V,
                                int32_t *token_out, int32_t *parent_out, float *score_out, float *cand_val,
-                               int32_t *cand_tok, float *row_lse, cudaStream_t stream)
+                               int32_t *cand_tok, float *row_lse, uint32_t *part_key, int32_t *part_idx,
+                               cudaStream_t stream)
 {
     const int64_t rows = static_cast<int64_t>(R) * W;
     if (rows == 0) return cudaSuccess;
+    const int S = beam_select_slices(R, W);
     cudaError_t e = launch_dependent(row_select_kernel, dim3(static_cast<unsigned>(rows)), dim3(kSelThreads), 0,
                                      stream, logits, V, W, cand_val, cand_tok, row_lse);
     if (e != cudaSuccess) return e;
-    return launch_dependent(merge_select_kernel, dim3(static_cast<unsigned>(R)), dim3(kSelThreads), 0, stream,
-                            static_cast<const float *>(cand_val), static_cast<const int32_t *>(cand_tok),
-                            static_cast<const float *>(row_lse), cum, W, token_out, parent_out, score_out);
+    e = launch_dependent(merge_part_kernel, dim3(static_cast<unsigned>(static_cast<int64_t>(R) * S)),
+                         dim3(kSelThreads), 0, stream, static_cast<const float *>(cand_val),
+                         static_cast<const float *>(row_lse), cum, W, S, part_key, part_idx);
+    if (e != cudaSuccess) return e;
+    return launch_dependent(merge_final_kernel, dim3(static_cast<unsigned>(R)), dim3(kSelThreads), 0, stream,
+                            static_cast<const uint32_t *>(part_key), static_cast<const int32_t *>(part_idx),
+                            static_cast<const int32_t *>(cand_tok), W, S, token_out, parent_out, score_out);
 }
 
 }  // namespace bg

@@ -241,10 +241,10 @@ bg_status_t bg_beam_suffix_reorder(const void *src_k, const void *src_v,
  *   parent_out   int32 [R, W]  ... its parent beam b (in [0, W))
  *   score_out    fp32  [R, W]  ... its score (the new accumulated score)
  *   workspace    device scratch of at least bg_beam_select_workspace_size(R, W, V)
- *                bytes, 256-byte aligned (per-beam candidates between the two
- *                kernels); contents on entry do not matter
- * Outputs must not overlap the inputs or the workspace.  Two launches on
- * `stream`; the logits are read once.
+ *                bytes, 256-byte aligned (per-beam candidates and the merge's
+ *                intermediate survivors); contents on entry do not matter
+ * Outputs must not overlap the inputs or the workspace.  Three launches on
+ * `stream` (per-beam selection, then a two-level merge); the logits are read once.
  * Errors: BG_ERR_INVALID_ARG for NULL/misaligned pointers, R < 0, a too small
  * workspace or overlaps; BG_ERR_UNSUPPORTED unless 1 <= W <= BG_MAX_BEAM and
  * W <= V <= BG_MAX_VOCAB.
