@@ -153,10 +153,12 @@ __device__ __forceinline__ void for_each_key(int n, KeyFn key, Body body)
 }
 
 // Selection of the W highest keys of n elements (key(i) for element i; equal keys by
-// smaller i), given the level-1 histogram of key >> 20 in sh.hist.  Leaves the W
-// winners sorted in sh.ck/ci[0..W).  n >= W >= 1.
-template <typename KeyFn>
-__device__ void select_top(SelShared &sh, int n, int W, KeyFn key)
+// smaller i), given the level-1 histogram of key >> 20 in sh.hist.  visit(body) calls
+// body(i, key(i)) for every element this thread owns, in any order (the bulk passes);
+// key(i) itself serves the rare in-order pass over equal keys.  Leaves the W winners
+// sorted in sh.ck/ci[0..W).  n >= W >= 1.
+template <typename KeyFn, typename VisitFn>
+__device__ void select_top(SelShared &sh, int n, int W, KeyFn key, VisitFn visit)
 {
     const int tid = threadIdx.x;
     if (tid == 0) {
@@ -176,7 +178,7 @@ __device__ void select_top(SelShared &sh, int n, int W, KeyFn key)
         __syncthreads();
         for (int b = tid; b < kBins; b += kSelThreads) sh.hist[b] = 0u;
         __syncthreads();
-        for_each_key(n, key, [&](int, uint32_t k) {
+        visit([&](int, uint32_t k) {
             if ((k >> 20) == d1) atomicAdd(&sh.hist[(k >> 8) & 0xfffu], 1u);
         });
         __syncthreads();
@@ -191,7 +193,7 @@ __device__ void select_top(SelShared &sh, int n, int W, KeyFn key)
             __syncthreads();
             for (int b = tid; b < 256; b += kSelThreads) sh.hist[b] = 0u;
             __syncthreads();
-            for_each_key(n, key, [&](int, uint32_t k) {
+            visit([&](int, uint32_t k) {
                 if ((k >> 8) == pre) atomicAdd(&sh.hist[k & 0xffu], 1u);
             });
             __syncthreads();
@@ -202,7 +204,7 @@ __device__ void select_top(SelShared &sh, int n, int W, KeyFn key)
     }
     __syncthreads();
     if (!exact) {
-        for_each_key(n, key, [&](int i, uint32_t k) {
+        visit([&](int i, uint32_t k) {
             if (k >= lo_key) {
                 const int pos = atomicAdd(&sh.n_cand, 1);
                 sh.ck[pos] = k;
@@ -213,7 +215,7 @@ __device__ void select_top(SelShared &sh, int n, int W, KeyFn key)
     } else {
         // keys above T (fewer than W), then the first W - above keys equal to T in index order
         const uint32_t T = lo_key;
-        for_each_key(n, key, [&](int i, uint32_t k) {
+        visit([&](int i, uint32_t k) {
             if (k > T) {
                 const int pos = atomicAdd(&sh.n_cand, 1);
                 sh.ck[pos] = k;
@@ -268,8 +270,9 @@ __global__ void __launch_bounds__(kSelThreads)
         const float mx = fmaxf(fmaxf(a, b), fmaxf(c, d));
         const float mn = fmaxf(m, mx);
         if (mn > -INFINITY) {
-            s = s * ex2((m - mn) * kL2E) + ex2((a - mn) * kL2E) + ex2((b - mn) * kL2E) + ex2((c - mn) * kL2E) +
-                ex2((d - mn) * kL2E);
+            const float nl = -mn * kL2E;   // 2^(x log2e - mn log2e) = e^(x - mn), one FFMA per exponent
+            s = s * ex2(fmaf(m, kL2E, nl)) + ex2(fmaf(a, kL2E, nl)) + ex2(fmaf(b, kL2E, nl)) + ex2(fmaf(c, kL2E, nl)) +
+                ex2(fmaf(d, kL2E, nl));
             m = mn;
         }
         atomicAdd(&sh.hist[f2key(a) >> 20], 1u);
@@ -333,7 +336,38 @@ __global__ void __launch_bounds__(kSelThreads)
     }
     // pass 2 onward: the W best logits of the row (the row is still in L2)
     // evict-first: the gather pass is the row's last use
-    select_top(sh, V, W, [&](int i) -> uint32_t { return f2key(__ldcs(x + i)); });
+    auto key = [&](int i) -> uint32_t { return f2key(__ldcs(x + i)); };
+    auto visit = [&](auto &&body) {
+        if ((V & 3) == 0) {
+            // four float4 loads in flight per thread, four keys per load
+            const float4 *x4 = reinterpret_cast<const float4 *>(x);
+            const int n4 = V / 4;
+            int j = tid;
+            for (; j + 3 * kSelThreads < n4; j += 4 * kSelThreads) {
+                float4 f[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) f[u] = __ldcs(x4 + j + u * kSelThreads);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int i = 4 * (j + u * kSelThreads);
+                    body(i, f2key(f[u].x));
+                    body(i + 1, f2key(f[u].y));
+                    body(i + 2, f2key(f[u].z));
+                    body(i + 3, f2key(f[u].w));
+                }
+            }
+            for (; j < n4; j += kSelThreads) {
+                const float4 f = __ldcs(x4 + j);
+                body(4 * j, f2key(f.x));
+                body(4 * j + 1, f2key(f.y));
+                body(4 * j + 2, f2key(f.z));
+                body(4 * j + 3, f2key(f.w));
+            }
+        } else {
+            for_each_key(V, key, body);
+        }
+    };
+    select_top(sh, V, W, key, visit);
     for (int k = tid; k < W; k += kSelThreads) {
         cand_val[row * W + k] = key2f(sh.ck[k]);
         cand_tok[row * W + k] = sh.ci[k];
@@ -373,7 +407,7 @@ __global__ void __launch_bounds__(kSelThreads)
     __syncthreads();
     // equal scores: the smaller candidate number is the smaller b * V + v (beams in order,
     // and a beam's candidates with equal scores have equal logits, kept in token order)
-    select_top(sh, n, W, key);
+    select_top(sh, n, W, key, [&](auto &&body) { for_each_key(n, key, body); });
     const int64_t out = blockIdx.x * static_cast<int64_t>(W);
     for (int k = tid; k < W; k += kSelThreads) {
         part_key[out + k] = sh.ck[k];
@@ -402,7 +436,7 @@ __global__ void __launch_bounds__(kSelThreads)
     auto key = [&](int p) -> uint32_t { return pk[p]; };
     for_each_key(n, key, [&](int, uint32_t k) { atomicAdd(&sh.hist[k >> 20], 1u); });
     __syncthreads();
-    select_top(sh, n, W, key);
+    select_top(sh, n, W, key, [&](auto &&body) { for_each_key(n, key, body); });
     for (int k = tid; k < W; k += kSelThreads) {
         const int i = pi[sh.ci[k]];
         token_out[r * W + k] = cand_tok[r * W * W + i];
