@@ -2,11 +2,14 @@
 
     python -m attention_packed_varlen_causal_gb300.profile_case prefill_only --iters 3
     python -m attention_packed_varlen_causal_gb300.profile_case beam_long --iters 2
+    python -m attention_packed_varlen_causal_gb300.profile_case select_long --iters 2
 
 Prefill workloads (tiny, prefill_only, skewed) call bg_packed_prefill_attn
 ``iters`` times on one layer of inputs; decode workloads (beam_short,
 beam_long) run ``iters`` complete beam searches of one layer (per step: the
-suffix reorder + append, then the decode attention).  Inputs are drawn on the
+suffix reorder + append, then the decode attention); selection workloads
+(select_short, select_long) call bg_beam_select ``iters`` times on the beam
+configurations' shapes with fp32 logits N(0, 3) over 65,536 tokens.  Inputs are drawn on the
 device with a seeded generator, shaped as in ``workloads``.  Nothing is
 timed here: use ncu (or bench.py for timings).
 """
@@ -30,7 +33,8 @@ def main(argv=None):
     from attention_packed_varlen_causal_gb300 import workloads as wl
 
     ap = argparse.ArgumentParser()
-    ap.add_argument("workload", choices=sorted(list(wl.PREFILL_CONFIGS) + list(wl.DECODE_CONFIGS)))
+    select = {"select_short": "beam_short", "select_long": "beam_long"}
+    ap.add_argument("workload", choices=sorted(list(wl.PREFILL_CONFIGS) + list(wl.DECODE_CONFIGS) + list(select)))
     ap.add_argument("--iters", type=int, default=3)
     args = ap.parse_args(argv)
     build.build()
@@ -39,7 +43,18 @@ def main(argv=None):
     g = torch.Generator(device=dev)
     g.manual_seed(1234)
     bf = torch.bfloat16
-    if args.workload in wl.PREFILL_CONFIGS:
+    if args.workload in select:
+        cfg = wl.DECODE_CONFIGS[select[args.workload]]
+        R, W, V = cfg.R, cfg.W, 65536
+        logits = torch.randn((R, W, V), generator=g, device=dev) * 3.0
+        cum = torch.randn((R, W), generator=g, device=dev) - 3.0
+        tok = torch.empty((R, W), dtype=torch.int32, device=dev)
+        par = torch.empty_like(tok)
+        sc = torch.empty((R, W), dtype=torch.float32, device=dev)
+        ws = torch.empty(bg.bg_beam_select_workspace_size(R, W, V), dtype=torch.uint8, device=dev)
+        for _ in range(args.iters):
+            bg.bg_beam_select(logits, cum, tok, par, sc, workspace=ws)
+    elif args.workload in wl.PREFILL_CONFIGS:
         cfg = wl.PREFILL_CONFIGS[args.workload]
         lengths = wl.prefill_lengths(cfg)
         cu_np = wl.cu_from_lengths(lengths)

@@ -44,17 +44,17 @@ LAYERS = 28
 
 # DRAM bytes of one attn_kernel<Prefill,128> launch on one layer of the Prefill-Only batch
 # (dram__bytes_read.sum + dram__bytes_write.sum from one ncu capture, written up in
-# profiles/attn_kernel_prefill_prefill_only.md).  It holds only for the kernel sources it was
-# taken on, identified by `sources`; for any other sources the bench reports null.
+# profiles/attn_kernel_prefill_prefill_only.md).  It holds only for the sources that launch is
+# built from, identified by `sources` (kernel_sources_hash); otherwise the bench reports null.
 PREFILL_TRAFFIC = {"sources": "e7f2b68cff50cf36", "bytes": 649622528 + 244686080}
+# the files a bg_packed_prefill_attn launch is built from
+PREFILL_SOURCES = ["abi.cu", "prefill.cu", "bg_attn_kernel.cuh", "bg_ptx.cuh", "bg_internal.h"]
 
 
-def kernel_sources_hash():
-    import glob
+def kernel_sources_hash(names=PREFILL_SOURCES):
     import hashlib
     pkg = os.path.join(ROOT, "attention_packed_varlen_causal_gb300")
-    files = sorted(glob.glob(os.path.join(pkg, "csrc", "*.cu")) + glob.glob(os.path.join(pkg, "csrc", "*.cuh")) +
-                   glob.glob(os.path.join(pkg, "csrc", "*.h")) + glob.glob(os.path.join(ROOT, "include", "*.h")))
+    files = [os.path.join(pkg, "csrc", n) for n in names] + [os.path.join(ROOT, "include", "bg_attn.h")]
     h = hashlib.sha256()
     for f in files:
         h.update(os.path.basename(f).encode())
