@@ -46,7 +46,7 @@ LAYERS = 28
 # (dram__bytes_read.sum + dram__bytes_write.sum from one ncu capture, written up in
 # profiles/attn_kernel_prefill_prefill_only.md).  It holds only for the sources that launch is
 # built from, identified by `sources` (kernel_sources_hash); otherwise the bench reports null.
-PREFILL_TRAFFIC = {"sources": "e7f2b68cff50cf36", "bytes": 649622528 + 244686080}
+PREFILL_TRAFFIC = {"sources": "d29bd9c89bf50150", "bytes": 649762048 + 244366336}
 # the files a bg_packed_prefill_attn launch is built from
 PREFILL_SOURCES = ["abi.cu", "prefill.cu", "bg_attn_kernel.cuh", "bg_ptx.cuh", "bg_internal.h"]
 
