@@ -47,6 +47,8 @@ SIGNATURES = {
                              _P, _P], ctypes.c_int),
     "bg_beam_suffix_reorder": ([_P, _P, _P, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32, _P, _P],
                                ctypes.c_int),
+    "bg_beam_decode_step": ([_P, _P, _P, _P, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _I32,
+                             _I32, _I32, _F32, _P, _P, _P], ctypes.c_int),
     "bg_beam_select_workspace_size": ([_I32] * 3, _SZ),
     "bg_beam_select": ([_P, _P, _I32, _I32, _I32, _P, _P, _P, _P, _SZ, _P], ctypes.c_int),
 }
@@ -193,6 +195,27 @@ def bg_beam_suffix_reorder(src_k, src_v, dst_k, dst_v, parent_idx, n_tokens: int
                                        _ptr(dev_status), _stream(stream))
     _check("bg_beam_suffix_reorder", st)
     return dst_k, dst_v
+
+
+def bg_beam_decode_step(q, prompt_k, prompt_v, cu_prompt, max_prompt_len: int, src_suffix_k, src_suffix_v,
+                        parent_idx, new_k, new_v, dst_suffix_k, dst_suffix_v, suffix_len: int, out, *,
+                        scale: Optional[float] = None, dev_status=None, stream=None):
+    """One decode step in one call: dst[r,b,:t-1] = src[r,parent[r,b],:t-1], dst[r,b,t-1] = new[r,b],
+    then out = decode attention over [prompt ; dst[:, :, :t]] (t = suffix_len >= 1).
+    src/dst [R,W,S_max,Hkv,d] bf16 (src may be None when t == 1); parent_idx int32 [R,W];
+    new_k/new_v [R,W,Hkv,d]; out [R,W,Hq,d] (written)."""
+    R, W, Hq, d = q.shape
+    Hkv = prompt_k.shape[1]
+    S_max = dst_suffix_k.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    st = load().bg_beam_decode_step(_ptr(q), _ptr(prompt_k), _ptr(prompt_v), _ptr(cu_prompt), prompt_k.shape[0],
+                                    int(max_prompt_len), _ptr(src_suffix_k), _ptr(src_suffix_v), _ptr(parent_idx),
+                                    _ptr(new_k), _ptr(new_v), _ptr(dst_suffix_k), _ptr(dst_suffix_v),
+                                    int(suffix_len), S_max, R, W, Hq, Hkv, d, float(scale), _ptr(out),
+                                    _ptr(dev_status), _stream(stream))
+    _check("bg_beam_decode_step", st)
+    return out
 
 
 def bg_beam_select_workspace_size(R: int, W: int, V: int) -> int:

@@ -220,11 +220,31 @@ bg_status_t bg_packed_last_token_attn(const void *q, const void *k, const void *
     return BG_OK;
 }
 
-bg_status_t bg_beam_decode_attn(const void *q, const void *prompt_k, const void *prompt_v, const int32_t *cu_prompt,
-                                int32_t total_prompt_tokens, int32_t max_prompt_len, const void *suffix_k,
-                                const void *suffix_v, int32_t suffix_len, int32_t suffix_max, int32_t R, int32_t W,
-                                int32_t Hq, int32_t Hkv, int32_t head_dim, float scale, void *out,
-                                int32_t *dev_status, cudaStream_t stream)
+}  // extern "C"
+
+namespace {
+
+// Extra operands of a whole decode step (bg_beam_decode_step): the previous step's suffix, the
+// parent index and the new token's K/V.  Null for the plain decode attention.
+struct StepFuse {
+    const void *src_k, *src_v;
+    const int32_t *parent;
+    const void *new_k, *new_v;
+};
+
+// Decode work items: (request, kv head, nh query tiles of BT = 128 / g beams each).
+int32_t decode_pairs_per_rk(int32_t W, int32_t g, int nh)
+{
+    const int32_t BT = 128 / g;
+    const int32_t beam_tiles = (W + BT - 1) / BT;
+    return (beam_tiles + nh - 1) / nh;
+}
+
+bg_status_t decode_impl(const void *q, const void *prompt_k, const void *prompt_v, const int32_t *cu_prompt,
+                        int32_t total_prompt_tokens, int32_t max_prompt_len, const void *suffix_k, const void *suffix_v,
+                        int32_t suffix_len, int32_t suffix_max, int32_t R, int32_t W, int32_t Hq, int32_t Hkv,
+                        int32_t head_dim, float scale, void *out, int32_t *dev_status, const StepFuse *fz,
+                        cudaStream_t stream)
 {
     if (R < 0 || W <= 0 || Hq <= 0 || Hkv <= 0 || head_dim <= 0 || total_prompt_tokens < 0 || max_prompt_len < 0 ||
         suffix_len < 0 || suffix_max < 0 || suffix_len > suffix_max)
@@ -250,13 +270,32 @@ bg_status_t bg_beam_decode_attn(const void *q, const void *prompt_k, const void 
                                                                       overlap(out, qbytes, suffix_v, sbytes))))
         return BG_ERR_INVALID_ARG;
 
+    if (fz) {
+        // whole step: suffix_k/v receive this step's suffix from the reorder kernel before the
+        // attention kernel reads them, so no input may share their bytes
+        if (suffix_len < 1 || !fz->parent || !fz->new_k || !fz->new_v) return BG_ERR_INVALID_ARG;
+        if (suffix_len > 1 && (!fz->src_k || !fz->src_v)) return BG_ERR_INVALID_ARG;
+        if (!aligned(fz->parent, 4) || !aligned(fz->new_k, 16) || !aligned(fz->new_v, 16) ||
+            (fz->src_k && !aligned(fz->src_k, 16)) || (fz->src_v && !aligned(fz->src_v, 16)))
+            return BG_ERR_INVALID_ARG;
+        const size_t nbytes = static_cast<size_t>(R) * W * Hkv * head_dim * 2;
+        const size_t srcbytes = suffix_len > 1 ? sbytes : 0;
+        const void *rd[9] = {q, prompt_k, prompt_v, cu_prompt, fz->parent, fz->new_k, fz->new_v, fz->src_k, fz->src_v};
+        const size_t rdn[9] = {qbytes, pbytes, pbytes, static_cast<size_t>(R + 1) * 4, static_cast<size_t>(R) * W * 4,
+                               nbytes, nbytes, srcbytes, srcbytes};
+        for (int i = 0; i < 9; ++i)
+            if (overlap(suffix_k, sbytes, rd[i], rdn[i]) || overlap(suffix_v, sbytes, rd[i], rdn[i]) ||
+                (i >= 4 && overlap(out, qbytes, rd[i], rdn[i])))
+                return BG_ERR_INVALID_ARG;
+        if (overlap(suffix_k, sbytes, suffix_v, sbytes)) return BG_ERR_INVALID_ARG;
+    }
+
     const int nsm = sm_count();
     if (nsm <= 0) return BG_ERR_CUDA;
 
     const int nh = decode_tiles_per_cta();
     const int32_t BT = 128 / g;
-    const int32_t beam_tiles = (W + BT - 1) / BT;
-    const int32_t pairs = (beam_tiles + nh - 1) / nh;
+    const int32_t pairs = decode_pairs_per_rk(W, g, nh);
     const int64_t items = static_cast<int64_t>(R) * Hkv * pairs;
     if (items >= (int64_t(1) << 31)) return BG_ERR_UNSUPPORTED;
 
@@ -312,8 +351,46 @@ bg_status_t bg_beam_decode_attn(const void *q, const void *prompt_k, const void 
     p.suf_tx = (head_dim / 64) * 128 * t_suf * bpt;
     p.n_items_decode = static_cast<int32_t>(items);
     const int grid = static_cast<int>(items < nsm ? items : nsm);
-    if (launch_decode_attn(head_dim, tm_q, tm_k, tm_v, tm_sk, tm_sv, tm_o, p, grid, stream) != cudaSuccess) return BG_ERR_CUDA;
+    if (fz) {
+        // the step's reorder + append first (it moves nothing at t = 1 and then never reads src)
+        const void *sk = fz->src_k ? fz->src_k : suffix_k;
+        const void *sv = fz->src_v ? fz->src_v : suffix_v;
+        if (launch_suffix_reorder(sk, sv, const_cast<void *>(suffix_k), const_cast<void *>(suffix_v), fz->parent,
+                                  fz->new_k, fz->new_v, R, W, suffix_max, suffix_len - 1, Hkv, head_dim, dev_status,
+                                  stream) != cudaSuccess)
+            return BG_ERR_CUDA;
+    }
+    if (launch_decode_attn(head_dim, tm_q, tm_k, tm_v, tm_sk, tm_sv, tm_o, p, grid, stream) != cudaSuccess)
+        return BG_ERR_CUDA;
     return BG_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+bg_status_t bg_beam_decode_attn(const void *q, const void *prompt_k, const void *prompt_v, const int32_t *cu_prompt,
+                                int32_t total_prompt_tokens, int32_t max_prompt_len, const void *suffix_k,
+                                const void *suffix_v, int32_t suffix_len, int32_t suffix_max, int32_t R, int32_t W,
+                                int32_t Hq, int32_t Hkv, int32_t head_dim, float scale, void *out,
+                                int32_t *dev_status, cudaStream_t stream)
+{
+    return decode_impl(q, prompt_k, prompt_v, cu_prompt, total_prompt_tokens, max_prompt_len, suffix_k, suffix_v,
+                       suffix_len, suffix_max, R, W, Hq, Hkv, head_dim, scale, out, dev_status, nullptr, stream);
+}
+
+bg_status_t bg_beam_decode_step(const void *q, const void *prompt_k, const void *prompt_v, const int32_t *cu_prompt,
+                                int32_t total_prompt_tokens, int32_t max_prompt_len, const void *src_suffix_k,
+                                const void *src_suffix_v, const int32_t *parent_idx, const void *new_k,
+                                const void *new_v, void *dst_suffix_k, void *dst_suffix_v, int32_t suffix_len,
+                                int32_t suffix_max, int32_t R, int32_t W, int32_t Hq, int32_t Hkv, int32_t head_dim,
+                                float scale, void *out, int32_t *dev_status, cudaStream_t stream)
+{
+    if (suffix_len < 1) return BG_ERR_INVALID_ARG;
+    const StepFuse fz{src_suffix_k, src_suffix_v, parent_idx, new_k, new_v};
+    return decode_impl(q, prompt_k, prompt_v, cu_prompt, total_prompt_tokens, max_prompt_len, dst_suffix_k,
+                       dst_suffix_v, suffix_len, suffix_max, R, W, Hq, Hkv, head_dim, scale, out, dev_status, &fz,
+                       stream);
 }
 
 bg_status_t bg_beam_suffix_reorder(const void *src_k, const void *src_v, void *dst_k, void *dst_v,

@@ -2,12 +2,15 @@
 
     python -m attention_packed_varlen_causal_gb300.profile_case prefill_only --iters 3
     python -m attention_packed_varlen_causal_gb300.profile_case beam_long --iters 2
+    python -m attention_packed_varlen_causal_gb300.profile_case beam_long --iters 2 --two-call
     python -m attention_packed_varlen_causal_gb300.profile_case select_long --iters 2
 
 Prefill workloads (tiny, prefill_only, skewed) call bg_packed_prefill_attn
 ``iters`` times on one layer of inputs; decode workloads (beam_short,
-beam_long) run ``iters`` complete beam searches of one layer (per step: the
-suffix reorder + append, then the decode attention); selection workloads
+beam_long) run ``iters`` complete beam searches of one layer (per step the
+suffix reorder + append, then the decode attention: one bg_beam_decode_step
+call, or with ``--two-call`` bg_beam_suffix_reorder, then
+bg_beam_decode_attn); selection workloads
 (select_short, select_long) call bg_beam_select ``iters`` times on the beam
 configurations' shapes with fp32 logits N(0, 3) over 65,536 tokens.  Inputs are drawn on the
 device with a seeded generator, shaped as in ``workloads``.  Nothing is
@@ -36,6 +39,7 @@ def main(argv=None):
     select = {"select_short": "beam_short", "select_long": "beam_long"}
     ap.add_argument("workload", choices=sorted(list(wl.PREFILL_CONFIGS) + list(wl.DECODE_CONFIGS) + list(select)))
     ap.add_argument("--iters", type=int, default=3)
+    ap.add_argument("--two-call", action="store_true", help="decode: separate reorder and attention calls")
     args = ap.parse_args(argv)
     build.build()
     bg.load()
@@ -88,6 +92,10 @@ def main(argv=None):
         for _ in range(args.iters):
             for s in range(S):
                 src, dst = s % 2, 1 - s % 2
+                if not args.two_call:
+                    bg.bg_beam_decode_step(qs[s], pk, pv, cu, max(plen), sk[src], sv[src], parents[s], nk[s], nv[s],
+                                           sk[dst], sv[dst], s + 1, out)
+                    continue
                 bg.bg_beam_suffix_reorder(sk[src], sv[src], sk[dst], sv[dst], parents[s], s, new_k=nk[s],
                                           new_v=nv[s])
                 bg.bg_beam_decode_attn(qs[s], pk, pv, cu, max(plen), sk[dst], sv[dst], s + 1, out)

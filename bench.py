@@ -8,7 +8,8 @@ input:
      d 128) through all 28 layers, each layer with its own Q/K/V;
   2. a complete short-prompt beam search (32 requests, 128-token prompts,
      beam 100, 4 decode steps, 14/2 heads, d 64) through 28 layers: per step
-     and layer the suffix reorder + append, then decode attention;
+     and layer the suffix reorder + append, then decode attention (one
+     bg_beam_decode_step call);
   3. the same for the long-prompt beam search (16 requests, prompts
      U{400..500}, beam 400, 5 steps).
 The headline ``value`` is prefill TFLOP/s (causal FLOPs of valid tokens
@@ -46,7 +47,7 @@ LAYERS = 28
 # (dram__bytes_read.sum + dram__bytes_write.sum from one ncu capture, written up in
 # profiles/attn_kernel_prefill_prefill_only.md).  It holds only for the sources that launch is
 # built from, identified by `sources` (kernel_sources_hash); otherwise the bench reports null.
-PREFILL_TRAFFIC = {"sources": "d29bd9c89bf50150", "bytes": 649762048 + 244366336}
+PREFILL_TRAFFIC = {"sources": "54dc67af6ae6fea8", "bytes": 648953600 + 244135424}
 # the files a bg_packed_prefill_attn launch is built from
 PREFILL_SOURCES = ["abi.cu", "prefill.cu", "bg_attn_kernel.cuh", "bg_ptx.cuh", "bg_internal.h"]
 
@@ -243,17 +244,18 @@ class DecodeStack:
             by += b
         self.flops_per_search = fl * layers
         self.bytes_per_search = by * layers
-        self.launches = 2 * S * layers
+        self.launches = 2 * S * layers            # reorder + attention per step and layer
 
     def enqueue(self, stream):
         bg = self.bg
         for s in range(self.cfg.steps):
             src, dst = s % 2, 1 - s % 2
             for l in range(self.layers):
-                bg.bg_beam_suffix_reorder(self.sk[l][src], self.sv[l][src], self.sk[l][dst], self.sv[l][dst],
-                                          self.parent[s], s, new_k=self.nk[l][s], new_v=self.nv[l][s], stream=stream)
-                bg.bg_beam_decode_attn(self.q[l][s], self.pk[l], self.pv[l], self.cu, max(self.plen),
-                                       self.sk[l][dst], self.sv[l][dst], s + 1, self.out[l], stream=stream)
+                # reorder + append into dst, then attention over it
+                bg.bg_beam_decode_step(self.q[l][s], self.pk[l], self.pv[l], self.cu, max(self.plen),
+                                       self.sk[l][src], self.sv[l][src], self.parent[s], self.nk[l][s],
+                                       self.nv[l][s], self.sk[l][dst], self.sv[l][dst], s + 1, self.out[l],
+                                       stream=stream)
 
     def capture(self, stream):
         import torch
@@ -384,7 +386,10 @@ def run_ours(args):
                 "us_per_step": round(us_per_step, 3), "roofline_us_per_step": round(roof_us, 3),
                 "roofline_frac": round(roof_us / us_per_step, 4),
                 "bound": "tensor" if t_flops > t_bytes else "hbm",
-                "us_per_step_definition": "one decode step of one layer: suffix reorder+append, then attention"}
+                "us_per_step_definition": "one decode step of one layer: suffix reorder+append, then attention, "
+                                          "one bg_beam_decode_step call (two launches)"}
+
+    decode = {"beam_short": dec_report(dec_s, short_ms), "beam_long": dec_report(dec_l, long_ms)}
 
     # e2e: one layer per step through the C ABI with host buffers (pinned),
     # H2D of q, k, v, cu_seqlens and D2H of the output inside the timed region
@@ -422,7 +427,7 @@ def run_ours(args):
                          f"{pre.bytes / 1e6:.0f} MB > 129 MB L2), no flush needed", "parallelism": f"replicas x{world}"},
         "prefill": {"ms_per_step": round(prefill_ms / args.steps, 3), "tflops_per_gpu": round(per_gpu_tflops, 3),
                     "avg_call_us": round(avg_call_s * 1e6, 2), "tokens_per_s": round(world * pre.T * layers * args.steps / (prefill_ms / 1e3), 1)},
-        "decode": {"beam_short": dec_report(dec_s, short_ms), "beam_long": dec_report(dec_l, long_ms)},
+        "decode": decode,
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk, "gpu_launches": launches,
         "last_token": last, "beam_select": select,
     }

@@ -224,6 +224,48 @@ bg_status_t bg_beam_suffix_reorder(const void *src_k, const void *src_v,
                                    int32_t *dev_status, cudaStream_t stream);
 
 /*
+ * One whole beam-search decode step in one call: the suffix reorder by the
+ * parent index with the append of the step's token, then the decode
+ * attention over [prompt ; the new suffix].
+ * Source: sections 1.1 and 1.2 of the page above, as for
+ * bg_beam_suffix_reorder and bg_beam_decode_attn.  With t = suffix_len >= 1
+ * the call is exactly
+ *     bg_beam_suffix_reorder(src, dst, parent_idx, new, n_tokens = t - 1)
+ *     bg_beam_decode_attn(q, ..., suffix = dst, suffix_len = t)
+ * with the arguments of both checked together before anything is enqueued:
+ * two launches on `stream`, the second one started by programmatic dependent
+ * launch so that its prologue overlaps the first.  dst then holds the
+ * reordered suffix, the next step's src.
+ *
+ *   q, prompt_k, prompt_v, cu_prompt, total_prompt_tokens, max_prompt_len,
+ *   R, W, Hq, Hkv, head_dim, scale, out    as in bg_beam_decode_attn
+ *   src_suffix_k, src_suffix_v   bf16 [R, W, suffix_max, Hkv, head_dim], the
+ *                                previous step's suffix; slots 0..t-2 read;
+ *                                may be NULL when suffix_len == 1
+ *   parent_idx                   int32 [R, W], device, each in [0, W)
+ *   new_k, new_v                 bf16 [R, W, Hkv, head_dim], the step's token
+ *   dst_suffix_k, dst_suffix_v   bf16 [R, W, suffix_max, Hkv, head_dim];
+ *                                slots 0..t-1 written; must not overlap any
+ *                                input, out or each other
+ *   suffix_len                   t, 1 .. suffix_max
+ * Beams whose parent index is out of range are left untouched in dst and
+ * raise BG_DEVSTAT_PARENT (the attention output is then undefined).
+ * Errors: those of the two calls it stands for, and BG_ERR_INVALID_ARG for
+ * suffix_len < 1 or an overlap of dst or out with an input.
+ */
+bg_status_t bg_beam_decode_step(const void *q, const void *prompt_k, const void *prompt_v,
+                                const int32_t *cu_prompt, int32_t total_prompt_tokens,
+                                int32_t max_prompt_len,
+                                const void *src_suffix_k, const void *src_suffix_v,
+                                const int32_t *parent_idx,
+                                const void *new_k, const void *new_v,
+                                void *dst_suffix_k, void *dst_suffix_v,
+                                int32_t suffix_len, int32_t suffix_max,
+                                int32_t R, int32_t W, int32_t Hq, int32_t Hkv, int32_t head_dim,
+                                float scale, void *out, int32_t *dev_status,
+                                cudaStream_t stream);
+
+/*
  * Beam candidate selection of one decode step.  Source: section 1.1 of the page
  * above: each step selects local candidates from every beam's token
  * distribution, merges them with the accumulated scores and keeps W candidate

@@ -128,6 +128,31 @@ def test_reorder_host_validation(lib, kw, expect):
     assert reorder(lib, **kw) == expect
 
 
+def step(lib, **kw):
+    a = dict(q=FAKE, pk=FAKE * 2, pv=FAKE * 3, cu=FAKE * 4, P=100, maxP=60, sk=FAKE * 8, sv=FAKE * 16,
+             par=FAKE * 24, nk=FAKE * 32, nv=FAKE * 40, dk=FAKE * 48, dv=FAKE * 56, t=2, S=4, R=2, W=5, Hq=14, Hkv=2,
+             d=64, scale=0.125, out=FAKE * 64, st=None, stream=None)
+    a.update(kw)
+    return lib.bg_beam_decode_step(a["q"], a["pk"], a["pv"], a["cu"], a["P"], a["maxP"], a["sk"], a["sv"], a["par"],
+                                   a["nk"], a["nv"], a["dk"], a["dv"], a["t"], a["S"], a["R"], a["W"], a["Hq"],
+                                   a["Hkv"], a["d"], a["scale"], a["out"], a["st"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(t=0), 1), (dict(t=5), 1), (dict(par=None), 1), (dict(nk=None), 1), (dict(nv=None), 1),
+    (dict(sk=None), 1),                                  # t = 2 moves one slot: src is needed
+    (dict(dk=FAKE * 8), 1),                              # dst is src
+    (dict(dk=FAKE), 1), (dict(dv=FAKE * 2 + 256), 1),    # dst inside q / the prompt K
+    (dict(dv=FAKE * 48 + 256), 1),                       # dst K and V overlap
+    (dict(dk=FAKE * 24), 1), (dict(dk=FAKE * 32), 1),    # dst over the parents / the new token
+    (dict(out=FAKE * 24), 1), (dict(out=FAKE * 40), 1),  # out over the parents / the new token
+    (dict(par=FAKE * 24 + 2), 1), (dict(nk=FAKE * 32 + 8), 1), (dict(sk=FAKE * 8 + 8), 1),
+    (dict(d=32), 2), (dict(S=17, t=2), 2), (dict(Hq=15), 1), (dict(R=0), 0),
+])
+def test_decode_step_host_validation(lib, kw, expect):
+    assert step(lib, **kw) == expect
+
+
 def test_beam_select_host_checks(lib):
     ws = lib.bg_beam_select_workspace_size(32, 100, 65536)
     assert ws % 256 == 0 and ws >= 32 * 100 * 100 * 8 + 32 * 100 * 4
