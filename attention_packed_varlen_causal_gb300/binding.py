@@ -50,6 +50,7 @@ SIGNATURES = {
     "bg_beam_decode_step": ([_P, _P, _P, _P, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _I32,
                              _I32, _I32, _F32, _P, _P, _P], ctypes.c_int),
     "bg_beam_select_workspace_size": ([_I32] * 3, _SZ),
+    "bg_selftest_wait_timeout": ([_P, _P, _P], ctypes.c_int),
     "bg_beam_select": ([_P, _P, _I32, _I32, _I32, _P, _P, _P, _P, _SZ, _P], ctypes.c_int),
 }
 
@@ -216,6 +217,13 @@ def bg_beam_decode_step(q, prompt_k, prompt_v, cu_prompt, max_prompt_len: int, s
                                     _ptr(dev_status), _stream(stream))
     _check("bg_beam_decode_step", st)
     return out
+
+
+def bg_selftest_wait_timeout(dev_status, waited_ns, *, stream=None):
+    """Makes one bounded pipeline wait run out on the device: dev_status (int32) receives
+    BG_DEVSTAT_TIMEOUT, waited_ns (int64) the nanoseconds waited."""
+    st = load().bg_selftest_wait_timeout(_ptr(dev_status), _ptr(waited_ns), _stream(stream))
+    _check("bg_selftest_wait_timeout", st)
 
 
 def bg_beam_select_workspace_size(R: int, W: int, V: int) -> int:

@@ -19,7 +19,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_PATH = os.path.join(PKG, "libbgattn.so")
-SOURCES = ["abi.cu", "prefill.cu", "decode.cu", "reorder.cu", "noalloc.cu", "lasttok.cu", "select.cu"]
+SOURCES = ["abi.cu", "prefill.cu", "decode.cu", "reorder.cu", "noalloc.cu", "lasttok.cu", "select.cu", "selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -471,4 +471,11 @@ bg_status_t bg_beam_select(const float *logits, const float *cum, int32_t R, int
     return BG_OK;
 }
 
+bg_status_t bg_selftest_wait_timeout(int32_t *dev_status, unsigned long long *waited_ns, cudaStream_t stream)
+{
+    if (!dev_status || !waited_ns || !aligned(dev_status, 4) || !aligned(waited_ns, 8)) return BG_ERR_INVALID_ARG;
+    if (launch_wait_timeout_selftest(dev_status, waited_ns, stream) != cudaSuccess) return BG_ERR_CUDA;
+    return BG_OK;
+}
+
 }  // extern "C"

@@ -107,8 +107,8 @@ struct AttnCfg {
     static constexpr int kStageBytes = 32 * 64;
     static constexpr int kOffBar = kOffStage + 4 * NH * kStageBytes;
     // q_full[2] q_empty[2] mma_final k_full[NK] k_empty[NK] v_full[NV] v_empty[NV] s_full[NH][NS]
-    // p_full[NH][NS] pv_done[NH][NS]
-    static constexpr int kNumBars = 5 + 2 * NK + 2 * NV + 3 * NS * NH;
+    // p_full[NH][NS] pv_done[NH][NS] o_staged[NH][2]
+    static constexpr int kNumBars = 5 + 2 * NK + 2 * NV + 3 * NS * NH + 2 * NH;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + slack for 1024-byte alignment
     static constexpr int kThreads = 128 * (1 + NH);
@@ -293,6 +293,12 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
     // the phase right after the last one its waiter already saw complete,
     // which is what makes a parity wait unambiguous.
     uint64_t *pv_done = p_full + NS * NH;   // [NH][NS]
+    // o_staged[h][e & 1] completes when the four warps of softmax warpgroup h have written their
+    // rows of its e-th TMA-stored output tile into the Q buffer.  No warp can arrive for the
+    // group's next such tile before this phase completes: its next epilogue runs after the scores
+    // of the item after next, whose Q load waits for the buffer this tile leaves from.  The second
+    // barrier per group keeps consecutive phases apart all the same.
+    uint64_t *o_staged = pv_done + NS * NH;   // [NH][2]
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
 
@@ -319,6 +325,7 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
             mbar_init(&p_full[i], 128);
             mbar_init(&pv_done[i], 1);
         }
+        for (int i = 0; i < 2 * NH; ++i) mbar_init(&o_staged[i], 4);   // one arrive per warp
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -560,6 +567,7 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
         // as the Q load), and one thread issues the tile stores and, once the TMA unit has read the
         // buffer, hands it back to the Q producer.  The warps do not wait for the global writes.
         // Other tiles, and every prefill tile, are stored row by row through the staging area.
+        uint32_t n_tma = 0;   // output tiles this warpgroup stored through the TMA unit so far
         auto epilogue = [&](const Item &I, float m, float l, uint32_t g_last, int qbi, bool via_tma,
                             auto &&release) -> bool {
                 // The commit after the item's last P.V covers every earlier MMA too.  (Items always
@@ -636,8 +644,15 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
                                 make_uint4(pk[32 * cb + 4 * c], pk[32 * cb + 4 * c + 1], pk[32 * cb + 4 * c + 2],
                                            pk[32 * cb + 4 * c + 3]);
                     fence_proxy_async_smem();          // generic-proxy writes -> the TMA unit's reads
-                    named_bar_sync(1 + h, 128);        // the warpgroup's four warps have written their rows
+                    __syncwarp();
+                    uint64_t *staged = &o_staged[2 * h + (n_tma & 1)];
+                    if (lane == 0) mbar_arrive(staged);
+                    const uint32_t staged_parity = (n_tma >> 1) & 1u;
+                    ++n_tma;
                     if (leader) {
+                        // a bounded wait (not a named barrier): if another warp of the group has
+                        // given up, this one gives up too instead of waiting forever
+                        if (!mbar_wait(staged, staged_parity, abort_flag)) return false;
 #pragma unroll
                         for (int cb = 0; cb < C::NB; ++cb) {
                             if constexpr (MODE == Mode::Prefill)

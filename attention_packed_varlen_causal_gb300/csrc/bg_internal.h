@@ -49,6 +49,10 @@ cudaError_t launch_suffix_reorder(const void *src_k, const void *src_v, void *ds
                                   int32_t W, int32_t suffix_max, int32_t n_tokens, int32_t Hkv, int32_t head_dim,
                                   int32_t *dev_status, cudaStream_t stream);
 
+// Diagnostic: one kernel whose only wait (bg::mbar_wait on an mbarrier nothing arrives on)
+// runs out; it ORs BG_DEVSTAT_TIMEOUT into *dev_status and writes the time it waited.
+cudaError_t launch_wait_timeout_selftest(int32_t *dev_status, unsigned long long *waited_ns, cudaStream_t stream);
+
 // Launches `kern` on `stream` with programmatic stream serialization: its CTAs may
 // start while the previous kernel of the stream still runs (that kernel lets them
 // with griddepcontrol.launch_dependents); every kernel of this library waits

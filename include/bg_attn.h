@@ -73,6 +73,21 @@ typedef enum {
 const char *bg_status_string(bg_status_t status);
 
 /*
+ * Diagnostic of the failure path.  Enqueues one small kernel whose only wait
+ * can never complete (an mbarrier that nothing arrives on), made through the
+ * same bounded-wait routine as every pipeline wait of the attention kernels.
+ * The wait gives up after the library's limit (about one second); the kernel
+ * then ORs BG_DEVSTAT_TIMEOUT into *dev_status, stores the nanoseconds it
+ * waited (device %globaltimer) in *waited_ns and returns, leaving the stream
+ * and the context usable.  Nothing faults, traps or hangs.
+ *   dev_status   device int32, 4-byte aligned
+ *   waited_ns    device uint64, 8-byte aligned
+ * Errors: BG_ERR_INVALID_ARG for NULL or misaligned pointers.
+ */
+bg_status_t bg_selftest_wait_timeout(int32_t *dev_status, unsigned long long *waited_ns,
+                                     cudaStream_t stream);
+
+/*
  * Bytes of device workspace bg_packed_prefill_attn needs for these sizes (an
  * upper bound that depends only on host-known sizes).  The workspace holds
  * the per-call work list the kernels build from cu_seqlens; it may be reused

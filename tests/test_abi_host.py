@@ -153,6 +153,13 @@ def test_decode_step_host_validation(lib, kw, expect):
     assert step(lib, **kw) == expect
 
 
+def test_selftest_host_checks(lib):
+    assert lib.bg_selftest_wait_timeout(None, FAKE, None) == binding.BG_ERR_INVALID_ARG
+    assert lib.bg_selftest_wait_timeout(FAKE, None, None) == binding.BG_ERR_INVALID_ARG
+    assert lib.bg_selftest_wait_timeout(FAKE + 2, FAKE * 2, None) == binding.BG_ERR_INVALID_ARG
+    assert lib.bg_selftest_wait_timeout(FAKE, FAKE * 2 + 4, None) == binding.BG_ERR_INVALID_ARG
+
+
 def test_beam_select_host_checks(lib):
     ws = lib.bg_beam_select_workspace_size(32, 100, 65536)
     assert ws % 256 == 0 and ws >= 32 * 100 * 100 * 8 + 32 * 100 * 4
