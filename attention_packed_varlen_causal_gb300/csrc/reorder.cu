@@ -9,7 +9,8 @@
 //
 // Pure data movement of bf16 bit patterns (bit-exact).  One warp per beam;
 // each beam's slots [0, n] are contiguous (n+1) * Hkv * head_dim bf16, so a
-// warp moves them with coalesced 16-byte loads and stores.  HBM-bound: it
+// warp moves them with coalesced 16-byte loads and stores, all of a batch's
+// loads issued before its stores.  HBM-bound: it
 // reads and writes 2 * n * Hkv * head_dim * 2 bytes per beam (+ the append).
 #include "bg_internal.h"
 #include "bg_ptx.cuh"
@@ -18,6 +19,7 @@ namespace bg {
 
 namespace {
 constexpr int kWarpsPerBlock = 8;
+constexpr int kBatch = 4;           // vectors of K and of V in flight per lane
 
 __global__ void __launch_bounds__(32 * kWarpsPerBlock)
     reorder_kernel(const uint4 *__restrict__ src_k, const uint4 *__restrict__ src_v, uint4 *__restrict__ dst_k,
@@ -39,21 +41,35 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock)
     const int64_t slab = static_cast<int64_t>(suffix_max) * vec_per_tok;     // vectors per beam
     const uint4 *sk = src_k + (r * W + par) * slab;
     const uint4 *sv = src_v + (r * W + par) * slab;
+    const uint4 *nk = new_k ? new_k + beam * vec_per_tok : nullptr;
+    const uint4 *nv = new_v ? new_v + beam * vec_per_tok : nullptr;
     uint4 *dk = dst_k + beam * slab;
     uint4 *dv = dst_v + beam * slab;
+    // slots [0, n) from the parent, then slot n from the new token: one contiguous run of dst.
+    // Up to kBatch vectors of K and of V per lane are loaded before any is stored, so the warp
+    // waits for memory about once per batch instead of once per vector.
     const int moved = n * vec_per_tok;
-    for (int i = lane; i < moved; i += 32) {
-        const uint4 a = sk[i];
-        const uint4 b = sv[i];
-        dk[i] = a;
-        dv[i] = b;
-    }
-    if (new_k != nullptr) {
-        const uint4 *nk = new_k + beam * vec_per_tok;
-        const uint4 *nv = new_v + beam * vec_per_tok;
-        for (int i = lane; i < vec_per_tok; i += 32) {
-            dk[moved + i] = nk[i];
-            dv[moved + i] = nv[i];
+    const int total = moved + (nk ? vec_per_tok : 0);
+    for (int base = 0; base < total; base += 32 * kBatch) {
+        uint4 a[kBatch], b[kBatch];
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k) {
+            const int i = base + lane + 32 * k;
+            if (i < moved) {
+                a[k] = sk[i];
+                b[k] = sv[i];
+            } else if (i < total) {
+                a[k] = nk[i - moved];
+                b[k] = nv[i - moved];
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k) {
+            const int i = base + lane + 32 * k;
+            if (i < total) {
+                dk[i] = a[k];
+                dv[i] = b[k];
+            }
         }
     }
 }
