@@ -47,7 +47,7 @@ LAYERS = 28
 # (dram__bytes_read.sum + dram__bytes_write.sum from one ncu capture, written up in
 # profiles/attn_kernel_prefill_prefill_only.md).  It holds only for the sources that launch is
 # built from, identified by `sources` (kernel_sources_hash); otherwise the bench reports null.
-PREFILL_TRAFFIC = {"sources": "54dc67af6ae6fea8", "bytes": 648953600 + 244135424}
+PREFILL_TRAFFIC = {"sources": "98df18b6da903670", "bytes": 649163520 + 244014080}
 # the files a bg_packed_prefill_attn launch is built from
 PREFILL_SOURCES = ["abi.cu", "prefill.cu", "bg_attn_kernel.cuh", "bg_ptx.cuh", "bg_internal.h"]
 
