@@ -109,10 +109,11 @@ class ClockSampler:
          "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
          "clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, directory=None):
+        import tempfile
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{gpu_index}.csv")
+        self.path = os.path.join(directory or tempfile.gettempdir(), f"bg_bench_clocks_gpu{gpu_index}.csv")
 
     def start(self):
         try:
@@ -344,7 +345,7 @@ def run_ours(args):
     for _ in range(args.warmup):
         one_step()
     torch.cuda.synchronize()
-    clocks = ClockSampler(local)
+    clocks = ClockSampler(local, args.clocks_dir)
     clocks.start()
     time.sleep(0.5)                      # let nvidia-smi start sampling
     if world > 1:
@@ -612,6 +613,8 @@ def main():
     ap.add_argument("--cpu-sample-seqs", type=int, default=240)
     ap.add_argument("--ref-sample-seqs", type=int, default=24)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--clocks-dir", default=None,
+                    help="where the raw nvidia-smi samples of the timed region go (default: the temp directory)")
     ap.add_argument("--traffic", type=float, default=None,
                     help="dram bytes per launch of the prefill kernel from the committed ncu summary")
     args = ap.parse_args()
