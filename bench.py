@@ -397,6 +397,7 @@ def run_ours(args):
     e2e = run_e2e(pre, device, stream, args)
     last = run_last_token(pre, stream, peaks)
     select = run_beam_select(device, stream, peaks)
+    skewed = run_skewed(device, stream, peaks)
 
     # oracle CPU baseline (rank 0, N = 1 only)
     cpu = None
@@ -430,7 +431,7 @@ def run_ours(args):
                     "avg_call_us": round(avg_call_s * 1e6, 2), "tokens_per_s": round(world * pre.T * layers * args.steps / (prefill_ms / 1e3), 1)},
         "decode": decode,
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk, "gpu_launches": launches,
-        "last_token": last, "beam_select": select,
+        "last_token": last, "beam_select": select, "skewed": skewed,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -466,6 +467,62 @@ def run_last_token(pre, stream, peaks, reps: int = 5):
             "us_per_layer": round(us, 2), "bytes_per_layer": by, "achieved_gbs": round(gbs, 1),
             "hbm_frac": round(gbs / peaks["hbm_gbs"], 4), "bound": "hbm",
             "definition": "bg_packed_last_token_attn per layer, timed apart from the step (not in value)"}
+
+
+def run_skewed(device, stream, peaks, reps: int = 5):
+    """The skewed packed-prefill stress workload, timed apart from the step: 4096 sequences,
+    L = clip(round(lognormal(5.5, 0.8)), 1, 2048), 16 Q / 8 KV heads, head_dim 128, 1 % of the
+    (token, kv head) K rows scaled by 8 (outlier logits).  One layer stays resident (16.7 GB,
+    far above L2); bg_packed_prefill_attn is called ``reps`` times after two warm-up calls,
+    CUDA events on the launching stream."""
+    import numpy as np
+    import torch
+    from attention_packed_varlen_causal_gb300 import binding as bg
+    cfg = wl.PREFILL_CONFIGS["skewed"]
+    lengths = wl.prefill_lengths(cfg)
+    cu_np = wl.cu_from_lengths(lengths)
+    T, Hq, Hkv, d = int(cu_np[-1]), cfg.Hq, cfg.Hkv, cfg.head_dim
+    g = torch.Generator(device=device)
+    g.manual_seed(5000)
+    q = torch.randn((T, Hq, d), generator=g, device=device).to(torch.bfloat16)
+    k = torch.randn((T, Hkv, d), generator=g, device=device).to(torch.bfloat16)
+    v = torch.randn((T, Hkv, d), generator=g, device=device).to(torch.bfloat16)
+    rows = T * Hkv
+    pick = np.random.default_rng(wl.SEED_OUTLIER).choice(rows, size=int(round(cfg.outlier_frac * rows)),
+                                                         replace=False)
+    pick = torch.from_numpy(pick.astype(np.int64)).to(device)
+    k2 = k.view(rows, d)
+    k2[pick] = k2[pick] * cfg.outlier_scale          # x8 is exact in bf16
+    out = torch.empty_like(q)
+    cu = torch.from_numpy(cu_np).to(device)
+    maxlen = max(lengths)
+    ws = torch.empty(bg.bg_packed_prefill_workspace_size(len(lengths), T, maxlen, Hq, Hkv, d), dtype=torch.uint8,
+                     device=device)
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            bg.bg_packed_prefill_attn(q, k, v, cu, maxlen, out, workspace=ws, stream=stream)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            bg.bg_packed_prefill_attn(q, k, v, cu, maxlen, out, workspace=ws, stream=stream)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / reps
+    flops = prefill_flops(lengths, Hq, d)
+    by = prefill_bytes(T, Hq, Hkv, d)
+    res = {"workload": f"skewed stress: {len(lengths)} seqs, L=clip(round(lognormal(5.5, 0.8)), 1, 2048) seed 0, "
+                       f"T={T}, Hq{Hq}/Hkv{Hkv} d{d}, causal, 1% of K rows x8, one layer (inputs > L2)",
+           "us_per_call": round(us, 1), "tflops": round(flops / us / 1e6, 2),
+           "pct_bf16_peak": round(flops / us / 1e6 / peaks["bf16_tflops"], 4),
+           "achieved_gbs": round(by / us / 1e3, 1), "hbm_frac": round(by / us / 1e3 / peaks["hbm_gbs"], 4),
+           "roofline_us": round(max(flops / (peaks["bf16_tflops"] * 1e6), by / (peaks["hbm_gbs"] * 1e3)), 1),
+           "flops": flops, "bytes": by,
+           "definition": "bg_packed_prefill_attn on one layer of the skewed workload, timed apart from the step "
+                         "(not in value)"}
+    del q, k, v, out, ws, k2, pick
+    torch.cuda.empty_cache()
+    return res
 
 
 SELECT_VOCAB = 65536   # the pages give no vocabulary size; selection cost is linear in it
