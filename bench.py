@@ -79,15 +79,15 @@ def prefill_bytes(T, Hq, Hkv, d):
 
 def decode_step_work(cfg, prompt_lengths, t):
     """FLOPs and algorithmic bytes of decode step t (1-based) for one layer:
-    reorder reads+writes t-1 suffix slots, the append writes slot t-1, the
-    attention reads Q, the prompt K/V once per request and t suffix slots per
-    beam, and writes O."""
+    reorder reads+writes t-1 suffix slots, the append reads the new token's
+    K/V and writes it to slot t-1, the attention reads Q, the prompt K/V once
+    per request and t suffix slots per beam, and writes O."""
     R, W, Hq, Hkv, d = cfg.R, cfg.W, cfg.Hq, cfg.Hkv, cfg.head_dim
     P = float(np.sum(prompt_lengths))
     rows = R * W * Hq
     flops = 4.0 * d * rows * (np.mean(prompt_lengths) + t)
     slot = R * W * Hkv * d * 2.0                     # one suffix slot of K (or V), all beams
-    reorder = 2 * 2 * slot * (t - 1) + 2 * slot      # K and V read + write, plus the append write
+    reorder = 2 * 2 * slot * (t - 1) + 2 * 2 * slot  # K and V read + write, plus the append's read + write
     attn = 2 * rows * d * 2.0 + 2 * P * Hkv * d * 2.0 + 2 * slot * t
     return flops, reorder + attn
 
