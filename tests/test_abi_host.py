@@ -31,6 +31,27 @@ def test_header_declares_the_boundary():
         assert n in names
 
 
+def header_constants():
+    """Every #define with a numeric value and every bg_status_t enumerator in bg_attn.h."""
+    text = open(os.path.join(ROOT, "include", "bg_attn.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    vals = {}
+    for name, expr in re.findall(r"#define[ \t]+(BG_[A-Z0-9_]+)[ \t]+([^\n]+)", text):
+        expr = re.sub(r"(?<=\d)u\b", "", expr.strip())       # 1u -> 1
+        vals[name] = int(eval(expr, {"__builtins__": {}}))    # literals and shifts only
+    for name, v in re.findall(r"\b(BG_[A-Z_]+)\s*=\s*(\d+)", text):
+        vals[name] = int(v)
+    return vals
+
+
+def test_binding_constants_match_the_header():
+    vals = header_constants()
+    assert len(vals) >= 15
+    for name, v in vals.items():
+        assert hasattr(binding, name), f"{name} is defined in bg_attn.h but not in the binding"
+        assert getattr(binding, name) == v, f"{name}: header {v}, binding {getattr(binding, name)}"
+
+
 def test_library_exports_every_declared_symbol(lib):
     for n in declared_functions():
         assert hasattr(lib, n), f"{n} declared in bg_attn.h but not exported"
