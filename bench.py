@@ -136,26 +136,35 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.f.close()
-        import datetime
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        rows = []
-        for line in open(self.path):
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 10:
-                continue
-            try:
-                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
-                rows.append((ts, float(parts[2]), float(parts[3]),
-                             [n for n, v in zip(names, parts[6:10]) if v.lower() == "active"]))
-            except ValueError:
-                continue
-        inside = [r for r in rows if t0 is not None and t0 - 0.05 <= r[0] <= t1 + 0.05]
-        use = inside if inside else rows
-        sm = [r[1] for r in use]
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(r[2] for r in use) if use else None,
-                "reasons": sorted({n for r in use for n in r[3]}), "samples": len(use),
-                "samples_in_timed_region": len(inside)}
+        with open(self.path) as f:
+            return summarize_clock_samples(f, t0, t1)
+
+
+def summarize_clock_samples(lines, t0=None, t1=None):
+    """Median SM clock, maximum SM clock and the throttle reasons seen, from nvidia-smi rows
+    (timestamp, index, clocks.sm, clocks.max.sm, power, active mask, hw_slowdown,
+    hw_thermal_slowdown, sw_thermal_slowdown, sw_power_cap).  Only rows inside the wall-clock
+    window [t0, t1] (50 ms of slack) count when there are any; otherwise all rows do."""
+    import datetime
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    rows = []
+    for line in lines:
+        parts = [p.strip() for p in line.split(",")]
+        if len(parts) < 10:
+            continue
+        try:
+            ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            rows.append((ts, float(parts[2]), float(parts[3]),
+                         [n for n, v in zip(names, parts[6:10]) if v.lower() == "active"]))
+        except ValueError:
+            continue
+    inside = [r for r in rows if t0 is not None and t0 - 0.05 <= r[0] <= t1 + 0.05]
+    use = inside if inside else rows
+    sm = [r[1] for r in use]
+    return {"sm_mhz": statistics.median(sm) if sm else None,
+            "sm_max_mhz": max(r[2] for r in use) if use else None,
+            "reasons": sorted({n for r in use for n in r[3]}), "samples": len(use),
+            "samples_in_timed_region": len(inside)}
 
 
 def dist_env():
