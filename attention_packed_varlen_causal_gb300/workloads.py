@@ -164,6 +164,19 @@ def make_prefill_inputs(lengths, Hq: int, Hkv: int, head_dim: int, *, layer: int
             "Hq": Hq, "Hkv": Hkv, "head_dim": head_dim, "max_seqlen": int(max(lengths) if len(lengths) else 0)}
 
 
+def make_prefill_config_prefix(cfg: PrefillConfig, n_seqs: int, layer: int = 0) -> dict:
+    """The first ``n_seqs`` sequences of a configuration's inputs, without drawing the rest.
+
+    With one generator per tensor, the first n values a generator draws do not depend on
+    how many it draws in all, so the first T' tokens of Q, K and V come out exactly as in
+    the whole configuration.  That holds only without a shared generator and without
+    outlier rows (their choice depends on T); other configurations are refused."""
+    if cfg.single_seed_qkv is not None or cfg.outlier_frac > 0.0:
+        raise ValueError(f"{cfg.name}: a prefix of its inputs is not a prefix of the draws")
+    lengths = prefill_lengths(cfg)[:n_seqs]
+    return make_prefill_inputs(lengths, cfg.Hq, cfg.Hkv, cfg.head_dim, layer=layer)
+
+
 def make_prefill_config_inputs(cfg: PrefillConfig, layer: int = 0) -> dict:
     return make_prefill_inputs(prefill_lengths(cfg), cfg.Hq, cfg.Hkv, cfg.head_dim, layer=layer,
                                single_seed=cfg.single_seed_qkv, outlier_frac=cfg.outlier_frac,

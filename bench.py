@@ -285,14 +285,14 @@ def time_oracle_sample(layer_seqs: int = 240, seed_layer: int = 0):
     batch: the first `layer_seqs` sequences of one layer.  Returns
     (TFLOP/s, seconds, threads, description)."""
     import oracle
-    x = wl.make_prefill_config_inputs(wl.PREFILL_CONFIGS["prefill_only"], layer=seed_layer)
     n = layer_seqs
+    x = wl.make_prefill_config_prefix(wl.PREFILL_CONFIGS["prefill_only"], n, layer=seed_layer)
     cu = x["cu_seqlens"]
     T = int(cu[n])
-    lengths = x["lengths"][:n]
+    lengths = x["lengths"]
     scale = 1.0 / math.sqrt(x["head_dim"])
     t0 = time.perf_counter()
-    oracle.prefill(x["q"][:T], x["k"][:T], x["v"][:T], cu[:n + 1], scale)
+    oracle.prefill(x["q"], x["k"], x["v"], cu, scale)
     dt = time.perf_counter() - t0
     fl = prefill_flops(lengths, x["Hq"], x["head_dim"])
     desc = f"oracle fp64 prefill of {n} of 240 sequences of one layer ({T} tokens, {fl / 1e9:.1f} GFLOP)"

@@ -57,3 +57,23 @@ def test_generators_deterministic():
     d = wl.make_decode_problem(2, 3, 2, 4, 2, 8, [4, 0])
     assert d["cu_prompt"].tolist() == [0, 4, 4]
     assert all(p.min() >= 0 and p.max() < 3 for p in d["parent"])
+
+
+def test_prefix_of_a_configuration_is_the_prefix_of_its_draws():
+    # a small per-tensor-seed configuration: the prefix generator must give exactly the
+    # first tokens of the whole draw
+    cfg = wl.PrefillConfig("small", 7, 4, 2, 64, "uniform", lo=5, hi=40)
+    full = wl.make_prefill_config_inputs(cfg, layer=3)
+    for n in (1, 3, 7):
+        pre = wl.make_prefill_config_prefix(cfg, n, layer=3)
+        T = int(full["cu_seqlens"][n])
+        assert np.array_equal(pre["cu_seqlens"], full["cu_seqlens"][:n + 1])
+        for key in ("q", "k", "v"):
+            assert np.array_equal(pre[key], full[key][:T])
+
+
+def test_prefix_refused_where_it_is_not_a_prefix():
+    import pytest
+    for name in ("tiny", "skewed"):
+        with pytest.raises(ValueError):
+            wl.make_prefill_config_prefix(wl.PREFILL_CONFIGS[name], 2)
