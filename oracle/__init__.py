@@ -21,7 +21,7 @@ Contents
   * ``oracle_np``     an independent padded-plus-mask numpy formulation used
     to cross-check the C oracle (section 1.2 contrasts padding with packing).
   * ``fp8``           E4M3 codes with one power-of-two scale per tensor, and the
-    packed prefill over such inputs (the abstract's "selective FP8"; a reading
+    packed prefill with such Q and K and a bf16 V (the abstract's "selective FP8"; a reading
     for a future FP8 variant of the prefill kernel).  Pins in
     ``tests/test_oracle_fp8_pins.py``.
 

@@ -8,8 +8,8 @@
 * saturation, signed zero and NaN;
 * the per-tensor scale, the exactness of dequantisation in bf16 and the quantisation error
   bound (half a unit in the last place: 2^-4 relative for normal values);
-* the FP8 prefill against the independent padded-plus-mask formulation, and a length-1
-  sequence returning its own dequantised v row.
+* the prefill with FP8 Q and K against the independent padded-plus-mask formulation, and a
+  length-1 sequence returning its own v row.
 """
 import math
 
@@ -146,13 +146,14 @@ def test_fp8_prefill_against_the_padded_formulation():
     def codes(shape):
         c = rng.integers(0, 0x7F, size=shape).astype(np.uint8) | (rng.integers(0, 2, size=shape) * 0x80).astype(np.uint8)
         return c
-    qc, kc, vc = codes((T, Hq, d)), codes((T, Hkv, d)), codes((T, Hkv, d))
-    sq, sk, sv = 2.0 ** -6, 2.0 ** -7, 2.0 ** -5
-    got = fp8.prefill_fp8(qc, sq, kc, sk, vc, sv, cu, 1 / math.sqrt(d))
+    qc, kc = codes((T, Hq, d)), codes((T, Hkv, d))
+    vb = (rng.normal(0, 1, (T, Hkv, d)).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)   # bf16 V
+    sq, sk = 2.0 ** -6, 2.0 ** -7
+    got = fp8.prefill_fp8(qc, sq, kc, sk, vb, cu, 1 / math.sqrt(d))
     # the independent padded-plus-mask numpy formulation on the same dequantised values
-    ref = oracle_np.prefill_padded(fp8.dequantize_bf16_bits(qc, sq), fp8.dequantize_bf16_bits(kc, sk),
-                                   fp8.dequantize_bf16_bits(vc, sv), cu, 1 / math.sqrt(d))
+    ref = oracle_np.prefill_padded(fp8.dequantize_bf16_bits(qc, sq), fp8.dequantize_bf16_bits(kc, sk), vb, cu,
+                                   1 / math.sqrt(d))
     assert np.max(np.abs(got - ref)) <= 1e-12 * max(1.0, np.max(np.abs(ref)))
-    # a length-1 sequence returns its own (dequantised) v row
-    v0 = fp8.e4m3_decode(vc[0]) * sv
+    # a length-1 sequence returns its own v row
+    v0 = _bf16_bits_to_f64(vb[0])
     assert np.array_equal(got[0], np.repeat(v0, Hq // Hkv, axis=0))
