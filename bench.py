@@ -93,6 +93,18 @@ def decode_step_work(cfg, prompt_lengths, t):
 
 
 # --------------------------------------------------------------------------- helpers
+def decode_item_spread(cfg, n_sm: int, tiles_per_item: int = 2):
+    """How the decode attention's work items fall on the persistent CTAs (one per SM): an
+    item is a request x kv head x `tiles_per_item` query tiles of floor(128 / g) beams each,
+    and the CTAs take items round-robin.  Returns (items, CTAs, most items on one CTA)."""
+    g = cfg.Hq // cfg.Hkv
+    beams_per_tile = 128 // g
+    tiles = -(-cfg.W // beams_per_tile)
+    items = cfg.R * cfg.Hkv * (-(-tiles // tiles_per_item))
+    ctas = min(items, n_sm)
+    return items, ctas, -(-items // ctas) if ctas else 0
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -385,14 +397,18 @@ def run_ours(args):
     tflops = world * pre_flops_step * args.steps / (prefill_ms / 1e3) / 1e12
     per_gpu_tflops = pre_flops_step * args.steps / (prefill_ms / 1e3) / 1e12
 
+    n_sm = torch.cuda.get_device_properties(device).multi_processor_count
+
     def dec_report(dec, ms):
         cfg = dec.cfg
         us_per_step = ms * 1e3 / args.steps / (cfg.steps * layers)
         t_flops = dec.flops_per_search / (peaks["bf16_tflops"] * 1e12)
         t_bytes = dec.bytes_per_search / (peaks["hbm_gbs"] * 1e9)
         roof_us = max(t_flops, t_bytes) * 1e6 / (cfg.steps * layers)
+        items, ctas, most = decode_item_spread(cfg, n_sm)
         return {"workload": f"{cfg.name}: R{cfg.R} W{cfg.W} {cfg.steps} steps Hq{cfg.Hq}/Hkv{cfg.Hkv} d{cfg.head_dim}, "
                             f"{layers} layers, CUDA-graph replay",
+                "attention_items": items, "attention_ctas": ctas, "max_items_per_cta": most,
                 "us_per_step": round(us_per_step, 3), "roofline_us_per_step": round(roof_us, 3),
                 "roofline_frac": round(roof_us / us_per_step, 4),
                 "bound": "tensor" if t_flops > t_bytes else "hbm",

@@ -100,3 +100,12 @@ def test_first_step_moves_no_parent_slots():
     # one more slot reordered (read + write) and one more suffix slot read by the attention
     assert b2 - b1 == pytest.approx(3 * slot_kv, rel=1e-12)
     assert np.isfinite(b1)
+
+
+def test_decode_item_spread():
+    # 18-beam query tiles (g = 7), two per item, round-robin over 152 CTAs
+    short = wl.DECODE_CONFIGS["beam_short"]       # 100 beams: 6 tiles -> 3 items per (request, kv head)
+    assert bench.decode_item_spread(short, 152) == (32 * 2 * 3, 152, 2)
+    long_ = wl.DECODE_CONFIGS["beam_long"]        # 400 beams: 23 tiles -> 12 items per (request, kv head)
+    assert bench.decode_item_spread(long_, 152) == (16 * 2 * 12, 152, 3)
+    assert bench.decode_item_spread(short, 1000) == (192, 192, 1)
