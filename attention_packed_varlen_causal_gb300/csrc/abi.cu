@@ -115,30 +115,54 @@ size_t bg_packed_prefill_workspace_size(int32_t num_seqs, int32_t total_tokens, 
     return (bytes + 255) & ~size_t(255);
 }
 
-bg_status_t bg_packed_prefill_attn(const void *q, const void *k, const void *v, const int32_t *cu_seqlens,
+}  // extern "C"
+
+bg_status_t bg::prefill_check_args(const void *q, const void *k, const void *v, const int32_t *cu_seqlens,
                                    int32_t num_seqs, int32_t total_tokens, int32_t max_seqlen, int32_t Hq,
-                                   int32_t Hkv, int32_t head_dim, float scale, void *out, float *lse, void *workspace,
-                                   size_t workspace_bytes, int32_t *dev_status, cudaStream_t stream)
+                                   int32_t Hkv, int32_t head_dim, float scale, const void *out, const float *lse,
+                                   const int32_t *dev_status, bool *noop)
 {
+    *noop = false;
     if (num_seqs < 0 || total_tokens < 0 || max_seqlen < 0 || Hq <= 0 || Hkv <= 0 || head_dim <= 0)
         return BG_ERR_INVALID_ARG;
     if (Hq % Hkv != 0) return BG_ERR_INVALID_ARG;
     if (!std::isfinite(scale) || !(scale > 0.f)) return BG_ERR_INVALID_ARG;   // masked logits are -inf
     if (!supported_head_dim(head_dim) || max_seqlen > BG_MAX_SEQLEN) return BG_ERR_UNSUPPORTED;
-    if (num_seqs == 0 || total_tokens == 0) return BG_OK;
-    if (!q || !k || !v || !cu_seqlens || !out || !workspace) return BG_ERR_INVALID_ARG;
+    if (num_seqs == 0 || total_tokens == 0) {
+        *noop = true;
+        return BG_OK;
+    }
+    if (!q || !k || !v || !cu_seqlens || !out) return BG_ERR_INVALID_ARG;
     if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) || !aligned(cu_seqlens, 4) ||
-        !aligned(workspace, 256) || (lse && !aligned(lse, 4)) || (dev_status && !aligned(dev_status, 4)))
-        return BG_ERR_INVALID_ARG;
-    if (workspace_bytes < bg_packed_prefill_workspace_size(num_seqs, total_tokens, max_seqlen, Hq, Hkv, head_dim))
+        (lse && !aligned(lse, 4)) || (dev_status && !aligned(dev_status, 4)))
         return BG_ERR_INVALID_ARG;
     const size_t qbytes = static_cast<size_t>(total_tokens) * Hq * head_dim * 2;
     const size_t kvbytes = static_cast<size_t>(total_tokens) * Hkv * head_dim * 2;
     const size_t lsebytes = lse ? static_cast<size_t>(total_tokens) * Hq * 4 : 0;
     if (overlap(out, qbytes, q, qbytes) || overlap(out, qbytes, k, kvbytes) || overlap(out, qbytes, v, kvbytes) ||
-        overlap(out, qbytes, workspace, workspace_bytes) || overlap(lse, lsebytes, out, qbytes) ||
-        overlap(lse, lsebytes, q, qbytes) || overlap(lse, lsebytes, k, kvbytes) ||
-        overlap(lse, lsebytes, v, kvbytes) || overlap(lse, lsebytes, workspace, workspace_bytes))
+        overlap(lse, lsebytes, out, qbytes) || overlap(lse, lsebytes, q, qbytes) ||
+        overlap(lse, lsebytes, k, kvbytes) || overlap(lse, lsebytes, v, kvbytes))
+        return BG_ERR_INVALID_ARG;
+    return BG_OK;
+}
+
+extern "C" {
+
+bg_status_t bg_packed_prefill_attn(const void *q, const void *k, const void *v, const int32_t *cu_seqlens,
+                                   int32_t num_seqs, int32_t total_tokens, int32_t max_seqlen, int32_t Hq,
+                                   int32_t Hkv, int32_t head_dim, float scale, void *out, float *lse, void *workspace,
+                                   size_t workspace_bytes, int32_t *dev_status, cudaStream_t stream)
+{
+    bool noop = false;
+    const bg_status_t chk = prefill_check_args(q, k, v, cu_seqlens, num_seqs, total_tokens, max_seqlen, Hq, Hkv,
+                                               head_dim, scale, out, lse, dev_status, &noop);
+    if (chk != BG_OK || noop) return chk;
+    if (!workspace || !aligned(workspace, 256)) return BG_ERR_INVALID_ARG;
+    if (workspace_bytes < bg_packed_prefill_workspace_size(num_seqs, total_tokens, max_seqlen, Hq, Hkv, head_dim))
+        return BG_ERR_INVALID_ARG;
+    const size_t qbytes = static_cast<size_t>(total_tokens) * Hq * head_dim * 2;
+    const size_t lsebytes = lse ? static_cast<size_t>(total_tokens) * Hq * 4 : 0;
+    if (overlap(out, qbytes, workspace, workspace_bytes) || overlap(lse, lsebytes, workspace, workspace_bytes))
         return BG_ERR_INVALID_ARG;
 
     const int32_t g = Hq / Hkv;

@@ -15,6 +15,14 @@ namespace bg {
 
 struct AttnParams;
 
+// Host checks of bg_packed_prefill_attn's arguments other than the workspace (sizes, shape
+// support, scale, pointers, alignment, aliasing between the tensors).  Returns BG_OK or the
+// status the entry point returns; *noop is set when the call is a valid no-op.
+bg_status_t prefill_check_args(const void *q, const void *k, const void *v, const int32_t *cu_seqlens,
+                               int32_t num_seqs, int32_t total_tokens, int32_t max_seqlen, int32_t Hq,
+                               int32_t Hkv, int32_t head_dim, float scale, const void *out, const float *lse,
+                               const int32_t *dev_status, bool *noop);
+
 // Prefill: work-list pre-pass + attention kernel.  Maps are built by the
 // caller.  Returns cudaSuccess or the launch error.
 cudaError_t launch_prefill_worklist(const int32_t *cu_seqlens, int32_t num_seqs, int32_t total_tokens,

@@ -13,12 +13,14 @@
 // Cost of that convenience:
 //   * every GPU that loads the library holds kNoAllocScratchBytes of device
 //     memory until the process exits;
-//   * all calls on a device share the one array, so two calls that may run
+//   * all calls in one context share the one array, so two calls that may run
 //     at the same time on the GPU (different streams, overlapping graphs)
 //     race on it -- serialise them;
 //   * problems whose work list does not fit are rejected.
 // No clearing is needed between calls: each call's first kernel rewrites the
 // header and every work-list entry before the attention kernel reads them.
+#include <cudaTypedefs.h>
+
 #include <mutex>
 
 #include "bg_attn.h"
@@ -34,23 +36,71 @@ static_assert(kNoAllocScratchBytes % 256 == 0, "scratch size must keep 256-byte 
 // cudaGetSymbolAddress below.
 static __device__ __align__(256) unsigned char g_scratch[kNoAllocScratchBytes];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mutex;
-void *g_scratch_ptr[kMaxDevices] = {};
+// The array's device address is looked up once per CUDA context and cached
+// under that context's unique ID (cuCtxGetId).  A context made after
+// cudaDeviceReset, or a non-primary context the caller makes current, has a
+// new ID, so it gets its own lookup instead of a stale address.
+PFN_cuCtxGetCurrent_v4000 g_ctx_current = nullptr;
+PFN_cuCtxGetId_v12000 g_ctx_id = nullptr;
+std::once_flag g_entry_once;
 
-// Device address of g_scratch on the current device, looked up once per
-// device (with that device current) and cached.
-bg_status_t scratch_for_current_device(void **out)
+void resolve_entry_points()
 {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return BG_ERR_CUDA;
-    std::lock_guard<std::mutex> lock(g_mutex);
-    if (g_scratch_ptr[dev] == nullptr) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess || p == nullptr) return BG_ERR_CUDA;
-        g_scratch_ptr[dev] = p;
+    std::call_once(g_entry_once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_ctx_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(fn);
+        fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_ctx_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(fn);
+    });
+}
+
+constexpr int kCacheSlots = 64;
+struct Slot {
+    unsigned long long ctx_id;
+    void *ptr;
+};
+std::mutex g_mutex;
+Slot g_cache[kCacheSlots] = {};
+int g_next = 0;   // next slot to fill (oldest entry is replaced once all are used)
+
+// ID of the current context; makes the device's primary context current first if the
+// calling thread has none yet (cudaSetDevice binds it).
+bool current_context_id(unsigned long long *id)
+{
+    resolve_entry_points();
+    if (!g_ctx_current || !g_ctx_id) return false;
+    CUcontext ctx = nullptr;
+    if (g_ctx_current(&ctx) != CUDA_SUCCESS) return false;
+    if (ctx == nullptr) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || cudaSetDevice(dev) != cudaSuccess) return false;
+        if (g_ctx_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return false;
     }
-    *out = g_scratch_ptr[dev];
+    return g_ctx_id(ctx, id) == CUDA_SUCCESS;
+}
+
+// Device address of g_scratch in the current context.
+bg_status_t scratch_for_current_context(void **out)
+{
+    unsigned long long id = 0;
+    if (!current_context_id(&id)) return BG_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    for (int i = 0; i < kCacheSlots; ++i) {
+        if (g_cache[i].ptr != nullptr && g_cache[i].ctx_id == id) {
+            *out = g_cache[i].ptr;
+            return BG_OK;
+        }
+    }
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess || p == nullptr) return BG_ERR_CUDA;
+    g_cache[g_next] = Slot{id, p};
+    g_next = (g_next + 1) % kCacheSlots;
+    *out = p;
     return BG_OK;
 }
 
@@ -62,11 +112,16 @@ extern "C" bg_status_t bg_packed_prefill_attn_noalloc(const void *q, const void 
                                                       int32_t Hkv, int32_t head_dim, float scale, void *out,
                                                       float *lse, int32_t *dev_status, cudaStream_t stream)
 {
-    if (num_seqs < 0 || total_tokens < 0) return BG_ERR_INVALID_ARG;
+    // the same argument checks as bg_packed_prefill_attn come first, so an invalid call
+    // reports what is wrong with it whatever its size
+    bool noop = false;
+    const bg_status_t chk = bg::prefill_check_args(q, k, v, cu_seqlens, num_seqs, total_tokens, max_seqlen, Hq, Hkv,
+                                                   head_dim, scale, out, lse, dev_status, &noop);
+    if (chk != BG_OK || noop) return chk;
     const size_t need = bg_packed_prefill_workspace_size(num_seqs, total_tokens, max_seqlen, Hq, Hkv, head_dim);
     if (need > kNoAllocScratchBytes) return BG_ERR_UNSUPPORTED;   // work list would not fit the fixed scratch
     void *scratch = nullptr;
-    const bg_status_t st = scratch_for_current_device(&scratch);
+    const bg_status_t st = scratch_for_current_context(&scratch);
     if (st != BG_OK) return st;
     return bg_packed_prefill_attn(q, k, v, cu_seqlens, num_seqs, total_tokens, max_seqlen, Hq, Hkv, head_dim, scale,
                                   out, lse, scratch, kNoAllocScratchBytes, dev_status, stream);

@@ -42,11 +42,12 @@ from attention_packed_varlen_causal_gb300 import workloads as wl  # noqa: E402
 
 METRIC = "packed-prefill attn TFLOP/s (% bf16 peak); beam-decode attn µs/step (% roofline)"
 LAYERS = 28
+SPEC_HBM_GBS = 8000.0   # nominal GB300 HBM3e bandwidth (~8 TB/s), reported beside the measured copy peak
 
 # DRAM bytes of one attn_kernel<Prefill,128> launch on one layer of the Prefill-Only batch
-# (dram__bytes_read.sum + dram__bytes_write.sum from one ncu capture, written up in
-# profiles/attn_kernel_prefill_prefill_only.md).  It holds only for the sources that launch is
-# built from, identified by `sources` (kernel_sources_hash); otherwise the bench reports null.
+# (dram__bytes_read.sum + dram__bytes_write.sum from one ncu capture of that launch).  It holds
+# only for the sources that launch is built from, identified by `sources`
+# (kernel_sources_hash); otherwise the bench reports null.
 PREFILL_TRAFFIC = {"sources": "98df18b6da903670", "bytes": 649163520 + 244014080}
 # the files a bg_packed_prefill_attn launch is built from
 PREFILL_SOURCES = ["abi.cu", "prefill.cu", "bg_attn_kernel.cuh", "bg_ptx.cuh", "bg_internal.h"]
@@ -311,6 +312,83 @@ def time_oracle_sample(layer_seqs: int = 240, seed_layer: int = 0):
     return fl / dt / 1e12, dt, oracle.num_threads(), desc
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the platform string)."""
+    import platform
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.processor() or platform.machine()
+
+
+def time_oracle_configs(skewed_seqs: int = 160):
+    """The fp64 oracle, as it stands, on every workload (one layer each), timed on the host
+    cores: the tiny prefill, a stated sample of the skewed layer (its first ``skewed_seqs``
+    sequences), and for both beam searches one decode step (the last, longest one) and one
+    complete search of one layer (per step the history reorder through the parent index, the
+    append and the attention).  The Prefill-Only layer is timed by time_oracle_sample."""
+    import oracle
+    res = {}
+    # tiny
+    cfg = wl.PREFILL_CONFIGS["tiny"]
+    x = wl.make_prefill_config_inputs(cfg)
+    fl = prefill_flops(x["lengths"], x["Hq"], x["head_dim"])
+    t0 = time.perf_counter()
+    oracle.prefill(x["q"], x["k"], x["v"], x["cu_seqlens"], 1.0 / math.sqrt(x["head_dim"]))
+    dt = time.perf_counter() - t0
+    res["tiny"] = {"seconds": round(dt, 4), "gflop": round(fl / 1e9, 3), "tflops": round(fl / dt / 1e12, 6),
+                   "sample": "the whole tiny layer (4 sequences, T = 392)"}
+    # skewed: the first sequences of the layer, with the layer's 1 % outlier K rows drawn over them
+    cfg = wl.PREFILL_CONFIGS["skewed"]
+    lengths = wl.prefill_lengths(cfg)[:skewed_seqs]
+    x = wl.make_prefill_inputs(lengths, cfg.Hq, cfg.Hkv, cfg.head_dim, outlier_frac=cfg.outlier_frac,
+                               outlier_scale=cfg.outlier_scale)
+    fl = prefill_flops(lengths, cfg.Hq, cfg.head_dim)
+    full = prefill_flops(wl.prefill_lengths(cfg), cfg.Hq, cfg.head_dim)
+    t0 = time.perf_counter()
+    oracle.prefill(x["q"], x["k"], x["v"], x["cu_seqlens"], 1.0 / math.sqrt(cfg.head_dim))
+    dt = time.perf_counter() - t0
+    res["skewed"] = {"seconds": round(dt, 3), "gflop": round(fl / 1e9, 2), "tflops": round(fl / dt / 1e12, 6),
+                     "sample": f"first {skewed_seqs} of 4096 sequences of one layer ({int(sum(lengths))} tokens, "
+                               f"{fl / 1e9:.1f} of the layer's {full / 1e9:.0f} GFLOP)",
+                     "full_layer_seconds_extrapolated": round(dt * full / fl, 1)}
+    # beam searches
+    for name in ("beam_short", "beam_long"):
+        cfg = wl.DECODE_CONFIGS[name]
+        pb = wl.make_decode_config_problem(cfg)
+        scale = 1.0 / math.sqrt(cfg.head_dim)
+        plen = pb["prompt_lengths"]
+        hist = oracle.BeamHistory(cfg.R, cfg.W)
+        step_s, step_fl = [], []
+        t_all = time.perf_counter()
+        for s in range(cfg.steps):
+            t0 = time.perf_counter()
+            hist.step(pb["parent"][s], pb["new_k"][s], pb["new_v"][s])
+            hk, hv = hist.materialise(cfg.Hkv, cfg.head_dim)
+            oracle.decode(pb["q"][s], pb["prompt_k"], pb["prompt_v"], pb["cu_prompt"], hk, hv, scale)
+            step_s.append(time.perf_counter() - t0)
+            step_fl.append(decode_step_work(cfg, plen, s + 1)[0])
+        dt_all = time.perf_counter() - t_all
+        res[name] = {"step_seconds": round(step_s[-1], 4), "step": cfg.steps,
+                     "step_tflops": round(step_fl[-1] / step_s[-1] / 1e12, 6),
+                     "search_seconds": round(dt_all, 3), "search_tflops": round(sum(step_fl) / dt_all / 1e12, 6),
+                     "us_per_step_avg": round(dt_all * 1e6 / cfg.steps, 1),
+                     "sample": f"one layer: the last decode step (suffix length {cfg.steps}), and the complete "
+                               f"{cfg.steps}-step search (history reorder + append + attention per step)"}
+    return res
+
+
 def run_ours(args):
     import torch
     rank, world, local = dist_env()
@@ -393,54 +471,88 @@ def run_ours(args):
     prefill_ms = max_over_ranks(prefill_ms, world, device)
     call_ms = [pre_start[j].elapsed_time(pre_end[j]) for j in range(n_ev)]
     avg_call_s = statistics.mean(call_ms) / 1e3
+    med_call_s = statistics.median(call_ms) / 1e3
     pre_flops_step = pre.flops * layers
     tflops = world * pre_flops_step * args.steps / (prefill_ms / 1e3) / 1e12
     per_gpu_tflops = pre_flops_step * args.steps / (prefill_ms / 1e3) / 1e12
 
     n_sm = torch.cuda.get_device_properties(device).multi_processor_count
 
+    def replay_median_ms(dec, reps):
+        """Median over ``reps`` individually timed replays of the whole search."""
+        evs = [(ev(), ev()) for _ in range(reps)]
+        with torch.cuda.stream(stream):
+            for a, b in evs:
+                a.record(stream)
+                dec.replay()
+                b.record(stream)
+        torch.cuda.synchronize()
+        return statistics.median(a.elapsed_time(b) for a, b in evs)
+
     def dec_report(dec, ms):
         cfg = dec.cfg
-        us_per_step = ms * 1e3 / args.steps / (cfg.steps * layers)
+        n_step = cfg.steps * layers
+        mean_us = ms * 1e3 / args.steps / n_step
+        med_ms = replay_median_ms(dec, args.reps)
+        us_per_step = med_ms * 1e3 / n_step
         t_flops = dec.flops_per_search / (peaks["bf16_tflops"] * 1e12)
         t_bytes = dec.bytes_per_search / (peaks["hbm_gbs"] * 1e9)
-        roof_us = max(t_flops, t_bytes) * 1e6 / (cfg.steps * layers)
+        roof_us = max(t_flops, t_bytes) * 1e6 / n_step
         items, ctas, most = decode_item_spread(cfg, n_sm)
         return {"workload": f"{cfg.name}: R{cfg.R} W{cfg.W} {cfg.steps} steps Hq{cfg.Hq}/Hkv{cfg.Hkv} d{cfg.head_dim}, "
                             f"{layers} layers, CUDA-graph replay",
                 "attention_items": items, "attention_ctas": ctas, "max_items_per_cta": most,
-                "us_per_step": round(us_per_step, 3), "roofline_us_per_step": round(roof_us, 3),
+                "us_per_step": round(us_per_step, 3), "us_per_step_mean_in_step": round(mean_us, 3),
+                "replays_timed": args.reps, "roofline_us_per_step": round(roof_us, 3),
                 "roofline_frac": round(roof_us / us_per_step, 4),
                 "bound": "tensor" if t_flops > t_bytes else "hbm",
-                "us_per_step_definition": "one decode step of one layer: suffix reorder+append, then attention, "
-                                          "one bg_beam_decode_step call (two launches)"}
+                "tokens_per_s": round(cfg.R * cfg.W * cfg.steps / (med_ms / 1e3), 1),
+                "tokens_per_s_definition": f"R*W*steps new tokens per search / time of the search's decode "
+                                           f"attention steps through all {layers} layers (attention only)",
+                "us_per_step_definition": "one decode step of one layer (bg_beam_decode_step: suffix reorder + "
+                                          "append, then attention), median over the timed replays of the whole "
+                                          "search / (steps x layers)",
+                "launches_per_step": dec.launches // n_step}
 
     decode = {"beam_short": dec_report(dec_s, short_ms), "beam_long": dec_report(dec_l, long_ms)}
+    tiny = run_tiny(device, stream, args.reps)
 
     # e2e: one layer per step through the C ABI with host buffers (pinned),
     # H2D of q, k, v, cu_seqlens and D2H of the output inside the timed region
     e2e = run_e2e(pre, device, stream, args)
     last = run_last_token(pre, stream, peaks)
-    select = run_beam_select(device, stream, peaks)
-    skewed = run_skewed(device, stream, peaks)
+    select = run_beam_select(device, stream, peaks, args.reps)
+    skewed = run_skewed(device, stream, peaks, args.reps)
 
     # oracle CPU baseline (rank 0, N = 1 only)
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         v, dt, thr, desc = time_oracle_sample(args.cpu_sample_seqs)
         cpu = {"value": round(v, 6), "unit": "TFLOP/s", "cores": thr, "kind": "oracle", "sample": desc,
-               "seconds": round(dt, 2)}
+               "seconds": round(dt, 2), "cpu_model": cpu_model(),
+               "per_config": {"prefill_only": {"seconds": round(dt, 3), "tflops": round(v, 6), "sample": desc}}}
+        cpu["per_config"].update(time_oracle_configs())
 
-    achieved = pre.bytes / avg_call_s / 1e9
+    achieved = pre.bytes / med_call_s / 1e9
     traffic = args.traffic
-    if traffic is None and kernel_sources_hash() == PREFILL_TRAFFIC["sources"]:
+    src_hash = kernel_sources_hash()
+    traffic_source = "--traffic argument" if traffic is not None else None
+    if traffic is None and src_hash == PREFILL_TRAFFIC["sources"]:
         traffic = PREFILL_TRAFFIC["bytes"]
+        traffic_source = f"stored ncu capture of this launch, prefill sources hash {src_hash}"
+    if traffic is None:
+        traffic_source = f"none: prefill sources (hash {src_hash}) changed since the stored capture"
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
+                "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic, "traffic_source": traffic_source,
                 "algorithmic_bytes_per_launch": pre.bytes,
+                "launch_us_median": round(med_call_s * 1e6, 2), "launch_us_mean": round(avg_call_s * 1e6, 2),
+                "launches_timed": n_ev,
                 "kernel": "bg_packed_prefill_attn (work-list pre-pass + attn_kernel<Prefill,128>)",
                 "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs, burst copy)",
-                "tensor_frac_of_bf16_peak": round(pre.flops / avg_call_s / 1e12 / peaks["bf16_tflops"], 4)}
+                "spec_hbm_gbs": SPEC_HBM_GBS, "frac_of_spec_hbm": round(achieved / SPEC_HBM_GBS, 4),
+                "tensor_frac_of_bf16_peak": round(pre.flops / med_call_s / 1e12 / peaks["bf16_tflops"], 4),
+                "tensor_frac_of_bf16_sustained": round(pre.flops / med_call_s / 1e12 /
+                                                       peaks["bf16_tflops_sustained"], 4)}
     launches = args.steps * (2 * layers + dec_s.launches + dec_l.launches)
     line = {
         "metric": METRIC, "value": round(tflops, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
@@ -456,7 +568,7 @@ def run_ours(args):
                     "avg_call_us": round(avg_call_s * 1e6, 2), "tokens_per_s": round(world * pre.T * layers * args.steps / (prefill_ms / 1e3), 1)},
         "decode": decode,
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk, "gpu_launches": launches,
-        "last_token": last, "beam_select": select, "skewed": skewed,
+        "last_token": last, "beam_select": select, "skewed": skewed, "tiny": tiny,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -464,7 +576,57 @@ def run_ours(args):
         torch.distributed.destroy_process_group()
 
 
-def run_last_token(pre, stream, peaks, reps: int = 5):
+def median_us_of_calls(stream, fns, reps):
+    """Median, in microseconds, over ``reps`` individually timed calls; call i runs fns[i % len(fns)]
+    (CUDA events on the launching stream around every call)."""
+    import torch
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    with torch.cuda.stream(stream):
+        for i, (a, b) in enumerate(evs):
+            a.record(stream)
+            fns[i % len(fns)]()
+            b.record(stream)
+    torch.cuda.synchronize()
+    return statistics.median(a.elapsed_time(b) for a, b in evs) * 1e3
+
+
+def run_tiny(device, stream, reps: int = 50):
+    """The tiny packed prefill (4 sequences {17, 64, 100, 211}, 16/8 heads, d 128), median over
+    ``reps`` individually timed calls.  The inputs (4.8 MB) would sit in L2, so the calls rotate
+    over enough copies in distinct buffers to cover four times the L2 size."""
+    import torch
+    from attention_packed_varlen_causal_gb300 import binding as bg
+    cfg = wl.PREFILL_CONFIGS["tiny"]
+    x = wl.make_prefill_config_inputs(cfg)
+    T, Hq, Hkv, d = x["q"].shape[0], x["Hq"], x["Hkv"], x["head_dim"]
+    by = prefill_bytes(T, Hq, Hkv, d)
+    l2 = int(getattr(torch.cuda.get_device_properties(device), "L2_cache_size", 129 << 20))
+    n_sets = max(2, int(math.ceil(4 * l2 / by)))
+
+    def dev(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(device)
+
+    q0, k0, v0 = dev(x["q"]), dev(x["k"]), dev(x["v"])
+    cu = torch.from_numpy(x["cu_seqlens"]).to(device)
+    sets = [(q0.clone(), k0.clone(), v0.clone(), torch.empty_like(q0)) for _ in range(n_sets)]
+    ws = torch.empty(bg.bg_packed_prefill_workspace_size(len(x["lengths"]), T, x["max_seqlen"], Hq, Hkv, d),
+                     dtype=torch.uint8, device=device)
+    fns = [lambda st=st: bg.bg_packed_prefill_attn(st[0], st[1], st[2], cu, x["max_seqlen"], st[3], workspace=ws,
+                                                    stream=stream) for st in sets]
+    for f in fns[:10]:
+        with torch.cuda.stream(stream):
+            f()
+    us = median_us_of_calls(stream, fns, max(reps, n_sets))
+    fl = prefill_flops(x["lengths"], Hq, d)
+    del sets
+    return {"workload": "tiny packed prefill: lengths {17, 64, 100, 211}, Hq16/Hkv8 d128, causal",
+            "us_per_call": round(us, 2), "tflops": round(fl / us / 1e6, 3), "gflop": round(fl / 1e9, 4),
+            "bytes": by, "l2": f"calls rotate over {n_sets} input copies ({n_sets * by / 1e6:.0f} MB >= 4x L2)",
+            "definition": f"median over {max(reps, n_sets)} individually timed bg_packed_prefill_attn calls "
+                          "(work-list pre-pass + attention)"}
+
+
+def run_last_token(pre, stream, peaks, reps: int = 56):
     """The Prefill-Only last-layer variant, timed apart from the step: attention of each
     sequence's last valid token over the layer's K/V (bg_packed_last_token_attn), on every
     layer's own K/V, CUDA events on the launching stream."""
@@ -474,27 +636,23 @@ def run_last_token(pre, stream, peaks, reps: int = 5):
     B = len(pre.lengths)
     qs = [pre.q[l].index_select(0, rows).contiguous() for l in range(len(pre.q))]
     out = torch.empty((B, pre.Hq, pre.d), dtype=torch.bfloat16, device=pre.q[0].device)
+    fns = [lambda l=l: bg.bg_packed_last_token_attn(qs[l], pre.k[l], pre.v[l], pre.cu, pre.maxlen, out,
+                                                     stream=stream) for l in range(len(qs))]
     with torch.cuda.stream(stream):
-        for l in range(len(qs)):
-            bg.bg_packed_last_token_attn(qs[l], pre.k[l], pre.v[l], pre.cu, pre.maxlen, out, stream=stream)
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(reps):
-            for l in range(len(qs)):
-                bg.bg_packed_last_token_attn(qs[l], pre.k[l], pre.v[l], pre.cu, pre.maxlen, out, stream=stream)
-        e1.record(stream)
+        for f in fns:
+            f()
     torch.cuda.synchronize()
-    us = e0.elapsed_time(e1) * 1e3 / (reps * len(qs))
+    us = median_us_of_calls(stream, fns, max(reps, 50))
     by = float(pre.T * pre.Hkv * pre.d * 2 * 2 + 2 * B * pre.Hq * pre.d * 2)   # K, V once; q in, out
     gbs = by / us / 1e3
     return {"workload": f"Prefill-Only batch, last valid token of each of {B} sequences, {len(qs)} layers",
             "us_per_layer": round(us, 2), "bytes_per_layer": by, "achieved_gbs": round(gbs, 1),
             "hbm_frac": round(gbs / peaks["hbm_gbs"], 4), "bound": "hbm",
-            "definition": "bg_packed_last_token_attn per layer, timed apart from the step (not in value)"}
+            "definition": "bg_packed_last_token_attn per layer (each layer's own K/V in turn), median over "
+                          f"{max(reps, 50)} individually timed calls, apart from the step (not in value)"}
 
 
-def run_skewed(device, stream, peaks, reps: int = 5):
+def run_skewed(device, stream, peaks, reps: int = 50):
     """The skewed packed-prefill stress workload, timed apart from the step: 4096 sequences,
     L = clip(round(lognormal(5.5, 0.8)), 1, 2048), 16 Q / 8 KV heads, head_dim 128, 1 % of the
     (token, kv head) K rows scaled by 8 (outlier logits).  One layer stays resident (16.7 GB,
@@ -523,17 +681,12 @@ def run_skewed(device, stream, peaks, reps: int = 5):
     maxlen = max(lengths)
     ws = torch.empty(bg.bg_packed_prefill_workspace_size(len(lengths), T, maxlen, Hq, Hkv, d), dtype=torch.uint8,
                      device=device)
+    call = lambda: bg.bg_packed_prefill_attn(q, k, v, cu, maxlen, out, workspace=ws, stream=stream)  # noqa: E731
     with torch.cuda.stream(stream):
-        for _ in range(2):
-            bg.bg_packed_prefill_attn(q, k, v, cu, maxlen, out, workspace=ws, stream=stream)
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(reps):
-            bg.bg_packed_prefill_attn(q, k, v, cu, maxlen, out, workspace=ws, stream=stream)
-        e1.record(stream)
+        for _ in range(3):
+            call()
     torch.cuda.synchronize()
-    us = e0.elapsed_time(e1) * 1e3 / reps
+    us = median_us_of_calls(stream, [call], reps)
     flops = prefill_flops(lengths, Hq, d)
     by = prefill_bytes(T, Hq, Hkv, d)
     res = {"workload": f"skewed stress: {len(lengths)} seqs, L=clip(round(lognormal(5.5, 0.8)), 1, 2048) seed 0, "
@@ -543,8 +696,8 @@ def run_skewed(device, stream, peaks, reps: int = 5):
            "achieved_gbs": round(by / us / 1e3, 1), "hbm_frac": round(by / us / 1e3 / peaks["hbm_gbs"], 4),
            "roofline_us": round(max(flops / (peaks["bf16_tflops"] * 1e6), by / (peaks["hbm_gbs"] * 1e3)), 1),
            "flops": flops, "bytes": by,
-           "definition": "bg_packed_prefill_attn on one layer of the skewed workload, timed apart from the step "
-                         "(not in value)"}
+           "definition": f"bg_packed_prefill_attn on one layer of the skewed workload, median over {reps} "
+                         "individually timed calls, apart from the step (not in value)"}
     del q, k, v, out, ws, k2, pick
     torch.cuda.empty_cache()
     return res
@@ -553,7 +706,7 @@ def run_skewed(device, stream, peaks, reps: int = 5):
 SELECT_VOCAB = 65536   # the pages give no vocabulary size; selection cost is linear in it
 
 
-def run_beam_select(device, stream, peaks, reps: int = 5):
+def run_beam_select(device, stream, peaks, reps: int = 50):
     """Beam candidate selection of one decode step (bg_beam_select) on the two beam
     configurations' shapes, timed apart from the step: fp32 logits N(0, 3) of every beam
     over SELECT_VOCAB tokens (0.84 / 1.68 GB, larger than L2), accumulated scores N(-3, 1)."""
@@ -571,24 +724,20 @@ def run_beam_select(device, stream, peaks, reps: int = 5):
         par = torch.empty((R, W), dtype=torch.int32, device=device)
         sc = torch.empty((R, W), dtype=torch.float32, device=device)
         ws = torch.empty(bg.bg_beam_select_workspace_size(R, W, V), dtype=torch.uint8, device=device)
+        call = lambda: bg.bg_beam_select(logits, cum, tok, par, sc, workspace=ws, stream=stream)  # noqa: E731
         with torch.cuda.stream(stream):
-            for _ in range(2):
-                bg.bg_beam_select(logits, cum, tok, par, sc, workspace=ws, stream=stream)
-            torch.cuda.synchronize()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            for _ in range(reps):
-                bg.bg_beam_select(logits, cum, tok, par, sc, workspace=ws, stream=stream)
-            e1.record(stream)
+            for _ in range(3):
+                call()
         torch.cuda.synchronize()
-        us = e0.elapsed_time(e1) * 1e3 / reps
+        us = median_us_of_calls(stream, [call], reps)
         by = float(R * W * V * 4 + R * W * 4 * 4)      # logits once; cum in; token, parent, score out
         gbs = by / us / 1e3
         res[name] = {"workload": f"R{R} W{W} V{V} fp32 logits", "us_per_call": round(us, 2), "bytes": by,
                      "achieved_gbs": round(gbs, 1), "hbm_frac": round(gbs / peaks["hbm_gbs"], 4)}
         del logits
     res["definition"] = ("bg_beam_select per decode step (per-beam logsumexp + top-W, merged by accumulated score), "
-                         "timed apart from the step (not in value); bound: HBM, logits read once")
+                         f"median over {reps} individually timed calls, apart from the step (not in value); "
+                         "bound: HBM, logits read once")
     return res
 
 
@@ -695,6 +844,8 @@ def main():
     ap.add_argument("--cpu-sample-seqs", type=int, default=240)
     ap.add_argument("--ref-sample-seqs", type=int, default=24)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--reps", type=int, default=50,
+                    help="individually timed repetitions behind every median (kernel legs)")
     ap.add_argument("--clocks-dir", default=None,
                     help="where the raw nvidia-smi samples of the timed region go (default: the temp directory)")
     ap.add_argument("--traffic", type=float, default=None,

@@ -321,19 +321,22 @@ bg_status_t bg_beam_select(const float *logits, const float *cum,
  * must not call cudaMalloc.
  *
  * Same arguments, semantics and errors as bg_packed_prefill_attn, minus the
- * workspace.  The work list lives in a fixed array of
- * BG_NOALLOC_SCRATCH_BYTES in the library's own device memory, which every
- * GPU that loads the library keeps until the process exits.  Limits and
- * rules:
- *   - problems with bg_packed_prefill_workspace_size(...) larger than
+ * workspace: the same argument checks run first.  The work list lives in a
+ * fixed array of BG_NOALLOC_SCRATCH_BYTES in the library's own device
+ * memory, which every GPU that loads the library keeps until the process
+ * exits.  Limits and rules:
+ *   - valid problems with bg_packed_prefill_workspace_size(...) larger than
  *     BG_NOALLOC_SCRATCH_BYTES (total_tokens/128 + num_seqs + 1 > 65520)
  *     return BG_ERR_UNSUPPORTED and enqueue nothing;
- *   - all calls on a device share that array: calls that can overlap on the
- *     GPU (different streams, concurrent graphs) race and must be
+ *   - all calls in one CUDA context share that array: calls that can overlap
+ *     on the GPU (different streams, concurrent graphs) race and must be
  *     serialised by the caller;
- *   - the first call on each device looks up the array's device address
- *     (cudaGetSymbolAddress, with that device current) and caches it; make
- *     that first call before any stream capture.
+ *   - the first call in each CUDA context looks up the array's device
+ *     address (cudaGetSymbolAddress, in the context current on the calling
+ *     thread) and caches it under the context's unique ID, so a context
+ *     created later (after cudaDeviceReset, or another context the caller
+ *     makes current) gets its own lookup; make the first call in a context
+ *     before any stream capture.
  * It never calls cudaMalloc, cudaFree or any allocating routine.
  */
 #define BG_NOALLOC_SCRATCH_BYTES (1u << 20)

@@ -1,9 +1,9 @@
 """Runs one hot-path call on a named workload a few times, for profilers.
 
-    python -m attention_packed_varlen_causal_gb300.profile_case prefill_only --iters 3
-    python -m attention_packed_varlen_causal_gb300.profile_case beam_long --iters 2
-    python -m attention_packed_varlen_causal_gb300.profile_case beam_long --iters 2 --two-call
-    python -m attention_packed_varlen_causal_gb300.profile_case select_long --iters 2
+    python profile_case.py prefill_only --iters 3
+    python profile_case.py beam_long --iters 2
+    python profile_case.py beam_long --iters 2 --two-call
+    python profile_case.py select_long --iters 2
 
 Prefill workloads (tiny, prefill_only, skewed) call bg_packed_prefill_attn
 ``iters`` times on one layer of inputs; decode workloads (beam_short,
@@ -22,7 +22,7 @@ import argparse
 import os
 import sys
 
-ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 

@@ -206,3 +206,35 @@ def test_beam_select_host_checks(lib):
     assert sel(wsb=16) == binding.BG_ERR_INVALID_ARG
     assert sel(tok=FAKE * 8 + 64, logits=FAKE * 8) == binding.BG_ERR_INVALID_ARG   # output inside the logits
     assert sel(par=FAKE * 3) == binding.BG_ERR_INVALID_ARG               # two outputs overlap
+
+
+_NOALLOC_CHECK = r"""
+import sys
+from attention_packed_varlen_causal_gb300 import binding as bg
+lib = bg.load()
+fake = 1 << 32          # 4 GiB apart: the tensors these sizes describe do not overlap
+def call(num_seqs, total, Hq, Hkv, q=fake):
+    return lib.bg_packed_prefill_attn_noalloc(q, fake * 2, fake * 3, fake * 4, num_seqs, total, 1, Hq, Hkv, 128,
+                                              0.1, fake * 5, None, None, None)
+# 200,000 sequences need more work-list entries than the fixed scratch holds
+print(call(200000, 200000, 16, 8),   # valid but too large
+      call(200000, 200000, 16, 7),   # Hq % Hkv != 0: the argument error wins over the size
+      call(200000, 200000, 16, 8, q=None))
+"""
+
+
+def test_noalloc_host_checks_run_in_order_without_a_device():
+    """bg_packed_prefill_attn_noalloc checks its arguments first (bad ones give
+    BG_ERR_INVALID_ARG whatever the size), then rejects a valid problem whose work list
+    does not fit its fixed scratch with BG_ERR_UNSUPPORTED, both before any CUDA call.
+    The calls run in a child process that sees no GPU, so even a regression of these
+    checks cannot launch anything on fake pointers: it would come back as BG_ERR_CUDA."""
+    import subprocess
+    import sys
+    build.build()
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run([sys.executable, "-c", _NOALLOC_CHECK], cwd=ROOT, env=env, capture_output=True, text=True,
+                       timeout=120)
+    assert r.returncode == 0, r.stderr
+    codes = [int(c) for c in r.stdout.split()]
+    assert codes == [binding.BG_ERR_UNSUPPORTED, binding.BG_ERR_INVALID_ARG, binding.BG_ERR_INVALID_ARG]
