@@ -39,6 +39,8 @@ SIGNATURES = {
     "bg_packed_prefill_workspace_size": ([_I32] * 6, _SZ),
     "bg_packed_prefill_attn": ([_P, _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32, _F32, _P, _P, _P, _SZ, _P, _P],
                                ctypes.c_int),
+    "bg_packed_prefill_attn_fp8": ([_P, _F32, _P, _F32, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32, _F32, _P, _P, _P,
+                                    _SZ, _P, _P], ctypes.c_int),
     "bg_packed_prefill_attn_noalloc": ([_P, _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32, _F32, _P, _P, _P, _P],
                                        ctypes.c_int),
     "bg_packed_last_token_attn": ([_P, _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32, _F32, _P, _P, _P, _P],
@@ -133,6 +135,30 @@ def bg_packed_prefill_attn(q, k, v, cu_seqlens, max_seqlen: int, out, *, lse=Non
                                        workspace.numel() * workspace.element_size(), _ptr(dev_status),
                                        _stream(stream))
     _check("bg_packed_prefill_attn", st)
+    return out
+
+
+def bg_packed_prefill_attn_fp8(q_codes, q_scale: float, k_codes, k_scale: float, v, cu_seqlens, max_seqlen: int, out,
+                               *, lse=None, scale: Optional[float] = None, workspace=None, dev_status=None,
+                               stream=None):
+    """q_codes uint8 [T,Hq,d] and k_codes uint8 [T,Hkv,d] E4M3 codes (torch.uint8 or
+    torch.float8_e4m3fn CUDA tensors) with their per-tensor scales; v bf16 [T,Hkv,d];
+    cu_seqlens int32 [B+1]; out bf16 [T,Hq,d] (written); lse fp32 [T,Hq] or None; workspace
+    as for bg_packed_prefill_attn.  ``scale`` is the softmax scale of the dequantised
+    values (default 1/sqrt(d))."""
+    T, Hq, d = q_codes.shape
+    Hkv = k_codes.shape[1]
+    B = cu_seqlens.numel() - 1
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    need = bg_packed_prefill_workspace_size(B, T, max_seqlen, Hq, Hkv, d)
+    if workspace is None:
+        raise ValueError(f"workspace of {need} bytes required (the library never allocates)")
+    st = load().bg_packed_prefill_attn_fp8(_ptr(q_codes), float(q_scale), _ptr(k_codes), float(k_scale), _ptr(v),
+                                           _ptr(cu_seqlens), B, T, int(max_seqlen), Hq, Hkv, d, float(scale), _ptr(out),
+                                           _ptr(lse), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                           _ptr(dev_status), _stream(stream))
+    _check("bg_packed_prefill_attn_fp8", st)
     return out
 
 

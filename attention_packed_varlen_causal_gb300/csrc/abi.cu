@@ -59,9 +59,9 @@ bool overlap(const void *a, size_t na, const void *b, size_t nb)
     return x < y + nb && y < x + na;
 }
 
-// bf16 tiled map, 128-byte swizzle, box inner extent 64 elements (128 bytes).
+// Tiled map (bf16 unless `type` says otherwise), 128-byte swizzle, box inner extent 128 bytes.
 bool encode_map(CUtensorMap *m, const void *base, int rank, const uint64_t *dims, const uint64_t *strides_bytes,
-                const uint32_t *box)
+                const uint32_t *box, CUtensorMapDataType type = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16)
 {
     auto fn = encoder();
     if (!fn) return false;
@@ -74,7 +74,7 @@ bool encode_map(CUtensorMap *m, const void *base, int rank, const uint64_t *dims
     }
     for (int i = 0; i < rank - 1; ++i) gstr[i] = strides_bytes[i];
     std::memset(m, 0, sizeof(*m));
-    const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<cuuint32_t>(rank), const_cast<void *>(base),
+    const CUresult r = fn(m, type, static_cast<cuuint32_t>(rank), const_cast<void *>(base),
                           gdim, gstr, bdim, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
@@ -120,7 +120,7 @@ size_t bg_packed_prefill_workspace_size(int32_t num_seqs, int32_t total_tokens, 
 bg_status_t bg::prefill_check_args(const void *q, const void *k, const void *v, const int32_t *cu_seqlens,
                                    int32_t num_seqs, int32_t total_tokens, int32_t max_seqlen, int32_t Hq,
                                    int32_t Hkv, int32_t head_dim, float scale, const void *out, const float *lse,
-                                   const int32_t *dev_status, bool *noop)
+                                   const int32_t *dev_status, bool *noop, int qk_elem_bytes)
 {
     *noop = false;
     if (num_seqs < 0 || total_tokens < 0 || max_seqlen < 0 || Hq <= 0 || Hkv <= 0 || head_dim <= 0)
@@ -136,27 +136,32 @@ bg_status_t bg::prefill_check_args(const void *q, const void *k, const void *v, 
     if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) || !aligned(cu_seqlens, 4) ||
         (lse && !aligned(lse, 4)) || (dev_status && !aligned(dev_status, 4)))
         return BG_ERR_INVALID_ARG;
-    const size_t qbytes = static_cast<size_t>(total_tokens) * Hq * head_dim * 2;
-    const size_t kvbytes = static_cast<size_t>(total_tokens) * Hkv * head_dim * 2;
+    const size_t obytes = static_cast<size_t>(total_tokens) * Hq * head_dim * 2;
+    const size_t qbytes = static_cast<size_t>(total_tokens) * Hq * head_dim * qk_elem_bytes;
+    const size_t kbytes = static_cast<size_t>(total_tokens) * Hkv * head_dim * qk_elem_bytes;
+    const size_t vbytes = static_cast<size_t>(total_tokens) * Hkv * head_dim * 2;
     const size_t lsebytes = lse ? static_cast<size_t>(total_tokens) * Hq * 4 : 0;
-    if (overlap(out, qbytes, q, qbytes) || overlap(out, qbytes, k, kvbytes) || overlap(out, qbytes, v, kvbytes) ||
-        overlap(lse, lsebytes, out, qbytes) || overlap(lse, lsebytes, q, qbytes) ||
-        overlap(lse, lsebytes, k, kvbytes) || overlap(lse, lsebytes, v, kvbytes))
+    if (overlap(out, obytes, q, qbytes) || overlap(out, obytes, k, kbytes) || overlap(out, obytes, v, vbytes) ||
+        overlap(lse, lsebytes, out, obytes) || overlap(lse, lsebytes, q, qbytes) ||
+        overlap(lse, lsebytes, k, kbytes) || overlap(lse, lsebytes, v, vbytes))
         return BG_ERR_INVALID_ARG;
     return BG_OK;
 }
 
-extern "C" {
+namespace {
 
-bg_status_t bg_packed_prefill_attn(const void *q, const void *k, const void *v, const int32_t *cu_seqlens,
-                                   int32_t num_seqs, int32_t total_tokens, int32_t max_seqlen, int32_t Hq,
-                                   int32_t Hkv, int32_t head_dim, float scale, void *out, float *lse, void *workspace,
-                                   size_t workspace_bytes, int32_t *dev_status, cudaStream_t stream)
+// bg_packed_prefill_attn (qk8 false: bf16 Q/K) and bg_packed_prefill_attn_fp8 (qk8 true: E4M3
+// Q/K codes, whose two per-tensor scales the caller has already folded into `scale`).
+bg_status_t prefill_impl(const void *q, const void *k, const void *v, const int32_t *cu_seqlens, int32_t num_seqs,
+                         int32_t total_tokens, int32_t max_seqlen, int32_t Hq, int32_t Hkv, int32_t head_dim,
+                         float scale, void *out, float *lse, void *workspace, size_t workspace_bytes,
+                         int32_t *dev_status, cudaStream_t stream, bool qk8)
 {
     bool noop = false;
     const bg_status_t chk = prefill_check_args(q, k, v, cu_seqlens, num_seqs, total_tokens, max_seqlen, Hq, Hkv,
-                                               head_dim, scale, out, lse, dev_status, &noop);
+                                               head_dim, scale, out, lse, dev_status, &noop, qk8 ? 1 : 2);
     if (chk != BG_OK || noop) return chk;
+    if (qk8 && head_dim != 128) return BG_ERR_UNSUPPORTED;
     if (!workspace || !aligned(workspace, 256)) return BG_ERR_INVALID_ARG;
     if (workspace_bytes < bg_packed_prefill_workspace_size(num_seqs, total_tokens, max_seqlen, Hq, Hkv, head_dim))
         return BG_ERR_INVALID_ARG;
@@ -176,15 +181,23 @@ bg_status_t bg_packed_prefill_attn(const void *q, const void *k, const void *v, 
 
     CUtensorMap tm_q, tm_k, tm_v, tm_o;
     const uint64_t D = static_cast<uint64_t>(head_dim);
+    const uint64_t E = qk8 ? 1 : 2;    // bytes per Q/K element
     const uint64_t dq[3] = {D, static_cast<uint64_t>(Hq), static_cast<uint64_t>(total_tokens)};
     const uint64_t sq[2] = {D * 2, static_cast<uint64_t>(Hq) * D * 2};
+    const uint64_t sq8[2] = {D * E, static_cast<uint64_t>(Hq) * D * E};
     const uint64_t dkv[3] = {D, static_cast<uint64_t>(Hkv), static_cast<uint64_t>(total_tokens)};
     const uint64_t skv[2] = {D * 2, static_cast<uint64_t>(Hkv) * D * 2};
-    // boxes: 64 columns (one 128-byte swizzle span) x one head x the kernel's tile height
+    const uint64_t sk8[2] = {D * E, static_cast<uint64_t>(Hkv) * D * E};
+    // boxes: one 128-byte swizzle span of columns (64 bf16 or 128 E4M3 codes) x one head x the
+    // kernel's tile height
+    const uint32_t qk_cols = static_cast<uint32_t>(128 / E);
     const uint32_t boxq[3] = {64, 1, static_cast<uint32_t>(bg::kRows)};
     const uint32_t boxkv[3] = {64, 1, static_cast<uint32_t>(bg::kKeys)};
-    // the output has the query's shape: whole 128-row tiles leave through the same box
-    if (!encode_map(&tm_q, q, 3, dq, sq, boxq) || !encode_map(&tm_k, k, 3, dkv, skv, boxkv) ||
+    const uint32_t boxq8[3] = {qk_cols, 1, static_cast<uint32_t>(bg::kRows)};
+    const uint32_t boxk8[3] = {qk_cols, 1, static_cast<uint32_t>(bg::kKeys)};
+    const CUtensorMapDataType qk_type = qk8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    // the output has the (bf16) query's shape: whole 128-row tiles leave through the same box
+    if (!encode_map(&tm_q, q, 3, dq, sq8, boxq8, qk_type) || !encode_map(&tm_k, k, 3, dkv, sk8, boxk8, qk_type) ||
         !encode_map(&tm_v, v, 3, dkv, skv, boxkv) || !encode_map(&tm_o, out, 3, dq, sq, boxq))
         return BG_ERR_CUDA;
 
@@ -210,8 +223,38 @@ bg_status_t bg_packed_prefill_attn(const void *q, const void *k, const void *v, 
     p.n_head_groups = Hkv * groups_per_kv;
     p.lse = lse;
     const int grid = static_cast<int>(items_bound < nsm ? items_bound : nsm);
-    if (launch_prefill_attn(head_dim, tm_q, tm_k, tm_v, tm_o, p, grid, stream) != cudaSuccess) return BG_ERR_CUDA;
-    return BG_OK;
+    const cudaError_t e = qk8 ? launch_prefill_attn_fp8(head_dim, tm_q, tm_k, tm_v, tm_o, p, grid, stream)
+                              : launch_prefill_attn(head_dim, tm_q, tm_k, tm_v, tm_o, p, grid, stream);
+    return e == cudaSuccess ? BG_OK : BG_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+bg_status_t bg_packed_prefill_attn(const void *q, const void *k, const void *v, const int32_t *cu_seqlens,
+                                   int32_t num_seqs, int32_t total_tokens, int32_t max_seqlen, int32_t Hq,
+                                   int32_t Hkv, int32_t head_dim, float scale, void *out, float *lse, void *workspace,
+                                   size_t workspace_bytes, int32_t *dev_status, cudaStream_t stream)
+{
+    return prefill_impl(q, k, v, cu_seqlens, num_seqs, total_tokens, max_seqlen, Hq, Hkv, head_dim, scale, out, lse,
+                        workspace, workspace_bytes, dev_status, stream, false);
+}
+
+bg_status_t bg_packed_prefill_attn_fp8(const void *q_codes, float q_scale, const void *k_codes, float k_scale,
+                                       const void *v, const int32_t *cu_seqlens, int32_t num_seqs,
+                                       int32_t total_tokens, int32_t max_seqlen, int32_t Hq, int32_t Hkv,
+                                       int32_t head_dim, float scale, void *out, float *lse, void *workspace,
+                                       size_t workspace_bytes, int32_t *dev_status, cudaStream_t stream)
+{
+    if (!std::isfinite(q_scale) || !(q_scale > 0.f) || !std::isfinite(k_scale) || !(k_scale > 0.f))
+        return BG_ERR_INVALID_ARG;
+    // q . k over the dequantised values = (q_scale * k_scale) * (codes . codes): the tensor
+    // cores multiply the codes, the two scales join the softmax scale
+    const double s = static_cast<double>(scale) * q_scale * k_scale;
+    if (!(s > 0.0) || s > 3.0e38) return BG_ERR_INVALID_ARG;
+    return prefill_impl(q_codes, k_codes, v, cu_seqlens, num_seqs, total_tokens, max_seqlen, Hq, Hkv, head_dim,
+                        static_cast<float>(s), out, lse, workspace, workspace_bytes, dev_status, stream, true);
 }
 
 bg_status_t bg_packed_last_token_attn(const void *q, const void *k, const void *v, const int32_t *cu_seqlens,

@@ -65,8 +65,8 @@ namespace bg {
 
 constexpr int kRows = 128;                 // query rows per tile = TMEM lanes
 constexpr int kKeys = 64;                  // keys per K/V tile
-constexpr int kQBox = 128 * 128;           // 128 rows x 64 bf16 (one 128-byte-swizzled column block)
-constexpr int kKVBox = 64 * 128;           // 64 rows x 64 bf16
+constexpr int kQBox = 128 * 128;           // 128 rows x 128 bytes (one 128-byte-swizzled column block)
+constexpr int kKVBox = 64 * 128;           // 64 rows x 128 bytes
 constexpr float kRescaleLog2 = 8.0f;       // rescale O only if the max grew by more than 2^8
 
 enum class Mode : int { Prefill = 0, Decode = 1 };
@@ -95,15 +95,21 @@ struct AttnParams {
     int32_t n_items_decode;
 };
 
-template <int D, int NH, int NK, int NV, int NS>
+// QK8: Q and K arrive as one-byte E4M3 codes and Q.K^T runs as kind::f8f6f4 (V, P and P.V
+// stay bf16); otherwise every operand is bf16.
+template <int D, int NH, int NK, int NV, int NS, bool QK8 = false>
 struct AttnCfg {
-    static constexpr int NB = D / 64;                       // 128-byte column blocks per row
-    static constexpr int kQBytes = NH * NB * kQBox;         // one Q buffer (NH tiles)
-    static constexpr int kTileBytes = NB * kKVBox;          // one K or V tile
+    static constexpr int NB = D / 64;                       // 128-byte column blocks of a bf16 row (V, O)
+    static constexpr int NBQ = QK8 ? D / 128 : D / 64;      // 128-byte column blocks of a Q or K row
+    static constexpr int kQKElemsPerBlock = QK8 ? 128 : 64; // Q/K elements per column block
+    static constexpr int kQBytes = NH * NBQ * kQBox;        // one Q buffer (NH tiles)
+    static constexpr int kKTileBytes = NBQ * kKVBox;        // one K tile
+    static constexpr int kTileBytes = NB * kKVBox;          // one V tile
     static constexpr int kOffQ = 0;                         // two Q buffers
     static constexpr int kOffK = kOffQ + 2 * kQBytes;
-    static constexpr int kOffV = kOffK + NK * kTileBytes;
+    static constexpr int kOffV = kOffK + NK * kKTileBytes;
     static constexpr int kOffStage = kOffV + NV * kTileBytes;     // 2 KB per softmax warp
+    static_assert(!QK8 || D == 128, "E4M3 Q/K rows are one 128-byte column block (head_dim 128)");
     static constexpr int kStageBytes = 32 * 64;
     static constexpr int kOffBar = kOffStage + 4 * NH * kStageBytes;
     // q_full[2] q_empty[2] mma_final k_full[NK] k_empty[NK] v_full[NV] v_empty[NV] s_full[NH][NS]
@@ -267,14 +273,15 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volati
     return ok != 0;
 }
 
-template <Mode MODE, int D, int NH, int NK, int NV, int NS>
+template <Mode MODE, int D, int NH, int NK, int NV, int NS, bool QK8 = false>
 __global__ void __launch_bounds__(128 * (1 + NH), 1)
     attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_sk,
                 const __grid_constant__ CUtensorMap tm_sv, const __grid_constant__ CUtensorMap tm_o,
                 const AttnParams p)
 {
-    using C = AttnCfg<D, NH, NK, NV, NS>;
+    using C = AttnCfg<D, NH, NK, NV, NS, QK8>;
+    static_assert(!QK8 || MODE == Mode::Prefill, "E4M3 Q/K is a prefill variant");
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte alignment of the shared-window offset (swizzle-128B atoms need it)
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -381,14 +388,14 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
                 if (use > 0 && !warp_wait(&q_empty[qb], (use - 1) & 1, abort_flag)) break;
                 uint8_t *qdst = smem + C::kOffQ + qb * C::kQBytes;
                 if constexpr (MODE == Mode::Prefill) {
-                    mbar_arrive_expect_tx_w(leader, &q_full[qb], NH * C::NB * kQBox);
+                    mbar_arrive_expect_tx_w(leader, &q_full[qb], NH * C::NBQ * kQBox);
                     const int row = w.I.seq_start + w.I.qt * kRows;
 #pragma unroll
                     for (int h = 0; h < NH; ++h)
 #pragma unroll
-                        for (int b = 0; b < C::NB; ++b)
-                            tma_load_3d_w(leader, qdst + (h * C::NB + b) * kQBox, &tm_q, &q_full[qb], b * 64, w.I.head0 + h,
-                                          row, pol_q);
+                        for (int b = 0; b < C::NBQ; ++b)
+                            tma_load_3d_w(leader, qdst + (h * C::NBQ + b) * kQBox, &tm_q, &q_full[qb],
+                                          b * C::kQKElemsPerBlock, w.I.head0 + h, row, pol_q);
                 } else {
                     const uint32_t box = static_cast<uint32_t>(p.BT * p.g * 128);
                     mbar_arrive_expect_tx_w(leader, &q_full[qb], NH * C::NB * box);
@@ -403,13 +410,14 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
             const int st = n_kv % NK;
             const uint32_t use = n_kv / NK;
             if (use > 0 && !warp_wait(&k_empty[st], (use - 1) & 1, abort_flag)) break;
-            uint8_t *kdst = smem + C::kOffK + st * C::kTileBytes;
+            uint8_t *kdst = smem + C::kOffK + st * C::kKTileBytes;
             if (MODE == Mode::Prefill || w.j < w.I.n_prompt) {
                 const int row = w.I.kv_row0 + w.j * kKeys;
-                mbar_arrive_expect_tx_w(leader, &k_full[st], C::kTileBytes);
+                mbar_arrive_expect_tx_w(leader, &k_full[st], C::kKTileBytes);
 #pragma unroll
-                for (int b = 0; b < C::NB; ++b)
-                    tma_load_3d_w(leader, kdst + b * kKVBox, &tm_k, &k_full[st], b * 64, w.I.kh, row, pol_kv);
+                for (int b = 0; b < C::NBQ; ++b)
+                    tma_load_3d_w(leader, kdst + b * kKVBox, &tm_k, &k_full[st], b * C::kQKElemsPerBlock, w.I.kh, row,
+                                  pol_kv);
             } else {
                 // suffix slots 0..t-1 of suf_bpt consecutive beams: rows beam-major
                 const int beam = w.I.r * p.W + w.I.bt0 * p.BT + (w.j - w.I.n_prompt) * p.suf_bpt;
@@ -478,7 +486,7 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
         // path (each costs the issuing loop tens of cycles per step).
         if (lane == 0) {
             const int h = (warp == 1) ? 0 : 1;
-            constexpr uint32_t kIdescQK = idesc_bf16_f32(128, kKeys, 0);
+            constexpr uint32_t kIdescQK = QK8 ? idesc_e4m3_f32(128, kKeys) : idesc_bf16_f32(128, kKeys, 0);
             constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, 1);
             // Base descriptors, built once; an operand at byte offset `off` from a base is the
             // base plus off / 16 (the start-address field, no carry: shared memory < 256 KB).
@@ -498,14 +506,17 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
                 const int st = g % NK;
                 if (!mbar_wait(&k_full[st], (g / NK) & 1, abort_flag)) return false;
                 const uint64_t dqb = dq0 + static_cast<uint64_t>((t.qbuf() * C::kQBytes) >> 4);
-                const uint64_t dks = dk0 + static_cast<uint64_t>((st * C::kTileBytes) >> 4);
+                const uint64_t dks = dk0 + static_cast<uint64_t>((st * C::kKTileBytes) >> 4);
                 // S(h, g%NS) holds P of tile g-NS, read by the P.V this thread issued just before
                 // this QK.  tcgen05.mma operations issued by one thread execute in issue order, so
                 // this QK cannot overwrite P before that P.V has read it: no wait for its completion.
                 tc_fence_after();
-                const uint64_t dqh = dqb + static_cast<uint64_t>((h * C::NB * kQBox) >> 4);
+                const uint64_t dqh = dqb + static_cast<uint64_t>((h * C::NBQ * kQBox) >> 4);
                 static_assert(kQBox == 16384 && kKVBox == 8192, "mma_qk_tile hard-codes the column-block strides");
-                mma_qk_tile<C::NB>(tmem + C::col_s(h, g % NS), dqh, dks, kIdescQK, &s_full[NS * h + g % NS]);
+                if constexpr (QK8)
+                    mma_qk_tile_e4m3(tmem + C::col_s(h, g % NS), dqh, dks, kIdescQK, &s_full[NS * h + g % NS]);
+                else
+                    mma_qk_tile<C::NBQ>(tmem + C::col_s(h, g % NS), dqh, dks, kIdescQK, &s_full[NS * h + g % NS]);
                 // the item's Q buffer is free once its last QK has completed, unless the epilogue
                 // stores the output tile out of it
                 if (t.j == t.I.n_tiles - 1 && !tile_store_via_tma<MODE>(p, t.I, h))

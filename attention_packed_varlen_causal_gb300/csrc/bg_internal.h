@@ -16,12 +16,13 @@ namespace bg {
 struct AttnParams;
 
 // Host checks of bg_packed_prefill_attn's arguments other than the workspace (sizes, shape
-// support, scale, pointers, alignment, aliasing between the tensors).  Returns BG_OK or the
+// support, scale, pointers, alignment, aliasing between the tensors; Q and K elements of
+// `qk_elem_bytes` bytes, V and the output bf16).  Returns BG_OK or the
 // status the entry point returns; *noop is set when the call is a valid no-op.
 bg_status_t prefill_check_args(const void *q, const void *k, const void *v, const int32_t *cu_seqlens,
                                int32_t num_seqs, int32_t total_tokens, int32_t max_seqlen, int32_t Hq,
                                int32_t Hkv, int32_t head_dim, float scale, const void *out, const float *lse,
-                               const int32_t *dev_status, bool *noop);
+                               const int32_t *dev_status, bool *noop, int qk_elem_bytes = 2);
 
 // Prefill: work-list pre-pass + attention kernel.  Maps are built by the
 // caller.  Returns cudaSuccess or the launch error.
@@ -31,6 +32,9 @@ cudaError_t launch_prefill_worklist(const int32_t *cu_seqlens, int32_t num_seqs,
 cudaError_t launch_prefill_attn(int head_dim, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
                                 const CUtensorMap &tm_v, const CUtensorMap &tm_o, const AttnParams &p, int grid,
                                 cudaStream_t stream);
+cudaError_t launch_prefill_attn_fp8(int head_dim, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
+                                    const CUtensorMap &tm_v, const CUtensorMap &tm_o, const AttnParams &p, int grid,
+                                    cudaStream_t stream);
 int prefill_heads_per_cta();
 
 cudaError_t launch_decode_attn(int head_dim, const CUtensorMap &tm_q, const CUtensorMap &tm_k,

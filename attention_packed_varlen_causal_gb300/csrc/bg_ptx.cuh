@@ -395,6 +395,26 @@ __device__ __forceinline__ void mma_qk_tile<2>(uint32_t d_tmem, uint64_t dq, uin
         : "memory");
 }
 
+// The same S = Q K^T over one 128-byte column block of E4M3 codes (head_dim 128): kind::f8f6f4,
+// K = 32 one-byte elements per MMA, so A and B again advance 32 bytes (2 descriptor units) per
+// step and the block takes 4 MMAs; then a commit to `bar`.
+__device__ __forceinline__ void mma_qk_tile_e4m3(uint32_t d_tmem, uint64_t dq, uint64_t dk, uint32_t idesc,
+                                                 uint64_t *bar)
+{
+    asm volatile(
+        "{\n\t.reg .pred pf, pt;\n\t.reg .b64 a1, a2, a3, b1, b2, b3;\n\t"
+        "setp.ne.b32 pf, 0, 0;\n\tsetp.eq.b32 pt, 0, 0;\n\t"
+        "add.s64 a1, %1, 2;\n\tadd.s64 a2, %1, 4;\n\tadd.s64 a3, %1, 6;\n\t"
+        "add.s64 b1, %2, 2;\n\tadd.s64 b2, %2, 4;\n\tadd.s64 b3, %2, 6;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, pf;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], a1, b1, %3, pt;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], a2, b2, %3, pt;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], a3, b3, %3, pt;\n\t"
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%4];\n\t}" ::"r"(d_tmem),
+        "l"(dq), "l"(dk), "r"(idesc), "r"(smem_u32(bar))
+        : "memory");
+}
+
 // O (+)= P V over 64 keys: A = P in TMEM (8 columns per 16 keys), B = V (MN-major,
 // 16 key rows = 2048 bytes = 128 units per step); the first MMA accumulates only
 // if `acc`; then a commit to `bar`.
@@ -488,6 +508,17 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int b_mn_maj
            | (1u << 7)                                 // A format: bf16
            | (1u << 10)                                // B format: bf16
            | (static_cast<uint32_t>(b_mn_major) << 16) // B major-ness
+           | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
+           | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
+}
+
+// Instruction descriptor of tcgen05.mma kind::f8f6f4 with E4M3 A and B (format code 0 in both
+// fields), fp32 D, both operands K-major, M x N tile.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N)
+{
+    return (1u << 4)                                   // D format: f32
+           | (0u << 7)                                 // A format: E4M3
+           | (0u << 10)                                // B format: E4M3
            | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
            | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
 }

@@ -91,20 +91,20 @@ cudaError_t launch_prefill_worklist(const int32_t *cu_seqlens, int32_t num_seqs,
 namespace {
 constexpr int kNH = 2;   // query heads of one kv head per CTA (share every K/V tile)
 
-template <int D, int NK, int NV, int NS>
+template <int D, int NK, int NV, int NS, bool QK8>
 std::atomic<uint64_t> &smem_attr_done()
 {
     static std::atomic<uint64_t> mask{0};
     return mask;
 }
 
-template <int D, int NK, int NV, int NS>
+template <int D, int NK, int NV, int NS, bool QK8 = false>
 cudaError_t launch_one(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
                        const CUtensorMap &tm_o, const AttnParams &p, int grid, cudaStream_t stream)
 {
-    using C = AttnCfg<D, kNH, NK, NV, NS>;
-    auto kern = attn_kernel<Mode::Prefill, D, kNH, NK, NV, NS>;
-    cudaError_t e = ensure_smem_attribute(kern, C::kSmemBytes, smem_attr_done<D, NK, NV, NS>());
+    using C = AttnCfg<D, kNH, NK, NV, NS, QK8>;
+    auto kern = attn_kernel<Mode::Prefill, D, kNH, NK, NV, NS, QK8>;
+    cudaError_t e = ensure_smem_attribute(kern, C::kSmemBytes, smem_attr_done<D, NK, NV, NS, QK8>());
     if (e != cudaSuccess) return e;
     return launch_dependent(kern, dim3(grid), dim3(C::kThreads), C::kSmemBytes, stream, tm_q, tm_k, tm_v, tm_k, tm_v,
                             tm_o, p);   // no suffix maps
@@ -119,6 +119,16 @@ cudaError_t launch_prefill_attn(int head_dim, const CUtensorMap &tm_q, const CUt
 {
     if (head_dim == 128) return launch_one<128, 2, 3, 2>(tm_q, tm_k, tm_v, tm_o, p, grid, stream);
     if (head_dim == 64) return launch_one<64, 4, 4, 3>(tm_q, tm_k, tm_v, tm_o, p, grid, stream);
+    return cudaErrorInvalidValue;
+}
+
+// E4M3 Q and K (one 8 KB K stage and one 16 KB Q tile per 128-byte row block), bf16 V: the
+// smaller K stages leave room for four K and four V stages.
+cudaError_t launch_prefill_attn_fp8(int head_dim, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
+                                    const CUtensorMap &tm_v, const CUtensorMap &tm_o, const AttnParams &p, int grid,
+                                    cudaStream_t stream)
+{
+    if (head_dim == 128) return launch_one<128, 4, 4, 2, true>(tm_q, tm_k, tm_v, tm_o, p, grid, stream);
     return cudaErrorInvalidValue;
 }
 

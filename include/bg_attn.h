@@ -134,6 +134,40 @@ bg_status_t bg_packed_prefill_attn(const void *q, const void *k, const void *v,
                                    int32_t *dev_status, cudaStream_t stream);
 
 /*
+ * Packed variable-length causal GQA prefill attention with FP8 (E4M3) Q and K.
+ * Source: the abstract of the page above counts "selective FP8" among the
+ * engine's mixed-precision choices without saying which matmuls use it; the
+ * reading taken here is that Q and K arrive as E4M3 codes with one scale per
+ * tensor while V, the softmax weights and P.V stay bf16.  The result is the
+ * attention of bg_packed_prefill_attn over the dequantised inputs:
+ *     q[p,h] = q_scale * e4m3(q_codes[p,h]),  k[j,kvh] = k_scale * e4m3(k_codes[j,kvh])
+ *     out[row p, h] = sum_{j<=p} softmax_j(scale * q[p,h] . k[j,kvh]) v[j,kvh]
+ * Q.K^T runs on the tensor cores over the codes (kind::f8f6f4, fp32
+ * accumulation) and the two scales join the softmax scale.
+ *
+ *   q_codes      uint8 E4M3 (OCP E4M3FN) codes [total_tokens, Hq, head_dim]
+ *   q_scale      finite, > 0 (the reading and its tests use powers of two,
+ *                which keep every dequantised value exact in bf16)
+ *   k_codes      uint8 E4M3 codes [total_tokens, Hkv, head_dim]
+ *   k_scale      finite, > 0
+ *   v            bf16 [total_tokens, Hkv, head_dim]
+ *   other arguments, the workspace and the outputs as in bg_packed_prefill_attn
+ *   (bg_packed_prefill_workspace_size gives the workspace size).
+ * NaN codes are not checked: they propagate to the rows they reach.
+ * Errors: as bg_packed_prefill_attn; BG_ERR_INVALID_ARG also for a scale
+ * that is not finite and > 0 or whose product with the others overflows;
+ * BG_ERR_UNSUPPORTED for head_dim != 128.
+ */
+bg_status_t bg_packed_prefill_attn_fp8(const void *q_codes, float q_scale,
+                                       const void *k_codes, float k_scale, const void *v,
+                                       const int32_t *cu_seqlens, int32_t num_seqs,
+                                       int32_t total_tokens, int32_t max_seqlen,
+                                       int32_t Hq, int32_t Hkv, int32_t head_dim, float scale,
+                                       void *out, float *lse,
+                                       void *workspace, size_t workspace_bytes,
+                                       int32_t *dev_status, cudaStream_t stream);
+
+/*
  * Attention of each packed sequence's last valid token only, for the last
  * layer of a Prefill-Only request.  Source: abstract and section 1.1 of the
  * page above (the request is answered from the next-token logits at each
