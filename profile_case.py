@@ -4,6 +4,7 @@
     python profile_case.py beam_long --iters 2
     python profile_case.py beam_long --iters 2 --two-call
     python profile_case.py select_long --iters 2
+    python profile_case.py prefill_only --iters 3 --fp8
 
 Prefill workloads (tiny, prefill_only, skewed) call bg_packed_prefill_attn
 ``iters`` times on one layer of inputs; decode workloads (beam_short,
@@ -19,6 +20,7 @@ timed here: use ncu (or bench.py for timings).
 from __future__ import annotations
 
 import argparse
+import math
 import os
 import sys
 
@@ -40,6 +42,7 @@ def main(argv=None):
     ap.add_argument("workload", choices=sorted(list(wl.PREFILL_CONFIGS) + list(wl.DECODE_CONFIGS) + list(select)))
     ap.add_argument("--iters", type=int, default=3)
     ap.add_argument("--two-call", action="store_true", help="decode: separate reorder and attention calls")
+    ap.add_argument("--fp8", action="store_true", help="prefill: E4M3 Q and K (bg_packed_prefill_attn_fp8)")
     args = ap.parse_args(argv)
     build.build()
     bg.load()
@@ -70,8 +73,18 @@ def main(argv=None):
         cu = torch.from_numpy(cu_np).to(dev)
         ws = torch.empty(bg.bg_packed_prefill_workspace_size(len(lengths), T, max(lengths), cfg.Hq, cfg.Hkv,
                                                              cfg.head_dim), dtype=torch.uint8, device=dev)
-        for _ in range(args.iters):
-            bg.bg_packed_prefill_attn(q, k, v, cu, max(lengths), out, workspace=ws)
+        if args.fp8:
+            # E4M3 codes of q and k with one power-of-two scale each (max |x| / scale <= 448)
+            codes = []
+            for x in (q, k):
+                s8 = 2.0 ** math.ceil(math.log2(float(x.abs().max().float().item()) / 448.0))
+                codes.append(((x.float() / s8).to(torch.float8_e4m3fn).view(torch.uint8), s8))
+            for _ in range(args.iters):
+                bg.bg_packed_prefill_attn_fp8(codes[0][0], codes[0][1], codes[1][0], codes[1][1], v, cu, max(lengths),
+                                              out, workspace=ws)
+        else:
+            for _ in range(args.iters):
+                bg.bg_packed_prefill_attn(q, k, v, cu, max(lengths), out, workspace=ws)
     else:
         cfg = wl.DECODE_CONFIGS[args.workload]
         plen = wl.decode_prompt_lengths(cfg)

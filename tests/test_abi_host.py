@@ -94,6 +94,27 @@ def test_prefill_host_validation(lib, kw, expect):
     assert prefill(lib, **kw) == expect
 
 
+def prefill_fp8(lib, **kw):
+    a = dict(q=FAKE, qs=0.5, k=FAKE * 2, ks=0.25, v=FAKE * 3, cu=FAKE * 4, B=2, T=10, maxlen=8, Hq=4, Hkv=2, d=128,
+             scale=0.125, out=FAKE * 5, lse=None, ws=FAKE * 6, wsb=1 << 20, st=None, stream=None)
+    a.update(kw)
+    return lib.bg_packed_prefill_attn_fp8(a["q"], a["qs"], a["k"], a["ks"], a["v"], a["cu"], a["B"], a["T"],
+                                          a["maxlen"], a["Hq"], a["Hkv"], a["d"], a["scale"], a["out"], a["lse"],
+                                          a["ws"], a["wsb"], a["st"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(q=None), 1), (dict(k=None), 1), (dict(v=None), 1), (dict(ws=None), 1), (dict(wsb=64), 1),
+    (dict(qs=0.0), 1), (dict(ks=-1.0), 1), (dict(qs=float("inf")), 1), (dict(ks=float("nan")), 1),
+    (dict(qs=1e30, ks=1e30), 1),                    # the folded scale overflows
+    (dict(d=64), 2), (dict(d=96), 2), (dict(Hq=6, Hkv=4), 1), (dict(scale=0.0), 1),
+    (dict(out=FAKE * 1 + 64), 1),                   # out overlaps the codes of q
+    (dict(B=0, q=None), 0),
+])
+def test_prefill_fp8_host_validation(lib, kw, expect):
+    assert prefill_fp8(lib, **kw) == expect
+
+
 def last_token(lib, **kw):
     a = dict(q=FAKE, k=FAKE * 2, v=FAKE * 3, cu=FAKE * 4, B=2, T=10, maxlen=8, Hq=4, Hkv=2, d=64, scale=0.125,
              out=FAKE * 5, lse=None, st=None, stream=None)
