@@ -805,7 +805,10 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
                         }
                     }
                     // p = 2^(s * scale * log2e - m), two columns per packed FMA; row sum in four
-                    // independent pair accumulators
+                    // independent pair accumulators.  The sum adds the bf16-rounded p that P.V
+                    // multiplies, so O / l is a weighted mean whose weights sum to one exactly:
+                    // the rounding of a dominant weight (up to 2^8 under the lazy rescale) then
+                    // cancels instead of scaling the whole row by up to 2^-9.
                     float2 rs[4];
 #pragma unroll
                     for (int q = 0; q < 4; ++q) rs[q] = make_float2(0.f, 0.f);
@@ -821,8 +824,8 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
                         for (int i = 0; i < 16; ++i) {
                             const float2 x = ffma2(make_float2(s[32 * c + 2 * i], s[32 * c + 2 * i + 1]), sl2x2, negm);
                             const float2 e = make_float2(ex2(x.x), ex2(x.y));
-                            rs[i & 3] = fadd2(rs[i & 3], e);
                             pk[i] = pack_bf16x2(e.x, e.y);
+                            rs[i & 3] = fadd2(rs[i & 3], unpack_bf16x2(pk[i]));
                         }
                         tmem_st16(tS + 16 * c, pk);   // P (bf16 pairs) over the first 32 columns of S
                     }

@@ -544,4 +544,10 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
+// The two bf16 of a packed pair as exact floats (a bf16 is the top half of a float).
+__device__ __forceinline__ float2 unpack_bf16x2(uint32_t u)
+{
+    return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xFFFF0000u));
+}
+
 }  // namespace bg

@@ -43,7 +43,8 @@ def quantize_bits(bits, chunk=1 << 26):
     amax = float(np.array([mag << 16], dtype=np.uint32).view(np.float32)[0])
     scale = ofp8.tensor_scale(np.array([amax]))
     all_bits = np.arange(65536, dtype=np.uint32)
-    vals = (all_bits << 16).view(np.float32).astype(np.float64)
+    with np.errstate(invalid="ignore"):                 # the NaN patterns map to the NaN code
+        vals = (all_bits << 16).view(np.float32).astype(np.float64)
     table = ofp8.e4m3_encode(vals / scale)
     codes = np.empty(flat.size, dtype=np.uint8)
     for i in range(0, flat.size, chunk):
