@@ -418,6 +418,23 @@ bg_status_t decode_impl(const void *q, const void *prompt_k, const void *prompt_
     p.suf_tx = (head_dim / 64) * 128 * t_suf * bpt;
     p.n_items_decode = static_cast<int32_t>(items);
     const int grid = static_cast<int>(items < nsm ? items : nsm);
+    if (fz && max_prompt_len > 0 && decode_step_fused_fits(head_dim, g, suffix_len)) {
+        // one launch: the attention kernel gathers each beam's suffix through the parent index
+        // as it reads it and writes the step's suffix itself
+        StepParams sp;
+        std::memset(&sp, 0, sizeof(sp));
+        sp.src_k = static_cast<const __nv_bfloat16 *>(fz->src_k);
+        sp.src_v = static_cast<const __nv_bfloat16 *>(fz->src_v);
+        sp.new_k = static_cast<const __nv_bfloat16 *>(fz->new_k);
+        sp.new_v = static_cast<const __nv_bfloat16 *>(fz->new_v);
+        sp.dst_k = static_cast<__nv_bfloat16 *>(const_cast<void *>(suffix_k));
+        sp.dst_v = static_cast<__nv_bfloat16 *>(const_cast<void *>(suffix_v));
+        sp.parent = fz->parent;
+        sp.suffix_max = suffix_max;
+        if (launch_decode_step_fused(head_dim, tm_q, tm_k, tm_v, tm_o, p, sp, grid, stream) != cudaSuccess)
+            return BG_ERR_CUDA;
+        return BG_OK;
+    }
     if (fz) {
         // the step's reorder + append first (it moves nothing at t = 1 and then never reads src)
         const void *sk = fz->src_k ? fz->src_k : suffix_k;
@@ -458,6 +475,15 @@ bg_status_t bg_beam_decode_step(const void *q, const void *prompt_k, const void 
     return decode_impl(q, prompt_k, prompt_v, cu_prompt, total_prompt_tokens, max_prompt_len, dst_suffix_k,
                        dst_suffix_v, suffix_len, suffix_max, R, W, Hq, Hkv, head_dim, scale, out, dev_status, &fz,
                        stream);
+}
+
+int32_t bg_beam_decode_step_launches(int32_t Hq, int32_t Hkv, int32_t head_dim, int32_t suffix_len,
+                                     int32_t max_prompt_len)
+{
+    if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || !supported_head_dim(head_dim) || Hq / Hkv > 128 ||
+        suffix_len < 1 || suffix_len > BG_MAX_SUFFIX || max_prompt_len < 0)
+        return 0;
+    return (max_prompt_len > 0 && decode_step_fused_fits(head_dim, Hq / Hkv, suffix_len)) ? 1 : 2;
 }
 
 bg_status_t bg_beam_suffix_reorder(const void *src_k, const void *src_v, void *dst_k, void *dst_v,

@@ -95,9 +95,25 @@ struct AttnParams {
     int32_t n_items_decode;
 };
 
+// Extra operands of the one-launch decode step (attn_kernel<Decode, ..., FUSED = true>): the
+// kernel gathers each beam's suffix through the parent index as it reads it and writes the
+// step's suffix for the next step.  Unused (zero) in every other instantiation.
+struct StepParams {
+    const __nv_bfloat16 *src_k, *src_v;   // previous suffix [R, W, S_max, Hkv, d]; slots 0..t-2 read
+    const __nv_bfloat16 *new_k, *new_v;   // the step's token [R, W, Hkv, d]
+    __nv_bfloat16 *dst_k, *dst_v;         // the step's suffix [R, W, S_max, Hkv, d]; slots 0..t-1 written
+    const int32_t *parent;                // [R, W], each in [0, W)
+    int32_t suffix_max;
+};
+
+// Per-warp suffix staging of the one-launch decode step: the K and V rows (t slots each) of
+// every beam that has a query row in the warp's 32 rows, one beam after the other.
+constexpr int kSufWarpBytes = 8192;
+constexpr int kSufMaxT = 8;                // suffix slots the one-launch step supports
+
 // QK8: Q and K arrive as one-byte E4M3 codes and Q.K^T runs as kind::f8f6f4 (V, P and P.V
 // stay bf16); otherwise every operand is bf16.
-template <int D, int NH, int NK, int NV, int NS, bool QK8 = false>
+template <int D, int NH, int NK, int NV, int NS, bool QK8 = false, bool FUSED = false>
 struct AttnCfg {
     static constexpr int NB = D / 64;                       // 128-byte column blocks of a bf16 row (V, O)
     static constexpr int NBQ = QK8 ? D / 128 : D / 64;      // 128-byte column blocks of a Q or K row
@@ -111,7 +127,9 @@ struct AttnCfg {
     static constexpr int kOffStage = kOffV + NV * kTileBytes;     // 2 KB per softmax warp
     static_assert(!QK8 || D == 128, "E4M3 Q/K rows are one 128-byte column block (head_dim 128)");
     static constexpr int kStageBytes = 32 * 64;
-    static constexpr int kOffBar = kOffStage + 4 * NH * kStageBytes;
+    static constexpr int kOffSuf = kOffStage + 4 * NH * kStageBytes;   // FUSED: kSufWarpBytes per softmax warp
+    static constexpr int kOffBar = kOffSuf + (FUSED ? 4 * NH * kSufWarpBytes : 0);
+    static_assert(!FUSED || D == 64, "the one-launch decode step stages 128-byte suffix rows (head_dim 64)");
     // q_full[2] q_empty[2] mma_final k_full[NK] k_empty[NK] v_full[NV] v_empty[NV] s_full[NH][NS]
     // p_full[NH][NS] pv_done[NH][NS] o_staged[NH][2]
     static constexpr int kNumBars = 5 + 2 * NK + 2 * NV + 3 * NS * NH + 2 * NH;
@@ -154,7 +172,10 @@ __device__ __forceinline__ int4 fetch_raw(const AttnParams &p, int it)
     }
 }
 
-template <Mode MODE, int NH>
+// FUSED (the one-launch decode step): the suffix is attended in the epilogue, not as key
+// tiles, and an item always streams at least one prompt tile (fully masked for an empty
+// prompt) so that its queries are loaded and its epilogue runs.
+template <Mode MODE, int NH, bool FUSED = false>
 __device__ __forceinline__ Item make_item(const AttnParams &p, int it, int4 raw)
 {
     Item I;
@@ -193,7 +214,12 @@ __device__ __forceinline__ Item make_item(const AttnParams &p, int it, int4 raw)
         int nb = p.W - I.bt0 * p.BT;
         if (nb > NH * p.BT) nb = NH * p.BT;
         const int n_suf = (ok && p.suffix_len > 0) ? (nb + p.suf_bpt - 1) / p.suf_bpt : 0;
-        I.n_tiles = I.n_prompt + n_suf;
+        if constexpr (FUSED) {
+            if (ok && I.n_prompt == 0) I.n_prompt = 1;
+            I.n_tiles = I.n_prompt;
+        } else {
+            I.n_tiles = I.n_prompt + n_suf;
+        }
         I.seq_start = 0;
         I.qt = 0;
         I.head0 = 0;
@@ -221,7 +247,7 @@ __device__ __forceinline__ bool tile_store_via_tma(const AttnParams &p, const It
 // Walks the (item, key tile) sequence of one CTA, skipping items without
 // tiles.  Every role walks the same sequence, so all agree on global tile
 // numbers (which pick K/V stages, S buffers and barrier phases).
-template <Mode MODE, int NH>
+template <Mode MODE, int NH, bool FUSED = false>
 struct TileWalker {
     int it, j;           // current item index and tile within it
     int n_items;
@@ -246,7 +272,7 @@ struct TileWalker {
         for (it += gridDim.x; it < n_items; it += gridDim.x) {
             const int4 raw = nxt_raw;
             if (it + static_cast<int>(gridDim.x) < n_items) nxt_raw = fetch_raw<MODE>(p, it + gridDim.x);
-            I = make_item<MODE, NH>(p, it, raw);
+            I = make_item<MODE, NH, FUSED>(p, it, raw);
             if (I.valid && I.n_tiles > 0) {
                 j = 0;
                 valid = true;
@@ -273,15 +299,16 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volati
     return ok != 0;
 }
 
-template <Mode MODE, int D, int NH, int NK, int NV, int NS, bool QK8 = false>
+template <Mode MODE, int D, int NH, int NK, int NV, int NS, bool QK8 = false, bool FUSED = false>
 __global__ void __launch_bounds__(128 * (1 + NH), 1)
     attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_sk,
                 const __grid_constant__ CUtensorMap tm_sv, const __grid_constant__ CUtensorMap tm_o,
-                const AttnParams p)
+                const AttnParams p, const StepParams sp)
 {
-    using C = AttnCfg<D, NH, NK, NV, NS, QK8>;
+    using C = AttnCfg<D, NH, NK, NV, NS, QK8, FUSED>;
     static_assert(!QK8 || MODE == Mode::Prefill, "E4M3 Q/K is a prefill variant");
+    static_assert(!FUSED || MODE == Mode::Decode, "the one-launch step is a decode variant");
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte alignment of the shared-window offset (swizzle-128B atoms need it)
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -341,7 +368,7 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
         // <= 64 rows; the rows past them keep what an earlier tile left (finite) or these
         // zeros, so the masked columns they feed multiply finite values only.
         uint4 *z4 = reinterpret_cast<uint4 *>(smem + C::kOffQ);
-        for (int i = threadIdx.x; i < C::kOffStage / 16; i += blockDim.x) z4[i] = make_uint4(0, 0, 0, 0);
+        for (int i = threadIdx.x; i < C::kOffBar / 16; i += blockDim.x) z4[i] = make_uint4(0, 0, 0, 0);
         fence_proxy_async_smem();
     }
     if (warp == 1) {
@@ -378,7 +405,7 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
         const uint32_t leader = (lane == 0) ? 1u : 0u;
         const uint64_t pol_q = l2_policy_evict_first();
         const uint64_t pol_kv = l2_policy_evict_last();
-        TileWalker<MODE, NH> w;
+        TileWalker<MODE, NH, FUSED> w;
         w.first(p, n_items);
         uint32_t n_kv = 0;                 // K/V tiles issued (global tile number)
         while (w.valid) {
@@ -446,7 +473,7 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
         const uint32_t leader = (lane == 0) ? 1u : 0u;
         const uint64_t pol_kv = l2_policy_evict_last();
         const uint64_t pol_q = l2_policy_evict_first();
-        TileWalker<MODE, NH> w;
+        TileWalker<MODE, NH, FUSED> w;
         w.first(p, n_items);
         uint32_t n_v = 0;
         while (w.valid) {
@@ -495,13 +522,13 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
             const uint64_t dv0 = sdesc_sw128(smem_u32(smem + C::kOffV), kKVBox, 1024);
             // `b` walks the tiles whose S is computed next, `a` (one behind) the tiles whose
             // P.V is accumulated next.
-            TileWalker<MODE, NH> b, a;
+            TileWalker<MODE, NH, FUSED> b, a;
             b.first(p, n_items);
             a = b;
             uint32_t gb = 0, ga = 0;           // global tile numbers of b and a
             bool ok = true;
 
-            auto issue_qk = [&](const TileWalker<MODE, NH> &t, uint32_t g) -> bool {
+            auto issue_qk = [&](const TileWalker<MODE, NH, FUSED> &t, uint32_t g) -> bool {
                 if (t.j == 0 && !mbar_wait(&q_full[t.qbuf()], t.quse() & 1, abort_flag)) return false;
                 const int st = g % NK;
                 if (!mbar_wait(&k_full[st], (g / NK) & 1, abort_flag)) return false;
@@ -519,7 +546,7 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
                     mma_qk_tile<C::NBQ>(tmem + C::col_s(h, g % NS), dqh, dks, kIdescQK, &s_full[NS * h + g % NS]);
                 // the item's Q buffer is free once its last QK has completed, unless the epilogue
                 // stores the output tile out of it
-                if (t.j == t.I.n_tiles - 1 && !tile_store_via_tma<MODE>(p, t.I, h))
+                if (!FUSED && t.j == t.I.n_tiles - 1 && !tile_store_via_tma<MODE>(p, t.I, h))
                     mma_commit(&q_empty[t.qbuf()]);
                 return true;
             };
@@ -578,8 +605,56 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
         // as the Q load), and one thread issues the tile stores and, once the TMA unit has read the
         // buffer, hands it back to the Q producer.  The warps do not wait for the global writes.
         // Other tiles, and every prefill tile, are stored row by row through the staging area.
-        uint32_t n_tma = 0;   // output tiles this warpgroup stored through the TMA unit so far
-        auto epilogue = [&](const Item &I, float m, float l, uint32_t g_last, int qbi, bool via_tma,
+        uint32_t n_tma = 0;   // epilogues of this warpgroup that used o_staged so far
+        // One-launch decode step (FUSED).  Each softmax warp stages, in its own area, the t K and
+        // V rows (kv head of the item) of every beam with a query row among its 32 rows: slots
+        // 0..t-2 from the parent's suffix in the previous step's buffer, slot t-1 from the step's
+        // new token (gather on read: no separate reorder pass).  The epilogue attends each row
+        // over its beam's staged rows on the CUDA cores, merges that into the prompt part of the
+        // online softmax, and writes the step's suffix of the beams whose first row is in the warp.
+        uint8_t *suf_area = smem + C::kOffSuf + (warp - 4) * kSufWarpBytes;
+        const int lb_first = FUSED ? (quad * 32) / p.g : 0;                       // first beam staged
+        const int suf_nb = FUSED ? min((quad * 32 + 31) / p.g, p.BT - 1) - lb_first + 1 : 0;
+        const int suf_stride = FUSED ? p.suffix_len * 256 + 16 : 0;   // bytes per beam (+16: bank spread)
+        // Issues the staging copies of item I (cp.async, completed by the epilogue's wait).  Lane i
+        // holds in `par` the parent of the warp's i-th beam.  Returns the mask of the warp's beams
+        // whose parent is out of range: their history rows are zero-filled, their suffix is not
+        // written, and BG_DEVSTAT_PARENT is raised.
+        auto issue_suffix = [&](const Item &I, int par) -> uint32_t {
+            const int t = p.suffix_len;
+            const int tile_beam0 = (I.bt0 + h) * p.BT;
+            const int64_t req_beam0 = static_cast<int64_t>(I.r) * p.W;
+            const bool lane_beam = lane < suf_nb && lb_first + lane < p.BT && tile_beam0 + lb_first + lane < p.W;
+            const bool badp = t > 1 && lane_beam && (par < 0 || par >= p.W);
+            const uint32_t bad = __ballot_sync(0xffffffffu, badp);
+            if (badp && p.dev_status) atomicOr(p.dev_status, BG_DEVSTAT_PARENT);
+            const int per_beam = t * 16;                 // 16-byte chunks of a beam's K and V rows
+            const int chunks = suf_nb * per_beam;
+            for (int base = 0; base < chunks; base += 32) {
+                const int q = base + lane;
+                const int bi = q / per_beam;
+                const int pb = __shfl_sync(0xffffffffu, par, bi & 31);
+                const int lb = lb_first + bi;
+                const int beam = tile_beam0 + lb;
+                if (q >= chunks || lb >= p.BT || beam >= p.W) continue;
+                const int rem = q - bi * per_beam;
+                const int kv = rem / (t * 8);
+                const int sl = (rem - kv * t * 8) >> 3;
+                const int c = rem & 7;
+                uint8_t *to = suf_area + bi * suf_stride + kv * t * 128 + sl * 128 + c * 16;
+                if (sl == t - 1) {
+                    cp_async_16(to, (kv ? sp.new_v : sp.new_k) + ((req_beam0 + beam) * p.Hkv + I.kh) * 64 + c * 8);
+                } else if ((bad >> bi) & 1u) {
+                    *reinterpret_cast<uint4 *>(to) = make_uint4(0, 0, 0, 0);
+                } else {
+                    cp_async_16(to, (kv ? sp.src_v : sp.src_k) +
+                                        (((req_beam0 + pb) * sp.suffix_max + sl) * p.Hkv + I.kh) * 64 + c * 8);
+                }
+            }
+            cp_async_commit();
+            return bad;
+        };
+        auto epilogue = [&](const Item &I, float m, float l, uint32_t g_last, int qbi, bool via_tma, uint32_t bad,
                             auto &&release) -> bool {
                 // The commit after the item's last P.V covers every earlier MMA too.  (Items always
                 // have tiles here; the test stays because ptxas allocates the prefill kernel's
@@ -629,20 +704,126 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
                 };
                 // O is read 64 columns at a time, normalised and packed to bf16 pairs (half the
                 // registers), and handed back to the next item's P.V before the stores
-                const float inv_l = 1.f / l;
-                const float2 il = make_float2(inv_l, inv_l);
                 uint32_t pk[D / 2];
+                if constexpr (FUSED) {
+                    // the row's beam's suffix: logits z_s = q . k_s over the staged rows, merged with
+                    // the prompt part (m, l, O) as one more online-softmax step, fp32 throughout
+                    cp_async_wait_all();
+                    __syncwarp();
+                    const int t = p.suffix_len;
+                    const int lb = row / p.g;
+                    const bool rvalid = lb < p.BT && (I.bt0 + h) * p.BT + lb < p.W;
+                    const uint8_t *ak = suf_area + (rvalid ? lb - lb_first : 0) * suf_stride;
+                    const uint8_t *av = ak + t * 128;
+                    const uint8_t *qrow = smem + C::kOffQ + qbi * C::kQBytes + h * C::NB * kQBox + row * 128;
+                    float z[kSufMaxT];
 #pragma unroll
-                for (int c2 = 0; c2 < D / 64; ++c2) {
-                    float o[64];
-                    tmem_ld64(tO + 64 * c2, o);
+                    for (int sl = 0; sl < kSufMaxT; ++sl) z[sl] = 0.f;
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const float2 x = fmul2(make_float2(o[2 * i], o[2 * i + 1]), il);
-                        pk[32 * c2 + i] = pack_bf16x2(x.x, x.y);
+                    for (int c = 0; c < 8; ++c) {
+                        const uint4 qv = *reinterpret_cast<const uint4 *>(qrow + ((c ^ (row & 7)) << 4));
+                        const float2 q0 = unpack_bf16x2(qv.x), q1 = unpack_bf16x2(qv.y);
+                        const float2 q2 = unpack_bf16x2(qv.z), q3 = unpack_bf16x2(qv.w);
+#pragma unroll
+                        for (int sl = 0; sl < kSufMaxT; ++sl) {
+                            if (sl < t) {
+                                const uint4 kq = *reinterpret_cast<const uint4 *>(ak + sl * 128 + c * 16);
+                                float2 a = fmul2(q0, unpack_bf16x2(kq.x));
+                                a = ffma2(q1, unpack_bf16x2(kq.y), a);
+                                a = ffma2(q2, unpack_bf16x2(kq.z), a);
+                                a = ffma2(q3, unpack_bf16x2(kq.w), a);
+                                z[sl] += a.x + a.y;
+                            }
+                        }
+                    }
+                    float mz = -INFINITY;
+#pragma unroll
+                    for (int sl = 0; sl < kSufMaxT; ++sl)
+                        if (sl < t) {
+                            z[sl] *= sl2;
+                            mz = fmaxf(mz, z[sl]);
+                        }
+                    const float m_new = fmaxf(m, mz);
+                    // a prompt part with no valid key (empty prompt) has O = 0 and l = 0
+                    const float alpha = (m == -INFINITY) ? 0.f : ex2(m - m_new);
+                    float lsum = l * alpha;
+                    float ps[kSufMaxT];
+#pragma unroll
+                    for (int sl = 0; sl < kSufMaxT; ++sl) {
+                        ps[sl] = (sl < t) ? ex2(z[sl] - m_new) : 0.f;
+                        lsum += ps[sl];
+                    }
+                    const float inv_l = 1.f / lsum;
+                    const float2 al2 = make_float2(alpha, alpha), il2 = make_float2(inv_l, inv_l);
+                    static_assert(!FUSED || D == 64, "two 32-column chunks");
+#pragma unroll
+                    for (int c2 = 0; c2 < D / 32; ++c2) {
+                        float o[32];
+                        tmem_ld32(tO + 32 * c2, o);
+                        float2 acc[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) acc[i] = fmul2(make_float2(o[2 * i], o[2 * i + 1]), al2);
+#pragma unroll
+                        for (int sl = 0; sl < kSufMaxT; ++sl) {
+                            if (sl < t) {
+                                const float2 pp = make_float2(ps[sl], ps[sl]);
+#pragma unroll
+                                for (int u = 0; u < 4; ++u) {
+                                    const uint4 vv = *reinterpret_cast<const uint4 *>(av + sl * 128 + c2 * 64 + u * 16);
+                                    acc[4 * u] = ffma2(pp, unpack_bf16x2(vv.x), acc[4 * u]);
+                                    acc[4 * u + 1] = ffma2(pp, unpack_bf16x2(vv.y), acc[4 * u + 1]);
+                                    acc[4 * u + 2] = ffma2(pp, unpack_bf16x2(vv.z), acc[4 * u + 2]);
+                                    acc[4 * u + 3] = ffma2(pp, unpack_bf16x2(vv.w), acc[4 * u + 3]);
+                                }
+                            }
+                        }
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const float2 x = fmul2(acc[i], il2);
+                            pk[16 * c2 + i] = pack_bf16x2(x.x, x.y);
+                        }
+                    }
+                } else {
+                    const float inv_l = 1.f / l;
+                    const float2 il = make_float2(inv_l, inv_l);
+#pragma unroll
+                    for (int c2 = 0; c2 < D / 64; ++c2) {
+                        float o[64];
+                        tmem_ld64(tO + 64 * c2, o);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            const float2 x = fmul2(make_float2(o[2 * i], o[2 * i + 1]), il);
+                            pk[32 * c2 + i] = pack_bf16x2(x.x, x.y);
+                        }
                     }
                 }
                 release();
+                if constexpr (FUSED) {
+                    // the step's suffix of the beams whose first query row is in this warp (each
+                    // beam and kv head has exactly one such warp in the grid), from the staged rows
+                    const int t = p.suffix_len;
+                    const int own_lo = (quad * 32 + p.g - 1) / p.g;
+                    const int own_hi = min((quad * 32 + 31) / p.g, p.BT - 1);
+                    const int per_beam = t * 16;
+                    const int chunks = own_hi >= own_lo ? (own_hi - own_lo + 1) * per_beam : 0;
+                    const int tile_beam0 = (I.bt0 + h) * p.BT;
+                    for (int q = lane; q < chunks; q += 32) {
+                        const int lb = own_lo + q / per_beam;
+                        const int beam = tile_beam0 + lb;
+                        const int bi = lb - lb_first;
+                        if (beam >= p.W || ((bad >> bi) & 1u)) continue;
+                        const int rem = q - (lb - own_lo) * per_beam;
+                        const int kv = rem / (t * 8);
+                        const int sl = (rem - kv * t * 8) >> 3;
+                        const int c = rem & 7;
+                        const uint4 val = *reinterpret_cast<const uint4 *>(suf_area + bi * suf_stride + kv * t * 128 +
+                                                                          sl * 128 + c * 16);
+                        __nv_bfloat16 *to = (kv ? sp.dst_v : sp.dst_k) +
+                                            (((static_cast<int64_t>(I.r) * p.W + beam) * sp.suffix_max + sl) * p.Hkv +
+                                             I.kh) * 64 + c * 8;
+                        *reinterpret_cast<uint4 *>(to) = val;
+                    }
+                }
                 const bool leader = quad == 0 && lane == 0;
                 if (MODE == Mode::Decode && via_tma) {
                     // row `row` of column block cb: 16-byte chunk c at (c ^ (row % 8)) in its 128-byte row
@@ -678,6 +859,19 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
                 } else {
 #pragma unroll
                     for (int c = 0; c < D / 32; ++c) put_chunk(c, pk + 16 * c);
+                    if constexpr (FUSED) {
+                        // the epilogue read the item's query rows: the Q buffer goes back to the
+                        // producer once all four warps of the group are past that read
+                        __syncwarp();
+                        uint64_t *staged = &o_staged[2 * h + (n_tma & 1)];
+                        if (lane == 0) mbar_arrive(staged);
+                        const uint32_t staged_parity = (n_tma >> 1) & 1u;
+                        ++n_tma;
+                        if (leader) {
+                            if (!mbar_wait(staged, staged_parity, abort_flag)) return false;
+                            mbar_arrive(&q_empty[qbi]);
+                        }
+                    }
                 }
                 if constexpr (MODE == Mode::Prefill) {
                     if (p.lse) {
@@ -696,10 +890,11 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
         uint32_t gp = 0;
         int nq = 0, qbp = 0;  // items with tiles entered so far (selects the Q buffer, as in TileWalker)
         bool tmap = false;    // the pending item's tile leaves through the TMA unit
+        uint32_t badp = 0;    // FUSED: the pending item's beams with a bad parent
         for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
             const int4 raw = nxt_raw;
             if (it + static_cast<int>(gridDim.x) < n_items) nxt_raw = fetch_raw<MODE>(p, it + gridDim.x);
-            const Item I = make_item<MODE, NH>(p, it, raw);
+            const Item I = make_item<MODE, NH, FUSED>(p, it, raw);
             if (!I.valid) {
                 if constexpr (MODE == Mode::Decode) {
                     if (h == 0 && row == 0 && p.dev_status) {
@@ -714,6 +909,15 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
             if (I.n_tiles == 0) continue;   // not produced by make_item for a valid item; skipped by every role
             ++nq;
             const bool tma_I = tile_store_via_tma<MODE>(p, I, h);
+            // FUSED: the parents of the warp's beams, loaded now and used after the first tile
+            int par_cur = 0;
+            uint32_t bad_cur = 0;
+            if constexpr (FUSED) {
+                const int lb = lb_first + lane;
+                const int beam = (I.bt0 + h) * p.BT + lb;
+                if (p.suffix_len > 1 && lane < suf_nb && lb < p.BT && beam < p.W)
+                    par_cur = sp.parent[static_cast<int64_t>(I.r) * p.W + beam];
+            }
             float m = -INFINITY;   // running max of scaled logits (base-2 units)
             float l = 0.f;         // running sum of exp2(logit - m)
             for (int j = 0; j < I.n_tiles; ++j, ++g) {
@@ -805,10 +1009,7 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
                         }
                     }
                     // p = 2^(s * scale * log2e - m), two columns per packed FMA; row sum in four
-                    // independent pair accumulators.  The sum adds the bf16-rounded p that P.V
-                    // multiplies, so O / l is a weighted mean whose weights sum to one exactly:
-                    // the rounding of a dominant weight (up to 2^8 under the lazy rescale) then
-                    // cancels instead of scaling the whole row by up to 2^-9.
+                    // independent pair accumulators.
                     float2 rs[4];
 #pragma unroll
                     for (int q = 0; q < 4; ++q) rs[q] = make_float2(0.f, 0.f);
@@ -817,6 +1018,13 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
                     // a prefill row always has key 0 in its first tile
                     const float mu = (MODE == Mode::Decode && m == -INFINITY) ? 0.f : m;
                     const float2 negm = make_float2(-mu, -mu);
+                    // P.V multiplies the bf16-rounded weights.  The row's largest weight is the
+                    // largest of its tile, and under the lazy rescale it can be anything up to 2^8,
+                    // so its rounding (up to 2^-9 of it) would scale the whole output row; the sum
+                    // takes that weight rounded as P.V sees it, which makes the dominant term of
+                    // O / l exact.  The other weights' roundings are smaller and partly cancel.
+                    const float pmax = ex2(ffma2(make_float2(mx, mx), sl2x2, negm).x);
+                    const float pmax_fix = __uint_as_float(pack_bf16x2(pmax, 0.f) << 16) - pmax;
 #pragma unroll
                     for (int c = 0; c < kKeys / 32; ++c) {
                         uint32_t pk[16];
@@ -824,19 +1032,19 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
                         for (int i = 0; i < 16; ++i) {
                             const float2 x = ffma2(make_float2(s[32 * c + 2 * i], s[32 * c + 2 * i + 1]), sl2x2, negm);
                             const float2 e = make_float2(ex2(x.x), ex2(x.y));
+                            rs[i & 3] = fadd2(rs[i & 3], e);
                             pk[i] = pack_bf16x2(e.x, e.y);
-                            rs[i & 3] = fadd2(rs[i & 3], unpack_bf16x2(pk[i]));
                         }
                         tmem_st16(tS + 16 * c, pk);   // P (bf16 pairs) over the first 32 columns of S
                     }
                     const float2 r01 = fadd2(rs[0], rs[1]), r23 = fadd2(rs[2], rs[3]);
-                    l += (r01.x + r23.x) + (r01.y + r23.y);
+                    l += ((r01.x + r23.x) + (r01.y + r23.y)) + pmax_fix;
                 }
                 tmem_st_wait();
                 tc_fence_before();
                 if (j == 0 && pend) {
                     // the previous item's O is read before this tile's P.V may overwrite it
-                    if (!epilogue(Ip, mp, lp, gp, qbp, tmap, [&]() {
+                    if (!epilogue(Ip, mp, lp, gp, qbp, tmap, badp, [&]() {
                             tc_fence_before();
                             mbar_arrive(&p_full[NS * h + g % NS]);
                         })) {
@@ -847,6 +1055,10 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
                 } else {
                     mbar_arrive(&p_full[NS * h + g % NS]);
                 }
+                // the staging area is free once the previous item's epilogue has run
+                if constexpr (FUSED) {
+                    if (j == 0) bad_cur = issue_suffix(I, par_cur);
+                }
             }
             if (!ok) break;
             pend = true;
@@ -856,10 +1068,13 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
             mp = m;
             lp = l;
             gp = g - 1;
+            badp = bad_cur;
         }
-        if (ok && pend) ok = epilogue(Ip, mp, lp, gp, qbp, tmap, []() {});
-        // every tile store this thread issued has written global memory before the CTA exits
+        if (ok && pend) ok = epilogue(Ip, mp, lp, gp, qbp, tmap, badp, []() {});
+        // every tile store this thread issued has written global memory before the CTA exits, and
+        // no staging copy is still in flight (a time-out may have skipped an epilogue's wait)
         if (quad == 0 && lane == 0) bulk_wait_all();
+        if constexpr (FUSED) cp_async_wait_all();
 
         (void)ok;
     }

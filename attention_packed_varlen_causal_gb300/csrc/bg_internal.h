@@ -14,6 +14,7 @@
 namespace bg {
 
 struct AttnParams;
+struct StepParams;
 
 // Host checks of bg_packed_prefill_attn's arguments other than the workspace (sizes, shape
 // support, scale, pointers, alignment, aliasing between the tensors; Q and K elements of
@@ -41,6 +42,13 @@ cudaError_t launch_decode_attn(int head_dim, const CUtensorMap &tm_q, const CUte
                                const CUtensorMap &tm_v, const CUtensorMap &tm_sk, const CUtensorMap &tm_sv,
                                const CUtensorMap &tm_o, const AttnParams &p, int grid, cudaStream_t stream);
 int decode_tiles_per_cta();
+// The one-launch decode step (suffix gathered through the parent index, attended in the
+// epilogue, the step's suffix written by the same kernel): whether its per-warp staging holds
+// the suffix of this shape, and its launch.
+bool decode_step_fused_fits(int head_dim, int g, int suffix_len);
+cudaError_t launch_decode_step_fused(int head_dim, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
+                                     const CUtensorMap &tm_v, const CUtensorMap &tm_o, const AttnParams &p,
+                                     const StepParams &sp, int grid, cudaStream_t stream);
 
 // Attention of each sequence's last valid token (one CTA per sequence and kv head).
 cudaError_t launch_last_token_attn(int head_dim, const void *q, const void *k, const void *v, const int32_t *cu,

@@ -124,6 +124,23 @@ __device__ __forceinline__ float ex2(float x)
     return y;
 }
 
+// ------------------------------------------------------------------ cp.async (16-byte, L2 only)
+// Asynchronous global -> shared copy of 16 bytes (both addresses 16-byte aligned); the data is
+// in shared memory once this thread's cp_async_wait_all returns.  A generic-proxy write: threads
+// that read it with ordinary loads need only the wait and a barrier among themselves.
+__device__ __forceinline__ void cp_async_16(void *smem_dst, const void *gmem_src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gmem_src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit()
+{
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all()
+{
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map)
 {

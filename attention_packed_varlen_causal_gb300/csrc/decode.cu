@@ -6,7 +6,9 @@
 // queries of all beams x group heads of one kv head form 128-row tiles that
 // run on the tensor cores against the prompt K/V, read once per tile pair
 // (and from L2 for the sibling tiles).  The few suffix keys of each beam
-// follow as extra key tiles of the same item (see attn_kernel<Decode>).
+// follow as extra key tiles of the same item (see attn_kernel<Decode>), or,
+// in the one-launch decode step, are gathered through the parent index and
+// attended on the CUDA cores in the epilogue (attn_kernel<Decode, FUSED>).
 #include "bg_attn_kernel.cuh"
 #include "bg_internal.h"
 
@@ -17,24 +19,24 @@ namespace bg {
 namespace {
 constexpr int kNH = 2;   // query tiles (of the same request and kv head) per CTA
 
-template <int D, int NK, int NV, int NS>
+template <int D, int NK, int NV, int NS, bool FUSED>
 std::atomic<uint64_t> &smem_attr_done()
 {
     static std::atomic<uint64_t> mask{0};
     return mask;
 }
 
-template <int D, int NK, int NV, int NS>
+template <int D, int NK, int NV, int NS, bool FUSED = false>
 cudaError_t launch_one(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
                        const CUtensorMap &tm_sk, const CUtensorMap &tm_sv, const CUtensorMap &tm_o,
-                       const AttnParams &p, int grid, cudaStream_t stream)
+                       const AttnParams &p, const StepParams &sp, int grid, cudaStream_t stream)
 {
-    using C = AttnCfg<D, kNH, NK, NV, NS>;
-    auto kern = attn_kernel<Mode::Decode, D, kNH, NK, NV, NS>;
-    cudaError_t e = ensure_smem_attribute(kern, C::kSmemBytes, smem_attr_done<D, NK, NV, NS>());
+    using C = AttnCfg<D, kNH, NK, NV, NS, false, FUSED>;
+    auto kern = attn_kernel<Mode::Decode, D, kNH, NK, NV, NS, false, FUSED>;
+    cudaError_t e = ensure_smem_attribute(kern, C::kSmemBytes, smem_attr_done<D, NK, NV, NS, FUSED>());
     if (e != cudaSuccess) return e;
     return launch_dependent(kern, dim3(grid), dim3(C::kThreads), C::kSmemBytes, stream, tm_q, tm_k, tm_v, tm_sk,
-                            tm_sv, tm_o, p);
+                            tm_sv, tm_o, p, sp);
 }
 }  // namespace
 
@@ -44,8 +46,30 @@ cudaError_t launch_decode_attn(int head_dim, const CUtensorMap &tm_q, const CUte
                                const CUtensorMap &tm_v, const CUtensorMap &tm_sk, const CUtensorMap &tm_sv,
                                const CUtensorMap &tm_o, const AttnParams &p, int grid, cudaStream_t stream)
 {
-    if (head_dim == 64) return launch_one<64, 4, 4, 3>(tm_q, tm_k, tm_v, tm_sk, tm_sv, tm_o, p, grid, stream);
-    if (head_dim == 128) return launch_one<128, 3, 2, 2>(tm_q, tm_k, tm_v, tm_sk, tm_sv, tm_o, p, grid, stream);
+    const StepParams none = {};
+    if (head_dim == 64) return launch_one<64, 4, 4, 3>(tm_q, tm_k, tm_v, tm_sk, tm_sv, tm_o, p, none, grid, stream);
+    if (head_dim == 128) return launch_one<128, 3, 2, 2>(tm_q, tm_k, tm_v, tm_sk, tm_sv, tm_o, p, none, grid, stream);
+    return cudaErrorInvalidValue;
+}
+
+bool decode_step_fused_fits(int head_dim, int g, int suffix_len)
+{
+    if (head_dim != 64 || g < 1 || g > 128 || suffix_len < 1 || suffix_len > kSufMaxT) return false;
+    const int BT = 128 / g;
+    const int stride = suffix_len * 256 + 16;
+    for (int quad = 0; quad < 4; ++quad) {
+        const int first = (quad * 32) / g;
+        const int last = ((quad * 32 + 31) / g) < BT - 1 ? (quad * 32 + 31) / g : BT - 1;
+        if ((last - first + 1) * stride > kSufWarpBytes) return false;
+    }
+    return true;
+}
+
+cudaError_t launch_decode_step_fused(int head_dim, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
+                                     const CUtensorMap &tm_v, const CUtensorMap &tm_o, const AttnParams &p,
+                                     const StepParams &sp, int grid, cudaStream_t stream)
+{
+    if (head_dim == 64) return launch_one<64, 4, 4, 3, true>(tm_q, tm_k, tm_v, tm_q, tm_q, tm_o, p, sp, grid, stream);
     return cudaErrorInvalidValue;
 }
 
