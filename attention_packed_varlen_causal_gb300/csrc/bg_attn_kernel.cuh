@@ -109,7 +109,7 @@ struct StepParams {
 // Per-warp suffix staging of the one-launch decode step: the K and V rows (t slots each) of
 // every beam that has a query row in the warp's 32 rows, one beam after the other.
 constexpr int kSufWarpBytes = 8192;
-constexpr int kSufMaxT = 8;                // suffix slots the one-launch step supports
+constexpr int kSufMaxT = BG_MAX_SUFFIX;    // suffix slots the one-launch step supports
 
 // QK8: Q and K arrive as one-byte E4M3 codes and Q.K^T runs as kind::f8f6f4 (V, P and P.V
 // stay bf16); otherwise every operand is bf16.
@@ -706,8 +706,11 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
                 // registers), and handed back to the next item's P.V before the stores
                 uint32_t pk[D / 2];
                 if constexpr (FUSED) {
-                    // the row's beam's suffix: logits z_s = q . k_s over the staged rows, merged with
-                    // the prompt part (m, l, O) as one more online-softmax step, fp32 throughout
+                    // the row's beam's suffix, one slot at a time as further online-softmax steps
+                    // over the staged rows, O in registers, fp32 throughout.  A runtime loop over the
+                    // slots keeps the code small: this epilogue is inlined at two call sites, and an
+                    // unrolled version's size made instruction fetch the kernel's bottleneck.
+                    static_assert(!FUSED || D == 64, "two 32-column chunks");
                     cp_async_wait_all();
                     __syncwarp();
                     const int t = p.suffix_len;
@@ -716,72 +719,57 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
                     const uint8_t *ak = suf_area + (rvalid ? lb - lb_first : 0) * suf_stride;
                     const uint8_t *av = ak + t * 128;
                     const uint8_t *qrow = smem + C::kOffQ + qbi * C::kQBytes + h * C::NB * kQBox + row * 128;
-                    float z[kSufMaxT];
-#pragma unroll
-                    for (int sl = 0; sl < kSufMaxT; ++sl) z[sl] = 0.f;
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        const uint4 qv = *reinterpret_cast<const uint4 *>(qrow + ((c ^ (row & 7)) << 4));
-                        const float2 q0 = unpack_bf16x2(qv.x), q1 = unpack_bf16x2(qv.y);
-                        const float2 q2 = unpack_bf16x2(qv.z), q3 = unpack_bf16x2(qv.w);
-#pragma unroll
-                        for (int sl = 0; sl < kSufMaxT; ++sl) {
-                            if (sl < t) {
-                                const uint4 kq = *reinterpret_cast<const uint4 *>(ak + sl * 128 + c * 16);
-                                float2 a = fmul2(q0, unpack_bf16x2(kq.x));
-                                a = ffma2(q1, unpack_bf16x2(kq.y), a);
-                                a = ffma2(q2, unpack_bf16x2(kq.z), a);
-                                a = ffma2(q3, unpack_bf16x2(kq.w), a);
-                                z[sl] += a.x + a.y;
-                            }
-                        }
-                    }
-                    float mz = -INFINITY;
-#pragma unroll
-                    for (int sl = 0; sl < kSufMaxT; ++sl)
-                        if (sl < t) {
-                            z[sl] *= sl2;
-                            mz = fmaxf(mz, z[sl]);
-                        }
-                    const float m_new = fmaxf(m, mz);
-                    // a prompt part with no valid key (empty prompt) has O = 0 and l = 0
-                    const float alpha = (m == -INFINITY) ? 0.f : ex2(m - m_new);
-                    float lsum = l * alpha;
-                    float ps[kSufMaxT];
-#pragma unroll
-                    for (int sl = 0; sl < kSufMaxT; ++sl) {
-                        ps[sl] = (sl < t) ? ex2(z[sl] - m_new) : 0.f;
-                        lsum += ps[sl];
-                    }
-                    const float inv_l = 1.f / lsum;
-                    const float2 al2 = make_float2(alpha, alpha), il2 = make_float2(inv_l, inv_l);
-                    static_assert(!FUSED || D == 64, "two 32-column chunks");
-#pragma unroll
-                    for (int c2 = 0; c2 < D / 32; ++c2) {
+                    float2 o2[32];
+                    {
                         float o[32];
-                        tmem_ld32(tO + 32 * c2, o);
-                        float2 acc[16];
+                        tmem_ld32(tO, o);
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) acc[i] = fmul2(make_float2(o[2 * i], o[2 * i + 1]), al2);
+                        for (int i = 0; i < 16; ++i) o2[i] = make_float2(o[2 * i], o[2 * i + 1]);
+                        tmem_ld32(tO + 32, o);
 #pragma unroll
-                        for (int sl = 0; sl < kSufMaxT; ++sl) {
-                            if (sl < t) {
-                                const float2 pp = make_float2(ps[sl], ps[sl]);
+                        for (int i = 0; i < 16; ++i) o2[16 + i] = make_float2(o[2 * i], o[2 * i + 1]);
+                    }
+                    float mr = m, lr = l;   // a prompt part with no valid key has m = -inf, O = 0, l = 0
+#pragma unroll 1
+                    for (int sl = 0; sl < t; ++sl) {
+                        float2 a = make_float2(0.f, 0.f);
 #pragma unroll
-                                for (int u = 0; u < 4; ++u) {
-                                    const uint4 vv = *reinterpret_cast<const uint4 *>(av + sl * 128 + c2 * 64 + u * 16);
-                                    acc[4 * u] = ffma2(pp, unpack_bf16x2(vv.x), acc[4 * u]);
-                                    acc[4 * u + 1] = ffma2(pp, unpack_bf16x2(vv.y), acc[4 * u + 1]);
-                                    acc[4 * u + 2] = ffma2(pp, unpack_bf16x2(vv.z), acc[4 * u + 2]);
-                                    acc[4 * u + 3] = ffma2(pp, unpack_bf16x2(vv.w), acc[4 * u + 3]);
-                                }
-                            }
+                        for (int c = 0; c < 8; ++c) {
+                            const uint4 qv = *reinterpret_cast<const uint4 *>(qrow + ((c ^ (row & 7)) << 4));
+                            const uint4 kq = *reinterpret_cast<const uint4 *>(ak + sl * 128 + c * 16);
+                            a = ffma2(unpack_bf16x2(qv.x), unpack_bf16x2(kq.x), a);
+                            a = ffma2(unpack_bf16x2(qv.y), unpack_bf16x2(kq.y), a);
+                            a = ffma2(unpack_bf16x2(qv.z), unpack_bf16x2(kq.z), a);
+                            a = ffma2(unpack_bf16x2(qv.w), unpack_bf16x2(kq.w), a);
                         }
+                        const float z = (a.x + a.y) * sl2;
+                        const float mn = fmaxf(mr, z);
+                        if (__any_sync(0xffffffffu, mn > mr)) {
+                            const float al = (mr == -INFINITY) ? 0.f : ex2(mr - mn);
+                            const float2 al2 = make_float2(al, al);
+                            lr *= al;
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            const float2 x = fmul2(acc[i], il2);
-                            pk[16 * c2 + i] = pack_bf16x2(x.x, x.y);
+                            for (int i = 0; i < 32; ++i) o2[i] = fmul2(o2[i], al2);
                         }
+                        mr = mn;
+                        const float pz = ex2(z - mn);
+                        lr += pz;
+                        const float2 pp = make_float2(pz, pz);
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) {
+                            const uint4 vv = *reinterpret_cast<const uint4 *>(av + sl * 128 + u * 16);
+                            o2[4 * u] = ffma2(pp, unpack_bf16x2(vv.x), o2[4 * u]);
+                            o2[4 * u + 1] = ffma2(pp, unpack_bf16x2(vv.y), o2[4 * u + 1]);
+                            o2[4 * u + 2] = ffma2(pp, unpack_bf16x2(vv.z), o2[4 * u + 2]);
+                            o2[4 * u + 3] = ffma2(pp, unpack_bf16x2(vv.w), o2[4 * u + 3]);
+                        }
+                    }
+                    const float inv_l = 1.f / lr;
+                    const float2 il2 = make_float2(inv_l, inv_l);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const float2 x = fmul2(o2[i], il2);
+                        pk[i] = pack_bf16x2(x.x, x.y);
                     }
                 } else {
                     const float inv_l = 1.f / l;
@@ -807,11 +795,12 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
                     const int per_beam = t * 16;
                     const int chunks = own_hi >= own_lo ? (own_hi - own_lo + 1) * per_beam : 0;
                     const int tile_beam0 = (I.bt0 + h) * p.BT;
-                    for (int q = lane; q < chunks; q += 32) {
+                    for (int base = 0; base < chunks; base += 32) {   // same trip count in every lane
+                        const int q = base + lane;
                         const int lb = own_lo + q / per_beam;
                         const int beam = tile_beam0 + lb;
                         const int bi = lb - lb_first;
-                        if (beam >= p.W || ((bad >> bi) & 1u)) continue;
+                        if (q >= chunks || beam >= p.W || ((bad >> bi) & 1u)) continue;
                         const int rem = q - (lb - own_lo) * per_beam;
                         const int kv = rem / (t * 8);
                         const int sl = (rem - kv * t * 8) >> 3;

@@ -267,7 +267,9 @@ class DecodeStack:
             by += b
         self.flops_per_search = fl * layers
         self.bytes_per_search = by * layers
-        self.launches = 2 * S * layers            # reorder + attention per step and layer
+        # kernels per step and layer: 1 for the one-launch step, 2 for reorder + attention
+        self.launches = layers * sum(bg.bg_beam_decode_step_launches(Hq, Hkv, d, t, max(self.plen))
+                                     for t in range(1, S + 1))
 
     def enqueue(self, stream):
         bg = self.bg
@@ -510,9 +512,9 @@ def run_ours(args):
                 "tokens_per_s_definition": f"R*W*steps new tokens per search / time of the search's decode "
                                            f"attention steps through all {layers} layers (attention only)",
                 "us_per_step_definition": "one decode step of one layer (bg_beam_decode_step: suffix reorder + "
-                                          "append, then attention), median over the timed replays of the whole "
+                                          "append and attention), median over the timed replays of the whole "
                                           "search / (steps x layers)",
-                "launches_per_step": dec.launches // n_step}
+                "launches_per_step": round(dec.launches / n_step, 3)}
 
     decode = {"beam_short": dec_report(dec_s, short_ms), "beam_long": dec_report(dec_l, long_ms)}
     tiny = run_tiny(device, stream, args.reps)

@@ -323,10 +323,10 @@ bg_status_t bg_beam_decode_step(const void *q, const void *prompt_k, const void 
 
 /*
  * Number of kernels one bg_beam_decode_step call with these sizes enqueues:
- * 1 where its one-launch form applies -- head_dim 64, suffix_len <= 8, the
- * t suffix rows (K and V) of the beams that own query rows in any 32-row
- * group of a 128-row query tile fit an 8 KB staging area, and
- * max_prompt_len > 0 -- else 2; 0 for sizes the call rejects.  Host-only,
+ * 1 where its one-launch form applies -- head_dim 64, the t suffix rows
+ * (K and V) of the beams that own query rows in any 32-row group of a
+ * 128-row query tile fit an 8 KB staging area (t * 256 + 16 bytes per
+ * beam), and max_prompt_len > 0 -- else 2; 0 for sizes the call rejects.  Host-only,
  * never fails otherwise.
  */
 int32_t bg_beam_decode_step_launches(int32_t Hq, int32_t Hkv, int32_t head_dim,

@@ -263,7 +263,8 @@ def test_noalloc_host_checks_run_in_order_without_a_device():
 
 @pytest.mark.parametrize("args,expect", [
     ((14, 2, 64, 1, 128), 1), ((14, 2, 64, 5, 500), 1), ((14, 2, 64, 6, 500), 2),   # 6 beams x t rows per warp
-    ((14, 2, 128, 1, 128), 2), ((4, 4, 64, 1, 64), 2), ((64, 1, 64, 8, 10), 1), ((64, 1, 64, 9, 10), 2),
+    ((14, 2, 128, 1, 128), 2), ((4, 4, 64, 1, 64), 2), ((64, 1, 64, 16, 10), 1), ((32, 2, 64, 15, 9), 1),
+    ((32, 2, 64, 16, 9), 2),
     ((14, 2, 64, 3, 0), 2),                                                          # no prompt keys anywhere
     ((14, 2, 64, 0, 128), 0), ((14, 3, 64, 1, 128), 0), ((14, 2, 96, 1, 128), 0), ((14, 2, 64, 17, 128), 0),
 ])
