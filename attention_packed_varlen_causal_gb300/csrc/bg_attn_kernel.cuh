@@ -128,7 +128,10 @@ struct AttnCfg {
     static_assert(!QK8 || D == 128, "E4M3 Q/K rows are one 128-byte column block (head_dim 128)");
     static constexpr int kStageBytes = 32 * 64;
     static constexpr int kOffSuf = kOffStage + 4 * NH * kStageBytes;   // FUSED: kSufWarpBytes per softmax warp
-    static constexpr int kOffBar = kOffSuf + (FUSED ? 4 * NH * kSufWarpBytes : 0);
+    // FUSED: per softmax warp 256 bytes: the parents of its beams (32 int32), then the mask of
+    // beams with a bad parent
+    static constexpr int kOffSufPar = kOffSuf + (FUSED ? 4 * NH * kSufWarpBytes : 0);
+    static constexpr int kOffBar = kOffSufPar + (FUSED ? 4 * NH * 256 : 0);
     static_assert(!FUSED || D == 64, "the one-launch decode step stages 128-byte suffix rows (head_dim 64)");
     // q_full[2] q_empty[2] mma_final k_full[NK] k_empty[NK] v_full[NV] v_empty[NV] s_full[NH][NS]
     // p_full[NH][NS] pv_done[NH][NS] o_staged[NH][2]
@@ -612,36 +615,54 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
         // new token (gather on read: no separate reorder pass).  The epilogue attends each row
         // over its beam's staged rows on the CUDA cores, merges that into the prompt part of the
         // online softmax, and writes the step's suffix of the beams whose first row is in the warp.
-        uint8_t *suf_area = smem + C::kOffSuf + (warp - 4) * kSufWarpBytes;
-        const int lb_first = FUSED ? (quad * 32) / p.g : 0;                       // first beam staged
-        const int suf_nb = FUSED ? min((quad * 32 + 31) / p.g, p.BT - 1) - lb_first + 1 : 0;
-        const int suf_stride = FUSED ? p.suffix_len * 256 + 16 : 0;   // bytes per beam (+16: bank spread)
-        // Issues the staging copies of item I (cp.async, completed by the epilogue's wait).  Lane i
-        // holds in `par` the parent of the warp's i-th beam.  Returns the mask of the warp's beams
-        // whose parent is out of range: their history rows are zero-filled, their suffix is not
-        // written, and BG_DEVSTAT_PARENT is raised.
-        auto issue_suffix = [&](const Item &I, int par) -> uint32_t {
+        // (The values below are recomputed where they are used, so that nothing of this stays live
+        // in registers through the softmax loop, which runs at the register limit.)
+        auto suf_area = [&]() { return smem + C::kOffSuf + (warp - 4) * kSufWarpBytes; };
+        auto suf_par = [&]() { return reinterpret_cast<int32_t *>(smem + C::kOffSufPar + (warp - 4) * 256); };
+        auto lb_first = [&]() { return (quad * 32) / p.g; };                                 // first beam staged
+        auto suf_nb = [&]() { return min((quad * 32 + 31) / p.g, p.BT - 1) - lb_first() + 1; };   // beams staged
+        auto suf_stride = [&]() { return p.suffix_len * 256 + 16; };   // bytes per beam (+16: bank spread)
+        // Starts the loads of the parents of item I's beams that have rows in this warp (lane i:
+        // beam i), into the warp's parent slots.
+        auto fetch_parents = [&](const Item &I) {
+            const int lb = lb_first() + lane;
+            const int beam = (I.bt0 + h) * p.BT + lb;
+            if (p.suffix_len > 1 && lane < suf_nb() && lb < p.BT && beam < p.W)
+                cp_async_4(suf_par() + lane, sp.parent + static_cast<int64_t>(I.r) * p.W + beam);
+            cp_async_commit();
+        };
+        // Issues the staging copies of item I (cp.async, completed by the epilogue's wait), once its
+        // parents have arrived.  The beams whose parent is out of range get zero history rows, their
+        // suffix is not written (mask in the warp's slot after the parents), and BG_DEVSTAT_PARENT
+        // is raised.
+        auto issue_suffix = [&](const Item &I) {
+            cp_async_wait_all();
+            __syncwarp();
             const int t = p.suffix_len;
+            const int lbf = lb_first(), nb = suf_nb(), stride = suf_stride();
+            uint8_t *area = suf_area();
+            const int par = (t > 1 && lane < nb) ? suf_par()[lane] : 0;
             const int tile_beam0 = (I.bt0 + h) * p.BT;
             const int64_t req_beam0 = static_cast<int64_t>(I.r) * p.W;
-            const bool lane_beam = lane < suf_nb && lb_first + lane < p.BT && tile_beam0 + lb_first + lane < p.W;
+            const bool lane_beam = lane < nb && lbf + lane < p.BT && tile_beam0 + lbf + lane < p.W;
             const bool badp = t > 1 && lane_beam && (par < 0 || par >= p.W);
             const uint32_t bad = __ballot_sync(0xffffffffu, badp);
             if (badp && p.dev_status) atomicOr(p.dev_status, BG_DEVSTAT_PARENT);
+            if (lane == 0) reinterpret_cast<volatile uint32_t *>(suf_par())[32] = bad;
             const int per_beam = t * 16;                 // 16-byte chunks of a beam's K and V rows
-            const int chunks = suf_nb * per_beam;
+            const int chunks = nb * per_beam;
             for (int base = 0; base < chunks; base += 32) {
                 const int q = base + lane;
                 const int bi = q / per_beam;
                 const int pb = __shfl_sync(0xffffffffu, par, bi & 31);
-                const int lb = lb_first + bi;
+                const int lb = lbf + bi;
                 const int beam = tile_beam0 + lb;
                 if (q >= chunks || lb >= p.BT || beam >= p.W) continue;
                 const int rem = q - bi * per_beam;
                 const int kv = rem / (t * 8);
                 const int sl = (rem - kv * t * 8) >> 3;
                 const int c = rem & 7;
-                uint8_t *to = suf_area + bi * suf_stride + kv * t * 128 + sl * 128 + c * 16;
+                uint8_t *to = area + bi * stride + kv * t * 128 + sl * 128 + c * 16;
                 if (sl == t - 1) {
                     cp_async_16(to, (kv ? sp.new_v : sp.new_k) + ((req_beam0 + beam) * p.Hkv + I.kh) * 64 + c * 8);
                 } else if ((bad >> bi) & 1u) {
@@ -652,9 +673,8 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
                 }
             }
             cp_async_commit();
-            return bad;
         };
-        auto epilogue = [&](const Item &I, float m, float l, uint32_t g_last, int qbi, bool via_tma, uint32_t bad,
+        auto epilogue = [&](const Item &I, float m, float l, uint32_t g_last, int qbi, bool via_tma,
                             auto &&release) -> bool {
                 // The commit after the item's last P.V covers every earlier MMA too.  (Items always
                 // have tiles here; the test stays because ptxas allocates the prefill kernel's
@@ -711,12 +731,10 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
                     // slots keeps the code small: this epilogue is inlined at two call sites, and an
                     // unrolled version's size made instruction fetch the kernel's bottleneck.
                     static_assert(!FUSED || D == 64, "two 32-column chunks");
-                    cp_async_wait_all();
-                    __syncwarp();
                     const int t = p.suffix_len;
                     const int lb = row / p.g;
                     const bool rvalid = lb < p.BT && (I.bt0 + h) * p.BT + lb < p.W;
-                    const uint8_t *ak = suf_area + (rvalid ? lb - lb_first : 0) * suf_stride;
+                    const uint8_t *ak = suf_area() + (rvalid ? lb - lb_first() : 0) * suf_stride();
                     const uint8_t *av = ak + t * 128;
                     const uint8_t *qrow = smem + C::kOffQ + qbi * C::kQBytes + h * C::NB * kQBox + row * 128;
                     float2 o2[32];
@@ -729,6 +747,11 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
 #pragma unroll
                         for (int i = 0; i < 16; ++i) o2[16 + i] = make_float2(o[2 * i], o[2 * i + 1]);
                     }
+                    // O is in registers: the next item's first P.V may overwrite it while the suffix
+                    // is attended below
+                    release();
+                    cp_async_wait_all();
+                    __syncwarp();
                     float mr = m, lr = l;   // a prompt part with no valid key has m = -inf, O = 0, l = 0
 #pragma unroll 1
                     for (int sl = 0; sl < t; ++sl) {
@@ -784,12 +807,15 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
                             pk[32 * c2 + i] = pack_bf16x2(x.x, x.y);
                         }
                     }
+                    release();
                 }
-                release();
                 if constexpr (FUSED) {
                     // the step's suffix of the beams whose first query row is in this warp (each
                     // beam and kv head has exactly one such warp in the grid), from the staged rows
                     const int t = p.suffix_len;
+                    const uint32_t bad = reinterpret_cast<volatile uint32_t *>(suf_par())[32];
+                    const int lbf = lb_first(), stride = suf_stride();
+                    const uint8_t *area = suf_area();
                     const int own_lo = (quad * 32 + p.g - 1) / p.g;
                     const int own_hi = min((quad * 32 + 31) / p.g, p.BT - 1);
                     const int per_beam = t * 16;
@@ -799,14 +825,14 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
                         const int q = base + lane;
                         const int lb = own_lo + q / per_beam;
                         const int beam = tile_beam0 + lb;
-                        const int bi = lb - lb_first;
+                        const int bi = lb - lbf;
                         if (q >= chunks || beam >= p.W || ((bad >> bi) & 1u)) continue;
                         const int rem = q - (lb - own_lo) * per_beam;
                         const int kv = rem / (t * 8);
                         const int sl = (rem - kv * t * 8) >> 3;
                         const int c = rem & 7;
-                        const uint4 val = *reinterpret_cast<const uint4 *>(suf_area + bi * suf_stride + kv * t * 128 +
-                                                                          sl * 128 + c * 16);
+                        const uint4 val = *reinterpret_cast<const uint4 *>(area + bi * stride + kv * t * 128 + sl * 128 +
+                                                                          c * 16);
                         __nv_bfloat16 *to = (kv ? sp.dst_v : sp.dst_k) +
                                             (((static_cast<int64_t>(I.r) * p.W + beam) * sp.suffix_max + sl) * p.Hkv +
                                              I.kh) * 64 + c * 8;
@@ -879,7 +905,6 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
         uint32_t gp = 0;
         int nq = 0, qbp = 0;  // items with tiles entered so far (selects the Q buffer, as in TileWalker)
         bool tmap = false;    // the pending item's tile leaves through the TMA unit
-        uint32_t badp = 0;    // FUSED: the pending item's beams with a bad parent
         for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
             const int4 raw = nxt_raw;
             if (it + static_cast<int>(gridDim.x) < n_items) nxt_raw = fetch_raw<MODE>(p, it + gridDim.x);
@@ -898,14 +923,13 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
             if (I.n_tiles == 0) continue;   // not produced by make_item for a valid item; skipped by every role
             ++nq;
             const bool tma_I = tile_store_via_tma<MODE>(p, I, h);
-            // FUSED: the parents of the warp's beams, loaded now and used after the first tile
-            int par_cur = 0;
-            uint32_t bad_cur = 0;
+            // FUSED: the parents of the warp's beams load now; the staging copies start at once for
+            // the CTA's first item (their latency then overlaps its first Q/K loads), else after the
+            // first tile, once the previous item's epilogue has freed the staging area
+            const bool pend_at_start = pend;
             if constexpr (FUSED) {
-                const int lb = lb_first + lane;
-                const int beam = (I.bt0 + h) * p.BT + lb;
-                if (p.suffix_len > 1 && lane < suf_nb && lb < p.BT && beam < p.W)
-                    par_cur = sp.parent[static_cast<int64_t>(I.r) * p.W + beam];
+                fetch_parents(I);
+                if (!pend) issue_suffix(I);
             }
             float m = -INFINITY;   // running max of scaled logits (base-2 units)
             float l = 0.f;         // running sum of exp2(logit - m)
@@ -1033,7 +1057,7 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
                 tc_fence_before();
                 if (j == 0 && pend) {
                     // the previous item's O is read before this tile's P.V may overwrite it
-                    if (!epilogue(Ip, mp, lp, gp, qbp, tmap, badp, [&]() {
+                    if (!epilogue(Ip, mp, lp, gp, qbp, tmap, [&]() {
                             tc_fence_before();
                             mbar_arrive(&p_full[NS * h + g % NS]);
                         })) {
@@ -1046,7 +1070,7 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
                 }
                 // the staging area is free once the previous item's epilogue has run
                 if constexpr (FUSED) {
-                    if (j == 0) bad_cur = issue_suffix(I, par_cur);
+                    if (j == 0 && pend_at_start) issue_suffix(I);
                 }
             }
             if (!ok) break;
@@ -1057,9 +1081,8 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
             mp = m;
             lp = l;
             gp = g - 1;
-            badp = bad_cur;
         }
-        if (ok && pend) ok = epilogue(Ip, mp, lp, gp, qbp, tmap, badp, []() {});
+        if (ok && pend) ok = epilogue(Ip, mp, lp, gp, qbp, tmap, []() {});
         // every tile store this thread issued has written global memory before the CTA exits, and
         // no staging copy is still in flight (a time-out may have skipped an epilogue's wait)
         if (quad == 0 && lane == 0) bulk_wait_all();

@@ -132,6 +132,11 @@ __device__ __forceinline__ void cp_async_16(void *smem_dst, const void *gmem_src
 {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gmem_src) : "memory");
 }
+// 4-byte variant (through L1; both addresses 4-byte aligned).
+__device__ __forceinline__ void cp_async_4(void *smem_dst, const void *gmem_src)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(smem_dst)), "l"(gmem_src) : "memory");
+}
 __device__ __forceinline__ void cp_async_commit()
 {
     asm volatile("cp.async.commit_group;" ::: "memory");
