@@ -68,6 +68,13 @@ constexpr int kKeys = 64;                  // keys per K/V tile
 constexpr int kQBox = 128 * 128;           // 128 rows x 128 bytes (one 128-byte-swizzled column block)
 constexpr int kKVBox = 64 * 128;           // 64 rows x 128 bytes
 constexpr float kRescaleLog2 = 8.0f;       // rescale O only if the max grew by more than 2^8
+// Registers per thread after the split: the four TMA / MMA warps and the NH = 2 softmax
+// warpgroups (384 threads, at most 168 registers each at launch: 4*32*64 + 8*32*216 = 63,488
+// <= 64,512).
+constexpr int kRegsLaunch = 168;
+constexpr int kRegsLight = 64;
+constexpr int kRegsSoftmax = 216;
+static_assert(4 * 32 * kRegsLight + 8 * 32 * kRegsSoftmax <= 384 * kRegsLaunch, "register split exceeds the launch");
 
 enum class Mode : int { Prefill = 0, Decode = 1 };
 
@@ -312,6 +319,9 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
     using C = AttnCfg<D, NH, NK, NV, NS, QK8, FUSED>;
     static_assert(!QK8 || MODE == Mode::Prefill, "E4M3 Q/K is a prefill variant");
     static_assert(!FUSED || MODE == Mode::Decode, "the one-launch step is a decode variant");
+    // one CTA of 384 threads per SM: the launch bounds give each thread at most 65,536 / 384, i.e.
+    // kRegsLaunch registers, the budget of the register split below
+    static_assert(NH == 2 && 65536 / (128 * (1 + NH)) / 8 * 8 == kRegsLaunch, "register split assumes 384 threads");
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte alignment of the shared-window offset (swizzle-128B atoms need it)
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -401,7 +411,12 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
         n_items = p.n_items_decode;
     }
 
+    // Register split (setmaxnreg, per warp, at the start of each role): the TMA and MMA warps run
+    // with kRegsLight registers and the softmax warps with kRegsSoftmax, where the launch gives
+    // every thread 168.  The total stays within the launch's allocation (checked below), so the
+    // softmax warps' increase is always granted, from the registers the other warps return.
     if (warp == 0) {
+        reg_dealloc<kRegsLight>();
         // =============================================================== producer
         // The whole warp runs the loop (warp-uniform control flow and operands); lane 0
         // issues each copy.
@@ -472,6 +487,7 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
         }
         __syncwarp();
     } else if (warp == 2) {
+        reg_dealloc<kRegsLight>();
         // =============================================================== V producer
         const uint32_t leader = (lane == 0) ? 1u : 0u;
         const uint64_t pol_kv = l2_policy_evict_last();
@@ -508,6 +524,7 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
         }
         __syncwarp();
     } else if (warp == 1 || (NH == 2 && warp == 3)) {
+        reg_dealloc<kRegsLight>();
         // =============================================================== MMA issuers
         // One thread per query tile (lane 0 of warp 1: tile 0, of warp 3: tile 1), so the two
         // tiles' QK -> softmax -> P.V chains do not wait for each other.  The thread waits on
@@ -585,6 +602,7 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
         }
         __syncwarp();
     } else if (warp >= 4) {
+        reg_alloc<kRegsSoftmax>();
         // =============================================================== softmax + epilogue
         const int h = (warp - 4) >> 2;
         const int quad = warp & 3;

@@ -98,6 +98,20 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t *bar, uint32_t parity)
     }
 }
 
+// ------------------------------------------------------------------ register split
+// The calling warp's register allocation becomes N per thread (a multiple of 8): returned to
+// the CTA's pool, or taken from it (waiting until other warps have returned enough).
+template <int N>
+__device__ __forceinline__ void reg_dealloc()
+{
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N) : "memory");
+}
+template <int N>
+__device__ __forceinline__ void reg_alloc()
+{
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N) : "memory");
+}
+
 // ------------------------------------------------------------------ dependent launch
 // Programmatic dependent launch (PTX griddepcontrol).  grid_dep_launch lets the
 // next kernel of the stream, when it was launched with programmatic stream
