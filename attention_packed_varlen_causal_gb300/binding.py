@@ -52,7 +52,6 @@ SIGNATURES = {
     "bg_beam_decode_step": ([_P, _P, _P, _P, _I32, _I32, _P, _P, _P, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _I32,
                              _I32, _I32, _F32, _P, _P, _P], ctypes.c_int),
     "bg_beam_select_workspace_size": ([_I32] * 3, _SZ),
-    "bg_beam_decode_step_launches": ([_I32] * 5, _I32),
     "bg_selftest_wait_timeout": ([_P, _P, _P], ctypes.c_int),
     "bg_beam_select": ([_P, _P, _I32, _I32, _I32, _P, _P, _P, _P, _SZ, _P], ctypes.c_int),
 }
@@ -244,12 +243,6 @@ def bg_beam_decode_step(q, prompt_k, prompt_v, cu_prompt, max_prompt_len: int, s
                                     _ptr(dev_status), _stream(stream))
     _check("bg_beam_decode_step", st)
     return out
-
-
-def bg_beam_decode_step_launches(Hq: int, Hkv: int, head_dim: int, suffix_len: int, max_prompt_len: int) -> int:
-    """Kernels one bg_beam_decode_step call with these sizes enqueues (1: the one-launch form,
-    2: reorder + attention, 0: sizes the call rejects)."""
-    return int(load().bg_beam_decode_step_launches(Hq, Hkv, head_dim, suffix_len, max_prompt_len))
 
 
 def bg_selftest_wait_timeout(dev_status, waited_ns, *, stream=None):

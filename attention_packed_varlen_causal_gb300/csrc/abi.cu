@@ -418,9 +418,9 @@ bg_status_t decode_impl(const void *q, const void *prompt_k, const void *prompt_
     p.suf_tx = (head_dim / 64) * 128 * t_suf * bpt;
     p.n_items_decode = static_cast<int32_t>(items);
     const int grid = static_cast<int>(items < nsm ? items : nsm);
-    if (fz && max_prompt_len > 0 && decode_step_fused_fits(head_dim, g, suffix_len)) {
-        // one launch: the attention kernel gathers each beam's suffix through the parent index
-        // as it reads it and writes the step's suffix itself
+    if (fz) {
+        // one launch: a gatherer warp of the attention kernel builds each suffix key tile from
+        // the previous step's suffix through the parent index and writes the step's suffix
         StepParams sp;
         std::memset(&sp, 0, sizeof(sp));
         sp.src_k = static_cast<const __nv_bfloat16 *>(fz->src_k);
@@ -434,15 +434,6 @@ bg_status_t decode_impl(const void *q, const void *prompt_k, const void *prompt_
         if (launch_decode_step_fused(head_dim, tm_q, tm_k, tm_v, tm_o, p, sp, grid, stream) != cudaSuccess)
             return BG_ERR_CUDA;
         return BG_OK;
-    }
-    if (fz) {
-        // the step's reorder + append first (it moves nothing at t = 1 and then never reads src)
-        const void *sk = fz->src_k ? fz->src_k : suffix_k;
-        const void *sv = fz->src_v ? fz->src_v : suffix_v;
-        if (launch_suffix_reorder(sk, sv, const_cast<void *>(suffix_k), const_cast<void *>(suffix_v), fz->parent,
-                                  fz->new_k, fz->new_v, R, W, suffix_max, suffix_len - 1, Hkv, head_dim, dev_status,
-                                  stream) != cudaSuccess)
-            return BG_ERR_CUDA;
     }
     if (launch_decode_attn(head_dim, tm_q, tm_k, tm_v, tm_sk, tm_sv, tm_o, p, grid, stream) != cudaSuccess)
         return BG_ERR_CUDA;
@@ -475,15 +466,6 @@ bg_status_t bg_beam_decode_step(const void *q, const void *prompt_k, const void 
     return decode_impl(q, prompt_k, prompt_v, cu_prompt, total_prompt_tokens, max_prompt_len, dst_suffix_k,
                        dst_suffix_v, suffix_len, suffix_max, R, W, Hq, Hkv, head_dim, scale, out, dev_status, &fz,
                        stream);
-}
-
-int32_t bg_beam_decode_step_launches(int32_t Hq, int32_t Hkv, int32_t head_dim, int32_t suffix_len,
-                                     int32_t max_prompt_len)
-{
-    if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || !supported_head_dim(head_dim) || Hq / Hkv > 128 ||
-        suffix_len < 1 || suffix_len > BG_MAX_SUFFIX || max_prompt_len < 0)
-        return 0;
-    return (max_prompt_len > 0 && decode_step_fused_fits(head_dim, Hq / Hkv, suffix_len)) ? 1 : 2;
 }
 
 bg_status_t bg_beam_suffix_reorder(const void *src_k, const void *src_v, void *dst_k, void *dst_v,

@@ -68,13 +68,6 @@ constexpr int kKeys = 64;                  // keys per K/V tile
 constexpr int kQBox = 128 * 128;           // 128 rows x 128 bytes (one 128-byte-swizzled column block)
 constexpr int kKVBox = 64 * 128;           // 64 rows x 128 bytes
 constexpr float kRescaleLog2 = 8.0f;       // rescale O only if the max grew by more than 2^8
-// Registers per thread after the split: the four TMA / MMA warps and the NH = 2 softmax
-// warpgroups (384 threads, at most 168 registers each at launch: 4*32*64 + 8*32*216 = 63,488
-// <= 64,512).
-constexpr int kRegsLaunch = 168;
-constexpr int kRegsLight = 64;
-constexpr int kRegsSoftmax = 216;
-static_assert(4 * 32 * kRegsLight + 8 * 32 * kRegsSoftmax <= 384 * kRegsLaunch, "register split exceeds the launch");
 
 enum class Mode : int { Prefill = 0, Decode = 1 };
 
@@ -102,9 +95,9 @@ struct AttnParams {
     int32_t n_items_decode;
 };
 
-// Extra operands of the one-launch decode step (attn_kernel<Decode, ..., FUSED = true>): the
-// kernel gathers each beam's suffix through the parent index as it reads it and writes the
-// step's suffix for the next step.  Unused (zero) in every other instantiation.
+// Extra operands of the one-launch decode step (attn_kernel<Decode, ..., FUSED = true>): a helper
+// warp builds the suffix key tiles itself, gathering each beam's rows through the parent index,
+// and writes the step's suffix for the next step.  Unused (zero) in every other instantiation.
 struct StepParams {
     const __nv_bfloat16 *src_k, *src_v;   // previous suffix [R, W, S_max, Hkv, d]; slots 0..t-2 read
     const __nv_bfloat16 *new_k, *new_v;   // the step's token [R, W, Hkv, d]
@@ -112,11 +105,6 @@ struct StepParams {
     const int32_t *parent;                // [R, W], each in [0, W)
     int32_t suffix_max;
 };
-
-// Per-warp suffix staging of the one-launch decode step: the K and V rows (t slots each) of
-// every beam that has a query row in the warp's 32 rows, one beam after the other.
-constexpr int kSufWarpBytes = 8192;
-constexpr int kSufMaxT = BG_MAX_SUFFIX;    // suffix slots the one-launch step supports
 
 // QK8: Q and K arrive as one-byte E4M3 codes and Q.K^T runs as kind::f8f6f4 (V, P and P.V
 // stay bf16); otherwise every operand is bf16.
@@ -134,18 +122,24 @@ struct AttnCfg {
     static constexpr int kOffStage = kOffV + NV * kTileBytes;     // 2 KB per softmax warp
     static_assert(!QK8 || D == 128, "E4M3 Q/K rows are one 128-byte column block (head_dim 128)");
     static constexpr int kStageBytes = 32 * 64;
-    static constexpr int kOffSuf = kOffStage + 4 * NH * kStageBytes;   // FUSED: kSufWarpBytes per softmax warp
-    // FUSED: per softmax warp 256 bytes: the parents of its beams (32 int32), then the mask of
-    // beams with a bad parent
-    static constexpr int kOffSufPar = kOffSuf + (FUSED ? 4 * NH * kSufWarpBytes : 0);
-    static constexpr int kOffBar = kOffSufPar + (FUSED ? 4 * NH * 256 : 0);
-    static_assert(!FUSED || D == 64, "the one-launch decode step stages 128-byte suffix rows (head_dim 64)");
+    static constexpr int kOffBar = kOffStage + 4 * NH * kStageBytes;
     // q_full[2] q_empty[2] mma_final k_full[NK] k_empty[NK] v_full[NV] v_empty[NV] s_full[NH][NS]
     // p_full[NH][NS] pv_done[NH][NS] o_staged[NH][2]
     static constexpr int kNumBars = 5 + 2 * NK + 2 * NV + 3 * NS * NH + 2 * NH;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + slack for 1024-byte alignment
-    static constexpr int kThreads = 128 * (1 + NH);
+    // FUSED: one more warp (the suffix gatherer) after the softmax warpgroups
+    static constexpr int kThreads = 128 * (1 + NH) + (FUSED ? 32 : 0);
+    // Register split (setmaxnreg): the kernel is compiled for kRegsLaunch registers per thread
+    // (__maxnreg__), which the launcher checks against the compiled kernel before every launch;
+    // the TMA, MMA and gatherer warps then run with kRegsLight and the 8 softmax warps with
+    // kRegsSoftmax, within the launch's total (kSplitRegs).
+    static constexpr int kRegsLaunch = FUSED ? 152 : 168;
+    static constexpr int kRegsLight = 64;
+    static constexpr int kRegsSoftmax = FUSED ? 200 : 216;
+    static constexpr int kSplitRegs = (kThreads / 32 - 8) * 32 * kRegsLight + 8 * 32 * kRegsSoftmax;
+    static_assert(kThreads * kRegsLaunch <= 65536, "the launch must fit the register file");
+    static_assert(kSplitRegs <= kThreads * kRegsLaunch, "register split exceeds the launch's allocation");
     static constexpr int kColO = 64 * NS * NH;
     static constexpr int kColsUsed = 64 * NS * NH + D * NH;
     static constexpr int kTmemCols = kColsUsed <= 128 ? 128 : kColsUsed <= 256 ? 256 : 512;
@@ -182,10 +176,7 @@ __device__ __forceinline__ int4 fetch_raw(const AttnParams &p, int it)
     }
 }
 
-// FUSED (the one-launch decode step): the suffix is attended in the epilogue, not as key
-// tiles, and an item always streams at least one prompt tile (fully masked for an empty
-// prompt) so that its queries are loaded and its epilogue runs.
-template <Mode MODE, int NH, bool FUSED = false>
+template <Mode MODE, int NH>
 __device__ __forceinline__ Item make_item(const AttnParams &p, int it, int4 raw)
 {
     Item I;
@@ -224,12 +215,7 @@ __device__ __forceinline__ Item make_item(const AttnParams &p, int it, int4 raw)
         int nb = p.W - I.bt0 * p.BT;
         if (nb > NH * p.BT) nb = NH * p.BT;
         const int n_suf = (ok && p.suffix_len > 0) ? (nb + p.suf_bpt - 1) / p.suf_bpt : 0;
-        if constexpr (FUSED) {
-            if (ok && I.n_prompt == 0) I.n_prompt = 1;
-            I.n_tiles = I.n_prompt;
-        } else {
-            I.n_tiles = I.n_prompt + n_suf;
-        }
+        I.n_tiles = I.n_prompt + n_suf;
         I.seq_start = 0;
         I.qt = 0;
         I.head0 = 0;
@@ -257,7 +243,7 @@ __device__ __forceinline__ bool tile_store_via_tma(const AttnParams &p, const It
 // Walks the (item, key tile) sequence of one CTA, skipping items without
 // tiles.  Every role walks the same sequence, so all agree on global tile
 // numbers (which pick K/V stages, S buffers and barrier phases).
-template <Mode MODE, int NH, bool FUSED = false>
+template <Mode MODE, int NH>
 struct TileWalker {
     int it, j;           // current item index and tile within it
     int n_items;
@@ -282,7 +268,7 @@ struct TileWalker {
         for (it += gridDim.x; it < n_items; it += gridDim.x) {
             const int4 raw = nxt_raw;
             if (it + static_cast<int>(gridDim.x) < n_items) nxt_raw = fetch_raw<MODE>(p, it + gridDim.x);
-            I = make_item<MODE, NH, FUSED>(p, it, raw);
+            I = make_item<MODE, NH>(p, it, raw);
             if (I.valid && I.n_tiles > 0) {
                 j = 0;
                 valid = true;
@@ -310,7 +296,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volati
 }
 
 template <Mode MODE, int D, int NH, int NK, int NV, int NS, bool QK8 = false, bool FUSED = false>
-__global__ void __launch_bounds__(128 * (1 + NH), 1)
+__global__ void __maxnreg__((AttnCfg<D, NH, NK, NV, NS, QK8, FUSED>::kRegsLaunch))
     attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_sk,
                 const __grid_constant__ CUtensorMap tm_sv, const __grid_constant__ CUtensorMap tm_o,
@@ -319,9 +305,7 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
     using C = AttnCfg<D, NH, NK, NV, NS, QK8, FUSED>;
     static_assert(!QK8 || MODE == Mode::Prefill, "E4M3 Q/K is a prefill variant");
     static_assert(!FUSED || MODE == Mode::Decode, "the one-launch step is a decode variant");
-    // one CTA of 384 threads per SM: the launch bounds give each thread at most 65,536 / 384, i.e.
-    // kRegsLaunch registers, the budget of the register split below
-    static_assert(NH == 2 && 65536 / (128 * (1 + NH)) / 8 * 8 == kRegsLaunch, "register split assumes 384 threads");
+    static_assert(NH == 2, "the register split and the warp roles assume two query tiles per CTA");
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte alignment of the shared-window offset (swizzle-128B atoms need it)
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -381,7 +365,7 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
         // <= 64 rows; the rows past them keep what an earlier tile left (finite) or these
         // zeros, so the masked columns they feed multiply finite values only.
         uint4 *z4 = reinterpret_cast<uint4 *>(smem + C::kOffQ);
-        for (int i = threadIdx.x; i < C::kOffBar / 16; i += blockDim.x) z4[i] = make_uint4(0, 0, 0, 0);
+        for (int i = threadIdx.x; i < C::kOffStage / 16; i += blockDim.x) z4[i] = make_uint4(0, 0, 0, 0);
         fence_proxy_async_smem();
     }
     if (warp == 1) {
@@ -411,19 +395,17 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
         n_items = p.n_items_decode;
     }
 
-    // Register split (setmaxnreg, per warp, at the start of each role): the TMA and MMA warps run
-    // with kRegsLight registers and the softmax warps with kRegsSoftmax, where the launch gives
-    // every thread 168.  The total stays within the launch's allocation (checked below), so the
-    // softmax warps' increase is always granted, from the registers the other warps return.
+    // Each role sets its register allocation first (see AttnCfg): the softmax warps' increase is
+    // granted from the registers the other warps return.
     if (warp == 0) {
-        reg_dealloc<kRegsLight>();
+        reg_dealloc<C::kRegsLight>();
         // =============================================================== producer
         // The whole warp runs the loop (warp-uniform control flow and operands); lane 0
         // issues each copy.
         const uint32_t leader = (lane == 0) ? 1u : 0u;
         const uint64_t pol_q = l2_policy_evict_first();
         const uint64_t pol_kv = l2_policy_evict_last();
-        TileWalker<MODE, NH, FUSED> w;
+        TileWalker<MODE, NH> w;
         w.first(p, n_items);
         uint32_t n_kv = 0;                 // K/V tiles issued (global tile number)
         while (w.valid) {
@@ -451,6 +433,12 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
                             tma_load_4d_w(leader, qdst + (h * C::NB + b) * kQBox, &tm_q, &q_full[qb], b * 64, 0, w.I.kh,
                                           w.I.r * p.W + (w.I.bt0 + h) * p.BT, pol_q);
                 }
+            }
+            if (FUSED && MODE == Mode::Decode && w.j >= w.I.n_prompt) {
+                // a suffix tile: the gatherer warp fills this stage
+                ++n_kv;
+                w.advance(p);
+                continue;
             }
             const int st = n_kv % NK;
             const uint32_t use = n_kv / NK;
@@ -487,15 +475,20 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
         }
         __syncwarp();
     } else if (warp == 2) {
-        reg_dealloc<kRegsLight>();
+        reg_dealloc<C::kRegsLight>();
         // =============================================================== V producer
         const uint32_t leader = (lane == 0) ? 1u : 0u;
         const uint64_t pol_kv = l2_policy_evict_last();
         const uint64_t pol_q = l2_policy_evict_first();
-        TileWalker<MODE, NH, FUSED> w;
+        TileWalker<MODE, NH> w;
         w.first(p, n_items);
         uint32_t n_v = 0;
         while (w.valid) {
+            if (FUSED && MODE == Mode::Decode && w.j >= w.I.n_prompt) {
+                ++n_v;                          // a suffix tile: filled by the gatherer warp
+                w.advance(p);
+                continue;
+            }
             const int st = n_v % NV;
             const uint32_t use = n_v / NV;
             if (use > 0 && !warp_wait(&v_empty[st], (use - 1) & 1, abort_flag)) break;
@@ -523,8 +516,8 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
             }
         }
         __syncwarp();
-    } else if (warp == 1 || (NH == 2 && warp == 3)) {
-        reg_dealloc<kRegsLight>();
+    } else if (warp == 1 || warp == 3) {
+        reg_dealloc<C::kRegsLight>();
         // =============================================================== MMA issuers
         // One thread per query tile (lane 0 of warp 1: tile 0, of warp 3: tile 1), so the two
         // tiles' QK -> softmax -> P.V chains do not wait for each other.  The thread waits on
@@ -542,13 +535,13 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
             const uint64_t dv0 = sdesc_sw128(smem_u32(smem + C::kOffV), kKVBox, 1024);
             // `b` walks the tiles whose S is computed next, `a` (one behind) the tiles whose
             // P.V is accumulated next.
-            TileWalker<MODE, NH, FUSED> b, a;
+            TileWalker<MODE, NH> b, a;
             b.first(p, n_items);
             a = b;
             uint32_t gb = 0, ga = 0;           // global tile numbers of b and a
             bool ok = true;
 
-            auto issue_qk = [&](const TileWalker<MODE, NH, FUSED> &t, uint32_t g) -> bool {
+            auto issue_qk = [&](const TileWalker<MODE, NH> &t, uint32_t g) -> bool {
                 if (t.j == 0 && !mbar_wait(&q_full[t.qbuf()], t.quse() & 1, abort_flag)) return false;
                 const int st = g % NK;
                 if (!mbar_wait(&k_full[st], (g / NK) & 1, abort_flag)) return false;
@@ -566,7 +559,7 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
                     mma_qk_tile<C::NBQ>(tmem + C::col_s(h, g % NS), dqh, dks, kIdescQK, &s_full[NS * h + g % NS]);
                 // the item's Q buffer is free once its last QK has completed, unless the epilogue
                 // stores the output tile out of it
-                if (!FUSED && t.j == t.I.n_tiles - 1 && !tile_store_via_tma<MODE>(p, t.I, h))
+                if (t.j == t.I.n_tiles - 1 && !tile_store_via_tma<MODE>(p, t.I, h))
                     mma_commit(&q_empty[t.qbuf()]);
                 return true;
             };
@@ -601,8 +594,8 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
             mbar_wait_drain(mma_final, 0);
         }
         __syncwarp();
-    } else if (warp >= 4) {
-        reg_alloc<kRegsSoftmax>();
+    } else if (warp >= 4 && warp < 4 + 4 * NH) {
+        reg_alloc<C::kRegsSoftmax>();
         // =============================================================== softmax + epilogue
         const int h = (warp - 4) >> 2;
         const int quad = warp & 3;
@@ -626,72 +619,7 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
         // as the Q load), and one thread issues the tile stores and, once the TMA unit has read the
         // buffer, hands it back to the Q producer.  The warps do not wait for the global writes.
         // Other tiles, and every prefill tile, are stored row by row through the staging area.
-        uint32_t n_tma = 0;   // epilogues of this warpgroup that used o_staged so far
-        // One-launch decode step (FUSED).  Each softmax warp stages, in its own area, the t K and
-        // V rows (kv head of the item) of every beam with a query row among its 32 rows: slots
-        // 0..t-2 from the parent's suffix in the previous step's buffer, slot t-1 from the step's
-        // new token (gather on read: no separate reorder pass).  The epilogue attends each row
-        // over its beam's staged rows on the CUDA cores, merges that into the prompt part of the
-        // online softmax, and writes the step's suffix of the beams whose first row is in the warp.
-        // (The values below are recomputed where they are used, so that nothing of this stays live
-        // in registers through the softmax loop, which runs at the register limit.)
-        auto suf_area = [&]() { return smem + C::kOffSuf + (warp - 4) * kSufWarpBytes; };
-        auto suf_par = [&]() { return reinterpret_cast<int32_t *>(smem + C::kOffSufPar + (warp - 4) * 256); };
-        auto lb_first = [&]() { return (quad * 32) / p.g; };                                 // first beam staged
-        auto suf_nb = [&]() { return min((quad * 32 + 31) / p.g, p.BT - 1) - lb_first() + 1; };   // beams staged
-        auto suf_stride = [&]() { return p.suffix_len * 256 + 16; };   // bytes per beam (+16: bank spread)
-        // Starts the loads of the parents of item I's beams that have rows in this warp (lane i:
-        // beam i), into the warp's parent slots.
-        auto fetch_parents = [&](const Item &I) {
-            const int lb = lb_first() + lane;
-            const int beam = (I.bt0 + h) * p.BT + lb;
-            if (p.suffix_len > 1 && lane < suf_nb() && lb < p.BT && beam < p.W)
-                cp_async_4(suf_par() + lane, sp.parent + static_cast<int64_t>(I.r) * p.W + beam);
-            cp_async_commit();
-        };
-        // Issues the staging copies of item I (cp.async, completed by the epilogue's wait), once its
-        // parents have arrived.  The beams whose parent is out of range get zero history rows, their
-        // suffix is not written (mask in the warp's slot after the parents), and BG_DEVSTAT_PARENT
-        // is raised.
-        auto issue_suffix = [&](const Item &I) {
-            cp_async_wait_all();
-            __syncwarp();
-            const int t = p.suffix_len;
-            const int lbf = lb_first(), nb = suf_nb(), stride = suf_stride();
-            uint8_t *area = suf_area();
-            const int par = (t > 1 && lane < nb) ? suf_par()[lane] : 0;
-            const int tile_beam0 = (I.bt0 + h) * p.BT;
-            const int64_t req_beam0 = static_cast<int64_t>(I.r) * p.W;
-            const bool lane_beam = lane < nb && lbf + lane < p.BT && tile_beam0 + lbf + lane < p.W;
-            const bool badp = t > 1 && lane_beam && (par < 0 || par >= p.W);
-            const uint32_t bad = __ballot_sync(0xffffffffu, badp);
-            if (badp && p.dev_status) atomicOr(p.dev_status, BG_DEVSTAT_PARENT);
-            if (lane == 0) reinterpret_cast<volatile uint32_t *>(suf_par())[32] = bad;
-            const int per_beam = t * 16;                 // 16-byte chunks of a beam's K and V rows
-            const int chunks = nb * per_beam;
-            for (int base = 0; base < chunks; base += 32) {
-                const int q = base + lane;
-                const int bi = q / per_beam;
-                const int pb = __shfl_sync(0xffffffffu, par, bi & 31);
-                const int lb = lbf + bi;
-                const int beam = tile_beam0 + lb;
-                if (q >= chunks || lb >= p.BT || beam >= p.W) continue;
-                const int rem = q - bi * per_beam;
-                const int kv = rem / (t * 8);
-                const int sl = (rem - kv * t * 8) >> 3;
-                const int c = rem & 7;
-                uint8_t *to = area + bi * stride + kv * t * 128 + sl * 128 + c * 16;
-                if (sl == t - 1) {
-                    cp_async_16(to, (kv ? sp.new_v : sp.new_k) + ((req_beam0 + beam) * p.Hkv + I.kh) * 64 + c * 8);
-                } else if ((bad >> bi) & 1u) {
-                    *reinterpret_cast<uint4 *>(to) = make_uint4(0, 0, 0, 0);
-                } else {
-                    cp_async_16(to, (kv ? sp.src_v : sp.src_k) +
-                                        (((req_beam0 + pb) * sp.suffix_max + sl) * p.Hkv + I.kh) * 64 + c * 8);
-                }
-            }
-            cp_async_commit();
-        };
+        uint32_t n_tma = 0;   // output tiles this warpgroup stored through the TMA unit so far
         auto epilogue = [&](const Item &I, float m, float l, uint32_t g_last, int qbi, bool via_tma,
                             auto &&release) -> bool {
                 // The commit after the item's last P.V covers every earlier MMA too.  (Items always
@@ -742,121 +670,20 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
                 };
                 // O is read 64 columns at a time, normalised and packed to bf16 pairs (half the
                 // registers), and handed back to the next item's P.V before the stores
+                const float inv_l = 1.f / l;
+                const float2 il = make_float2(inv_l, inv_l);
                 uint32_t pk[D / 2];
-                if constexpr (FUSED) {
-                    // the row's beam's suffix, one slot at a time as further online-softmax steps
-                    // over the staged rows, O in registers, fp32 throughout.  A runtime loop over the
-                    // slots keeps the code small: this epilogue is inlined at two call sites, and an
-                    // unrolled version's size made instruction fetch the kernel's bottleneck.
-                    static_assert(!FUSED || D == 64, "two 32-column chunks");
-                    const int t = p.suffix_len;
-                    const int lb = row / p.g;
-                    const bool rvalid = lb < p.BT && (I.bt0 + h) * p.BT + lb < p.W;
-                    const uint8_t *ak = suf_area() + (rvalid ? lb - lb_first() : 0) * suf_stride();
-                    const uint8_t *av = ak + t * 128;
-                    const uint8_t *qrow = smem + C::kOffQ + qbi * C::kQBytes + h * C::NB * kQBox + row * 128;
-                    float2 o2[32];
-                    {
-                        float o[32];
-                        tmem_ld32(tO, o);
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) o2[i] = make_float2(o[2 * i], o[2 * i + 1]);
-                        tmem_ld32(tO + 32, o);
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) o2[16 + i] = make_float2(o[2 * i], o[2 * i + 1]);
-                    }
-                    // O is in registers: the next item's first P.V may overwrite it while the suffix
-                    // is attended below
-                    release();
-                    cp_async_wait_all();
-                    __syncwarp();
-                    float mr = m, lr = l;   // a prompt part with no valid key has m = -inf, O = 0, l = 0
-#pragma unroll 1
-                    for (int sl = 0; sl < t; ++sl) {
-                        float2 a = make_float2(0.f, 0.f);
-#pragma unroll
-                        for (int c = 0; c < 8; ++c) {
-                            const uint4 qv = *reinterpret_cast<const uint4 *>(qrow + ((c ^ (row & 7)) << 4));
-                            const uint4 kq = *reinterpret_cast<const uint4 *>(ak + sl * 128 + c * 16);
-                            a = ffma2(unpack_bf16x2(qv.x), unpack_bf16x2(kq.x), a);
-                            a = ffma2(unpack_bf16x2(qv.y), unpack_bf16x2(kq.y), a);
-                            a = ffma2(unpack_bf16x2(qv.z), unpack_bf16x2(kq.z), a);
-                            a = ffma2(unpack_bf16x2(qv.w), unpack_bf16x2(kq.w), a);
-                        }
-                        const float z = (a.x + a.y) * sl2;
-                        const float mn = fmaxf(mr, z);
-                        if (__any_sync(0xffffffffu, mn > mr)) {
-                            const float al = (mr == -INFINITY) ? 0.f : ex2(mr - mn);
-                            const float2 al2 = make_float2(al, al);
-                            lr *= al;
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) o2[i] = fmul2(o2[i], al2);
-                        }
-                        mr = mn;
-                        const float pz = ex2(z - mn);
-                        lr += pz;
-                        const float2 pp = make_float2(pz, pz);
-#pragma unroll
-                        for (int u = 0; u < 8; ++u) {
-                            const uint4 vv = *reinterpret_cast<const uint4 *>(av + sl * 128 + u * 16);
-                            o2[4 * u] = ffma2(pp, unpack_bf16x2(vv.x), o2[4 * u]);
-                            o2[4 * u + 1] = ffma2(pp, unpack_bf16x2(vv.y), o2[4 * u + 1]);
-                            o2[4 * u + 2] = ffma2(pp, unpack_bf16x2(vv.z), o2[4 * u + 2]);
-                            o2[4 * u + 3] = ffma2(pp, unpack_bf16x2(vv.w), o2[4 * u + 3]);
-                        }
-                    }
-                    const float inv_l = 1.f / lr;
-                    const float2 il2 = make_float2(inv_l, inv_l);
+                for (int c2 = 0; c2 < D / 64; ++c2) {
+                    float o[64];
+                    tmem_ld64(tO + 64 * c2, o);
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
-                        const float2 x = fmul2(o2[i], il2);
-                        pk[i] = pack_bf16x2(x.x, x.y);
-                    }
-                } else {
-                    const float inv_l = 1.f / l;
-                    const float2 il = make_float2(inv_l, inv_l);
-#pragma unroll
-                    for (int c2 = 0; c2 < D / 64; ++c2) {
-                        float o[64];
-                        tmem_ld64(tO + 64 * c2, o);
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) {
-                            const float2 x = fmul2(make_float2(o[2 * i], o[2 * i + 1]), il);
-                            pk[32 * c2 + i] = pack_bf16x2(x.x, x.y);
-                        }
-                    }
-                    release();
-                }
-                if constexpr (FUSED) {
-                    // the step's suffix of the beams whose first query row is in this warp (each
-                    // beam and kv head has exactly one such warp in the grid), from the staged rows
-                    const int t = p.suffix_len;
-                    const uint32_t bad = reinterpret_cast<volatile uint32_t *>(suf_par())[32];
-                    const int lbf = lb_first(), stride = suf_stride();
-                    const uint8_t *area = suf_area();
-                    const int own_lo = (quad * 32 + p.g - 1) / p.g;
-                    const int own_hi = min((quad * 32 + 31) / p.g, p.BT - 1);
-                    const int per_beam = t * 16;
-                    const int chunks = own_hi >= own_lo ? (own_hi - own_lo + 1) * per_beam : 0;
-                    const int tile_beam0 = (I.bt0 + h) * p.BT;
-                    for (int base = 0; base < chunks; base += 32) {   // same trip count in every lane
-                        const int q = base + lane;
-                        const int lb = own_lo + q / per_beam;
-                        const int beam = tile_beam0 + lb;
-                        const int bi = lb - lbf;
-                        if (q >= chunks || beam >= p.W || ((bad >> bi) & 1u)) continue;
-                        const int rem = q - (lb - own_lo) * per_beam;
-                        const int kv = rem / (t * 8);
-                        const int sl = (rem - kv * t * 8) >> 3;
-                        const int c = rem & 7;
-                        const uint4 val = *reinterpret_cast<const uint4 *>(area + bi * stride + kv * t * 128 + sl * 128 +
-                                                                          c * 16);
-                        __nv_bfloat16 *to = (kv ? sp.dst_v : sp.dst_k) +
-                                            (((static_cast<int64_t>(I.r) * p.W + beam) * sp.suffix_max + sl) * p.Hkv +
-                                             I.kh) * 64 + c * 8;
-                        *reinterpret_cast<uint4 *>(to) = val;
+                        const float2 x = fmul2(make_float2(o[2 * i], o[2 * i + 1]), il);
+                        pk[32 * c2 + i] = pack_bf16x2(x.x, x.y);
                     }
                 }
+                release();
                 const bool leader = quad == 0 && lane == 0;
                 if (MODE == Mode::Decode && via_tma) {
                     // row `row` of column block cb: 16-byte chunk c at (c ^ (row % 8)) in its 128-byte row
@@ -892,19 +719,6 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
                 } else {
 #pragma unroll
                     for (int c = 0; c < D / 32; ++c) put_chunk(c, pk + 16 * c);
-                    if constexpr (FUSED) {
-                        // the epilogue read the item's query rows: the Q buffer goes back to the
-                        // producer once all four warps of the group are past that read
-                        __syncwarp();
-                        uint64_t *staged = &o_staged[2 * h + (n_tma & 1)];
-                        if (lane == 0) mbar_arrive(staged);
-                        const uint32_t staged_parity = (n_tma >> 1) & 1u;
-                        ++n_tma;
-                        if (leader) {
-                            if (!mbar_wait(staged, staged_parity, abort_flag)) return false;
-                            mbar_arrive(&q_empty[qbi]);
-                        }
-                    }
                 }
                 if constexpr (MODE == Mode::Prefill) {
                     if (p.lse) {
@@ -926,7 +740,7 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
         for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
             const int4 raw = nxt_raw;
             if (it + static_cast<int>(gridDim.x) < n_items) nxt_raw = fetch_raw<MODE>(p, it + gridDim.x);
-            const Item I = make_item<MODE, NH, FUSED>(p, it, raw);
+            const Item I = make_item<MODE, NH>(p, it, raw);
             if (!I.valid) {
                 if constexpr (MODE == Mode::Decode) {
                     if (h == 0 && row == 0 && p.dev_status) {
@@ -941,14 +755,6 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
             if (I.n_tiles == 0) continue;   // not produced by make_item for a valid item; skipped by every role
             ++nq;
             const bool tma_I = tile_store_via_tma<MODE>(p, I, h);
-            // FUSED: the parents of the warp's beams load now; the staging copies start at once for
-            // the CTA's first item (their latency then overlaps its first Q/K loads), else after the
-            // first tile, once the previous item's epilogue has freed the staging area
-            const bool pend_at_start = pend;
-            if constexpr (FUSED) {
-                fetch_parents(I);
-                if (!pend) issue_suffix(I);
-            }
             float m = -INFINITY;   // running max of scaled logits (base-2 units)
             float l = 0.f;         // running sum of exp2(logit - m)
             for (int j = 0; j < I.n_tiles; ++j, ++g) {
@@ -1086,10 +892,6 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
                 } else {
                     mbar_arrive(&p_full[NS * h + g % NS]);
                 }
-                // the staging area is free once the previous item's epilogue has run
-                if constexpr (FUSED) {
-                    if (j == 0 && pend_at_start) issue_suffix(I);
-                }
             }
             if (!ok) break;
             pend = true;
@@ -1101,12 +903,111 @@ __global__ void __launch_bounds__(128 * (1 + NH), 1)
             gp = g - 1;
         }
         if (ok && pend) ok = epilogue(Ip, mp, lp, gp, qbp, tmap, []() {});
-        // every tile store this thread issued has written global memory before the CTA exits, and
-        // no staging copy is still in flight (a time-out may have skipped an epilogue's wait)
+        // every tile store this thread issued has written global memory before the CTA exits
         if (quad == 0 && lane == 0) bulk_wait_all();
-        if constexpr (FUSED) cp_async_wait_all();
 
         (void)ok;
+    }
+
+    if constexpr (FUSED) {
+        if (warp == 4 + 4 * NH) {
+            reg_dealloc<C::kRegsLight>();
+            // =========================================================== suffix gatherer
+            // Builds every suffix key tile of the CTA's items in the K and V stages the producers
+            // leave to it, straight from the previous step's buffer: row (beam b, slot s) of a tile
+            // is slot s of beam parent[b] for s < t-1 and the step's new token for s = t-1 (the
+            // reorder of the beam's suffix, gathered as it is read).  Each lane copies 16-byte
+            // chunks with cp.async into the 128-byte-swizzled layout the tensor cores read (the
+            // layout a TMA tile load writes), then orders them before the MMAs' reads
+            // (fence.proxy.async) and completes the stages' full barriers.  The staged rows are
+            // then written to dst, the step's suffix: every (beam, kv head) is in exactly one
+            // suffix tile of one item, so each row of dst is written once.
+            constexpr int kCpr = D / 8;                  // 16-byte chunks per row
+            const int t = p.suffix_len;
+            TileWalker<MODE, NH> w;
+            w.first(p, n_items);
+            uint32_t n_kv = 0;
+            while (w.valid) {
+                if (w.j < w.I.n_prompt) {
+                    ++n_kv;
+                    w.advance(p);
+                    continue;
+                }
+                const int stk = n_kv % NK, stv = n_kv % NV;
+                const uint32_t usek = n_kv / NK, usev = n_kv / NV;
+                if (usek > 0 && !warp_wait(&k_empty[stk], (usek - 1) & 1, abort_flag)) break;
+                if (usev > 0 && !warp_wait(&v_empty[stv], (usev - 1) & 1, abort_flag)) break;
+                // the tile's beams: suf_bpt consecutive beams of the item, cut at the item's end
+                const int first = w.I.bt0 * p.BT + (w.j - w.I.n_prompt) * p.suf_bpt;
+                const int item_end = min(p.W, (w.I.bt0 + NH) * p.BT);
+                const int nb = min(p.suf_bpt, item_end - first);
+                const int64_t req0 = static_cast<int64_t>(w.I.r) * p.W;
+                // parents of the tile's beams (at most 64): lane i holds those of beams i and 32 + i
+                int par0 = 0, par1 = 0;
+                if (t > 1) {
+                    if (lane < nb) par0 = sp.parent[req0 + first + lane];
+                    if (lane + 32 < nb) par1 = sp.parent[req0 + first + 32 + lane];
+                }
+                const bool bad0 = t > 1 && lane < nb && (par0 < 0 || par0 >= p.W);
+                const bool bad1 = t > 1 && lane + 32 < nb && (par1 < 0 || par1 >= p.W);
+                const uint32_t badm0 = __ballot_sync(0xffffffffu, bad0), badm1 = __ballot_sync(0xffffffffu, bad1);
+                if ((bad0 || bad1) && p.dev_status) atomicOr(p.dev_status, BG_DEVSTAT_PARENT);
+                uint8_t *kst = smem + C::kOffK + stk * C::kKTileBytes;
+                uint8_t *vst = smem + C::kOffV + stv * C::kTileBytes;
+                const int chunks = nb * t * kCpr;        // per tensor (K and V alike)
+                for (int base = 0; base < 2 * chunks; base += 32) {   // same trip count in every lane
+                    const int q = base + lane;
+                    const int kv = q >= chunks ? 1 : 0;
+                    const int qq = q - kv * chunks;
+                    const int row = qq / kCpr;               // beam-major: row = pos * t + s
+                    const int c = qq - row * kCpr;
+                    const int pos = row / t;
+                    const int sl = row - pos * t;
+                    const int pa = __shfl_sync(0xffffffffu, par0, pos & 31);
+                    const int pb = __shfl_sync(0xffffffffu, par1, pos & 31);
+                    if (q >= 2 * chunks) continue;
+                    const int par = pos < 32 ? pa : pb;
+                    const bool bad = ((pos < 32 ? badm0 : badm1) >> (pos & 31)) & 1u;
+                    uint8_t *to = (kv ? vst : kst) + (c >> 3) * kKVBox + row * 128 + (((c & 7) ^ (row & 7)) << 4);
+                    if (sl == t - 1) {
+                        cp_async_16(to, (kv ? sp.new_v : sp.new_k) + ((req0 + first + pos) * p.Hkv + w.I.kh) * D + c * 8);
+                    } else if (bad) {
+                        *reinterpret_cast<uint4 *>(to) = make_uint4(0, 0, 0, 0);
+                    } else {
+                        cp_async_16(to, (kv ? sp.src_v : sp.src_k) +
+                                            (((req0 + par) * sp.suffix_max + sl) * p.Hkv + w.I.kh) * D + c * 8);
+                    }
+                }
+                cp_async_commit();
+                cp_async_wait_all();
+                fence_proxy_async_smem();                // generic-proxy writes -> the tensor cores' reads
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&k_full[stk]);
+                    mbar_arrive(&v_full[stv]);
+                }
+                // the step's suffix, from the staged rows (beams with a bad parent left untouched)
+                for (int base = 0; base < 2 * chunks; base += 32) {
+                    const int q = base + lane;
+                    if (q >= 2 * chunks) continue;
+                    const int kv = q >= chunks ? 1 : 0;
+                    const int qq = q - kv * chunks;
+                    const int row = qq / kCpr;
+                    const int c = qq - row * kCpr;
+                    const int pos = row / t;
+                    const int sl = row - pos * t;
+                    if (((pos < 32 ? badm0 : badm1) >> (pos & 31)) & 1u) continue;
+                    const uint8_t *from = (kv ? vst : kst) + (c >> 3) * kKVBox + row * 128 + (((c & 7) ^ (row & 7)) << 4);
+                    __nv_bfloat16 *to = (kv ? sp.dst_v : sp.dst_k) +
+                                        (((req0 + first + pos) * sp.suffix_max + sl) * p.Hkv + w.I.kh) * D + c * 8;
+                    *reinterpret_cast<uint4 *>(to) = *reinterpret_cast<const uint4 *>(from);
+                }
+                ++n_kv;
+                w.advance(p);
+            }
+            cp_async_wait_all();
+            __syncwarp();
+        }
     }
 
     // ------------------------------------------------------------------ teardown

@@ -42,10 +42,8 @@ cudaError_t launch_decode_attn(int head_dim, const CUtensorMap &tm_q, const CUte
                                const CUtensorMap &tm_v, const CUtensorMap &tm_sk, const CUtensorMap &tm_sv,
                                const CUtensorMap &tm_o, const AttnParams &p, int grid, cudaStream_t stream);
 int decode_tiles_per_cta();
-// The one-launch decode step (suffix gathered through the parent index, attended in the
-// epilogue, the step's suffix written by the same kernel): whether its per-warp staging holds
-// the suffix of this shape, and its launch.
-bool decode_step_fused_fits(int head_dim, int g, int suffix_len);
+// The one-launch decode step: the attention kernel with a gatherer warp that builds the suffix
+// key tiles through the parent index and writes the step's suffix.
 cudaError_t launch_decode_step_fused(int head_dim, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
                                      const CUtensorMap &tm_v, const CUtensorMap &tm_o, const AttnParams &p,
                                      const StepParams &sp, int grid, cudaStream_t stream);
@@ -109,6 +107,26 @@ cudaError_t ensure_smem_attribute(Kern kern, int bytes, std::atomic<uint64_t> &d
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
     return e;
+}
+
+// The attention kernels split the registers of their launch between warp roles (setmaxnreg),
+// and a split larger than the launch's allocation would wait forever.  Before launching, the
+// compiled kernel's registers per thread (looked up once per device) times its threads must
+// cover the split; otherwise the launch is refused (cudaErrorInvalidConfiguration).
+template <typename Kern>
+cudaError_t check_register_split(Kern kern, int threads, int split_regs, std::atomic<uint64_t> &done)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
+    if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+    cudaFuncAttributes a{};
+    e = cudaFuncGetAttributes(&a, kern);
+    if (e != cudaSuccess) return e;
+    if (a.numRegs * threads < split_regs) return cudaErrorInvalidConfiguration;
+    if (bit) done.fetch_or(bit, std::memory_order_acq_rel);
+    return cudaSuccess;
 }
 
 // Work-list layout inside the caller's workspace.

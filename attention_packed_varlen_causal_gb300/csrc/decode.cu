@@ -6,9 +6,10 @@
 // queries of all beams x group heads of one kv head form 128-row tiles that
 // run on the tensor cores against the prompt K/V, read once per tile pair
 // (and from L2 for the sibling tiles).  The few suffix keys of each beam
-// follow as extra key tiles of the same item (see attn_kernel<Decode>), or,
-// in the one-launch decode step, are gathered through the parent index and
-// attended on the CUDA cores in the epilogue (attn_kernel<Decode, FUSED>).
+// follow as extra key tiles of the same item (see attn_kernel<Decode>); in
+// the one-launch decode step a gatherer warp builds those tiles straight
+// from the previous step's suffix through the parent index and writes the
+// step's suffix (attn_kernel<Decode, FUSED>).
 #include "bg_attn_kernel.cuh"
 #include "bg_internal.h"
 
@@ -35,6 +36,9 @@ cudaError_t launch_one(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const C
     auto kern = attn_kernel<Mode::Decode, D, kNH, NK, NV, NS, false, FUSED>;
     cudaError_t e = ensure_smem_attribute(kern, C::kSmemBytes, smem_attr_done<D, NK, NV, NS, FUSED>());
     if (e != cudaSuccess) return e;
+    static std::atomic<uint64_t> split_checked{0};
+    e = check_register_split(kern, C::kThreads, C::kSplitRegs, split_checked);
+    if (e != cudaSuccess) return e;
     return launch_dependent(kern, dim3(grid), dim3(C::kThreads), C::kSmemBytes, stream, tm_q, tm_k, tm_v, tm_sk,
                             tm_sv, tm_o, p, sp);
 }
@@ -52,24 +56,12 @@ cudaError_t launch_decode_attn(int head_dim, const CUtensorMap &tm_q, const CUte
     return cudaErrorInvalidValue;
 }
 
-bool decode_step_fused_fits(int head_dim, int g, int suffix_len)
-{
-    if (head_dim != 64 || g < 1 || g > 128 || suffix_len < 1 || suffix_len > kSufMaxT) return false;
-    const int BT = 128 / g;
-    const int stride = suffix_len * 256 + 16;
-    for (int quad = 0; quad < 4; ++quad) {
-        const int first = (quad * 32) / g;
-        const int last = ((quad * 32 + 31) / g) < BT - 1 ? (quad * 32 + 31) / g : BT - 1;
-        if ((last - first + 1) * stride > kSufWarpBytes) return false;
-    }
-    return true;
-}
-
 cudaError_t launch_decode_step_fused(int head_dim, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
                                      const CUtensorMap &tm_v, const CUtensorMap &tm_o, const AttnParams &p,
                                      const StepParams &sp, int grid, cudaStream_t stream)
 {
     if (head_dim == 64) return launch_one<64, 4, 4, 3, true>(tm_q, tm_k, tm_v, tm_q, tm_q, tm_o, p, sp, grid, stream);
+    if (head_dim == 128) return launch_one<128, 3, 2, 2, true>(tm_q, tm_k, tm_v, tm_q, tm_q, tm_o, p, sp, grid, stream);
     return cudaErrorInvalidValue;
 }
 

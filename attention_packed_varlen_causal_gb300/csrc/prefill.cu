@@ -106,6 +106,9 @@ cudaError_t launch_one(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const C
     auto kern = attn_kernel<Mode::Prefill, D, kNH, NK, NV, NS, QK8>;
     cudaError_t e = ensure_smem_attribute(kern, C::kSmemBytes, smem_attr_done<D, NK, NV, NS, QK8>());
     if (e != cudaSuccess) return e;
+    static std::atomic<uint64_t> split_checked{0};
+    e = check_register_split(kern, C::kThreads, C::kSplitRegs, split_checked);
+    if (e != cudaSuccess) return e;
     const StepParams none = {};
     return launch_dependent(kern, dim3(grid), dim3(C::kThreads), C::kSmemBytes, stream, tm_q, tm_k, tm_v, tm_k, tm_v,
                             tm_o, p, none);   // no suffix maps, no step operands

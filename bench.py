@@ -267,9 +267,7 @@ class DecodeStack:
             by += b
         self.flops_per_search = fl * layers
         self.bytes_per_search = by * layers
-        # kernels per step and layer: 1 for the one-launch step, 2 for reorder + attention
-        self.launches = layers * sum(bg.bg_beam_decode_step_launches(Hq, Hkv, d, t, max(self.plen))
-                                     for t in range(1, S + 1))
+        self.launches = S * layers                # one kernel per step and layer
 
     def enqueue(self, stream):
         bg = self.bg

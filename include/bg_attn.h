@@ -281,17 +281,12 @@ bg_status_t bg_beam_suffix_reorder(const void *src_k, const void *src_v,
  * the call computes
  *     bg_beam_suffix_reorder(src, dst, parent_idx, new, n_tokens = t - 1)
  *     bg_beam_decode_attn(q, ..., suffix = dst, suffix_len = t)
- * with the arguments of both checked together before anything is enqueued;
- * dst then holds the reordered suffix (bit for bit), the next step's src.
- * Two forms, chosen from the sizes (bg_beam_decode_step_launches tells which):
- *   - one launch, where it applies: the attention kernel gathers each beam's
- *     suffix rows through parent_idx as it reads them (no separate reorder
- *     pass), attends them on the CUDA cores in fp32 after the shared-prompt
- *     tiles, and writes dst itself;
- *   - otherwise the two calls above as two launches, the second one started
- *     by programmatic dependent launch so that its prologue overlaps the first.
- * Both give outputs within the parity tolerance of each other; the suffix in
- * dst is the same.
+ * with the arguments of both checked together before anything is enqueued,
+ * and gives bit for bit the same output and dst; dst then holds the
+ * reordered suffix, the next step's src.  It runs as ONE launch: a gatherer
+ * warp of the attention kernel builds each suffix key tile straight from src
+ * through parent_idx (no separate reorder pass, no re-read of dst) and
+ * writes the tile's rows to dst, while the other warps attend.
  *
  *   q, prompt_k, prompt_v, cu_prompt, total_prompt_tokens, max_prompt_len,
  *   R, W, Hq, Hkv, head_dim, scale, out    as in bg_beam_decode_attn
@@ -320,17 +315,6 @@ bg_status_t bg_beam_decode_step(const void *q, const void *prompt_k, const void 
                                 int32_t R, int32_t W, int32_t Hq, int32_t Hkv, int32_t head_dim,
                                 float scale, void *out, int32_t *dev_status,
                                 cudaStream_t stream);
-
-/*
- * Number of kernels one bg_beam_decode_step call with these sizes enqueues:
- * 1 where its one-launch form applies -- head_dim 64, the t suffix rows
- * (K and V) of the beams that own query rows in any 32-row group of a
- * 128-row query tile fit an 8 KB staging area (t * 256 + 16 bytes per
- * beam), and max_prompt_len > 0 -- else 2; 0 for sizes the call rejects.  Host-only,
- * never fails otherwise.
- */
-int32_t bg_beam_decode_step_launches(int32_t Hq, int32_t Hkv, int32_t head_dim,
-                                     int32_t suffix_len, int32_t max_prompt_len);
 
 /*
  * Beam candidate selection of one decode step.  Source: section 1.1 of the page

@@ -259,14 +259,3 @@ def test_noalloc_host_checks_run_in_order_without_a_device():
     assert r.returncode == 0, r.stderr
     codes = [int(c) for c in r.stdout.split()]
     assert codes == [binding.BG_ERR_UNSUPPORTED, binding.BG_ERR_INVALID_ARG, binding.BG_ERR_INVALID_ARG]
-
-
-@pytest.mark.parametrize("args,expect", [
-    ((14, 2, 64, 1, 128), 1), ((14, 2, 64, 5, 500), 1), ((14, 2, 64, 6, 500), 2),   # 6 beams x t rows per warp
-    ((14, 2, 128, 1, 128), 2), ((4, 4, 64, 1, 64), 2), ((64, 1, 64, 16, 10), 1), ((32, 2, 64, 15, 9), 1),
-    ((32, 2, 64, 16, 9), 2),
-    ((14, 2, 64, 3, 0), 2),                                                          # no prompt keys anywhere
-    ((14, 2, 64, 0, 128), 0), ((14, 3, 64, 1, 128), 0), ((14, 2, 96, 1, 128), 0), ((14, 2, 64, 17, 128), 0),
-])
-def test_decode_step_launch_count(lib, args, expect):
-    assert lib.bg_beam_decode_step_launches(*args) == expect

@@ -6,11 +6,10 @@ three ways on the same seeded inputs:
   * the suffix it leaves in dst equals the oracle's explicit per-beam histories
     bit for bit;
   * the output matches the fp64 oracle within the decode tolerance;
-  * against the two separate calls (bg_beam_suffix_reorder, then
-    bg_beam_decode_attn): the suffix is bit-identical; the output is
-    bit-identical where the step runs as those two launches, and within the
-    parity tolerance where it runs in one launch (the suffix is then attended
-    on the CUDA cores in fp32, so its rounding differs).
+  * output and suffix are bit-identical to the two separate calls
+    (bg_beam_suffix_reorder, then bg_beam_decode_attn): the step's one launch
+    builds the same suffix key tiles through the parent index that the two
+    calls build by moving the suffix first.
 Both suffix buffers start as bf16 NaN, so a row read before it was written
 would poison the output."""
 import math
@@ -76,18 +75,6 @@ class Beams:
         return out
 
 
-def launches(pr, t):
-    return bg.bg_beam_decode_step_launches(pr["Hq"], pr["Hkv"], pr["head_dim"], t, pr["max_prompt_len"])
-
-
-def test_one_launch_form_covers_the_beam_configs():
-    """Both beam searches of the benchmark take the one-launch step at every suffix length."""
-    for name in ("beam_short", "beam_long"):
-        cfg = wl.DECODE_CONFIGS[name]
-        for t in range(1, cfg.steps + 1):
-            assert bg.bg_beam_decode_step_launches(cfg.Hq, cfg.Hkv, cfg.head_dim, t, 500) == 1, (name, t)
-
-
 def run_and_check(pr, suffix_max=None, requests=None, what="", against_two_call=True):
     R, W, d = pr["R"], pr["W"], pr["head_dim"]
     steps = pr["steps"]
@@ -113,11 +100,8 @@ def run_and_check(pr, suffix_max=None, requests=None, what="", against_two_call=
         assert_parity(from_dev(out)[reqs], ref, f"{what} step {s}")
         if pair is not None:
             out2 = pair.step(s)
-            if launches(pr, s + 1) == 2:
-                np.testing.assert_array_equal(bits_from_dev(out), bits_from_dev(out2),
-                                              err_msg=f"{what} step {s}: one call vs two calls")
-            else:
-                assert_parity(from_dev(out)[reqs], from_dev(out2)[reqs], f"{what} step {s}: one launch vs two")
+            np.testing.assert_array_equal(bits_from_dev(out), bits_from_dev(out2),
+                                          err_msg=f"{what} step {s}: one call vs two calls")
             np.testing.assert_array_equal(bits_from_dev(one.k[one.cur])[:, :, :s + 1],
                                           bits_from_dev(pair.k[pair.cur])[:, :, :s + 1])
             np.testing.assert_array_equal(bits_from_dev(one.v[one.cur])[:, :, :s + 1],
@@ -134,9 +118,7 @@ def test_step_small_parity(Hq, Hkv, d):
 
 
 def test_step_long_suffix():
-    # t up to BG_MAX_SUFFIX: four beams per suffix tile, many (beam, slot) rows per item; the
-    # first steps run in one launch, the later ones (t > 5 at 7 query heads per kv head) as two,
-    # each reading the suffix the other form wrote
+    # t up to BG_MAX_SUFFIX: four beams per suffix tile, many (beam, slot) rows per item
     pr = wl.make_decode_problem(2, 11, bg.BG_MAX_SUFFIX, 14, 2, 64, [70, 0])
     run_and_check(pr, suffix_max=bg.BG_MAX_SUFFIX, what="t up to 16")
 
