@@ -134,11 +134,13 @@ struct AttnCfg {
     // (__maxnreg__), which the launcher checks against the compiled kernel before every launch;
     // the TMA, MMA and gatherer warps then run with kRegsLight and the 8 softmax warps with
     // kRegsSoftmax, within the launch's total (kSplitRegs).
-    static constexpr int kRegsLaunch = FUSED ? 152 : 168;
+    // (13 warps: the register file is handed out to a CTA as if its warps were rounded up to a
+    // multiple of four, so 16 x 32 x 128 = 65,536 is the most a 416-thread CTA can launch with.)
+    static constexpr int kRegsLaunch = FUSED ? 128 : 168;
     static constexpr int kRegsLight = 64;
-    static constexpr int kRegsSoftmax = FUSED ? 200 : 216;
+    static constexpr int kRegsSoftmax = FUSED ? 168 : 216;
     static constexpr int kSplitRegs = (kThreads / 32 - 8) * 32 * kRegsLight + 8 * 32 * kRegsSoftmax;
-    static_assert(kThreads * kRegsLaunch <= 65536, "the launch must fit the register file");
+    static_assert((kThreads + 127) / 128 * 128 * kRegsLaunch <= 65536, "the launch must fit the register file");
     static_assert(kSplitRegs <= kThreads * kRegsLaunch, "register split exceeds the launch's allocation");
     static constexpr int kColO = 64 * NS * NH;
     static constexpr int kColsUsed = 64 * NS * NH + D * NH;
