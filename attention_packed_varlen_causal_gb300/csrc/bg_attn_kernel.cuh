@@ -136,10 +136,12 @@ struct AttnCfg {
     // kRegsSoftmax, within the launch's total (kSplitRegs).
     // (13 warps: the register file is handed out to a CTA as if its warps were rounded up to a
     // multiple of four, so 16 x 32 x 128 = 65,536 is the most a 416-thread CTA can launch with.)
+    // Warps 0-3 run with kRegsLight, the 8 softmax warps with kRegsSoftmax, and the gatherer warp
+    // (FUSED; it alone cannot change its allocation) keeps kRegsLaunch.
     static constexpr int kRegsLaunch = FUSED ? 128 : 168;
-    static constexpr int kRegsLight = 64;
+    static constexpr int kRegsLight = FUSED ? 48 : 64;
     static constexpr int kRegsSoftmax = FUSED ? 168 : 216;
-    static constexpr int kSplitRegs = (kThreads / 32 - 8) * 32 * kRegsLight + 8 * 32 * kRegsSoftmax;
+    static constexpr int kSplitRegs = 4 * 32 * kRegsLight + 8 * 32 * kRegsSoftmax + (FUSED ? 32 * kRegsLaunch : 0);
     static_assert((kThreads + 127) / 128 * 128 * kRegsLaunch <= 65536, "the launch must fit the register file");
     static_assert(kSplitRegs <= kThreads * kRegsLaunch, "register split exceeds the launch's allocation");
     static constexpr int kColO = 64 * NS * NH;
@@ -397,10 +399,14 @@ __global__ void __maxnreg__((AttnCfg<D, NH, NK, NV, NS, QK8, FUSED>::kRegsLaunch
         n_items = p.n_items_decode;
     }
 
-    // Each role sets its register allocation first (see AttnCfg): the softmax warps' increase is
-    // granted from the registers the other warps return.
+    // Register split (see AttnCfg).  setmaxnreg must be executed by all four warps of a warpgroup
+    // at the same instruction, so the split is made per warpgroup before the roles branch: the
+    // TMA / MMA warpgroup (warps 0-3) returns registers, the softmax warpgroups take them.  The
+    // gatherer warp of the one-launch decode step (warp 12, alone in its warpgroup) keeps its
+    // launch allocation.
+    if (warp < 4) {
+    reg_dealloc<C::kRegsLight>();
     if (warp == 0) {
-        reg_dealloc<C::kRegsLight>();
         // =============================================================== producer
         // The whole warp runs the loop (warp-uniform control flow and operands); lane 0
         // issues each copy.
@@ -477,7 +483,6 @@ __global__ void __maxnreg__((AttnCfg<D, NH, NK, NV, NS, QK8, FUSED>::kRegsLaunch
         }
         __syncwarp();
     } else if (warp == 2) {
-        reg_dealloc<C::kRegsLight>();
         // =============================================================== V producer
         const uint32_t leader = (lane == 0) ? 1u : 0u;
         const uint64_t pol_kv = l2_policy_evict_last();
@@ -518,9 +523,8 @@ __global__ void __maxnreg__((AttnCfg<D, NH, NK, NV, NS, QK8, FUSED>::kRegsLaunch
             }
         }
         __syncwarp();
-    } else if (warp == 1 || warp == 3) {
-        reg_dealloc<C::kRegsLight>();
-        // =============================================================== MMA issuers
+    } else {
+        // =============================================================== MMA issuers (warps 1, 3)
         // One thread per query tile (lane 0 of warp 1: tile 0, of warp 3: tile 1), so the two
         // tiles' QK -> softmax -> P.V chains do not wait for each other.  The thread waits on
         // the barriers itself and issues every tcgen05.mma and commit of its tile: no
@@ -596,7 +600,8 @@ __global__ void __maxnreg__((AttnCfg<D, NH, NK, NV, NS, QK8, FUSED>::kRegsLaunch
             mbar_wait_drain(mma_final, 0);
         }
         __syncwarp();
-    } else if (warp >= 4 && warp < 4 + 4 * NH) {
+    }
+    } else if (warp < 4 + 4 * NH) {
         reg_alloc<C::kRegsSoftmax>();
         // =============================================================== softmax + epilogue
         const int h = (warp - 4) >> 2;
@@ -913,7 +918,6 @@ __global__ void __maxnreg__((AttnCfg<D, NH, NK, NV, NS, QK8, FUSED>::kRegsLaunch
 
     if constexpr (FUSED) {
         if (warp == 4 + 4 * NH) {
-            reg_dealloc<C::kRegsLight>();
             // =========================================================== suffix gatherer
             // Builds every suffix key tile of the CTA's items in the K and V stages the producers
             // leave to it, straight from the previous step's buffer: row (beam b, slot s) of a tile
