@@ -924,10 +924,11 @@ __global__ void __maxnreg__((AttnCfg<D, NH, NK, NV, NS, QK8, FUSED>::kRegsLaunch
             // is slot s of beam parent[b] for s < t-1 and the step's new token for s = t-1 (the
             // reorder of the beam's suffix, gathered as it is read).  Each lane copies 16-byte
             // chunks with cp.async into the 128-byte-swizzled layout the tensor cores read (the
-            // layout a TMA tile load writes), then orders them before the MMAs' reads
-            // (fence.proxy.async) and completes the stages' full barriers.  The staged rows are
-            // then written to dst, the step's suffix: every (beam, kv head) is in exactly one
-            // suffix tile of one item, so each row of dst is written once.
+            // layout a TMA tile load writes) and orders them before the MMAs' reads
+            // (fence.proxy.async); the staged rows also go to dst, the step's suffix (every
+            // (beam, kv head) is in exactly one suffix tile of one item, so each row of dst is
+            // written once), before the stage's full barrier completes, so the stage cannot be
+            // refilled while they are read.
             constexpr int kCpr = D / 8;                  // 16-byte chunks per row
             const int t = p.suffix_len;
             TileWalker<MODE, NH> w;
@@ -939,10 +940,6 @@ __global__ void __maxnreg__((AttnCfg<D, NH, NK, NV, NS, QK8, FUSED>::kRegsLaunch
                     w.advance(p);
                     continue;
                 }
-                const int stk = n_kv % NK, stv = n_kv % NV;
-                const uint32_t usek = n_kv / NK, usev = n_kv / NV;
-                if (usek > 0 && !warp_wait(&k_empty[stk], (usek - 1) & 1, abort_flag)) break;
-                if (usev > 0 && !warp_wait(&v_empty[stv], (usev - 1) & 1, abort_flag)) break;
                 // the tile's beams: suf_bpt consecutive beams of the item, cut at the item's end
                 const int first = w.I.bt0 * p.BT + (w.j - w.I.n_prompt) * p.suf_bpt;
                 const int item_end = min(p.W, (w.I.bt0 + NH) * p.BT);
@@ -958,56 +955,63 @@ __global__ void __maxnreg__((AttnCfg<D, NH, NK, NV, NS, QK8, FUSED>::kRegsLaunch
                 const bool bad1 = t > 1 && lane + 32 < nb && (par1 < 0 || par1 >= p.W);
                 const uint32_t badm0 = __ballot_sync(0xffffffffu, bad0), badm1 = __ballot_sync(0xffffffffu, bad1);
                 if ((bad0 || bad1) && p.dev_status) atomicOr(p.dev_status, BG_DEVSTAT_PARENT);
-                uint8_t *kst = smem + C::kOffK + stk * C::kKTileBytes;
-                uint8_t *vst = smem + C::kOffV + stv * C::kTileBytes;
-                const int chunks = nb * t * kCpr;        // per tensor (K and V alike)
-                for (int base = 0; base < 2 * chunks; base += 32) {   // same trip count in every lane
-                    const int q = base + lane;
-                    const int kv = q >= chunks ? 1 : 0;
-                    const int qq = q - kv * chunks;
-                    const int row = qq / kCpr;               // beam-major: row = pos * t + s
-                    const int c = qq - row * kCpr;
-                    const int pos = row / t;
-                    const int sl = row - pos * t;
-                    const int pa = __shfl_sync(0xffffffffu, par0, pos & 31);
-                    const int pb = __shfl_sync(0xffffffffu, par1, pos & 31);
-                    if (q >= 2 * chunks) continue;
-                    const int par = pos < 32 ? pa : pb;
-                    const bool bad = ((pos < 32 ? badm0 : badm1) >> (pos & 31)) & 1u;
-                    uint8_t *to = (kv ? vst : kst) + (c >> 3) * kKVBox + row * 128 + (((c & 7) ^ (row & 7)) << 4);
-                    if (sl == t - 1) {
-                        cp_async_16(to, (kv ? sp.new_v : sp.new_k) + ((req0 + first + pos) * p.Hkv + w.I.kh) * D + c * 8);
-                    } else if (bad) {
-                        *reinterpret_cast<uint4 *>(to) = make_uint4(0, 0, 0, 0);
-                    } else {
-                        cp_async_16(to, (kv ? sp.src_v : sp.src_k) +
-                                            (((req0 + par) * sp.suffix_max + sl) * p.Hkv + w.I.kh) * D + c * 8);
+                const int chunks = nb * t * kCpr;
+                // K first, then V, each like its TMA producer: wait for the stage, fill it, write
+                // its rows to dst, then complete the stage's full barrier.  (V's stage may be freed
+                // only by this tile's own scores, which need its K, so V must not hold K back.)
+                bool ok = true;
+#pragma unroll 1
+                for (int kv = 0; kv < 2 && ok; ++kv) {
+                    const int st = kv ? static_cast<int>(n_kv % NV) : static_cast<int>(n_kv % NK);
+                    const uint32_t use = kv ? n_kv / NV : n_kv / NK;
+                    uint64_t *empty = kv ? &v_empty[st] : &k_empty[st];
+                    uint64_t *full = kv ? &v_full[st] : &k_full[st];
+                    if (use > 0 && !warp_wait(empty, (use - 1) & 1, abort_flag)) {
+                        ok = false;
+                        break;
                     }
+                    uint8_t *stage = kv ? smem + C::kOffV + st * C::kTileBytes : smem + C::kOffK + st * C::kKTileBytes;
+                    const __nv_bfloat16 *src = kv ? sp.src_v : sp.src_k;
+                    const __nv_bfloat16 *nw = kv ? sp.new_v : sp.new_k;
+                    __nv_bfloat16 *dst = kv ? sp.dst_v : sp.dst_k;
+                    for (int base = 0; base < chunks; base += 32) {   // same trip count in every lane
+                        const int q = base + lane;
+                        const int row = q / kCpr;                // beam-major: row = pos * t + s
+                        const int c = q - row * kCpr;
+                        const int pos = row / t;
+                        const int sl = row - pos * t;
+                        const int pa = __shfl_sync(0xffffffffu, par0, pos & 31);
+                        const int pb = __shfl_sync(0xffffffffu, par1, pos & 31);
+                        if (q >= chunks) continue;
+                        const int par = pos < 32 ? pa : pb;
+                        const bool bad = ((pos < 32 ? badm0 : badm1) >> (pos & 31)) & 1u;
+                        uint8_t *to = stage + (c >> 3) * kKVBox + row * 128 + (((c & 7) ^ (row & 7)) << 4);
+                        if (sl == t - 1)
+                            cp_async_16(to, nw + ((req0 + first + pos) * p.Hkv + w.I.kh) * D + c * 8);
+                        else if (bad)
+                            *reinterpret_cast<uint4 *>(to) = make_uint4(0, 0, 0, 0);
+                        else
+                            cp_async_16(to, src + (((req0 + par) * sp.suffix_max + sl) * p.Hkv + w.I.kh) * D + c * 8);
+                    }
+                    cp_async_commit();
+                    cp_async_wait_all();
+                    fence_proxy_async_smem();            // generic-proxy writes -> the tensor cores' reads
+                    __syncwarp();
+                    // the step's suffix, from the staged rows (beams with a bad parent left untouched)
+                    for (int q = lane; q < chunks; q += 32) {
+                        const int row = q / kCpr;
+                        const int c = q - row * kCpr;
+                        const int pos = row / t;
+                        const int sl = row - pos * t;
+                        if (((pos < 32 ? badm0 : badm1) >> (pos & 31)) & 1u) continue;
+                        const uint8_t *from = stage + (c >> 3) * kKVBox + row * 128 + (((c & 7) ^ (row & 7)) << 4);
+                        *reinterpret_cast<uint4 *>(dst + (((req0 + first + pos) * sp.suffix_max + sl) * p.Hkv + w.I.kh) * D +
+                                                   c * 8) = *reinterpret_cast<const uint4 *>(from);
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(full);
                 }
-                cp_async_commit();
-                cp_async_wait_all();
-                fence_proxy_async_smem();                // generic-proxy writes -> the tensor cores' reads
-                __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(&k_full[stk]);
-                    mbar_arrive(&v_full[stv]);
-                }
-                // the step's suffix, from the staged rows (beams with a bad parent left untouched)
-                for (int base = 0; base < 2 * chunks; base += 32) {
-                    const int q = base + lane;
-                    if (q >= 2 * chunks) continue;
-                    const int kv = q >= chunks ? 1 : 0;
-                    const int qq = q - kv * chunks;
-                    const int row = qq / kCpr;
-                    const int c = qq - row * kCpr;
-                    const int pos = row / t;
-                    const int sl = row - pos * t;
-                    if (((pos < 32 ? badm0 : badm1) >> (pos & 31)) & 1u) continue;
-                    const uint8_t *from = (kv ? vst : kst) + (c >> 3) * kKVBox + row * 128 + (((c & 7) ^ (row & 7)) << 4);
-                    __nv_bfloat16 *to = (kv ? sp.dst_v : sp.dst_k) +
-                                        (((req0 + first + pos) * sp.suffix_max + sl) * p.Hkv + w.I.kh) * D + c * 8;
-                    *reinterpret_cast<uint4 *>(to) = *reinterpret_cast<const uint4 *>(from);
-                }
+                if (!ok) break;
                 ++n_kv;
                 w.advance(p);
             }
