@@ -125,7 +125,8 @@ struct AttnCfg {
     static constexpr int kOffBar = kOffStage + 4 * NH * kStageBytes;
     // q_full[2] q_empty[2] mma_final k_full[NK] k_empty[NK] v_full[NV] v_empty[NV] s_full[NH][NS]
     // p_full[NH][NS] pv_done[NH][NS] o_staged[NH][2]
-    static constexpr int kNumBars = 5 + 2 * NK + 2 * NV + 3 * NS * NH + 2 * NH;
+    // FUSED adds suf_go_k[NK] and suf_go_v[NV]: a producer hands a stage to the gatherer
+    static constexpr int kNumBars = 5 + 2 * NK + 2 * NV + 3 * NS * NH + 2 * NH + (FUSED ? NK + NV : 0);
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + slack for 1024-byte alignment
     // FUSED: one more warp (the suffix gatherer) after the softmax warpgroups
@@ -334,6 +335,13 @@ __global__ void __maxnreg__((AttnCfg<D, NH, NK, NV, NS, QK8, FUSED>::kRegsLaunch
     // of the item after next, whose Q load waits for the buffer this tile leaves from.  The second
     // barrier per group keeps consecutive phases apart all the same.
     uint64_t *o_staged = pv_done + NS * NH;   // [NH][2]
+    // FUSED: suf_go_k[s] / suf_go_v[s] complete a phase when the K / V producer, having waited for
+    // stage s to be free for a suffix tile (its own wait, so its phase tracking stays exact), hands
+    // the stage to the gatherer instead of loading it.  A producer cannot hand the same stage over
+    // again before the gatherer has filled it and it has been consumed and freed, so every gatherer
+    // wait on them is for the phase right after the last one it saw.
+    uint64_t *suf_go_k = o_staged + 2 * NH;   // [NK]
+    uint64_t *suf_go_v = suf_go_k + NK;       // [NV]
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
 
@@ -361,6 +369,10 @@ __global__ void __maxnreg__((AttnCfg<D, NH, NK, NV, NS, QK8, FUSED>::kRegsLaunch
             mbar_init(&pv_done[i], 1);
         }
         for (int i = 0; i < 2 * NH; ++i) mbar_init(&o_staged[i], 4);   // one arrive per warp
+        if constexpr (FUSED) {
+            for (int i = 0; i < NK; ++i) mbar_init(&suf_go_k[i], 1);
+            for (int i = 0; i < NV; ++i) mbar_init(&suf_go_v[i], 1);
+        }
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -442,15 +454,16 @@ __global__ void __maxnreg__((AttnCfg<D, NH, NK, NV, NS, QK8, FUSED>::kRegsLaunch
                                           w.I.r * p.W + (w.I.bt0 + h) * p.BT, pol_q);
                 }
             }
+            const int st = n_kv % NK;
+            const uint32_t use = n_kv / NK;
+            if (use > 0 && !warp_wait(&k_empty[st], (use - 1) & 1, abort_flag)) break;
             if (FUSED && MODE == Mode::Decode && w.j >= w.I.n_prompt) {
-                // a suffix tile: the gatherer warp fills this stage
+                // a suffix tile: the stage is free, the gatherer warp fills it
+                if (lane == 0) mbar_arrive(&suf_go_k[st]);
                 ++n_kv;
                 w.advance(p);
                 continue;
             }
-            const int st = n_kv % NK;
-            const uint32_t use = n_kv / NK;
-            if (use > 0 && !warp_wait(&k_empty[st], (use - 1) & 1, abort_flag)) break;
             uint8_t *kdst = smem + C::kOffK + st * C::kKTileBytes;
             if (MODE == Mode::Prefill || w.j < w.I.n_prompt) {
                 const int row = w.I.kv_row0 + w.j * kKeys;
@@ -491,14 +504,16 @@ __global__ void __maxnreg__((AttnCfg<D, NH, NK, NV, NS, QK8, FUSED>::kRegsLaunch
         w.first(p, n_items);
         uint32_t n_v = 0;
         while (w.valid) {
-            if (FUSED && MODE == Mode::Decode && w.j >= w.I.n_prompt) {
-                ++n_v;                          // a suffix tile: filled by the gatherer warp
-                w.advance(p);
-                continue;
-            }
             const int st = n_v % NV;
             const uint32_t use = n_v / NV;
             if (use > 0 && !warp_wait(&v_empty[st], (use - 1) & 1, abort_flag)) break;
+            if (FUSED && MODE == Mode::Decode && w.j >= w.I.n_prompt) {
+                // a suffix tile: the stage is free, the gatherer warp fills it
+                if (lane == 0) mbar_arrive(&suf_go_v[st]);
+                ++n_v;
+                w.advance(p);
+                continue;
+            }
             uint8_t *vdst = smem + C::kOffV + st * C::kTileBytes;
             if (MODE == Mode::Prefill || w.j < w.I.n_prompt) {
                 const int row = w.I.kv_row0 + w.j * kKeys;
@@ -922,7 +937,10 @@ __global__ void __maxnreg__((AttnCfg<D, NH, NK, NV, NS, QK8, FUSED>::kRegsLaunch
             // Builds every suffix key tile of the CTA's items in the K and V stages the producers
             // leave to it, straight from the previous step's buffer: row (beam b, slot s) of a tile
             // is slot s of beam parent[b] for s < t-1 and the step's new token for s = t-1 (the
-            // reorder of the beam's suffix, gathered as it is read).  Each lane copies 16-byte
+            // reorder of the beam's suffix, gathered as it is read).  The producers still wait for
+            // each such stage to be free and then hand it over (suf_go_k / suf_go_v); the
+            // gatherer waits only on those hand-overs, never on the empty barriers, whose phases
+            // it would not all see.  Each lane copies 16-byte
             // chunks with cp.async into the 128-byte-swizzled layout the tensor cores read (the
             // layout a TMA tile load writes) and orders them before the MMAs' reads
             // (fence.proxy.async); the staged rows also go to dst, the step's suffix (every
@@ -934,6 +952,7 @@ __global__ void __maxnreg__((AttnCfg<D, NH, NK, NV, NS, QK8, FUSED>::kRegsLaunch
             TileWalker<MODE, NH> w;
             w.first(p, n_items);
             uint32_t n_kv = 0;
+            uint32_t go_phase = 0;   // bit s: phase parity the next wait on suf_go_k[s] (bit 16 + s: suf_go_v[s]) expects
             while (w.valid) {
                 if (w.j < w.I.n_prompt) {
                     ++n_kv;
@@ -963,13 +982,14 @@ __global__ void __maxnreg__((AttnCfg<D, NH, NK, NV, NS, QK8, FUSED>::kRegsLaunch
 #pragma unroll 1
                 for (int kv = 0; kv < 2 && ok; ++kv) {
                     const int st = kv ? static_cast<int>(n_kv % NV) : static_cast<int>(n_kv % NK);
-                    const uint32_t use = kv ? n_kv / NV : n_kv / NK;
-                    uint64_t *empty = kv ? &v_empty[st] : &k_empty[st];
+                    uint64_t *go = kv ? &suf_go_v[st] : &suf_go_k[st];
                     uint64_t *full = kv ? &v_full[st] : &k_full[st];
-                    if (use > 0 && !warp_wait(empty, (use - 1) & 1, abort_flag)) {
+                    const uint32_t bit = 1u << (st + (kv ? 16 : 0));
+                    if (!warp_wait(go, (go_phase & bit) ? 1u : 0u, abort_flag)) {
                         ok = false;
                         break;
                     }
+                    go_phase ^= bit;
                     uint8_t *stage = kv ? smem + C::kOffV + st * C::kTileBytes : smem + C::kOffK + st * C::kKTileBytes;
                     const __nv_bfloat16 *src = kv ? sp.src_v : sp.src_k;
                     const __nv_bfloat16 *nw = kv ? sp.new_v : sp.new_k;
