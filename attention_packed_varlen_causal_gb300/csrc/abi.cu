@@ -418,7 +418,7 @@ bg_status_t decode_impl(const void *q, const void *prompt_k, const void *prompt_
     p.suf_tx = (head_dim / 64) * 128 * t_suf * bpt;
     p.n_items_decode = static_cast<int32_t>(items);
     const int grid = static_cast<int>(items < nsm ? items : nsm);
-    if (fz) {
+    if (fz && decode_step_one_launch(head_dim)) {
         // one launch: a gatherer warp of the attention kernel builds each suffix key tile from
         // the previous step's suffix through the parent index and writes the step's suffix
         StepParams sp;
@@ -434,6 +434,16 @@ bg_status_t decode_impl(const void *q, const void *prompt_k, const void *prompt_
         if (launch_decode_step_fused(head_dim, tm_q, tm_k, tm_v, tm_o, p, sp, grid, stream) != cudaSuccess)
             return BG_ERR_CUDA;
         return BG_OK;
+    }
+    if (fz) {
+        // two launches: the step's reorder + append first (it moves nothing at t = 1 and then
+        // never reads src), then the attention over the new suffix
+        const void *sk = fz->src_k ? fz->src_k : suffix_k;
+        const void *sv = fz->src_v ? fz->src_v : suffix_v;
+        if (launch_suffix_reorder(sk, sv, const_cast<void *>(suffix_k), const_cast<void *>(suffix_v), fz->parent,
+                                  fz->new_k, fz->new_v, R, W, suffix_max, suffix_len - 1, Hkv, head_dim, dev_status,
+                                  stream) != cudaSuccess)
+            return BG_ERR_CUDA;
     }
     if (launch_decode_attn(head_dim, tm_q, tm_k, tm_v, tm_sk, tm_sv, tm_o, p, grid, stream) != cudaSuccess)
         return BG_ERR_CUDA;

@@ -122,7 +122,10 @@ struct AttnCfg {
     static constexpr int kOffStage = kOffV + NV * kTileBytes;     // 2 KB per softmax warp
     static_assert(!QK8 || D == 128, "E4M3 Q/K rows are one 128-byte column block (head_dim 128)");
     static constexpr int kStageBytes = 32 * 64;
-    static constexpr int kOffBar = kOffStage + 4 * NH * kStageBytes;
+    // FUSED: the gatherer's two private staging tiles (K and V each, in the ring's layout)
+    static constexpr int kOffGather = kOffStage + 4 * NH * kStageBytes;
+    static constexpr int kGatherBytes = FUSED ? 2 * (kKTileBytes + kTileBytes) : 0;
+    static constexpr int kOffBar = kOffGather + kGatherBytes;
     // q_full[2] q_empty[2] mma_final k_full[NK] k_empty[NK] v_full[NV] v_empty[NV] s_full[NH][NS]
     // p_full[NH][NS] pv_done[NH][NS] o_staged[NH][2]
     // FUSED adds suf_go_k[NK] and suf_go_v[NV]: a producer hands a stage to the gatherer
@@ -380,8 +383,10 @@ __global__ void __maxnreg__((AttnCfg<D, NH, NK, NV, NS, QK8, FUSED>::kRegsLaunch
         // Decode query tiles fill only BT*g <= 128 rows and suffix key tiles only suf_bpt*t
         // <= 64 rows; the rows past them keep what an earlier tile left (finite) or these
         // zeros, so the masked columns they feed multiply finite values only.
+        // (FUSED: the gatherer's staging tiles too: a stage copy moves all 64 rows of a tile)
         uint4 *z4 = reinterpret_cast<uint4 *>(smem + C::kOffQ);
-        for (int i = threadIdx.x; i < C::kOffStage / 16; i += blockDim.x) z4[i] = make_uint4(0, 0, 0, 0);
+        constexpr int kZeroEnd = FUSED ? C::kOffBar : C::kOffStage;
+        for (int i = threadIdx.x; i < kZeroEnd / 16; i += blockDim.x) z4[i] = make_uint4(0, 0, 0, 0);
         fence_proxy_async_smem();
     }
     if (warp == 1) {
@@ -937,103 +942,149 @@ __global__ void __maxnreg__((AttnCfg<D, NH, NK, NV, NS, QK8, FUSED>::kRegsLaunch
             // Builds every suffix key tile of the CTA's items in the K and V stages the producers
             // leave to it, straight from the previous step's buffer: row (beam b, slot s) of a tile
             // is slot s of beam parent[b] for s < t-1 and the step's new token for s = t-1 (the
-            // reorder of the beam's suffix, gathered as it is read).  The producers still wait for
-            // each such stage to be free and then hand it over (suf_go_k / suf_go_v); the
-            // gatherer waits only on those hand-overs, never on the empty barriers, whose phases
-            // it would not all see.  Each lane copies 16-byte
-            // chunks with cp.async into the 128-byte-swizzled layout the tensor cores read (the
-            // layout a TMA tile load writes) and orders them before the MMAs' reads
-            // (fence.proxy.async); the staged rows also go to dst, the step's suffix (every
-            // (beam, kv head) is in exactly one suffix tile of one item, so each row of dst is
-            // written once), before the stage's full barrier completes, so the stage cannot be
-            // refilled while they are read.
+            // reorder of the beam's suffix, gathered as it is read).  Each lane copies 16-byte
+            // chunks with cp.async into one of two private staging tiles laid out as the ring's
+            // stages are (128-byte swizzle, the layout a TMA tile load writes), one suffix tile
+            // ahead, so the gather's memory latency stays off the pipeline.  The producers still
+            // wait for each suffix tile's stage to be free and then hand it over (suf_go_k /
+            // suf_go_v); the gatherer waits only on those hand-overs, never on the empty barriers,
+            // whose phases it would not all see.  A hand-over is served by a shared-to-shared copy
+            // ordered before the MMAs' reads (fence.proxy.async) and the stage's full barrier.  The
+            // staged rows then go to dst, the step's suffix: every (beam, kv head) is in exactly
+            // one suffix tile of one item, so each row of dst is written once.
             constexpr int kCpr = D / 8;                  // 16-byte chunks per row
             const int t = p.suffix_len;
-            TileWalker<MODE, NH> w;
-            w.first(p, n_items);
-            uint32_t n_kv = 0;
-            uint32_t go_phase = 0;   // bit s: phase parity the next wait on suf_go_k[s] (bit 16 + s: suf_go_v[s]) expects
-            while (w.valid) {
-                if (w.j < w.I.n_prompt) {
+            // One suffix tile: its place in the walk and the beams it holds.
+            struct SufTile {
+                bool valid;
+                uint32_t n;          // global tile number (picks the K and V stages)
+                int r, kh, first, nb;
+            };
+            // Walks the CTA's tiles to the next suffix tile (the same walk the producers make).
+            auto next_suffix = [&](TileWalker<MODE, NH> &w, uint32_t &n_kv) -> SufTile {
+                SufTile T{false, 0, 0, 0, 0, 0};
+                while (w.valid && w.j < w.I.n_prompt) {
                     ++n_kv;
                     w.advance(p);
-                    continue;
                 }
-                // the tile's beams: suf_bpt consecutive beams of the item, cut at the item's end
-                const int first = w.I.bt0 * p.BT + (w.j - w.I.n_prompt) * p.suf_bpt;
-                const int item_end = min(p.W, (w.I.bt0 + NH) * p.BT);
-                const int nb = min(p.suf_bpt, item_end - first);
-                const int64_t req0 = static_cast<int64_t>(w.I.r) * p.W;
-                // parents of the tile's beams (at most 64): lane i holds those of beams i and 32 + i
+                if (!w.valid) return T;
+                T.valid = true;
+                T.n = n_kv;
+                T.r = w.I.r;
+                T.kh = w.I.kh;
+                T.first = w.I.bt0 * p.BT + (w.j - w.I.n_prompt) * p.suf_bpt;
+                T.nb = min(p.suf_bpt, min(p.W, (w.I.bt0 + NH) * p.BT) - T.first);
+                ++n_kv;
+                w.advance(p);
+                return T;
+            };
+            // Gathers tile T's K and V rows into private staging buffer `buf` (cp.async, one
+            // commit group).  Returns the mask pair of beams with a bad parent (zero rows).
+            auto gather = [&](const SufTile &T, int buf, uint32_t &badm0, uint32_t &badm1) {
+                const int64_t req0 = static_cast<int64_t>(T.r) * p.W;
                 int par0 = 0, par1 = 0;
                 if (t > 1) {
-                    if (lane < nb) par0 = sp.parent[req0 + first + lane];
-                    if (lane + 32 < nb) par1 = sp.parent[req0 + first + 32 + lane];
+                    if (lane < T.nb) par0 = sp.parent[req0 + T.first + lane];
+                    if (lane + 32 < T.nb) par1 = sp.parent[req0 + T.first + 32 + lane];
                 }
-                const bool bad0 = t > 1 && lane < nb && (par0 < 0 || par0 >= p.W);
-                const bool bad1 = t > 1 && lane + 32 < nb && (par1 < 0 || par1 >= p.W);
-                const uint32_t badm0 = __ballot_sync(0xffffffffu, bad0), badm1 = __ballot_sync(0xffffffffu, bad1);
+                const bool bad0 = t > 1 && lane < T.nb && (par0 < 0 || par0 >= p.W);
+                const bool bad1 = t > 1 && lane + 32 < T.nb && (par1 < 0 || par1 >= p.W);
+                badm0 = __ballot_sync(0xffffffffu, bad0);
+                badm1 = __ballot_sync(0xffffffffu, bad1);
                 if ((bad0 || bad1) && p.dev_status) atomicOr(p.dev_status, BG_DEVSTAT_PARENT);
-                const int chunks = nb * t * kCpr;
-                // K first, then V, each like its TMA producer: wait for the stage, fill it, write
-                // its rows to dst, then complete the stage's full barrier.  (V's stage may be freed
-                // only by this tile's own scores, which need its K, so V must not hold K back.)
-                bool ok = true;
-#pragma unroll 1
-                for (int kv = 0; kv < 2 && ok; ++kv) {
-                    const int st = kv ? static_cast<int>(n_kv % NV) : static_cast<int>(n_kv % NK);
+                uint8_t *stg = smem + C::kOffGather + buf * (C::kKTileBytes + C::kTileBytes);
+                const int chunks = T.nb * t * kCpr;       // per tensor
+                for (int base = 0; base < 2 * chunks; base += 32) {   // same trip count in every lane
+                    const int q = base + lane;
+                    const int kv = q >= chunks ? 1 : 0;
+                    const int qq = q - kv * chunks;
+                    const int row = qq / kCpr;           // beam-major: row = pos * t + s
+                    const int c = qq - row * kCpr;
+                    const int pos = row / t;
+                    const int sl = row - pos * t;
+                    const int pa = __shfl_sync(0xffffffffu, par0, pos & 31);
+                    const int pb = __shfl_sync(0xffffffffu, par1, pos & 31);
+                    if (q >= 2 * chunks) continue;
+                    const int par = pos < 32 ? pa : pb;
+                    const bool bad = ((pos < 32 ? badm0 : badm1) >> (pos & 31)) & 1u;
+                    uint8_t *to = stg + kv * C::kKTileBytes + (c >> 3) * kKVBox + row * 128 + (((c & 7) ^ (row & 7)) << 4);
+                    if (sl == t - 1)
+                        cp_async_16(to, (kv ? sp.new_v : sp.new_k) + ((req0 + T.first + pos) * p.Hkv + T.kh) * D + c * 8);
+                    else if (bad)
+                        *reinterpret_cast<uint4 *>(to) = make_uint4(0, 0, 0, 0);
+                    else
+                        cp_async_16(to, (kv ? sp.src_v : sp.src_k) +
+                                            (((req0 + par) * sp.suffix_max + sl) * p.Hkv + T.kh) * D + c * 8);
+                }
+                cp_async_commit();
+            };
+            TileWalker<MODE, NH> wn;         // walks one suffix tile ahead of the one delivered
+            wn.first(p, n_items);
+            uint32_t nn = 0;
+            uint32_t go_phase = 0;   // bit s: parity the next wait on suf_go_k[s] expects (bit 16 + s: suf_go_v[s])
+            uint32_t bad_c0 = 0, bad_c1 = 0, bad_n0 = 0, bad_n1 = 0;
+            SufTile cur = next_suffix(wn, nn);
+            if (cur.valid) gather(cur, 0, bad_c0, bad_c1);
+            int buf = 0;
+            bool ok = true;
+            while (cur.valid && ok) {
+                // prefetch the next suffix tile into the other buffer while this one is delivered
+                const SufTile nxt = next_suffix(wn, nn);
+                if (nxt.valid) gather(nxt, buf ^ 1, bad_n0, bad_n1);
+                // this tile's copies (the older group) have landed
+                if (nxt.valid)
+                    asm volatile("cp.async.wait_group 1;" ::: "memory");
+                else
+                    cp_async_wait_all();
+                __syncwarp();
+                const uint8_t *stg = smem + C::kOffGather + buf * (C::kKTileBytes + C::kTileBytes);
+                // deliver K, then V, each when its producer hands the ring stage over: a copy
+                // between shared-memory tiles of the same layout, ordered before the tensor cores'
+                // reads, then the stage's full barrier.  (K goes first: with two V stages and two
+                // score buffers V's stage is freed only by this tile's own scores.)
+                for (int kv = 0; kv < 2; ++kv) {
+                    const int st = kv ? static_cast<int>(cur.n % NV) : static_cast<int>(cur.n % NK);
                     uint64_t *go = kv ? &suf_go_v[st] : &suf_go_k[st];
-                    uint64_t *full = kv ? &v_full[st] : &k_full[st];
                     const uint32_t bit = 1u << (st + (kv ? 16 : 0));
                     if (!warp_wait(go, (go_phase & bit) ? 1u : 0u, abort_flag)) {
                         ok = false;
                         break;
                     }
                     go_phase ^= bit;
+                    const int bytes = kv ? C::kTileBytes : C::kKTileBytes;
                     uint8_t *stage = kv ? smem + C::kOffV + st * C::kTileBytes : smem + C::kOffK + st * C::kKTileBytes;
-                    const __nv_bfloat16 *src = kv ? sp.src_v : sp.src_k;
-                    const __nv_bfloat16 *nw = kv ? sp.new_v : sp.new_k;
-                    __nv_bfloat16 *dst = kv ? sp.dst_v : sp.dst_k;
-                    for (int base = 0; base < chunks; base += 32) {   // same trip count in every lane
-                        const int q = base + lane;
-                        const int row = q / kCpr;                // beam-major: row = pos * t + s
-                        const int c = q - row * kCpr;
-                        const int pos = row / t;
-                        const int sl = row - pos * t;
-                        const int pa = __shfl_sync(0xffffffffu, par0, pos & 31);
-                        const int pb = __shfl_sync(0xffffffffu, par1, pos & 31);
-                        if (q >= chunks) continue;
-                        const int par = pos < 32 ? pa : pb;
-                        const bool bad = ((pos < 32 ? badm0 : badm1) >> (pos & 31)) & 1u;
-                        uint8_t *to = stage + (c >> 3) * kKVBox + row * 128 + (((c & 7) ^ (row & 7)) << 4);
-                        if (sl == t - 1)
-                            cp_async_16(to, nw + ((req0 + first + pos) * p.Hkv + w.I.kh) * D + c * 8);
-                        else if (bad)
-                            *reinterpret_cast<uint4 *>(to) = make_uint4(0, 0, 0, 0);
-                        else
-                            cp_async_16(to, src + (((req0 + par) * sp.suffix_max + sl) * p.Hkv + w.I.kh) * D + c * 8);
-                    }
-                    cp_async_commit();
-                    cp_async_wait_all();
+                    const uint4 *from = reinterpret_cast<const uint4 *>(stg + kv * C::kKTileBytes);
+                    uint4 *to = reinterpret_cast<uint4 *>(stage);
+                    for (int i = lane; i < bytes / 16; i += 32) to[i] = from[i];
                     fence_proxy_async_smem();            // generic-proxy writes -> the tensor cores' reads
                     __syncwarp();
-                    // the step's suffix, from the staged rows (beams with a bad parent left untouched)
-                    for (int q = lane; q < chunks; q += 32) {
-                        const int row = q / kCpr;
-                        const int c = q - row * kCpr;
-                        const int pos = row / t;
-                        const int sl = row - pos * t;
-                        if (((pos < 32 ? badm0 : badm1) >> (pos & 31)) & 1u) continue;
-                        const uint8_t *from = stage + (c >> 3) * kKVBox + row * 128 + (((c & 7) ^ (row & 7)) << 4);
-                        *reinterpret_cast<uint4 *>(dst + (((req0 + first + pos) * sp.suffix_max + sl) * p.Hkv + w.I.kh) * D +
-                                                   c * 8) = *reinterpret_cast<const uint4 *>(from);
-                    }
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(full);
+                    if (lane == 0) mbar_arrive(kv ? &v_full[st] : &k_full[st]);
                 }
                 if (!ok) break;
-                ++n_kv;
-                w.advance(p);
+                // the step's suffix, from the staged rows (beams with a bad parent left untouched)
+                {
+                    const int64_t req0 = static_cast<int64_t>(cur.r) * p.W;
+                    const int chunks = cur.nb * t * kCpr;
+                    for (int q = lane; q < 2 * chunks; q += 32) {
+                        const int kv = q >= chunks ? 1 : 0;
+                        const int qq = q - kv * chunks;
+                        const int row = qq / kCpr;
+                        const int c = qq - row * kCpr;
+                        const int pos = row / t;
+                        const int sl = row - pos * t;
+                        if (((pos < 32 ? bad_c0 : bad_c1) >> (pos & 31)) & 1u) continue;
+                        const uint8_t *from = stg + kv * C::kKTileBytes + (c >> 3) * kKVBox + row * 128 +
+                                              (((c & 7) ^ (row & 7)) << 4);
+                        __nv_bfloat16 *dst = kv ? sp.dst_v : sp.dst_k;
+                        *reinterpret_cast<uint4 *>(dst + (((req0 + cur.first + pos) * sp.suffix_max + sl) * p.Hkv + cur.kh) * D +
+                                                   c * 8) = *reinterpret_cast<const uint4 *>(from);
+                    }
+                }
+                __syncwarp();                            // the buffer is read before it is refilled
+                cur = nxt;
+                bad_c0 = bad_n0;
+                bad_c1 = bad_n1;
+                buf ^= 1;
             }
             cp_async_wait_all();
             __syncwarp();

@@ -43,7 +43,9 @@ cudaError_t launch_decode_attn(int head_dim, const CUtensorMap &tm_q, const CUte
                                const CUtensorMap &tm_o, const AttnParams &p, int grid, cudaStream_t stream);
 int decode_tiles_per_cta();
 // The one-launch decode step: the attention kernel with a gatherer warp that builds the suffix
-// key tiles through the parent index and writes the step's suffix.
+// key tiles through the parent index and writes the step's suffix (head_dim 64; the head_dim 128
+// kernel has no shared memory left for the gatherer's staging, its step is reorder + attention).
+bool decode_step_one_launch(int head_dim);
 cudaError_t launch_decode_step_fused(int head_dim, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
                                      const CUtensorMap &tm_v, const CUtensorMap &tm_o, const AttnParams &p,
                                      const StepParams &sp, int grid, cudaStream_t stream);

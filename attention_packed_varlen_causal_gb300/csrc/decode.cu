@@ -61,8 +61,10 @@ cudaError_t launch_decode_step_fused(int head_dim, const CUtensorMap &tm_q, cons
                                      const StepParams &sp, int grid, cudaStream_t stream)
 {
     if (head_dim == 64) return launch_one<64, 4, 4, 3, true>(tm_q, tm_k, tm_v, tm_q, tm_q, tm_o, p, sp, grid, stream);
-    if (head_dim == 128) return launch_one<128, 3, 2, 2, true>(tm_q, tm_k, tm_v, tm_q, tm_q, tm_o, p, sp, grid, stream);
-    return cudaErrorInvalidValue;
+    return cudaErrorInvalidValue;   // head_dim 128: no shared memory left for the gatherer's staging
 }
+
+bool decode_step_one_launch(int head_dim) { return head_dim == 64; }
+
 
 }  // namespace bg
