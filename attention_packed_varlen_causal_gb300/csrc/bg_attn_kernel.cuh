@@ -122,10 +122,14 @@ struct AttnCfg {
     static constexpr int kOffStage = kOffV + NV * kTileBytes;     // 2 KB per softmax warp
     static_assert(!QK8 || D == 128, "E4M3 Q/K rows are one 128-byte column block (head_dim 128)");
     static constexpr int kStageBytes = 32 * 64;
-    // FUSED: the gatherer's two private staging tiles (K and V each, in the ring's layout)
+    // FUSED: the gatherer's kGatherBufs private staging tiles (K and V each, in the ring's
+    // layout), then per buffer the tile's record (8 int32: stage number, request, kv head, first
+    // beam, beams, bad-parent masks)
+    static constexpr int kGatherBufs = 4;
     static constexpr int kOffGather = kOffStage + 4 * NH * kStageBytes;
-    static constexpr int kGatherBytes = FUSED ? 2 * (kKTileBytes + kTileBytes) : 0;
-    static constexpr int kOffBar = kOffGather + kGatherBytes;
+    static constexpr int kGatherBytes = FUSED ? kGatherBufs * (kKTileBytes + kTileBytes) : 0;
+    static constexpr int kOffGatherRec = kOffGather + kGatherBytes;
+    static constexpr int kOffBar = kOffGatherRec + (FUSED ? kGatherBufs * 32 : 0);
     // q_full[2] q_empty[2] mma_final k_full[NK] k_empty[NK] v_full[NV] v_empty[NV] s_full[NH][NS]
     // p_full[NH][NS] pv_done[NH][NS] o_staged[NH][2]
     // FUSED adds suf_go_k[NK] and suf_go_v[NV]: a producer hands a stage to the gatherer
@@ -954,46 +958,58 @@ __global__ void __maxnreg__((AttnCfg<D, NH, NK, NV, NS, QK8, FUSED>::kRegsLaunch
             // one suffix tile of one item, so each row of dst is written once.
             constexpr int kCpr = D / 8;                  // 16-byte chunks per row
             const int t = p.suffix_len;
-            // One suffix tile: its place in the walk and the beams it holds.
-            struct SufTile {
-                bool valid;
-                uint32_t n;          // global tile number (picks the K and V stages)
-                int r, kh, first, nb;
-            };
-            // Walks the CTA's tiles to the next suffix tile (the same walk the producers make).
-            auto next_suffix = [&](TileWalker<MODE, NH> &w, uint32_t &n_kv) -> SufTile {
-                SufTile T{false, 0, 0, 0, 0, 0};
-                while (w.valid && w.j < w.I.n_prompt) {
-                    ++n_kv;
-                    w.advance(p);
+            // A pipeline over the CTA's suffix tiles, in walk order: tile i is delivered while
+            // the data of tiles i+1 .. i+B-1 (B = kGatherBufs) is in flight into their staging
+            // buffers and the parents of tile i+B are loading into registers, so neither the
+            // parents' nor the rows' memory latency waits in front of a delivery.
+            constexpr int B = C::kGatherBufs;
+            int32_t *rec_base = reinterpret_cast<int32_t *>(smem + C::kOffGatherRec);   // [B][8]
+            TileWalker<MODE, NH> wn;     // the next suffix tile to prefetch
+            wn.first(p, n_items);
+            uint32_t nn = 0;
+            // Moves wn to the next suffix tile; returns false at the end of the walk.
+            auto advance_to_suffix = [&]() -> bool {
+                while (wn.valid && wn.j < wn.I.n_prompt) {
+                    ++nn;
+                    wn.advance(p);
                 }
-                if (!w.valid) return T;
-                T.valid = true;
-                T.n = n_kv;
-                T.r = w.I.r;
-                T.kh = w.I.kh;
-                T.first = w.I.bt0 * p.BT + (w.j - w.I.n_prompt) * p.suf_bpt;
-                T.nb = min(p.suf_bpt, min(p.W, (w.I.bt0 + NH) * p.BT) - T.first);
-                ++n_kv;
-                w.advance(p);
-                return T;
+                return wn.valid;
             };
-            // Gathers tile T's K and V rows into private staging buffer `buf` (cp.async, one
-            // commit group).  Returns the mask pair of beams with a bad parent (zero rows).
-            auto gather = [&](const SufTile &T, int buf, uint32_t &badm0, uint32_t &badm1) {
-                const int64_t req0 = static_cast<int64_t>(T.r) * p.W;
-                int par0 = 0, par1 = 0;
+            // The parents of the suffix tile at wn (plain loads: they land while other work runs).
+            auto load_parents = [&](int &pa0, int &pa1) {
+                pa0 = 0;
+                pa1 = 0;
                 if (t > 1) {
-                    if (lane < T.nb) par0 = sp.parent[req0 + T.first + lane];
-                    if (lane + 32 < T.nb) par1 = sp.parent[req0 + T.first + 32 + lane];
+                    const int first = wn.I.bt0 * p.BT + (wn.j - wn.I.n_prompt) * p.suf_bpt;
+                    const int nb = min(p.suf_bpt, min(p.W, (wn.I.bt0 + NH) * p.BT) - first);
+                    const int64_t b0 = static_cast<int64_t>(wn.I.r) * p.W + first;
+                    if (lane < nb) pa0 = sp.parent[b0 + lane];
+                    if (lane + 32 < nb) pa1 = sp.parent[b0 + 32 + lane];
                 }
-                const bool bad0 = t > 1 && lane < T.nb && (par0 < 0 || par0 >= p.W);
-                const bool bad1 = t > 1 && lane + 32 < T.nb && (par1 < 0 || par1 >= p.W);
-                badm0 = __ballot_sync(0xffffffffu, bad0);
-                badm1 = __ballot_sync(0xffffffffu, bad1);
+            };
+            // Starts the gather of the suffix tile at wn (parents pa0 / pa1) into buffer `buf`,
+            // records it, and moves wn past it (one cp.async group).
+            auto gather = [&](int buf, int pa0, int pa1) {
+                const int first = wn.I.bt0 * p.BT + (wn.j - wn.I.n_prompt) * p.suf_bpt;
+                const int nb = min(p.suf_bpt, min(p.W, (wn.I.bt0 + NH) * p.BT) - first);
+                const int64_t req0 = static_cast<int64_t>(wn.I.r) * p.W;
+                const int kh = wn.I.kh;
+                const bool bad0 = t > 1 && lane < nb && (pa0 < 0 || pa0 >= p.W);
+                const bool bad1 = t > 1 && lane + 32 < nb && (pa1 < 0 || pa1 >= p.W);
+                const uint32_t badm0 = __ballot_sync(0xffffffffu, bad0), badm1 = __ballot_sync(0xffffffffu, bad1);
                 if ((bad0 || bad1) && p.dev_status) atomicOr(p.dev_status, BG_DEVSTAT_PARENT);
+                if (lane == 0) {
+                    int32_t *rec = rec_base + buf * 8;
+                    rec[0] = static_cast<int32_t>(nn);
+                    rec[1] = wn.I.r;
+                    rec[2] = kh;
+                    rec[3] = first;
+                    rec[4] = nb;
+                    rec[5] = static_cast<int32_t>(badm0);
+                    rec[6] = static_cast<int32_t>(badm1);
+                }
                 uint8_t *stg = smem + C::kOffGather + buf * (C::kKTileBytes + C::kTileBytes);
-                const int chunks = T.nb * t * kCpr;       // per tensor
+                const int chunks = nb * t * kCpr;         // per tensor
                 for (int base = 0; base < 2 * chunks; base += 32) {   // same trip count in every lane
                     const int q = base + lane;
                     const int kv = q >= chunks ? 1 : 0;
@@ -1002,48 +1018,56 @@ __global__ void __maxnreg__((AttnCfg<D, NH, NK, NV, NS, QK8, FUSED>::kRegsLaunch
                     const int c = qq - row * kCpr;
                     const int pos = row / t;
                     const int sl = row - pos * t;
-                    const int pa = __shfl_sync(0xffffffffu, par0, pos & 31);
-                    const int pb = __shfl_sync(0xffffffffu, par1, pos & 31);
+                    const int sa = __shfl_sync(0xffffffffu, pa0, pos & 31);
+                    const int sb = __shfl_sync(0xffffffffu, pa1, pos & 31);
                     if (q >= 2 * chunks) continue;
-                    const int par = pos < 32 ? pa : pb;
+                    const int par = pos < 32 ? sa : sb;
                     const bool bad = ((pos < 32 ? badm0 : badm1) >> (pos & 31)) & 1u;
                     uint8_t *to = stg + kv * C::kKTileBytes + (c >> 3) * kKVBox + row * 128 + (((c & 7) ^ (row & 7)) << 4);
                     if (sl == t - 1)
-                        cp_async_16(to, (kv ? sp.new_v : sp.new_k) + ((req0 + T.first + pos) * p.Hkv + T.kh) * D + c * 8);
+                        cp_async_16(to, (kv ? sp.new_v : sp.new_k) + ((req0 + first + pos) * p.Hkv + kh) * D + c * 8);
                     else if (bad)
                         *reinterpret_cast<uint4 *>(to) = make_uint4(0, 0, 0, 0);
                     else
-                        cp_async_16(to, (kv ? sp.src_v : sp.src_k) +
-                                            (((req0 + par) * sp.suffix_max + sl) * p.Hkv + T.kh) * D + c * 8);
+                        cp_async_16(to, (kv ? sp.src_v : sp.src_k) + (((req0 + par) * sp.suffix_max + sl) * p.Hkv + kh) * D +
+                                            c * 8);
                 }
                 cp_async_commit();
+                ++nn;
+                wn.advance(p);
             };
-            TileWalker<MODE, NH> wn;         // walks one suffix tile ahead of the one delivered
-            wn.first(p, n_items);
-            uint32_t nn = 0;
+            // prologue: the first B-1 suffix tiles in flight, the parents of the B-th loading
+            int inflight = 0;            // gathered, not yet delivered
+            int pa0 = 0, pa1 = 0;
+            bool more = advance_to_suffix();
+            while (more && inflight < B - 1) {
+                load_parents(pa0, pa1);
+                gather(inflight, pa0, pa1);
+                ++inflight;
+                more = advance_to_suffix();
+            }
+            if (more) load_parents(pa0, pa1);
             uint32_t go_phase = 0;   // bit s: parity the next wait on suf_go_k[s] expects (bit 16 + s: suf_go_v[s])
-            uint32_t bad_c0 = 0, bad_c1 = 0, bad_n0 = 0, bad_n1 = 0;
-            SufTile cur = next_suffix(wn, nn);
-            if (cur.valid) gather(cur, 0, bad_c0, bad_c1);
-            int buf = 0;
             bool ok = true;
-            while (cur.valid && ok) {
-                // prefetch the next suffix tile into the other buffer while this one is delivered
-                const SufTile nxt = next_suffix(wn, nn);
-                if (nxt.valid) gather(nxt, buf ^ 1, bad_n0, bad_n1);
-                // this tile's copies (the older group) have landed
-                if (nxt.valid)
+            for (int i = 0; inflight > 0 && ok; ++i) {
+                const int buf = i % B;
+                // tile i's group is the oldest: wait until at most the younger ones are pending
+                if (inflight >= 3)
+                    asm volatile("cp.async.wait_group 2;" ::: "memory");
+                else if (inflight == 2)
                     asm volatile("cp.async.wait_group 1;" ::: "memory");
                 else
                     cp_async_wait_all();
                 __syncwarp();
+                const int32_t *rec = rec_base + buf * 8;
+                const uint32_t n = static_cast<uint32_t>(rec[0]);
                 const uint8_t *stg = smem + C::kOffGather + buf * (C::kKTileBytes + C::kTileBytes);
                 // deliver K, then V, each when its producer hands the ring stage over: a copy
                 // between shared-memory tiles of the same layout, ordered before the tensor cores'
                 // reads, then the stage's full barrier.  (K goes first: with two V stages and two
                 // score buffers V's stage is freed only by this tile's own scores.)
                 for (int kv = 0; kv < 2; ++kv) {
-                    const int st = kv ? static_cast<int>(cur.n % NV) : static_cast<int>(cur.n % NK);
+                    const int st = kv ? static_cast<int>(n % NV) : static_cast<int>(n % NK);
                     uint64_t *go = kv ? &suf_go_v[st] : &suf_go_k[st];
                     const uint32_t bit = 1u << (st + (kv ? 16 : 0));
                     if (!warp_wait(go, (go_phase & bit) ? 1u : 0u, abort_flag)) {
@@ -1055,16 +1079,27 @@ __global__ void __maxnreg__((AttnCfg<D, NH, NK, NV, NS, QK8, FUSED>::kRegsLaunch
                     uint8_t *stage = kv ? smem + C::kOffV + st * C::kTileBytes : smem + C::kOffK + st * C::kKTileBytes;
                     const uint4 *from = reinterpret_cast<const uint4 *>(stg + kv * C::kKTileBytes);
                     uint4 *to = reinterpret_cast<uint4 *>(stage);
-                    for (int i = lane; i < bytes / 16; i += 32) to[i] = from[i];
+                    for (int k = lane; k < bytes / 16; k += 32) to[k] = from[k];
                     fence_proxy_async_smem();            // generic-proxy writes -> the tensor cores' reads
                     __syncwarp();
                     if (lane == 0) mbar_arrive(kv ? &v_full[st] : &k_full[st]);
                 }
                 if (!ok) break;
+                --inflight;
+                // refill the pipeline: gather the tile whose parents have landed, start the next
+                // parents, while this tile's rows go to dst below
+                if (more) {
+                    gather((i + B - 1) % B, pa0, pa1);    // the buffer delivered in the previous round
+                    ++inflight;
+                    more = advance_to_suffix();
+                    if (more) load_parents(pa0, pa1);
+                }
                 // the step's suffix, from the staged rows (beams with a bad parent left untouched)
                 {
-                    const int64_t req0 = static_cast<int64_t>(cur.r) * p.W;
-                    const int chunks = cur.nb * t * kCpr;
+                    const int r = rec[1], kh = rec[2], first = rec[3], nb = rec[4];
+                    const uint32_t bm0 = static_cast<uint32_t>(rec[5]), bm1 = static_cast<uint32_t>(rec[6]);
+                    const int64_t req0 = static_cast<int64_t>(r) * p.W;
+                    const int chunks = nb * t * kCpr;
                     for (int q = lane; q < 2 * chunks; q += 32) {
                         const int kv = q >= chunks ? 1 : 0;
                         const int qq = q - kv * chunks;
@@ -1072,19 +1107,15 @@ __global__ void __maxnreg__((AttnCfg<D, NH, NK, NV, NS, QK8, FUSED>::kRegsLaunch
                         const int c = qq - row * kCpr;
                         const int pos = row / t;
                         const int sl = row - pos * t;
-                        if (((pos < 32 ? bad_c0 : bad_c1) >> (pos & 31)) & 1u) continue;
+                        if (((pos < 32 ? bm0 : bm1) >> (pos & 31)) & 1u) continue;
                         const uint8_t *from = stg + kv * C::kKTileBytes + (c >> 3) * kKVBox + row * 128 +
                                               (((c & 7) ^ (row & 7)) << 4);
                         __nv_bfloat16 *dst = kv ? sp.dst_v : sp.dst_k;
-                        *reinterpret_cast<uint4 *>(dst + (((req0 + cur.first + pos) * sp.suffix_max + sl) * p.Hkv + cur.kh) * D +
+                        *reinterpret_cast<uint4 *>(dst + (((req0 + first + pos) * sp.suffix_max + sl) * p.Hkv + kh) * D +
                                                    c * 8) = *reinterpret_cast<const uint4 *>(from);
                     }
                 }
-                __syncwarp();                            // the buffer is read before it is refilled
-                cur = nxt;
-                bad_c0 = bad_n0;
-                bad_c1 = bad_n1;
-                buf ^= 1;
+                __syncwarp();                            // buffer `buf` is read before it is refilled
             }
             cp_async_wait_all();
             __syncwarp();
