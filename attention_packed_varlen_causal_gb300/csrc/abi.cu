@@ -418,26 +418,9 @@ bg_status_t decode_impl(const void *q, const void *prompt_k, const void *prompt_
     p.suf_tx = (head_dim / 64) * 128 * t_suf * bpt;
     p.n_items_decode = static_cast<int32_t>(items);
     const int grid = static_cast<int>(items < nsm ? items : nsm);
-    if (fz && decode_step_one_launch(head_dim)) {
-        // one launch: a gatherer warp of the attention kernel builds each suffix key tile from
-        // the previous step's suffix through the parent index and writes the step's suffix
-        StepParams sp;
-        std::memset(&sp, 0, sizeof(sp));
-        sp.src_k = static_cast<const __nv_bfloat16 *>(fz->src_k);
-        sp.src_v = static_cast<const __nv_bfloat16 *>(fz->src_v);
-        sp.new_k = static_cast<const __nv_bfloat16 *>(fz->new_k);
-        sp.new_v = static_cast<const __nv_bfloat16 *>(fz->new_v);
-        sp.dst_k = static_cast<__nv_bfloat16 *>(const_cast<void *>(suffix_k));
-        sp.dst_v = static_cast<__nv_bfloat16 *>(const_cast<void *>(suffix_v));
-        sp.parent = fz->parent;
-        sp.suffix_max = suffix_max;
-        if (launch_decode_step_fused(head_dim, tm_q, tm_k, tm_v, tm_o, p, sp, grid, stream) != cudaSuccess)
-            return BG_ERR_CUDA;
-        return BG_OK;
-    }
     if (fz) {
-        // two launches: the step's reorder + append first (it moves nothing at t = 1 and then
-        // never reads src), then the attention over the new suffix
+        // the step's reorder + append first (it moves nothing at t = 1 and then never reads src),
+        // then the attention over the new suffix
         const void *sk = fz->src_k ? fz->src_k : suffix_k;
         const void *sv = fz->src_v ? fz->src_v : suffix_v;
         if (launch_suffix_reorder(sk, sv, const_cast<void *>(suffix_k), const_cast<void *>(suffix_v), fz->parent,

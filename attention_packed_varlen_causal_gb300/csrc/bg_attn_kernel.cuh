@@ -95,20 +95,9 @@ struct AttnParams {
     int32_t n_items_decode;
 };
 
-// Extra operands of the one-launch decode step (attn_kernel<Decode, ..., FUSED = true>): a helper
-// warp builds the suffix key tiles itself, gathering each beam's rows through the parent index,
-// and writes the step's suffix for the next step.  Unused (zero) in every other instantiation.
-struct StepParams {
-    const __nv_bfloat16 *src_k, *src_v;   // previous suffix [R, W, S_max, Hkv, d]; slots 0..t-2 read
-    const __nv_bfloat16 *new_k, *new_v;   // the step's token [R, W, Hkv, d]
-    __nv_bfloat16 *dst_k, *dst_v;         // the step's suffix [R, W, S_max, Hkv, d]; slots 0..t-1 written
-    const int32_t *parent;                // [R, W], each in [0, W)
-    int32_t suffix_max;
-};
-
 // QK8: Q and K arrive as one-byte E4M3 codes and Q.K^T runs as kind::f8f6f4 (V, P and P.V
 // stay bf16); otherwise every operand is bf16.
-template <int D, int NH, int NK, int NV, int NS, bool QK8 = false, bool FUSED = false>
+template <int D, int NH, int NK, int NV, int NS, bool QK8 = false>
 struct AttnCfg {
     static constexpr int NB = D / 64;                       // 128-byte column blocks of a bf16 row (V, O)
     static constexpr int NBQ = QK8 ? D / 128 : D / 64;      // 128-byte column blocks of a Q or K row
@@ -122,35 +111,22 @@ struct AttnCfg {
     static constexpr int kOffStage = kOffV + NV * kTileBytes;     // 2 KB per softmax warp
     static_assert(!QK8 || D == 128, "E4M3 Q/K rows are one 128-byte column block (head_dim 128)");
     static constexpr int kStageBytes = 32 * 64;
-    // FUSED: the gatherer's kGatherBufs private staging tiles (K and V each, in the ring's
-    // layout), then per buffer the tile's record (8 int32: stage number, request, kv head, first
-    // beam, beams, bad-parent masks)
-    static constexpr int kGatherBufs = 4;
-    static constexpr int kOffGather = kOffStage + 4 * NH * kStageBytes;
-    static constexpr int kGatherBytes = FUSED ? kGatherBufs * (kKTileBytes + kTileBytes) : 0;
-    static constexpr int kOffGatherRec = kOffGather + kGatherBytes;
-    static constexpr int kOffBar = kOffGatherRec + (FUSED ? kGatherBufs * 32 : 0);
+    static constexpr int kOffBar = kOffStage + 4 * NH * kStageBytes;
     // q_full[2] q_empty[2] mma_final k_full[NK] k_empty[NK] v_full[NV] v_empty[NV] s_full[NH][NS]
     // p_full[NH][NS] pv_done[NH][NS] o_staged[NH][2]
-    // FUSED adds suf_go_k[NK] and suf_go_v[NV]: a producer hands a stage to the gatherer
-    static constexpr int kNumBars = 5 + 2 * NK + 2 * NV + 3 * NS * NH + 2 * NH + (FUSED ? NK + NV : 0);
+    static constexpr int kNumBars = 5 + 2 * NK + 2 * NV + 3 * NS * NH + 2 * NH;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + slack for 1024-byte alignment
-    // FUSED: one more warp (the suffix gatherer) after the softmax warpgroups
-    static constexpr int kThreads = 128 * (1 + NH) + (FUSED ? 32 : 0);
+    static constexpr int kThreads = 128 * (1 + NH);
     // Register split (setmaxnreg): the kernel is compiled for kRegsLaunch registers per thread
     // (__maxnreg__), which the launcher checks against the compiled kernel before every launch;
-    // the TMA, MMA and gatherer warps then run with kRegsLight and the 8 softmax warps with
-    // kRegsSoftmax, within the launch's total (kSplitRegs).
-    // (13 warps: the register file is handed out to a CTA as if its warps were rounded up to a
-    // multiple of four, so 16 x 32 x 128 = 65,536 is the most a 416-thread CTA can launch with.)
-    // Warps 0-3 run with kRegsLight, the 8 softmax warps with kRegsSoftmax, and the gatherer warp
-    // (FUSED; it alone cannot change its allocation) keeps kRegsLaunch.
-    static constexpr int kRegsLaunch = FUSED ? 128 : 168;
-    static constexpr int kRegsLight = FUSED ? 48 : 64;
-    static constexpr int kRegsSoftmax = FUSED ? 168 : 216;
-    static constexpr int kSplitRegs = 4 * 32 * kRegsLight + 8 * 32 * kRegsSoftmax + (FUSED ? 32 * kRegsLaunch : 0);
-    static_assert((kThreads + 127) / 128 * 128 * kRegsLaunch <= 65536, "the launch must fit the register file");
+    // warps 0-3 (TMA and MMA) then run with kRegsLight and the 8 softmax warps with kRegsSoftmax,
+    // within the launch's total (kSplitRegs).
+    static constexpr int kRegsLaunch = 168;
+    static constexpr int kRegsLight = 64;
+    static constexpr int kRegsSoftmax = 216;
+    static constexpr int kSplitRegs = 4 * 32 * kRegsLight + 8 * 32 * kRegsSoftmax;
+    static_assert(kThreads * kRegsLaunch <= 65536, "the launch must fit the register file");
     static_assert(kSplitRegs <= kThreads * kRegsLaunch, "register split exceeds the launch's allocation");
     static constexpr int kColO = 64 * NS * NH;
     static constexpr int kColsUsed = 64 * NS * NH + D * NH;
@@ -307,16 +283,15 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volati
     return ok != 0;
 }
 
-template <Mode MODE, int D, int NH, int NK, int NV, int NS, bool QK8 = false, bool FUSED = false>
-__global__ void __maxnreg__((AttnCfg<D, NH, NK, NV, NS, QK8, FUSED>::kRegsLaunch))
+template <Mode MODE, int D, int NH, int NK, int NV, int NS, bool QK8 = false>
+__global__ void __maxnreg__((AttnCfg<D, NH, NK, NV, NS, QK8>::kRegsLaunch))
     attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_sk,
                 const __grid_constant__ CUtensorMap tm_sv, const __grid_constant__ CUtensorMap tm_o,
-                const AttnParams p, const StepParams sp)
+                const AttnParams p)
 {
-    using C = AttnCfg<D, NH, NK, NV, NS, QK8, FUSED>;
+    using C = AttnCfg<D, NH, NK, NV, NS, QK8>;
     static_assert(!QK8 || MODE == Mode::Prefill, "E4M3 Q/K is a prefill variant");
-    static_assert(!FUSED || MODE == Mode::Decode, "the one-launch step is a decode variant");
     static_assert(NH == 2, "the register split and the warp roles assume two query tiles per CTA");
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte alignment of the shared-window offset (swizzle-128B atoms need it)
@@ -342,13 +317,6 @@ __global__ void __maxnreg__((AttnCfg<D, NH, NK, NV, NS, QK8, FUSED>::kRegsLaunch
     // of the item after next, whose Q load waits for the buffer this tile leaves from.  The second
     // barrier per group keeps consecutive phases apart all the same.
     uint64_t *o_staged = pv_done + NS * NH;   // [NH][2]
-    // FUSED: suf_go_k[s] / suf_go_v[s] complete a phase when the K / V producer, having waited for
-    // stage s to be free for a suffix tile (its own wait, so its phase tracking stays exact), hands
-    // the stage to the gatherer instead of loading it.  A producer cannot hand the same stage over
-    // again before the gatherer has filled it and it has been consumed and freed, so every gatherer
-    // wait on them is for the phase right after the last one it saw.
-    uint64_t *suf_go_k = o_staged + 2 * NH;   // [NK]
-    uint64_t *suf_go_v = suf_go_k + NK;       // [NV]
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::kOffMisc + 4);
 
@@ -376,10 +344,6 @@ __global__ void __maxnreg__((AttnCfg<D, NH, NK, NV, NS, QK8, FUSED>::kRegsLaunch
             mbar_init(&pv_done[i], 1);
         }
         for (int i = 0; i < 2 * NH; ++i) mbar_init(&o_staged[i], 4);   // one arrive per warp
-        if constexpr (FUSED) {
-            for (int i = 0; i < NK; ++i) mbar_init(&suf_go_k[i], 1);
-            for (int i = 0; i < NV; ++i) mbar_init(&suf_go_v[i], 1);
-        }
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -387,10 +351,8 @@ __global__ void __maxnreg__((AttnCfg<D, NH, NK, NV, NS, QK8, FUSED>::kRegsLaunch
         // Decode query tiles fill only BT*g <= 128 rows and suffix key tiles only suf_bpt*t
         // <= 64 rows; the rows past them keep what an earlier tile left (finite) or these
         // zeros, so the masked columns they feed multiply finite values only.
-        // (FUSED: the gatherer's staging tiles too: a stage copy moves all 64 rows of a tile)
         uint4 *z4 = reinterpret_cast<uint4 *>(smem + C::kOffQ);
-        constexpr int kZeroEnd = FUSED ? C::kOffBar : C::kOffStage;
-        for (int i = threadIdx.x; i < kZeroEnd / 16; i += blockDim.x) z4[i] = make_uint4(0, 0, 0, 0);
+        for (int i = threadIdx.x; i < C::kOffStage / 16; i += blockDim.x) z4[i] = make_uint4(0, 0, 0, 0);
         fence_proxy_async_smem();
     }
     if (warp == 1) {
@@ -422,9 +384,7 @@ __global__ void __maxnreg__((AttnCfg<D, NH, NK, NV, NS, QK8, FUSED>::kRegsLaunch
 
     // Register split (see AttnCfg).  setmaxnreg must be executed by all four warps of a warpgroup
     // at the same instruction, so the split is made per warpgroup before the roles branch: the
-    // TMA / MMA warpgroup (warps 0-3) returns registers, the softmax warpgroups take them.  The
-    // gatherer warp of the one-launch decode step (warp 12, alone in its warpgroup) keeps its
-    // launch allocation.
+    // TMA / MMA warpgroup (warps 0-3) returns registers, the softmax warpgroups take them.
     if (warp < 4) {
     reg_dealloc<C::kRegsLight>();
     if (warp == 0) {
@@ -466,13 +426,6 @@ __global__ void __maxnreg__((AttnCfg<D, NH, NK, NV, NS, QK8, FUSED>::kRegsLaunch
             const int st = n_kv % NK;
             const uint32_t use = n_kv / NK;
             if (use > 0 && !warp_wait(&k_empty[st], (use - 1) & 1, abort_flag)) break;
-            if (FUSED && MODE == Mode::Decode && w.j >= w.I.n_prompt) {
-                // a suffix tile: the stage is free, the gatherer warp fills it
-                if (lane == 0) mbar_arrive(&suf_go_k[st]);
-                ++n_kv;
-                w.advance(p);
-                continue;
-            }
             uint8_t *kdst = smem + C::kOffK + st * C::kKTileBytes;
             if (MODE == Mode::Prefill || w.j < w.I.n_prompt) {
                 const int row = w.I.kv_row0 + w.j * kKeys;
@@ -516,13 +469,6 @@ __global__ void __maxnreg__((AttnCfg<D, NH, NK, NV, NS, QK8, FUSED>::kRegsLaunch
             const int st = n_v % NV;
             const uint32_t use = n_v / NV;
             if (use > 0 && !warp_wait(&v_empty[st], (use - 1) & 1, abort_flag)) break;
-            if (FUSED && MODE == Mode::Decode && w.j >= w.I.n_prompt) {
-                // a suffix tile: the stage is free, the gatherer warp fills it
-                if (lane == 0) mbar_arrive(&suf_go_v[st]);
-                ++n_v;
-                w.advance(p);
-                continue;
-            }
             uint8_t *vdst = smem + C::kOffV + st * C::kTileBytes;
             if (MODE == Mode::Prefill || w.j < w.I.n_prompt) {
                 const int row = w.I.kv_row0 + w.j * kKeys;
@@ -938,188 +884,6 @@ __global__ void __maxnreg__((AttnCfg<D, NH, NK, NV, NS, QK8, FUSED>::kRegsLaunch
         if (quad == 0 && lane == 0) bulk_wait_all();
 
         (void)ok;
-    }
-
-    if constexpr (FUSED) {
-        if (warp == 4 + 4 * NH) {
-            // =========================================================== suffix gatherer
-            // Builds every suffix key tile of the CTA's items in the K and V stages the producers
-            // leave to it, straight from the previous step's buffer: row (beam b, slot s) of a tile
-            // is slot s of beam parent[b] for s < t-1 and the step's new token for s = t-1 (the
-            // reorder of the beam's suffix, gathered as it is read).  Each lane copies 16-byte
-            // chunks with cp.async into one of two private staging tiles laid out as the ring's
-            // stages are (128-byte swizzle, the layout a TMA tile load writes), one suffix tile
-            // ahead, so the gather's memory latency stays off the pipeline.  The producers still
-            // wait for each suffix tile's stage to be free and then hand it over (suf_go_k /
-            // suf_go_v); the gatherer waits only on those hand-overs, never on the empty barriers,
-            // whose phases it would not all see.  A hand-over is served by a shared-to-shared copy
-            // ordered before the MMAs' reads (fence.proxy.async) and the stage's full barrier.  The
-            // staged rows then go to dst, the step's suffix: every (beam, kv head) is in exactly
-            // one suffix tile of one item, so each row of dst is written once.
-            constexpr int kCpr = D / 8;                  // 16-byte chunks per row
-            const int t = p.suffix_len;
-            // A pipeline over the CTA's suffix tiles, in walk order: tile i is delivered while
-            // the data of tiles i+1 .. i+B-1 (B = kGatherBufs) is in flight into their staging
-            // buffers and the parents of tile i+B are loading into registers, so neither the
-            // parents' nor the rows' memory latency waits in front of a delivery.
-            constexpr int B = C::kGatherBufs;
-            int32_t *rec_base = reinterpret_cast<int32_t *>(smem + C::kOffGatherRec);   // [B][8]
-            TileWalker<MODE, NH> wn;     // the next suffix tile to prefetch
-            wn.first(p, n_items);
-            uint32_t nn = 0;
-            // Moves wn to the next suffix tile; returns false at the end of the walk.
-            auto advance_to_suffix = [&]() -> bool {
-                while (wn.valid && wn.j < wn.I.n_prompt) {
-                    ++nn;
-                    wn.advance(p);
-                }
-                return wn.valid;
-            };
-            // The parents of the suffix tile at wn (plain loads: they land while other work runs).
-            auto load_parents = [&](int &pa0, int &pa1) {
-                pa0 = 0;
-                pa1 = 0;
-                if (t > 1) {
-                    const int first = wn.I.bt0 * p.BT + (wn.j - wn.I.n_prompt) * p.suf_bpt;
-                    const int nb = min(p.suf_bpt, min(p.W, (wn.I.bt0 + NH) * p.BT) - first);
-                    const int64_t b0 = static_cast<int64_t>(wn.I.r) * p.W + first;
-                    if (lane < nb) pa0 = sp.parent[b0 + lane];
-                    if (lane + 32 < nb) pa1 = sp.parent[b0 + 32 + lane];
-                }
-            };
-            // Starts the gather of the suffix tile at wn (parents pa0 / pa1) into buffer `buf`,
-            // records it, and moves wn past it (one cp.async group).
-            auto gather = [&](int buf, int pa0, int pa1) {
-                const int first = wn.I.bt0 * p.BT + (wn.j - wn.I.n_prompt) * p.suf_bpt;
-                const int nb = min(p.suf_bpt, min(p.W, (wn.I.bt0 + NH) * p.BT) - first);
-                const int64_t req0 = static_cast<int64_t>(wn.I.r) * p.W;
-                const int kh = wn.I.kh;
-                const bool bad0 = t > 1 && lane < nb && (pa0 < 0 || pa0 >= p.W);
-                const bool bad1 = t > 1 && lane + 32 < nb && (pa1 < 0 || pa1 >= p.W);
-                const uint32_t badm0 = __ballot_sync(0xffffffffu, bad0), badm1 = __ballot_sync(0xffffffffu, bad1);
-                if ((bad0 || bad1) && p.dev_status) atomicOr(p.dev_status, BG_DEVSTAT_PARENT);
-                if (lane == 0) {
-                    int32_t *rec = rec_base + buf * 8;
-                    rec[0] = static_cast<int32_t>(nn);
-                    rec[1] = wn.I.r;
-                    rec[2] = kh;
-                    rec[3] = first;
-                    rec[4] = nb;
-                    rec[5] = static_cast<int32_t>(badm0);
-                    rec[6] = static_cast<int32_t>(badm1);
-                }
-                uint8_t *stg = smem + C::kOffGather + buf * (C::kKTileBytes + C::kTileBytes);
-                const int chunks = nb * t * kCpr;         // per tensor
-                for (int base = 0; base < 2 * chunks; base += 32) {   // same trip count in every lane
-                    const int q = base + lane;
-                    const int kv = q >= chunks ? 1 : 0;
-                    const int qq = q - kv * chunks;
-                    const int row = qq / kCpr;           // beam-major: row = pos * t + s
-                    const int c = qq - row * kCpr;
-                    const int pos = row / t;
-                    const int sl = row - pos * t;
-                    const int sa = __shfl_sync(0xffffffffu, pa0, pos & 31);
-                    const int sb = __shfl_sync(0xffffffffu, pa1, pos & 31);
-                    if (q >= 2 * chunks) continue;
-                    const int par = pos < 32 ? sa : sb;
-                    const bool bad = ((pos < 32 ? badm0 : badm1) >> (pos & 31)) & 1u;
-                    uint8_t *to = stg + kv * C::kKTileBytes + (c >> 3) * kKVBox + row * 128 + (((c & 7) ^ (row & 7)) << 4);
-                    if (sl == t - 1)
-                        cp_async_16(to, (kv ? sp.new_v : sp.new_k) + ((req0 + first + pos) * p.Hkv + kh) * D + c * 8);
-                    else if (bad)
-                        *reinterpret_cast<uint4 *>(to) = make_uint4(0, 0, 0, 0);
-                    else
-                        cp_async_16(to, (kv ? sp.src_v : sp.src_k) + (((req0 + par) * sp.suffix_max + sl) * p.Hkv + kh) * D +
-                                            c * 8);
-                }
-                cp_async_commit();
-                ++nn;
-                wn.advance(p);
-            };
-            // prologue: the first B-1 suffix tiles in flight, the parents of the B-th loading
-            int inflight = 0;            // gathered, not yet delivered
-            int pa0 = 0, pa1 = 0;
-            bool more = advance_to_suffix();
-            while (more && inflight < B - 1) {
-                load_parents(pa0, pa1);
-                gather(inflight, pa0, pa1);
-                ++inflight;
-                more = advance_to_suffix();
-            }
-            if (more) load_parents(pa0, pa1);
-            uint32_t go_phase = 0;   // bit s: parity the next wait on suf_go_k[s] expects (bit 16 + s: suf_go_v[s])
-            bool ok = true;
-            for (int i = 0; inflight > 0 && ok; ++i) {
-                const int buf = i % B;
-                // tile i's group is the oldest: wait until at most the younger ones are pending
-                if (inflight >= 3)
-                    asm volatile("cp.async.wait_group 2;" ::: "memory");
-                else if (inflight == 2)
-                    asm volatile("cp.async.wait_group 1;" ::: "memory");
-                else
-                    cp_async_wait_all();
-                __syncwarp();
-                const int32_t *rec = rec_base + buf * 8;
-                const uint32_t n = static_cast<uint32_t>(rec[0]);
-                const uint8_t *stg = smem + C::kOffGather + buf * (C::kKTileBytes + C::kTileBytes);
-                // deliver K, then V, each when its producer hands the ring stage over: a copy
-                // between shared-memory tiles of the same layout, ordered before the tensor cores'
-                // reads, then the stage's full barrier.  (K goes first: with two V stages and two
-                // score buffers V's stage is freed only by this tile's own scores.)
-                for (int kv = 0; kv < 2; ++kv) {
-                    const int st = kv ? static_cast<int>(n % NV) : static_cast<int>(n % NK);
-                    uint64_t *go = kv ? &suf_go_v[st] : &suf_go_k[st];
-                    const uint32_t bit = 1u << (st + (kv ? 16 : 0));
-                    if (!warp_wait(go, (go_phase & bit) ? 1u : 0u, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    go_phase ^= bit;
-                    const int bytes = kv ? C::kTileBytes : C::kKTileBytes;
-                    uint8_t *stage = kv ? smem + C::kOffV + st * C::kTileBytes : smem + C::kOffK + st * C::kKTileBytes;
-                    const uint4 *from = reinterpret_cast<const uint4 *>(stg + kv * C::kKTileBytes);
-                    uint4 *to = reinterpret_cast<uint4 *>(stage);
-                    for (int k = lane; k < bytes / 16; k += 32) to[k] = from[k];
-                    fence_proxy_async_smem();            // generic-proxy writes -> the tensor cores' reads
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(kv ? &v_full[st] : &k_full[st]);
-                }
-                if (!ok) break;
-                --inflight;
-                // refill the pipeline: gather the tile whose parents have landed, start the next
-                // parents, while this tile's rows go to dst below
-                if (more) {
-                    gather((i + B - 1) % B, pa0, pa1);    // the buffer delivered in the previous round
-                    ++inflight;
-                    more = advance_to_suffix();
-                    if (more) load_parents(pa0, pa1);
-                }
-                // the step's suffix, from the staged rows (beams with a bad parent left untouched)
-                {
-                    const int r = rec[1], kh = rec[2], first = rec[3], nb = rec[4];
-                    const uint32_t bm0 = static_cast<uint32_t>(rec[5]), bm1 = static_cast<uint32_t>(rec[6]);
-                    const int64_t req0 = static_cast<int64_t>(r) * p.W;
-                    const int chunks = nb * t * kCpr;
-                    for (int q = lane; q < 2 * chunks; q += 32) {
-                        const int kv = q >= chunks ? 1 : 0;
-                        const int qq = q - kv * chunks;
-                        const int row = qq / kCpr;
-                        const int c = qq - row * kCpr;
-                        const int pos = row / t;
-                        const int sl = row - pos * t;
-                        if (((pos < 32 ? bm0 : bm1) >> (pos & 31)) & 1u) continue;
-                        const uint8_t *from = stg + kv * C::kKTileBytes + (c >> 3) * kKVBox + row * 128 +
-                                              (((c & 7) ^ (row & 7)) << 4);
-                        __nv_bfloat16 *dst = kv ? sp.dst_v : sp.dst_k;
-                        *reinterpret_cast<uint4 *>(dst + (((req0 + first + pos) * sp.suffix_max + sl) * p.Hkv + kh) * D +
-                                                   c * 8) = *reinterpret_cast<const uint4 *>(from);
-                    }
-                }
-                __syncwarp();                            // buffer `buf` is read before it is refilled
-            }
-            cp_async_wait_all();
-            __syncwarp();
-        }
     }
 
     // ------------------------------------------------------------------ teardown

@@ -14,7 +14,6 @@
 namespace bg {
 
 struct AttnParams;
-struct StepParams;
 
 // Host checks of bg_packed_prefill_attn's arguments other than the workspace (sizes, shape
 // support, scale, pointers, alignment, aliasing between the tensors; Q and K elements of
@@ -42,13 +41,6 @@ cudaError_t launch_decode_attn(int head_dim, const CUtensorMap &tm_q, const CUte
                                const CUtensorMap &tm_v, const CUtensorMap &tm_sk, const CUtensorMap &tm_sv,
                                const CUtensorMap &tm_o, const AttnParams &p, int grid, cudaStream_t stream);
 int decode_tiles_per_cta();
-// The one-launch decode step: the attention kernel with a gatherer warp that builds the suffix
-// key tiles through the parent index and writes the step's suffix (head_dim 64; the head_dim 128
-// kernel has no shared memory left for the gatherer's staging, its step is reorder + attention).
-bool decode_step_one_launch(int head_dim);
-cudaError_t launch_decode_step_fused(int head_dim, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
-                                     const CUtensorMap &tm_v, const CUtensorMap &tm_o, const AttnParams &p,
-                                     const StepParams &sp, int grid, cudaStream_t stream);
 
 // Attention of each sequence's last valid token (one CTA per sequence and kv head).
 cudaError_t launch_last_token_attn(int head_dim, const void *q, const void *k, const void *v, const int32_t *cu,

@@ -138,28 +138,6 @@ __device__ __forceinline__ float ex2(float x)
     return y;
 }
 
-// ------------------------------------------------------------------ cp.async (16-byte, L2 only)
-// Asynchronous global -> shared copy of 16 bytes (both addresses 16-byte aligned); the data is
-// in shared memory once this thread's cp_async_wait_all returns.  A generic-proxy write: threads
-// that read it with ordinary loads need only the wait and a barrier among themselves.
-__device__ __forceinline__ void cp_async_16(void *smem_dst, const void *gmem_src)
-{
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gmem_src) : "memory");
-}
-// 4-byte variant (through L1; both addresses 4-byte aligned).
-__device__ __forceinline__ void cp_async_4(void *smem_dst, const void *gmem_src)
-{
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(smem_dst)), "l"(gmem_src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit()
-{
-    asm volatile("cp.async.commit_group;" ::: "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all()
-{
-    asm volatile("cp.async.wait_all;" ::: "memory");
-}
-
 // ------------------------------------------------------------------ TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map)
 {
@@ -578,12 +556,6 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 {
     __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&h);
-}
-
-// The two bf16 of a packed pair as exact floats (a bf16 is the top half of a float).
-__device__ __forceinline__ float2 unpack_bf16x2(uint32_t u)
-{
-    return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xFFFF0000u));
 }
 
 }  // namespace bg

@@ -6,10 +6,7 @@
 // queries of all beams x group heads of one kv head form 128-row tiles that
 // run on the tensor cores against the prompt K/V, read once per tile pair
 // (and from L2 for the sibling tiles).  The few suffix keys of each beam
-// follow as extra key tiles of the same item (see attn_kernel<Decode>); in
-// the one-launch decode step a gatherer warp builds those tiles straight
-// from the previous step's suffix through the parent index and writes the
-// step's suffix (attn_kernel<Decode, FUSED>).
+// follow as extra key tiles of the same item (see attn_kernel<Decode>).
 #include "bg_attn_kernel.cuh"
 #include "bg_internal.h"
 
@@ -20,27 +17,27 @@ namespace bg {
 namespace {
 constexpr int kNH = 2;   // query tiles (of the same request and kv head) per CTA
 
-template <int D, int NK, int NV, int NS, bool FUSED>
+template <int D, int NK, int NV, int NS>
 std::atomic<uint64_t> &smem_attr_done()
 {
     static std::atomic<uint64_t> mask{0};
     return mask;
 }
 
-template <int D, int NK, int NV, int NS, bool FUSED = false>
+template <int D, int NK, int NV, int NS>
 cudaError_t launch_one(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
                        const CUtensorMap &tm_sk, const CUtensorMap &tm_sv, const CUtensorMap &tm_o,
-                       const AttnParams &p, const StepParams &sp, int grid, cudaStream_t stream)
+                       const AttnParams &p, int grid, cudaStream_t stream)
 {
-    using C = AttnCfg<D, kNH, NK, NV, NS, false, FUSED>;
-    auto kern = attn_kernel<Mode::Decode, D, kNH, NK, NV, NS, false, FUSED>;
-    cudaError_t e = ensure_smem_attribute(kern, C::kSmemBytes, smem_attr_done<D, NK, NV, NS, FUSED>());
+    using C = AttnCfg<D, kNH, NK, NV, NS>;
+    auto kern = attn_kernel<Mode::Decode, D, kNH, NK, NV, NS>;
+    cudaError_t e = ensure_smem_attribute(kern, C::kSmemBytes, smem_attr_done<D, NK, NV, NS>());
     if (e != cudaSuccess) return e;
     static std::atomic<uint64_t> split_checked{0};
     e = check_register_split(kern, C::kThreads, C::kSplitRegs, split_checked);
     if (e != cudaSuccess) return e;
     return launch_dependent(kern, dim3(grid), dim3(C::kThreads), C::kSmemBytes, stream, tm_q, tm_k, tm_v, tm_sk,
-                            tm_sv, tm_o, p, sp);
+                            tm_sv, tm_o, p);
 }
 }  // namespace
 
@@ -50,21 +47,11 @@ cudaError_t launch_decode_attn(int head_dim, const CUtensorMap &tm_q, const CUte
                                const CUtensorMap &tm_v, const CUtensorMap &tm_sk, const CUtensorMap &tm_sv,
                                const CUtensorMap &tm_o, const AttnParams &p, int grid, cudaStream_t stream)
 {
-    const StepParams none = {};
-    if (head_dim == 64) return launch_one<64, 4, 4, 3>(tm_q, tm_k, tm_v, tm_sk, tm_sv, tm_o, p, none, grid, stream);
-    if (head_dim == 128) return launch_one<128, 3, 2, 2>(tm_q, tm_k, tm_v, tm_sk, tm_sv, tm_o, p, none, grid, stream);
+    if (head_dim == 64) return launch_one<64, 4, 4, 3>(tm_q, tm_k, tm_v, tm_sk, tm_sv, tm_o, p, grid, stream);
+    if (head_dim == 128) return launch_one<128, 3, 2, 2>(tm_q, tm_k, tm_v, tm_sk, tm_sv, tm_o, p, grid, stream);
     return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_decode_step_fused(int head_dim, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
-                                     const CUtensorMap &tm_v, const CUtensorMap &tm_o, const AttnParams &p,
-                                     const StepParams &sp, int grid, cudaStream_t stream)
-{
-    if (head_dim == 64) return launch_one<64, 4, 4, 3, true>(tm_q, tm_k, tm_v, tm_q, tm_q, tm_o, p, sp, grid, stream);
-    return cudaErrorInvalidValue;   // head_dim 128: no shared memory left for the gatherer's staging
-}
-
-bool decode_step_one_launch(int head_dim) { return head_dim == 64; }
 
 
 }  // namespace bg

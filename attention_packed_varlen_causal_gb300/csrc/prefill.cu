@@ -109,9 +109,8 @@ cudaError_t launch_one(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const C
     static std::atomic<uint64_t> split_checked{0};
     e = check_register_split(kern, C::kThreads, C::kSplitRegs, split_checked);
     if (e != cudaSuccess) return e;
-    const StepParams none = {};
     return launch_dependent(kern, dim3(grid), dim3(C::kThreads), C::kSmemBytes, stream, tm_q, tm_k, tm_v, tm_k, tm_v,
-                            tm_o, p, none);   // no suffix maps, no step operands
+                            tm_o, p);   // no suffix maps
 }
 }  // namespace
 

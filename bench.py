@@ -267,7 +267,7 @@ class DecodeStack:
             by += b
         self.flops_per_search = fl * layers
         self.bytes_per_search = by * layers
-        self.launches = S * layers * (1 if d == 64 else 2)   # one kernel per step and layer at head_dim 64
+        self.launches = 2 * S * layers            # reorder + attention per step and layer
 
     def enqueue(self, stream):
         bg = self.bg

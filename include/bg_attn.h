@@ -281,14 +281,10 @@ bg_status_t bg_beam_suffix_reorder(const void *src_k, const void *src_v,
  * the call computes
  *     bg_beam_suffix_reorder(src, dst, parent_idx, new, n_tokens = t - 1)
  *     bg_beam_decode_attn(q, ..., suffix = dst, suffix_len = t)
- * with the arguments of both checked together before anything is enqueued,
- * and gives bit for bit the same output and dst; dst then holds the
- * reordered suffix, the next step's src.  At head_dim 64 it runs as ONE
- * launch: a gatherer warp of the attention kernel builds each suffix key tile
- * straight from src through parent_idx (no separate reorder pass, no re-read
- * of dst) and writes the tile's rows to dst, while the other warps attend.
- * At head_dim 128 it is the two calls above as two launches on `stream`, the
- * second started by programmatic dependent launch.
+ * with the arguments of both checked together before anything is enqueued:
+ * two launches on `stream`, the second one started by programmatic dependent
+ * launch so that its prologue overlaps the first.  dst then holds the
+ * reordered suffix, the next step's src.
  *
  *   q, prompt_k, prompt_v, cu_prompt, total_prompt_tokens, max_prompt_len,
  *   R, W, Hq, Hkv, head_dim, scale, out    as in bg_beam_decode_attn

@@ -7,9 +7,7 @@ three ways on the same seeded inputs:
     bit for bit;
   * the output matches the fp64 oracle within the decode tolerance;
   * output and suffix are bit-identical to the two separate calls
-    (bg_beam_suffix_reorder, then bg_beam_decode_attn): the step's one launch
-    builds the same suffix key tiles through the parent index that the two
-    calls build by moving the suffix first.
+    (bg_beam_suffix_reorder, then bg_beam_decode_attn).
 Both suffix buffers start as bf16 NaN, so a row read before it was written
 would poison the output."""
 import math
