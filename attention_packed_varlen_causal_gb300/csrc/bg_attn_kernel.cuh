@@ -113,7 +113,7 @@ struct AttnCfg {
     static constexpr int kStageBytes = 32 * 64;
     static constexpr int kOffBar = kOffStage + 4 * NH * kStageBytes;
     // q_full[2] q_empty[2] mma_final k_full[NK] k_empty[NK] v_full[NV] v_empty[NV] s_full[NH][NS]
-    // p_full[NH][NS] pv_done[NH][NS] o_staged[NH][2]
+    // p_full[NH][NS] (one arrive per softmax warp) pv_done[NH][NS] o_staged[NH][2]
     static constexpr int kNumBars = 5 + 2 * NK + 2 * NV + 3 * NS * NH + 2 * NH;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + slack for 1024-byte alignment
@@ -340,7 +340,7 @@ __global__ void __maxnreg__((AttnCfg<D, NH, NK, NV, NS, QK8>::kRegsLaunch))
         }
         for (int i = 0; i < NS * NH; ++i) {
             mbar_init(&s_full[i], 1);
-            mbar_init(&p_full[i], 128);
+            mbar_init(&p_full[i], 4);     // one arrive per softmax warp
             mbar_init(&pv_done[i], 1);
         }
         for (int i = 0; i < 2 * NH; ++i) mbar_init(&o_staged[i], 4);   // one arrive per warp
@@ -860,14 +860,20 @@ __global__ void __maxnreg__((AttnCfg<D, NH, NK, NV, NS, QK8>::kRegsLaunch))
                     // the previous item's O is read before this tile's P.V may overwrite it
                     if (!epilogue(Ip, mp, lp, gp, qbp, tmap, [&]() {
                             tc_fence_before();
-                            mbar_arrive(&p_full[NS * h + g % NS]);
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(&p_full[NS * h + g % NS]);
                         })) {
                         ok = false;
                         break;
                     }
                     pend = false;
                 } else {
-                    mbar_arrive(&p_full[NS * h + g % NS]);
+                    // one arrive per warp: every lane's P stores are complete (wait::st) and
+                    // fenced (fence::before_thread_sync) before the warp synchronises, and the
+                    // arrive releases them to the MMA thread (32 arrives on one barrier from one
+                    // warp would be serialised, about 600 cycles per tile on this critical path)
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&p_full[NS * h + g % NS]);
                 }
             }
             if (!ok) break;
