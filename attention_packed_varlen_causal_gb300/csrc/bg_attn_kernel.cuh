@@ -597,6 +597,18 @@ __global__ void __maxnreg__((AttnCfg<D, NH, NK, NV, NS, QK8>::kRegsLaunch))
         // buffer, hands it back to the Q producer.  The warps do not wait for the global writes.
         // Other tiles, and every prefill tile, are stored row by row through the staging area.
         uint32_t n_tma = 0;   // output tiles this warpgroup stored through the TMA unit so far
+        // Q buffer (+1) that the group leader still has to hand back once the TMA unit has read
+        // the output tile it staged there, or 0.  Handed back after the next tile's scores are
+        // turned into P, or at the end of the item at the latest -- before the Q load of the item
+        // after next, which waits for it.
+        int q_release = 0;
+        auto release_q_buffer = [&]() {
+            if (q_release) {
+                bulk_wait_read_all();
+                mbar_arrive(&q_empty[q_release - 1]);
+                q_release = 0;
+            }
+        };
         auto epilogue = [&](const Item &I, float m, float l, uint32_t g_last, int qbi, bool via_tma,
                             auto &&release) -> bool {
                 // The commit after the item's last P.V covers every earlier MMA too.  (Items always
@@ -690,8 +702,10 @@ __global__ void __maxnreg__((AttnCfg<D, NH, NK, NV, NS, QK8>::kRegsLaunch))
                                 tma_store_4d(&tm_o, tile + cb * kQBox, cb * 64, 0, I.kh, I.r * p.W + (I.bt0 + h) * p.BT);
                         }
                         bulk_commit_group();
-                        bulk_wait_read_all();
-                        mbar_arrive(&q_empty[qbi]);    // the Q producer may refill the buffer
+                        // the Q buffer goes back to its producer once the TMA unit has read the
+                        // tile out of it; that wait happens later (release_q_buffer), so that this
+                        // thread's softmax work does not wait for it
+                        q_release = qbi + 1;
                     }
                 } else {
 #pragma unroll
@@ -874,8 +888,10 @@ __global__ void __maxnreg__((AttnCfg<D, NH, NK, NV, NS, QK8>::kRegsLaunch))
                     // warp would be serialised, about 600 cycles per tile on this critical path)
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&p_full[NS * h + g % NS]);
+                    if (quad == 0 && lane == 0) release_q_buffer();
                 }
             }
+            if (quad == 0 && lane == 0) release_q_buffer();   // an item of one tile
             if (!ok) break;
             pend = true;
             qbp = (nq - 1) & 1;
@@ -887,7 +903,10 @@ __global__ void __maxnreg__((AttnCfg<D, NH, NK, NV, NS, QK8>::kRegsLaunch))
         }
         if (ok && pend) ok = epilogue(Ip, mp, lp, gp, qbp, tmap, []() {});
         // every tile store this thread issued has written global memory before the CTA exits
-        if (quad == 0 && lane == 0) bulk_wait_all();
+        if (quad == 0 && lane == 0) {
+            release_q_buffer();
+            bulk_wait_all();
+        }
 
         (void)ok;
     }
