@@ -9,32 +9,48 @@
 // the W best (b, v) of a request are kept, best first, equal scores by the
 // smaller b * V + v.
 //
-// Two launches on the caller's stream:
-//   1. row_select_kernel, one CTA per beam row: one pass over the row from HBM
-//      computes its logsumexp (online max and sum of exponentials) and a
-//      4096-bin histogram of the top 12 bits of an order-preserving integer key
-//      of every logit; a second pass (the row is still in L2) gathers the
-//      logits at or above the bin that holds the W-th largest into shared
-//      memory (two more radix levels narrow the bin when it holds too many), a
-//      bitonic sort orders them, and the beam's W best (value, token) and its
-//      logsumexp go to the workspace.  A beam's W best tokens contain its whole
-//      share of the request's W best candidates.
-//   2. the merge, the same selection over the W x W local candidates of a request keyed
+// Three launches on the caller's stream:
+//   1. row_select_kernel, one CTA per beam row, two passes over the row.  The first
+//      (from HBM) computes the row's logsumexp and the maximum of each of 2048
+//      interleaved groups of its logits; those maxima are 2048 distinct logits, so
+//      the W-th largest of them (narrowed by a radix selection on an order-preserving
+//      integer key) bounds the row's W-th best from below.  The second pass (the row
+//      is still in L2) gathers the few logits at or above the bound into shared
+//      memory, and a bitonic sort in registers orders them: the beam's W best
+//      (value, token) and its logsumexp go to the workspace.  A beam's W best tokens
+//      contain its whole share of the request's W best candidates.
+//   2. the merge, a radix selection over the W x W local candidates of a request keyed
 //      by their scores, in two levels so that more than R CTAs share it:
 //      merge_part_kernel selects the W best of each of S slices of beams, and
-//      merge_final_kernel the W best of the S * W survivors of each request.
-// HBM-bound: the logits are read once; everything else stays on chip or in L2.
+//   3. merge_final_kernel the W best of the S * W survivors of each request.
+// HBM-bound: the logits come from HBM once; everything else stays on chip or in L2.
 #include "bg_internal.h"
 #include "bg_ptx.cuh"
 
 #include <stdint.h>
 
+#include <atomic>
+
 namespace bg {
 namespace {
 
 constexpr int kSelThreads = 512;
-constexpr int kCap = 2048;          // candidates a CTA can gather and sort
+constexpr int kCap = 2048;          // ck/ci entries: filtered logits, the sort's exchange halves
 constexpr int kBins = 4096;         // 12-bit radix digits
+
+// Row selection: kRowLoads float4 loads per thread in flight; 4 * kSelThreads groups
+// of logits give the maxima that bound the row's W-th best; the float4 groups holding a
+// logit at or above that bound are gathered, at most kGather logits (a row with more
+// takes the full radix path).
+constexpr int kRowLoads = 8;
+constexpr int kGather = 4096;
+constexpr int kBoundCap = 448;                         // group maxima at or above the bound
+constexpr int kRowDynSmem = kGather * 8;               // gathered logits: value + token
+static_assert(kGather % 4 == 0, "gathered float4 groups stay 16-byte aligned");
+static_assert(4 * kSelThreads >= BG_MAX_BEAM, "there are at least W group maxima");
+static_assert(kSelThreads / 32 <= 32, "one warp holds the per-warp totals");
+static_assert(kCap >= 2 * kSelThreads, "ck/ci hold the register sort's two exchange halves");
+static_assert(kSelThreads >= BG_MAX_BEAM, "a selection sorts W entries at once");
 
 // Order-preserving map fp32 -> uint32: a larger float gets a larger key (-inf lowest).
 __device__ __forceinline__ uint32_t f2key(float f)
@@ -47,10 +63,12 @@ __device__ __forceinline__ float key2f(uint32_t k)
     return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
 
-struct SelShared {
+// Shared state of a selection; CAP = the candidates it can gather and sort.
+template <int CAP>
+struct SelState {
     uint32_t hist[kBins];
-    uint32_t ck[kCap];
-    int32_t ci[kCap];
+    uint32_t ck[CAP];
+    int32_t ci[CAP];
     float red_m[kSelThreads / 32];
     float red_s[kSelThreads / 32];
     uint32_t warp_tot[kSelThreads / 32];
@@ -58,11 +76,17 @@ struct SelShared {
     uint32_t digit;        // selected bin of the current level
     uint32_t above;        // keys in higher bins of the current level (plus earlier levels)
 };
+using SelShared = SelState<kCap>;
+
+struct RowShared : SelState<kCap> {
+    int count;             // logits gathered by the second pass
+};
 
 // Finds, over hist[0..nbins), the bin d where the count of keys in bins >= d first
 // reaches `need` (counting from the top).  Writes sh.digit = d and adds the count of
 // keys in bins > d to sh.above.  nbins = kBins or 256; all threads call it.
-__device__ void find_digit(SelShared &sh, int nbins, uint32_t need)
+template <class Sh>
+__device__ void find_digit(Sh &sh, int nbins, uint32_t need)
 {
     const int tid = threadIdx.x;
     const int per = nbins / kSelThreads > 0 ? nbins / kSelThreads : 1;   // bins per thread (8 or 1)
@@ -81,8 +105,10 @@ __device__ void find_digit(SelShared &sh, int nbins, uint32_t need)
     }
     if (lane == 31) sh.warp_tot[warp] = incl;
     __syncthreads();
-    uint32_t before = 0;
-    for (int w = 0; w < warp; ++w) before += sh.warp_tot[w];
+    // totals of the warps before this one: lane w < warp contributes warp w's, summed over the warp
+    uint32_t before = lane < warp ? sh.warp_tot[lane] : 0u;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) before += __shfl_xor_sync(0xffffffffu, before, o);
     const uint32_t excl = before + incl - local;
     __syncthreads();
     if (tid < active && excl < need && excl + local >= need) {
@@ -101,42 +127,8 @@ __device__ void find_digit(SelShared &sh, int nbins, uint32_t need)
     __syncthreads();
 }
 
-// Sorts sh.ck/ci[0..n) (padded to a power of two with sentinels) so that higher keys
-// come first and equal keys keep the smaller index first.
-__device__ void sort_candidates(SelShared &sh, int n)
-{
-    int P = 2;
-    while (P < n) P <<= 1;
-    for (int i = n + threadIdx.x; i < P; i += kSelThreads) {
-        sh.ck[i] = 0u;
-        sh.ci[i] = 0x7fffffff;
-    }
-    __syncthreads();
-    for (int k = 2; k <= P; k <<= 1) {
-        for (int j = k >> 1; j > 0; j >>= 1) {
-            for (int i = threadIdx.x; i < P; i += kSelThreads) {
-                const int l = i ^ j;
-                if (l > i) {
-                    const uint32_t ka = sh.ck[i], kb = sh.ck[l];
-                    const int32_t ia = sh.ci[i], ib = sh.ci[l];
-                    const bool a_first = ka > kb || (ka == kb && ia < ib);
-                    const bool first_half = (i & k) == 0;
-                    if (first_half != a_first) {
-                        sh.ck[i] = kb;
-                        sh.ck[l] = ka;
-                        sh.ci[i] = ib;
-                        sh.ci[l] = ia;
-                    }
-                }
-            }
-            __syncthreads();
-        }
-    }
-}
-
 // Calls body(i, key(i)) for every element i < n owned by this thread, loading eight
-// keys before using any, so that eight loads per thread are in flight (the passes
-// over a row are otherwise bound by load latency, not bandwidth).
+// keys before using any, so that eight loads per thread are in flight.
 template <typename KeyFn, typename Body>
 __device__ __forceinline__ void for_each_key(int n, KeyFn key, Body body)
 {
@@ -152,77 +144,113 @@ __device__ __forceinline__ void for_each_key(int n, KeyFn key, Body body)
     for (; i < n; i += kSelThreads) body(i, key(i));
 }
 
+// Radix narrowing of the `need` highest keys, given the level-1 histogram of key >> 20
+// in sh.hist; visit(body) calls body(i, key) for every element this thread owns (keys
+// of 0 may stand for elements that take no part, if need never reaches them).  Returns
+// the bottom lo of a radix bin with between need and cap keys >= lo (exact = false), or,
+// when the last level's bin still holds too many, the exact key T of the need-th highest
+// (exact = true; sh.above = the number of keys > T, sh.hist[sh.digit] = the number of
+// keys equal to T).  Leaves sh.hist in use: the caller synchronises before clearing it.
+template <class Sh, typename VisitFn>
+__device__ uint32_t radix_cut(Sh &sh, uint32_t need, uint32_t cap, VisitFn visit, bool &exact)
+{
+    const int tid = threadIdx.x;
+    if (tid == 0) sh.above = 0;
+    __syncthreads();
+    exact = false;
+    find_digit(sh, kBins, need);
+    const uint32_t d1 = sh.digit;
+    if (sh.above + sh.hist[d1] <= cap) return d1 << 20;
+    // level 2: bits 19..8 of the keys in bin d1
+    const uint32_t need1 = need - sh.above;
+    __syncthreads();
+    for (int b = tid; b < kBins; b += kSelThreads) sh.hist[b] = 0u;
+    __syncthreads();
+    visit([&](int, uint32_t k) {
+        if ((k >> 20) == d1) atomicAdd(&sh.hist[(k >> 8) & 0xfffu], 1u);
+    });
+    __syncthreads();
+    find_digit(sh, kBins, need1);
+    const uint32_t d2 = sh.digit;
+    if (sh.above + sh.hist[d2] <= cap) return (d1 << 20) | (d2 << 8);
+    // level 3: bits 7..0 give the exact key T of the need-th element
+    const uint32_t need2 = need - sh.above;
+    const uint32_t pre = (d1 << 12) | d2;
+    __syncthreads();
+    for (int b = tid; b < 256; b += kSelThreads) sh.hist[b] = 0u;
+    __syncthreads();
+    visit([&](int, uint32_t k) {
+        if ((k >> 8) == pre) atomicAdd(&sh.hist[k & 0xffu], 1u);
+    });
+    __syncthreads();
+    find_digit(sh, 256, need2);
+    exact = true;
+    return (pre << 8) | sh.digit;
+}
+
+// Sorts one (key, token) per thread, threads [0, P) for P a power of two <= kSelThreads,
+// so that thread t ends with the t-th best (higher key first, equal keys by the smaller
+// token); a bitonic network whose exchanges at distance < 32 are warp shuffles and the
+// others go through xk/xt (two halves of 2 * kSelThreads entries, alternated so that one
+// barrier per exchange suffices).  Threads >= P sort their own entries among themselves.
+__device__ __forceinline__ void sort_in_registers(uint32_t &key, int32_t &tok, int P, uint32_t *xk, int32_t *xt)
+{
+    const int t = threadIdx.x;
+    int buf = 0;
+    for (int k = 2; k <= P; k <<= 1) {
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            uint32_t ok;
+            int32_t ot;
+            if (j < 32) {
+                ok = __shfl_xor_sync(0xffffffffu, key, j);
+                ot = __shfl_xor_sync(0xffffffffu, tok, j);
+            } else {
+                xk[buf * kSelThreads + t] = key;
+                xt[buf * kSelThreads + t] = tok;
+                __syncthreads();
+                ok = xk[buf * kSelThreads + (t ^ j)];
+                ot = xt[buf * kSelThreads + (t ^ j)];
+                buf ^= 1;
+            }
+            const bool mine_better = key > ok || (key == ok && tok < ot);
+            const bool keep_better = ((t & j) == 0) == ((t & k) == 0);
+            if (mine_better != keep_better) {
+                key = ok;
+                tok = ot;
+            }
+        }
+    }
+}
+
 // Selection of the W highest keys of n elements (key(i) for element i; equal keys by
 // smaller i), given the level-1 histogram of key >> 20 in sh.hist.  visit(body) calls
 // body(i, key(i)) for every element this thread owns, in any order (the bulk passes);
-// key(i) itself serves the rare in-order pass over equal keys.  Leaves the W winners
-// sorted in sh.ck/ci[0..W).  n >= W >= 1.
+// key(i) itself serves the rare in-order pass over equal keys.  At most kSelThreads
+// candidates are gathered and sorted in registers; leaves the W winners sorted in
+// sh.ck/ci[0..W).  n >= W >= 1, W <= kSelThreads.
 template <typename KeyFn, typename VisitFn>
 __device__ void select_top(SelShared &sh, int n, int W, KeyFn key, VisitFn visit)
 {
     const int tid = threadIdx.x;
-    if (tid == 0) {
-        sh.above = 0;
-        sh.n_cand = 0;
-    }
+    bool exact;
+    const uint32_t lo = radix_cut(sh, static_cast<uint32_t>(W), static_cast<uint32_t>(kSelThreads), visit, exact);
     __syncthreads();
-    find_digit(sh, kBins, static_cast<uint32_t>(W));
-    const uint32_t d1 = sh.digit;
-    uint32_t lo_key;                    // gather every key >= lo_key (all fit) ...
-    bool exact = false;                 // ... or, at the last level, keys > T and the first equal ones
-    if (sh.above + sh.hist[d1] <= static_cast<uint32_t>(kCap)) {
-        lo_key = d1 << 20;
-    } else {
-        // level 2: bits 19..8 of the keys in bin d1
-        const uint32_t need1 = static_cast<uint32_t>(W) - sh.above;
-        __syncthreads();
-        for (int b = tid; b < kBins; b += kSelThreads) sh.hist[b] = 0u;
-        __syncthreads();
-        visit([&](int, uint32_t k) {
-            if ((k >> 20) == d1) atomicAdd(&sh.hist[(k >> 8) & 0xfffu], 1u);
-        });
-        __syncthreads();
-        find_digit(sh, kBins, need1);
-        const uint32_t d2 = sh.digit;
-        if (sh.above + sh.hist[d2] <= static_cast<uint32_t>(kCap)) {
-            lo_key = (d1 << 20) | (d2 << 8);
-        } else {
-            // level 3: bits 7..0 give the exact key T of the W-th element
-            const uint32_t need2 = static_cast<uint32_t>(W) - sh.above;
-            const uint32_t pre = (d1 << 12) | d2;
-            __syncthreads();
-            for (int b = tid; b < 256; b += kSelThreads) sh.hist[b] = 0u;
-            __syncthreads();
-            visit([&](int, uint32_t k) {
-                if ((k >> 8) == pre) atomicAdd(&sh.hist[k & 0xffu], 1u);
-            });
-            __syncthreads();
-            find_digit(sh, 256, need2);
-            lo_key = (pre << 8) | sh.digit;
-            exact = true;
+    if (tid == 0) sh.n_cand = 0;
+    __syncthreads();
+    // every key >= lo (all fit), or, at the last level, the keys above T ...
+    visit([&](int i, uint32_t k) {
+        if (exact ? k > lo : k >= lo) {
+            const int pos = atomicAdd(&sh.n_cand, 1);
+            if (pos < kSelThreads) {   // always (at most kSelThreads qualify); guards shared memory
+                sh.ck[pos] = k;
+                sh.ci[pos] = i;
+            }
         }
-    }
+    });
     __syncthreads();
-    if (!exact) {
-        visit([&](int i, uint32_t k) {
-            if (k >= lo_key) {
-                const int pos = atomicAdd(&sh.n_cand, 1);
-                sh.ck[pos] = k;
-                sh.ci[pos] = i;
-            }
-        });
-        __syncthreads();
-    } else {
-        // keys above T (fewer than W), then the first W - above keys equal to T in index order
-        const uint32_t T = lo_key;
-        visit([&](int i, uint32_t k) {
-            if (k > T) {
-                const int pos = atomicAdd(&sh.n_cand, 1);
-                sh.ck[pos] = k;
-                sh.ci[pos] = i;
-            }
-        });
-        __syncthreads();
+    if (exact) {
+        // ... then the first W - above keys equal to T in index order
+        const uint32_t T = lo;
         const int base = sh.n_cand;
         const int need = W - base;
         int taken = 0;
@@ -248,66 +276,200 @@ __device__ void select_top(SelShared &sh, int n, int W, KeyFn key, VisitFn visit
         if (tid == 0) sh.n_cand = W;
         __syncthreads();
     }
-    sort_candidates(sh, sh.n_cand);
+    const int nc = min(sh.n_cand, kSelThreads);
+    uint32_t k = 0u;
+    int32_t t = 0x7fffffff;
+    if (tid < nc) {
+        k = sh.ck[tid];
+        t = sh.ci[tid];
+    }
+    __syncthreads();
+    int P = 32;
+    while (P < nc) P <<= 1;
+    sort_in_registers(k, t, P, sh.ck, sh.ci);
+    __syncthreads();
+    sh.ck[tid] = k;
+    sh.ci[tid] = t;
+    __syncthreads();
 }
 
+// Gathers into sh.ck/ci (key, token) a superset, at most cap >= W entries, of the W best
+// of the n buffered entries (key descending, token ascending), and returns the bound that
+// every later logit of the row must pass to possibly join them: key >= lo, or key > lo
+// when `strict` (later logits have larger tokens, so they lose ties at lo).
+template <class Sh>
+__device__ uint32_t row_reduce(Sh &sh, const float *bval, const int32_t *btok, int n, int V, int W, int cap,
+                               bool &strict)
+{
+    const int tid = threadIdx.x;
+    // an entry's key; 0 (below every logit's key) for the padding past V of a group
+    auto bkey = [&](int e) -> uint32_t { return btok[e] < V ? f2key(bval[e]) : 0u; };
+    for (int b = tid; b < kBins; b += kSelThreads) sh.hist[b] = 0u;
+    __syncthreads();
+    for (int e = tid; e < n; e += kSelThreads) atomicAdd(&sh.hist[bkey(e) >> 20], 1u);
+    __syncthreads();
+    auto visit = [&](auto &&body) {
+        for (int e = tid; e < n; e += kSelThreads) body(e, bkey(e));
+    };
+    bool exact;
+    const uint32_t lo = radix_cut(sh, static_cast<uint32_t>(W), static_cast<uint32_t>(cap), visit, exact);
+    const uint32_t above = exact ? sh.above : 0u;
+    const uint32_t n_eq = exact ? sh.hist[sh.digit] : 0u;
+    __syncthreads();
+    if (tid == 0) sh.n_cand = 0;
+    __syncthreads();
+    strict = exact;
+    auto append = [&](uint32_t k, int32_t tok) {
+        const int pos = atomicAdd(&sh.n_cand, 1);
+        if (pos < cap) {   // always (at most cap entries qualify); guards shared memory
+            sh.ck[pos] = k;
+            sh.ci[pos] = tok;
+        }
+    };
+    if (!exact || above + n_eq <= static_cast<uint32_t>(cap)) {
+        // every entry >= lo fits (with exact: all the entries tied at T come along)
+        visit([&](int e, uint32_t k) {
+            if (k >= lo) append(k, btok[e]);
+        });
+    } else {
+        // More entries tie at T than fit: the entries above T, then of the tied ones those
+        // with the smallest tokens, by the same radix narrowing over ~token (distinct keys,
+        // all >= 2^31 since tokens < 2^31; entries off T take key 0 and no part).
+        visit([&](int e, uint32_t k) {
+            if (k > lo) append(k, btok[e]);
+        });
+        auto visit_tok = [&](auto &&body) {
+            for (int e = tid; e < n; e += kSelThreads)
+                body(e, bkey(e) == lo ? ~static_cast<uint32_t>(btok[e]) : 0u);
+        };
+        for (int b = tid; b < kBins; b += kSelThreads) sh.hist[b] = 0u;
+        __syncthreads();
+        visit_tok([&](int, uint32_t k) {
+            if (k) atomicAdd(&sh.hist[k >> 20], 1u);
+        });
+        __syncthreads();
+        bool exact_tok;
+        const uint32_t lo_tok = radix_cut(sh, static_cast<uint32_t>(W) - above, static_cast<uint32_t>(cap) - above,
+                                          visit_tok, exact_tok);
+        __syncthreads();
+        visit_tok([&](int e, uint32_t k) {
+            if (k && k >= lo_tok) append(lo, btok[e]);
+        });
+    }
+    __syncthreads();
+    if (tid == 0 && sh.n_cand > cap) sh.n_cand = cap;
+    __syncthreads();
+    return lo;
+}
+
+// Streams the float4 groups [0, n4) of a row, this thread taking every kSelThreads-th:
+// consume(f, i0) gets four float4 at a time, groups i0 + u * kSelThreads (u < 4, -inf
+// past the row).  kRowLoads loads are in flight before the first is used, and each half
+// is reissued for the next batch as soon as it has been consumed; full batches load
+// without bounds checks.
+template <typename Load, typename Consume>
+__device__ __forceinline__ void stream_row(int n4, Load load, Consume consume)
+{
+    constexpr int U = kRowLoads, H = kRowLoads / 2;
+    constexpr int kStep = U * kSelThreads;
+    const float4 pad = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    const int tid = static_cast<int>(threadIdx.x);
+    // batch b0 covers groups [b0, b0 + kStep); b0 is the same in every thread, so every
+    // thread runs the same iterations (consume may use warp-wide votes)
+    auto fetch = [&](int b0, int u) -> float4 {
+        const int i = b0 + tid + u * kSelThreads;
+        return (b0 + kStep <= n4 || i < n4) ? load(i) : pad;
+    };
+    float4 f[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) f[u] = fetch(0, u);
+    for (int b0 = 0; b0 < n4; b0 += kStep) {
+        const int nx = b0 + kStep;
+        consume(f, b0 + tid);
+#pragma unroll
+        for (int u = 0; u < H; ++u) f[u] = fetch(nx, u);
+        consume(f + H, b0 + tid + H * kSelThreads);
+#pragma unroll
+        for (int u = H; u < U; ++u) f[u] = fetch(nx, u);
+    }
+}
+
+template <bool VEC>
 __global__ void __launch_bounds__(kSelThreads)
     row_select_kernel(const float *__restrict__ logits, int32_t V, int32_t W, float *__restrict__ cand_val,
                       int32_t *__restrict__ cand_tok, float *__restrict__ row_lse)
 {
-    __shared__ SelShared sh;
+    __shared__ RowShared sh;
+    extern __shared__ __align__(16) uint32_t row_buf[];
+    float *bval = reinterpret_cast<float *>(row_buf);
+    int32_t *btok = reinterpret_cast<int32_t *>(row_buf + kGather);
     grid_dep_launch();
     const int tid = threadIdx.x;
+    const int lane = tid & 31, warp = tid >> 5;
     for (int b = tid; b < kBins; b += kSelThreads) sh.hist[b] = 0u;
+    if (tid == 0) sh.count = 0;
     grid_dep_wait();     // the previous kernel of the stream has completed
     __syncthreads();
     const int64_t row = blockIdx.x;
     const float *x = logits + row * static_cast<int64_t>(V);
-    constexpr float kL2E = 1.4426950408889634f;
-    // pass 1: online max / sum of exponentials and the level-1 histogram
-    float m = -INFINITY, s = 0.f;
-    auto add4 = [&](float a, float b, float c, float d) {
-        const float mx = fmaxf(fmaxf(a, b), fmaxf(c, d));
-        const float mn = fmaxf(m, mx);
-        if (mn > -INFINITY) {
-            const float nl = -mn * kL2E;   // 2^(x log2e - mn log2e) = e^(x - mn), one FFMA per exponent
-            s = s * ex2(fmaf(m, kL2E, nl)) + ex2(fmaf(a, kL2E, nl)) + ex2(fmaf(b, kL2E, nl)) + ex2(fmaf(c, kL2E, nl)) +
-                ex2(fmaf(d, kL2E, nl));
-            m = mn;
-        }
-        atomicAdd(&sh.hist[f2key(a) >> 20], 1u);
-        atomicAdd(&sh.hist[f2key(b) >> 20], 1u);
-        atomicAdd(&sh.hist[f2key(c) >> 20], 1u);
-        atomicAdd(&sh.hist[f2key(d) >> 20], 1u);
+    const int n4 = (V + 3) >> 2;
+    // float4 group i of the row: logits 4i .. 4i+3 (-inf past V); VEC: V % 4 == 0, so the
+    // rows start 16-byte aligned, as the logits do
+    auto load_keep = [&](int i) -> float4 {      // first pass: the second reads it again (L2)
+        const int e = 4 * i;
+        if (VEC) return *reinterpret_cast<const float4 *>(x + e);
+        return make_float4(x[e], e + 1 < V ? x[e + 1] : -INFINITY, e + 2 < V ? x[e + 2] : -INFINITY,
+                           e + 3 < V ? x[e + 3] : -INFINITY);
     };
-    if ((V & 3) == 0) {
-        const float4 *x4 = reinterpret_cast<const float4 *>(x);
-        const int n4 = V / 4;
-        int i = tid;
-        for (; i + 3 * kSelThreads < n4; i += 4 * kSelThreads) {
-            float4 f[4];   // four loads in flight before any is used
+    auto load_last = [&](int i) -> float4 {      // second pass: the row's last use
+        const int e = 4 * i;
+        if (VEC) return __ldcs(reinterpret_cast<const float4 *>(x + e));
+        return make_float4(__ldcs(x + e), e + 1 < V ? __ldcs(x + e + 1) : -INFINITY,
+                           e + 2 < V ? __ldcs(x + e + 2) : -INFINITY, e + 3 < V ? __ldcs(x + e + 3) : -INFINITY);
+    };
+
+    // Pass 1 (HBM): the row's logsumexp, and the maximum of each of this thread's four
+    // interleaved groups of logits (components x, y, z, w of its float4 loads).
+    constexpr float kL2E = 1.4426950408889634f;
+    // Sum of exponentials relative to a lazily raised reference m (base-2 units):
+    // e^(x - M) = 2^(x log2e - m) * 2^(m - M log2e); m is raised (the sum rescaled) only
+    // when a logit exceeds it by more than 2^8, checked once per 16 logits.
+    float m = -INFINITY;
+    float2 acc = make_float2(0.f, 0.f);
+    const float2 l2e2 = make_float2(kL2E, kL2E);
+    float4 gmax = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    stream_row(n4, load_keep, [&](const float4 *f, int) {
+        gmax.x = fmaxf(fmaxf(gmax.x, f[0].x), fmaxf(fmaxf(f[1].x, f[2].x), f[3].x));
+        gmax.y = fmaxf(fmaxf(gmax.y, f[0].y), fmaxf(fmaxf(f[1].y, f[2].y), f[3].y));
+        gmax.z = fmaxf(fmaxf(gmax.z, f[0].z), fmaxf(fmaxf(f[1].z, f[2].z), f[3].z));
+        gmax.w = fmaxf(fmaxf(gmax.w, f[0].w), fmaxf(fmaxf(f[1].w, f[2].w), f[3].w));
+        float hm = -INFINITY;
 #pragma unroll
-            for (int u = 0; u < 4; ++u) f[u] = x4[i + u * kSelThreads];   // default caching: read again by the gather
+        for (int u = 0; u < 4; ++u) hm = fmaxf(hm, fmaxf(fmaxf(f[u].x, f[u].y), fmaxf(f[u].z, f[u].w)));
+        const float ml = hm * kL2E;
+        if (ml > m + 8.f) {
+            const float al = (m == -INFINITY) ? 0.f : ex2(m - ml);
+            acc = fmul2(acc, make_float2(al, al));
+            m = ml;
+        }
+        if (m > -INFINITY) {
+            const float2 nm = make_float2(-m, -m);
 #pragma unroll
-            for (int u = 0; u < 4; ++u) add4(f[u].x, f[u].y, f[u].z, f[u].w);
-        }
-        for (; i < n4; i += kSelThreads) {
-            const float4 f = x4[i];
-            add4(f.x, f.y, f.z, f.w);
-        }
-    } else {
-        for (int i = tid; i < V; i += kSelThreads) {
-            const float a = x[i];
-            const float mn = fmaxf(m, a);
-            if (mn > -INFINITY) {
-                s = s * ex2((m - mn) * kL2E) + ex2((a - mn) * kL2E);
-                m = mn;
+            for (int u = 0; u < 4; ++u) {
+                const float2 x01 = ffma2(make_float2(f[u].x, f[u].y), l2e2, nm);
+                const float2 x23 = ffma2(make_float2(f[u].z, f[u].w), l2e2, nm);
+                acc = fadd2(acc, fadd2(make_float2(ex2(x01.x), ex2(x01.y)), make_float2(ex2(x23.x), ex2(x23.y))));
             }
-            atomicAdd(&sh.hist[f2key(a) >> 20], 1u);
         }
-    }
-    // combine (m, s) over the CTA
-    const int lane = tid & 31, warp = tid >> 5;
+    });
+    // the group maxima into the level-1 histogram (padding-only groups count as -inf)
+    atomicAdd(&sh.hist[f2key(gmax.x) >> 20], 1u);
+    atomicAdd(&sh.hist[f2key(gmax.y) >> 20], 1u);
+    atomicAdd(&sh.hist[f2key(gmax.z) >> 20], 1u);
+    atomicAdd(&sh.hist[f2key(gmax.w) >> 20], 1u);
+    // logsumexp: back to (max in natural units, sum relative to it), combined over the CTA
+    float s = acc.x + acc.y;
+    m = m * 0.69314718055994530942f;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
@@ -333,44 +495,107 @@ __global__ void __launch_bounds__(kSelThreads)
             }
         }
         row_lse[row] = M + __logf(S);
+        sh.above = 0;
     }
-    // pass 2 onward: the W best logits of the row (the row is still in L2)
-    // evict-first: the gather pass is the row's last use
-    auto key = [&](int i) -> uint32_t { return f2key(__ldcs(x + i)); };
-    auto visit = [&](auto &&body) {
-        if ((V & 3) == 0) {
-            // four float4 loads in flight per thread, four keys per load
-            const float4 *x4 = reinterpret_cast<const float4 *>(x);
-            const int n4 = V / 4;
-            int j = tid;
-            for (; j + 3 * kSelThreads < n4; j += 4 * kSelThreads) {
-                float4 f[4];
+    __syncthreads();
+    // The bound lo: at least W group maxima have keys >= lo, and those maxima are W
+    // distinct logits, so every logit with key < lo has W better ones and cannot be kept.
+    // The radix narrowing over the maxima stops once at most kBoundCap of them are >= lo,
+    // which leaves about as many logits >= lo (rarely more than one per group).
+    const uint32_t gk[4] = {f2key(gmax.x), f2key(gmax.y), f2key(gmax.z), f2key(gmax.w)};
+    bool lo_exact;
+    const uint32_t lo = radix_cut(sh, static_cast<uint32_t>(W), static_cast<uint32_t>(kBoundCap),
+                                  [&](auto &&body) {
 #pragma unroll
-                for (int u = 0; u < 4; ++u) f[u] = __ldcs(x4 + j + u * kSelThreads);
+                                      for (int c = 0; c < 4; ++c) body(c, gk[c]);
+                                  },
+                                  lo_exact);
+    const float tf = lo <= 0x007fffffu ? -INFINITY : key2f(lo);   // keys below -inf's: NaN patterns
+
+    // Pass 2 (L2): gather every float4 group holding a logit >= tf (its other logits come
+    // along as harmless extra entries), one shared atomic per warp.
+    const uint32_t lt_mask = (1u << lane) - 1u;
+    stream_row(n4, load_last, [&](const float4 *f, int i0) {
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int i = 4 * (j + u * kSelThreads);
-                    body(i, f2key(f[u].x));
-                    body(i + 1, f2key(f[u].y));
-                    body(i + 2, f2key(f[u].z));
-                    body(i + 3, f2key(f[u].w));
+        for (int u = 0; u < 4; ++u) {
+            const int i = i0 + u * kSelThreads;
+            // (padding past the row is -inf: it passes only when tf is -inf, and its tokens
+            // past V give it key 0 below)
+            const bool hit = fmaxf(fmaxf(f[u].x, f[u].y), fmaxf(f[u].z, f[u].w)) >= tf;
+            const uint32_t bal = __ballot_sync(0xffffffffu, hit);
+            if (bal) {
+                int base = 0;
+                if (lane == 0) base = atomicAdd(&sh.count, 4 * __popc(bal));
+                base = __shfl_sync(0xffffffffu, base, 0);
+                const int pos = base + 4 * __popc(bal & lt_mask);
+                if (hit && pos + 4 <= kGather) {
+                    *reinterpret_cast<float4 *>(bval + pos) = f[u];
+                    *reinterpret_cast<int4 *>(btok + pos) = make_int4(4 * i, 4 * i + 1, 4 * i + 2, 4 * i + 3);
                 }
             }
-            for (; j < n4; j += kSelThreads) {
-                const float4 f = __ldcs(x4 + j);
-                body(4 * j, f2key(f.x));
-                body(4 * j + 1, f2key(f.y));
-                body(4 * j + 2, f2key(f.z));
-                body(4 * j + 3, f2key(f.w));
-            }
-        } else {
-            for_each_key(V, key, body);
         }
-    };
-    select_top(sh, V, W, key, visit);
-    for (int k = tid; k < W; k += kSelThreads) {
-        cand_val[row * W + k] = key2f(sh.ck[k]);
-        cand_tok[row * W + k] = sh.ci[k];
+    });
+    __syncthreads();
+    const int n = sh.count;
+    // an entry's key; the padding past V of a group takes key 0, below every logit's key
+    auto entry_key = [&](int e) -> uint32_t { return btok[e] < V ? f2key(bval[e]) : 0u; };
+    uint32_t key = 0u;
+    int32_t tok = 0x7fffffff;
+    int n_sort;                 // entries to sort, at most kSelThreads
+    if (n <= kGather) {
+        // the gathered logits with key >= lo (the rest of their groups dropped) into ck/ci
+        if (tid == 0) sh.n_cand = 0;
+        __syncthreads();
+        for (int e0 = 0; e0 < n; e0 += kSelThreads) {
+            const int e = e0 + tid;
+            const uint32_t k = e < n ? entry_key(e) : 0u;
+            const bool keep = e < n && k >= lo && k != 0u;
+            const uint32_t bal = __ballot_sync(0xffffffffu, keep);
+            if (bal) {
+                int base = 0;
+                if (lane == 0) base = atomicAdd(&sh.n_cand, __popc(bal));
+                base = __shfl_sync(0xffffffffu, base, 0);
+                const int pos = base + __popc(bal & lt_mask);
+                if (keep && pos < kCap) {
+                    sh.ck[pos] = k;
+                    sh.ci[pos] = btok[e];
+                }
+            }
+        }
+        __syncthreads();
+        const int kept = sh.n_cand;
+        if (kept <= kSelThreads) {
+            n_sort = kept;
+        } else {
+            // narrow the gathered entries to at most kSelThreads containing the W best
+            __syncthreads();
+            bool st;
+            row_reduce(sh, bval, btok, n, V, W, kSelThreads, st);
+            n_sort = sh.n_cand;
+        }
+    } else {
+        // more logits at the bound than fit (ties, or a flat row): the full radix selection
+        // over the row, a level-1 histogram pass and then the narrowing passes
+        for (int b = tid; b < kBins; b += kSelThreads) sh.hist[b] = 0u;
+        __syncthreads();
+        auto rkey = [&](int i) -> uint32_t { return f2key(x[i]); };
+        auto visit = [&](auto &&body) { for_each_key(V, rkey, body); };
+        visit([&](int, uint32_t k) { atomicAdd(&sh.hist[k >> 20], 1u); });
+        __syncthreads();
+        select_top(sh, V, W, rkey, visit);
+        n_sort = W;           // the W best, already in order
+    }
+    if (tid < n_sort) {
+        key = sh.ck[tid];
+        tok = sh.ci[tid];
+    }
+    __syncthreads();   // ck/ci serve as the sort's exchange buffers next
+    int P = 32;
+    while (P < n_sort) P <<= 1;
+    sort_in_registers(key, tok, P, sh.ck, sh.ci);
+    if (tid < W) {
+        cand_val[row * W + tid] = key2f(key);
+        cand_tok[row * W + tid] = tok;
     }
 }
 
@@ -464,8 +689,13 @@ cudaError_t launch_beam_select(const float *logits, const float *cum, int32_t R,
     const int64_t rows = static_cast<int64_t>(R) * W;
     if (rows == 0) return cudaSuccess;
     const int S = beam_select_slices(R, W);
-    cudaError_t e = launch_dependent(row_select_kernel, dim3(static_cast<unsigned>(rows)), dim3(kSelThreads), 0,
-                                     stream, logits, V, W, cand_val, cand_tok, row_lse);
+    static std::atomic<uint64_t> smem_set_vec{0}, smem_set_any{0};
+    const bool vec = (V & 3) == 0;
+    auto kern = vec ? row_select_kernel<true> : row_select_kernel<false>;
+    cudaError_t e = ensure_smem_attribute(kern, kRowDynSmem, vec ? smem_set_vec : smem_set_any);
+    if (e != cudaSuccess) return e;
+    e = launch_dependent(kern, dim3(static_cast<unsigned>(rows)), dim3(kSelThreads),
+                         static_cast<size_t>(kRowDynSmem), stream, logits, V, W, cand_val, cand_tok, row_lse);
     if (e != cudaSuccess) return e;
     e = launch_dependent(merge_part_kernel, dim3(static_cast<unsigned>(static_cast<int64_t>(R) * S)),
                          dim3(kSelThreads), 0, stream, static_cast<const float *>(cand_val),
