@@ -48,7 +48,7 @@ SPEC_HBM_GBS = 8000.0   # nominal GB300 HBM3e bandwidth (~8 TB/s), reported besi
 # (dram__bytes_read.sum + dram__bytes_write.sum from one ncu capture of that launch).  It holds
 # only for the sources that launch is built from, identified by `sources`
 # (kernel_sources_hash); otherwise the bench reports null.
-PREFILL_TRAFFIC = {"sources": "98df18b6da903670", "bytes": 649163520 + 244014080}
+PREFILL_TRAFFIC = {"sources": "5b1f8e65b4026414", "bytes": 648573952 + 243101184}
 # the files a bg_packed_prefill_attn launch is built from
 PREFILL_SOURCES = ["abi.cu", "prefill.cu", "bg_attn_kernel.cuh", "bg_ptx.cuh", "bg_internal.h"]
 
@@ -791,7 +791,7 @@ def run_beam_select(device, stream, peaks, reps: int = 50):
         del logits
     res["definition"] = ("bg_beam_select per decode step (per-beam logsumexp + top-W, merged by accumulated score), "
                          f"median over {reps} individually timed calls, apart from the step (not in value); "
-                         "bound: HBM, logits read once")
+                         "bound: HBM, logits read from HBM once (the second pass over a row hits L2)")
     return res
 
 
