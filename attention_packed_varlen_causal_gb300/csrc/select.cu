@@ -44,7 +44,7 @@ constexpr int kBins = 4096;         // 12-bit radix digits
 // takes the full radix path).
 constexpr int kRowLoads = 8;
 constexpr int kGather = 4096;
-constexpr int kBoundCap = 448;                         // group maxima at or above the bound
+constexpr int kBoundCap = 448;                         // most group maxima at or above the bound
 constexpr int kRowDynSmem = kGather * 8;               // gathered logits: value + token
 static_assert(kGather % 4 == 0, "gathered float4 groups stay 16-byte aligned");
 static_assert(4 * kSelThreads >= BG_MAX_BEAM, "there are at least W group maxima");
@@ -188,11 +188,12 @@ __device__ uint32_t radix_cut(Sh &sh, uint32_t need, uint32_t cap, VisitFn visit
     return (pre << 8) | sh.digit;
 }
 
-// Sorts one (key, token) per thread, threads [0, P) for P a power of two <= kSelThreads,
-// so that thread t ends with the t-th best (higher key first, equal keys by the smaller
-// token); a bitonic network whose exchanges at distance < 32 are warp shuffles and the
-// others go through xk/xt (two halves of 2 * kSelThreads entries, alternated so that one
-// barrier per exchange suffices).  Threads >= P sort their own entries among themselves.
+// Sorts one (key, token) per thread, threads [0, P) for P a power of two with
+// 32 <= P <= kSelThreads, so that thread t ends with the t-th best (higher key first, equal
+// keys by the smaller token); a bitonic network whose exchanges at distance < 32 are warp
+// shuffles and the others go through xk/xt (two halves of 2 * kSelThreads entries,
+// alternated so that one barrier per exchange suffices).  All threads call it; threads
+// >= P sort their own entries among themselves (pairs never cross a multiple of P).
 __device__ __forceinline__ void sort_in_registers(uint32_t &key, int32_t &tok, int P, uint32_t *xk, int32_t *xt)
 {
     const int t = threadIdx.x;
@@ -365,8 +366,9 @@ __device__ uint32_t row_reduce(Sh &sh, const float *bval, const int32_t *btok, i
 // Streams the float4 groups [0, n4) of a row, this thread taking every kSelThreads-th:
 // consume(f, i0) gets four float4 at a time, groups i0 + u * kSelThreads (u < 4, -inf
 // past the row).  kRowLoads loads are in flight before the first is used, and each half
-// is reissued for the next batch as soon as it has been consumed; full batches load
-// without bounds checks.
+// is reissued for the next batch as soon as it has been consumed.  Batches wholly inside
+// the row load without bounds checks; only the last, partial one checks.  Every thread
+// runs the same iterations (consume may use warp-wide votes).
 template <typename Load, typename Consume>
 __device__ __forceinline__ void stream_row(int n4, Load load, Consume consume)
 {
@@ -374,23 +376,44 @@ __device__ __forceinline__ void stream_row(int n4, Load load, Consume consume)
     constexpr int kStep = U * kSelThreads;
     const float4 pad = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
     const int tid = static_cast<int>(threadIdx.x);
-    // batch b0 covers groups [b0, b0 + kStep); b0 is the same in every thread, so every
-    // thread runs the same iterations (consume may use warp-wide votes)
-    auto fetch = [&](int b0, int u) -> float4 {
+    const int nfull = n4 / kStep;                       // batches with every group in the row
+    const bool tail = nfull * kStep < n4;
+    auto fetch_tail = [&](int b0, int u) -> float4 {
         const int i = b0 + tid + u * kSelThreads;
-        return (b0 + kStep <= n4 || i < n4) ? load(i) : pad;
+        return i < n4 ? load(i) : pad;
     };
     float4 f[U];
+    if (nfull > 0) {
 #pragma unroll
-    for (int u = 0; u < U; ++u) f[u] = fetch(0, u);
-    for (int b0 = 0; b0 < n4; b0 += kStep) {
-        const int nx = b0 + kStep;
+        for (int u = 0; u < U; ++u) f[u] = load(tid + u * kSelThreads);
+    } else {
+#pragma unroll
+        for (int u = 0; u < U; ++u) f[u] = fetch_tail(0, u);
+    }
+    for (int b = 0; b < nfull; ++b) {
+        const int b0 = b * kStep, nx = b0 + kStep;
+        const bool next_full = b + 1 < nfull;
         consume(f, b0 + tid);
+        if (next_full) {
 #pragma unroll
-        for (int u = 0; u < H; ++u) f[u] = fetch(nx, u);
+            for (int u = 0; u < H; ++u) f[u] = load(nx + tid + u * kSelThreads);
+        } else if (tail) {
+#pragma unroll
+            for (int u = 0; u < H; ++u) f[u] = fetch_tail(nx, u);
+        }
         consume(f + H, b0 + tid + H * kSelThreads);
+        if (next_full) {
 #pragma unroll
-        for (int u = H; u < U; ++u) f[u] = fetch(nx, u);
+            for (int u = H; u < U; ++u) f[u] = load(nx + tid + u * kSelThreads);
+        } else if (tail) {
+#pragma unroll
+            for (int u = H; u < U; ++u) f[u] = fetch_tail(nx, u);
+        }
+    }
+    if (tail) {
+        const int b0 = nfull * kStep;
+        consume(f, b0 + tid);
+        consume(f + H, b0 + tid + H * kSelThreads);
     }
 }
 
@@ -433,7 +456,7 @@ __global__ void __launch_bounds__(kSelThreads)
     constexpr float kL2E = 1.4426950408889634f;
     // Sum of exponentials relative to a lazily raised reference m (base-2 units):
     // e^(x - M) = 2^(x log2e - m) * 2^(m - M log2e); m is raised (the sum rescaled) only
-    // when a logit exceeds it by more than 2^8, checked once per 16 logits.
+    // when the running maximum exceeds it by more than 2^8, checked once per 16 logits.
     float m = -INFINITY;
     float2 acc = make_float2(0.f, 0.f);
     const float2 l2e2 = make_float2(kL2E, kL2E);
@@ -443,10 +466,8 @@ __global__ void __launch_bounds__(kSelThreads)
         gmax.y = fmaxf(fmaxf(gmax.y, f[0].y), fmaxf(fmaxf(f[1].y, f[2].y), f[3].y));
         gmax.z = fmaxf(fmaxf(gmax.z, f[0].z), fmaxf(fmaxf(f[1].z, f[2].z), f[3].z));
         gmax.w = fmaxf(fmaxf(gmax.w, f[0].w), fmaxf(fmaxf(f[1].w, f[2].w), f[3].w));
-        float hm = -INFINITY;
-#pragma unroll
-        for (int u = 0; u < 4; ++u) hm = fmaxf(hm, fmaxf(fmaxf(f[u].x, f[u].y), fmaxf(f[u].z, f[u].w)));
-        const float ml = hm * kL2E;
+        // the running maximum so far bounds these 16 logits as well as the batch's own would
+        const float ml = fmaxf(fmaxf(gmax.x, gmax.y), fmaxf(gmax.z, gmax.w)) * kL2E;
         if (ml > m + 8.f) {
             const float al = (m == -INFINITY) ? 0.f : ex2(m - ml);
             acc = fmul2(acc, make_float2(al, al));
@@ -500,11 +521,12 @@ __global__ void __launch_bounds__(kSelThreads)
     __syncthreads();
     // The bound lo: at least W group maxima have keys >= lo, and those maxima are W
     // distinct logits, so every logit with key < lo has W better ones and cannot be kept.
-    // The radix narrowing over the maxima stops once at most kBoundCap of them are >= lo,
+    // The radix narrowing over the maxima stops once at most bound_cap of them are >= lo,
     // which leaves about as many logits >= lo (rarely more than one per group).
     const uint32_t gk[4] = {f2key(gmax.x), f2key(gmax.y), f2key(gmax.z), f2key(gmax.w)};
     bool lo_exact;
-    const uint32_t lo = radix_cut(sh, static_cast<uint32_t>(W), static_cast<uint32_t>(kBoundCap),
+    const int bound_cap = min(kBoundCap, W + W / 2 + 32);   // >= W; fewer above the bound, fewer to sort
+    const uint32_t lo = radix_cut(sh, static_cast<uint32_t>(W), static_cast<uint32_t>(bound_cap),
                                   [&](auto &&body) {
 #pragma unroll
                                       for (int c = 0; c < 4; ++c) body(c, gk[c]);
