@@ -27,6 +27,7 @@
 #include "bg_internal.h"
 #include "bg_ptx.cuh"
 
+#include <cuda_bf16.h>
 #include <stdint.h>
 
 #include <atomic>
@@ -45,7 +46,12 @@ constexpr int kBins = 4096;         // 12-bit radix digits
 constexpr int kRowLoads = 8;
 constexpr int kGather = 4096;
 constexpr int kBoundCap = 448;                         // most group maxima at or above the bound
-constexpr int kRowDynSmem = kGather * 8;               // gathered logits: value + token
+constexpr int kGatherSmem = kGather * 8;               // gathered logits: value + token
+// Rows of at most kMaxStored float4 groups also keep, per group, its maximum truncated to
+// bf16 (2 bytes) in shared memory, so that the second pass re-reads only the groups that
+// can pass the bound instead of the whole row.
+constexpr int kMaxStored = 32768;
+constexpr int kRowDynSmemMax = kGatherSmem + kMaxStored * 2;
 static_assert(kGather % 4 == 0, "gathered float4 groups stay 16-byte aligned");
 static_assert(4 * kSelThreads >= BG_MAX_BEAM, "there are at least W group maxima");
 static_assert(kSelThreads / 32 <= 32, "one warp holds the per-warp totals");
@@ -436,6 +442,12 @@ __global__ void __launch_bounds__(kSelThreads)
     const int64_t row = blockIdx.x;
     const float *x = logits + row * static_cast<int64_t>(V);
     const int n4 = (V + 3) >> 2;
+    // group maxima kept for the second pass: this thread's j-th group (float4 tid + j *
+    // kSelThreads) at halfword tid * kJ + j, kJ = its groups rounded up to whole batches
+    const bool stored = n4 <= kMaxStored;
+    constexpr int kStep = kRowLoads * kSelThreads;
+    const int kJ = kRowLoads * ((n4 + kStep - 1) / kStep);
+    uint32_t *smax = row_buf + 2 * kGather + tid * (kJ / 2);   // this thread's kJ halfwords
     // float4 group i of the row: logits 4i .. 4i+3 (-inf past V); VEC: V % 4 == 0, so the
     // rows start 16-byte aligned, as the logits do
     auto load_keep = [&](int i) -> float4 {      // first pass: the second reads it again (L2)
@@ -461,7 +473,18 @@ __global__ void __launch_bounds__(kSelThreads)
     float2 acc = make_float2(0.f, 0.f);
     const float2 l2e2 = make_float2(kL2E, kL2E);
     float4 gmax = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-    stream_row(n4, load_keep, [&](const float4 *f, int) {
+    stream_row(n4, load_keep, [&](const float4 *f, int i0) {
+        if (stored) {
+            // the four groups' maxima as bf16 truncated toward zero (a monotone map, so a
+            // group whose maximum is >= the bound keeps a stored value >= the truncated bound)
+            uint32_t b[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                b[u] = __float_as_uint(fmaxf(fmaxf(f[u].x, f[u].y), fmaxf(f[u].z, f[u].w)));
+            const int j0 = (i0 - tid) / kSelThreads;   // a multiple of 4
+            *reinterpret_cast<uint2 *>(reinterpret_cast<uint16_t *>(smax) + j0) =
+                make_uint2(__byte_perm(b[0], b[1], 0x7632), __byte_perm(b[2], b[3], 0x7632));
+        }
         gmax.x = fmaxf(fmaxf(gmax.x, f[0].x), fmaxf(fmaxf(f[1].x, f[2].x), f[3].x));
         gmax.y = fmaxf(fmaxf(gmax.y, f[0].y), fmaxf(fmaxf(f[1].y, f[2].y), f[3].y));
         gmax.z = fmaxf(fmaxf(gmax.z, f[0].z), fmaxf(fmaxf(f[1].z, f[2].z), f[3].z));
@@ -534,9 +557,38 @@ __global__ void __launch_bounds__(kSelThreads)
                                   lo_exact);
     const float tf = lo <= 0x007fffffu ? -INFINITY : key2f(lo);   // keys below -inf's: NaN patterns
 
-    // Pass 2 (L2): gather every float4 group holding a logit >= tf (its other logits come
-    // along as harmless extra entries), one shared atomic per warp.
+    // Pass 2: gather every float4 group holding a logit >= tf (its other logits come along as
+    // harmless extra entries).
     const uint32_t lt_mask = (1u << lane) - 1u;
+    if (stored) {
+        // only the groups whose stored maximum passes the truncated bound are read again
+        const uint32_t tb = __float_as_uint(tf) >> 16;   // the bound truncated to bf16, twice
+        const uint32_t tbb = tb | (tb << 16);
+        const __nv_bfloat162 bound2 = *reinterpret_cast<const __nv_bfloat162 *>(&tbb);
+        for (int c = 0; c < kJ / 8; ++c) {
+            const uint4 w4 = reinterpret_cast<const uint4 *>(smax)[c];
+            const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const uint32_t m = __hge2_mask(*reinterpret_cast<const __nv_bfloat162 *>(&w[q]), bound2);
+                if (m) {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int i = tid + (8 * c + 2 * q + h) * kSelThreads;
+                        if (((m >> (16 * h)) & 1u) && i < n4) {
+                            const float4 f = load_last(i);
+                            const int pos = atomicAdd(&sh.count, 4);
+                            if (pos + 4 <= kGather) {
+                                *reinterpret_cast<float4 *>(bval + pos) = f;
+                                *reinterpret_cast<int4 *>(btok + pos) =
+                                    make_int4(4 * i, 4 * i + 1, 4 * i + 2, 4 * i + 3);
+                            }
+                        }
+                    }
+                }
+            }
+        }
+    } else {
     stream_row(n4, load_last, [&](const float4 *f, int i0) {
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
@@ -557,6 +609,7 @@ __global__ void __launch_bounds__(kSelThreads)
             }
         }
     });
+    }
     __syncthreads();
     const int n = sh.count;
     // an entry's key; the padding past V of a group takes key 0, below every logit's key
@@ -714,10 +767,15 @@ cudaError_t launch_beam_select(const float *logits, const float *cum, int32_t R,
     static std::atomic<uint64_t> smem_set_vec{0}, smem_set_any{0};
     const bool vec = (V & 3) == 0;
     auto kern = vec ? row_select_kernel<true> : row_select_kernel<false>;
-    cudaError_t e = ensure_smem_attribute(kern, kRowDynSmem, vec ? smem_set_vec : smem_set_any);
+    cudaError_t e = ensure_smem_attribute(kern, kRowDynSmemMax, vec ? smem_set_vec : smem_set_any);
     if (e != cudaSuccess) return e;
-    e = launch_dependent(kern, dim3(static_cast<unsigned>(rows)), dim3(kSelThreads),
-                         static_cast<size_t>(kRowDynSmem), stream, logits, V, W, cand_val, cand_tok, row_lse);
+    // the gather buffer, plus the stored group maxima when the row has at most kMaxStored groups
+    const int n4 = (V + 3) / 4;
+    constexpr int kStep = kRowLoads * kSelThreads;
+    const int kj = kRowLoads * ((n4 + kStep - 1) / kStep);
+    const size_t dyn = static_cast<size_t>(kGatherSmem) + (n4 <= kMaxStored ? static_cast<size_t>(kSelThreads) * kj * 2 : 0);
+    e = launch_dependent(kern, dim3(static_cast<unsigned>(rows)), dim3(kSelThreads), dyn, stream, logits, V, W,
+                         cand_val, cand_tok, row_lse);
     if (e != cudaSuccess) return e;
     e = launch_dependent(merge_part_kernel, dim3(static_cast<unsigned>(static_cast<int64_t>(R) * S)),
                          dim3(kSelThreads), 0, stream, static_cast<const float *>(cand_val),

@@ -185,3 +185,14 @@ def test_select_quantised_logits_ties(V):
     cum = np.full((R, W), -np.inf, dtype=np.float32)
     cum[:, 0] = 0.0
     check_against_oracle(logits, cum, exact_order=True)
+
+
+@pytest.mark.parametrize("V", [131072, 131077])
+def test_select_large_vocab(V):
+    # 131,072 logits is the largest row whose group maxima stay in shared memory for the second
+    # pass; one more float4 group (131,077) takes the path that streams the row again
+    R, W = 2, 48
+    rng = np.random.default_rng(29 + V)
+    logits = rng.normal(0, 3, size=(R, W, V)).astype(np.float32)
+    cum = rng.normal(-3, 1, size=(R, W)).astype(np.float32)
+    check_against_oracle(logits, cum)
