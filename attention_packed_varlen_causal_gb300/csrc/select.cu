@@ -52,6 +52,16 @@ constexpr int kGatherSmem = kGather * 8;               // gathered logits: value
 // can pass the bound instead of the whole row.
 constexpr int kMaxStored = 32768;
 constexpr int kRowDynSmemMax = kGatherSmem + kMaxStored * 2;
+// The merges keep their candidates' keys in shared memory: level 2 always (S * W <= 16 * 512
+// of them), level 1 when its largest slice, ceil(W / S) beams of W candidates, has at most
+// kMergeCacheKeys; otherwise level 1 recomputes them in every pass.
+constexpr int kMergeCacheKeys = 16384;
+constexpr int kMergeSmemMax = kMergeCacheKeys * 4;
+static_assert(16 * BG_MAX_BEAM <= kMergeCacheKeys, "level 2's keys always fit");
+__host__ __device__ inline bool merge_part_cached(int W, int S)
+{
+    return static_cast<int64_t>((W + S - 1) / S) * W <= kMergeCacheKeys;
+}
 static_assert(kGather % 4 == 0, "gathered float4 groups stay 16-byte aligned");
 static_assert(4 * kSelThreads >= BG_MAX_BEAM, "there are at least W group maxima");
 static_assert(kSelThreads / 32 <= 32, "one warp holds the per-warp totals");
@@ -698,13 +708,21 @@ __global__ void __launch_bounds__(kSelThreads)
     const float *lse = row_lse + r * W;
     const float *cr = cum + r * W;
     // local candidate p = candidate base + p: the k-th best token of beam b; its score as a key
-    auto key = [&](int p) -> uint32_t {
+    auto score_key = [&](int p) -> uint32_t {
         const int i = base + p;
         const int b = i / W;
         return f2key(cr[b] + (val[i] - lse[b]));
     };
-    for_each_key(n, key, [&](int, uint32_t k) { atomicAdd(&sh.hist[k >> 20], 1u); });
+    // the keys once into shared memory when they fit (every selection pass reads them again),
+    // with the level-1 histogram on the way
+    extern __shared__ __align__(16) uint32_t mkeys[];
+    const bool cached = merge_part_cached(W, S);
+    for_each_key(n, score_key, [&](int p, uint32_t k) {
+        if (cached) mkeys[p] = k;
+        atomicAdd(&sh.hist[k >> 20], 1u);
+    });
     __syncthreads();
+    auto key = [&](int p) -> uint32_t { return cached ? mkeys[p] : score_key(p); };
     // equal scores: the smaller candidate number is the smaller b * V + v (beams in order,
     // and a beam's candidates with equal scores have equal logits, kept in token order)
     select_top(sh, n, W, key, [&](auto &&body) { for_each_key(n, key, body); });
@@ -733,9 +751,15 @@ __global__ void __launch_bounds__(kSelThreads)
     const int n = S * W;
     const uint32_t *pk = part_key + r * n;
     const int32_t *pi = part_idx + r * n;
-    auto key = [&](int p) -> uint32_t { return pk[p]; };
-    for_each_key(n, key, [&](int, uint32_t k) { atomicAdd(&sh.hist[k >> 20], 1u); });
+    extern __shared__ __align__(16) uint32_t mkeys[];
+    for_each_key(
+        n, [&](int p) -> uint32_t { return pk[p]; },
+        [&](int p, uint32_t k) {
+            mkeys[p] = k;
+            atomicAdd(&sh.hist[k >> 20], 1u);
+        });
     __syncthreads();
+    auto key = [&](int p) -> uint32_t { return mkeys[p]; };
     select_top(sh, n, W, key, [&](auto &&body) { for_each_key(n, key, body); });
     for (int k = tid; k < W; k += kSelThreads) {
         const int i = pi[sh.ci[k]];
@@ -777,11 +801,18 @@ cudaError_t launch_beam_select(const float *logits, const float *cum, int32_t R,
     e = launch_dependent(kern, dim3(static_cast<unsigned>(rows)), dim3(kSelThreads), dyn, stream, logits, V, W,
                          cand_val, cand_tok, row_lse);
     if (e != cudaSuccess) return e;
+    static std::atomic<uint64_t> smem_set_part{0}, smem_set_final{0};
+    e = ensure_smem_attribute(merge_part_kernel, kMergeSmemMax, smem_set_part);
+    if (e != cudaSuccess) return e;
+    e = ensure_smem_attribute(merge_final_kernel, kMergeSmemMax, smem_set_final);
+    if (e != cudaSuccess) return e;
+    const size_t part_smem = merge_part_cached(W, S) ? static_cast<size_t>((W + S - 1) / S) * W * 4 : 0;
+    const size_t final_smem = static_cast<size_t>(S) * W * 4;
     e = launch_dependent(merge_part_kernel, dim3(static_cast<unsigned>(static_cast<int64_t>(R) * S)),
-                         dim3(kSelThreads), 0, stream, static_cast<const float *>(cand_val),
+                         dim3(kSelThreads), part_smem, stream, static_cast<const float *>(cand_val),
                          static_cast<const float *>(row_lse), cum, W, S, part_key, part_idx);
     if (e != cudaSuccess) return e;
-    return launch_dependent(merge_final_kernel, dim3(static_cast<unsigned>(R)), dim3(kSelThreads), 0, stream,
+    return launch_dependent(merge_final_kernel, dim3(static_cast<unsigned>(R)), dim3(kSelThreads), final_smem, stream,
                             static_cast<const uint32_t *>(part_key), static_cast<const int32_t *>(part_idx),
                             static_cast<const int32_t *>(cand_tok), W, S, token_out, parent_out, score_out);
 }

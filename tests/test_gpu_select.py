@@ -196,3 +196,13 @@ def test_select_large_vocab(V):
     logits = rng.normal(0, 3, size=(R, W, V)).astype(np.float32)
     cum = rng.normal(-3, 1, size=(R, W)).astype(np.float32)
     check_against_oracle(logits, cum)
+
+
+def test_select_many_requests_wide_beams():
+    # 24 requests at beam 512: 13 level-1 slices per request, whose 40 x 512 candidate keys are
+    # too many to keep in shared memory, so level 1 recomputes them in every pass
+    R, W, V = 24, 512, 600
+    rng = np.random.default_rng(30)
+    logits = rng.normal(0, 2, size=(R, W, V)).astype(np.float32)
+    cum = rng.normal(-3, 1, size=(R, W)).astype(np.float32)
+    check_against_oracle(logits, cum)
