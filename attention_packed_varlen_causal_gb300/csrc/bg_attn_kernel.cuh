@@ -367,6 +367,21 @@ __global__ void __maxnreg__((AttnCfg<D, NH, NK, NV, NS, QK8>::kRegsLaunch))
         if constexpr (MODE == Mode::Decode) {
             tma_prefetch_desc(&tm_sk);
             tma_prefetch_desc(&tm_sv);
+            // The first item's Q tiles into L2 while the previous kernel still runs: their place
+            // depends on the item number only (not on cu_prompt), and the Q load after the wait
+            // then comes from L2.
+            const int it = static_cast<int>(blockIdx.x);
+            if (it < p.n_items_decode) {
+                const int per_r = p.Hkv * p.pairs_per_rk;
+                const int r = it / per_r;
+                const int rem = it - r * per_r;
+                const int kh = rem / p.pairs_per_rk;
+                const int bt0 = (rem - kh * p.pairs_per_rk) * NH;
+#pragma unroll
+                for (int h = 0; h < NH; ++h)
+#pragma unroll
+                    for (int b = 0; b < C::NB; ++b) tma_prefetch_4d(&tm_q, b * 64, 0, kh, r * p.W + (bt0 + h) * p.BT);
+            }
         }
     }
     grid_dep_wait();     // the previous kernel of the stream has completed: inputs may be read
