@@ -39,6 +39,9 @@ SIGNATURES = {
     "bg_packed_prefill_workspace_size": ([_I32] * 6, _SZ),
     "bg_packed_prefill_attn": ([_P, _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32, _F32, _P, _P, _P, _SZ, _P, _P],
                                ctypes.c_int),
+    "bg_packed_prefill_plan": ([_P, _I32, _I32, _I32, _P, _SZ, _P, _P], ctypes.c_int),
+    "bg_packed_prefill_attn_planned": ([_P, _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32, _F32, _P, _P, _P, _SZ, _P,
+                                        _P], ctypes.c_int),
     "bg_packed_prefill_attn_fp8": ([_P, _F32, _P, _F32, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32, _F32, _P, _P, _P,
                                     _SZ, _P, _P], ctypes.c_int),
     "bg_packed_prefill_attn_noalloc": ([_P, _P, _P, _P, _I32, _I32, _I32, _I32, _I32, _I32, _F32, _P, _P, _P, _P],
@@ -135,6 +138,38 @@ def bg_packed_prefill_attn(q, k, v, cu_seqlens, max_seqlen: int, out, *, lse=Non
                                        workspace.numel() * workspace.element_size(), _ptr(dev_status),
                                        _stream(stream))
     _check("bg_packed_prefill_attn", st)
+    return out
+
+
+def bg_packed_prefill_plan(cu_seqlens, total_tokens: int, max_seqlen: int, *, workspace=None, dev_status=None,
+                           stream=None):
+    """The work list of a packing (cu_seqlens int32 [B+1] CUDA) into workspace, for
+    bg_packed_prefill_attn_planned calls with the same packing."""
+    B = cu_seqlens.numel() - 1
+    if workspace is None:
+        raise ValueError("workspace required (the library never allocates)")
+    st = load().bg_packed_prefill_plan(_ptr(cu_seqlens), B, int(total_tokens), int(max_seqlen), _ptr(workspace),
+                                       workspace.numel() * workspace.element_size(), _ptr(dev_status),
+                                       _stream(stream))
+    _check("bg_packed_prefill_plan", st)
+
+
+def bg_packed_prefill_attn_planned(q, k, v, cu_seqlens, max_seqlen: int, out, *, lse=None,
+                                   scale: Optional[float] = None, workspace=None, dev_status=None, stream=None):
+    """bg_packed_prefill_attn with the work list a bg_packed_prefill_plan call left in
+    workspace (same cu_seqlens, max_seqlen and total tokens)."""
+    T, Hq, d = q.shape
+    Hkv = k.shape[1]
+    B = cu_seqlens.numel() - 1
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if workspace is None:
+        raise ValueError("workspace required (the library never allocates)")
+    st = load().bg_packed_prefill_attn_planned(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), B, T, int(max_seqlen), Hq,
+                                               Hkv, d, float(scale), _ptr(out), _ptr(lse), _ptr(workspace),
+                                               workspace.numel() * workspace.element_size(), _ptr(dev_status),
+                                               _stream(stream))
+    _check("bg_packed_prefill_attn_planned", st)
     return out
 
 

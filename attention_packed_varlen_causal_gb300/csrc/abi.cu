@@ -152,10 +152,12 @@ namespace {
 
 // bg_packed_prefill_attn (qk8 false: bf16 Q/K) and bg_packed_prefill_attn_fp8 (qk8 true: E4M3
 // Q/K codes, whose two per-tensor scales the caller has already folded into `scale`).
+// with_plan: launch the work-list pre-pass first; otherwise the workspace holds a plan from
+// bg_packed_prefill_plan for the same cu_seqlens (bg_packed_prefill_attn_planned).
 bg_status_t prefill_impl(const void *q, const void *k, const void *v, const int32_t *cu_seqlens, int32_t num_seqs,
                          int32_t total_tokens, int32_t max_seqlen, int32_t Hq, int32_t Hkv, int32_t head_dim,
                          float scale, void *out, float *lse, void *workspace, size_t workspace_bytes,
-                         int32_t *dev_status, cudaStream_t stream, bool qk8)
+                         int32_t *dev_status, cudaStream_t stream, bool qk8, bool with_plan = true)
 {
     bool noop = false;
     const bg_status_t chk = prefill_check_args(q, k, v, cu_seqlens, num_seqs, total_tokens, max_seqlen, Hq, Hkv,
@@ -203,8 +205,9 @@ bg_status_t prefill_impl(const void *q, const void *k, const void *v, const int3
 
     int32_t *hdr = static_cast<int32_t *>(workspace);
     int4 *work = reinterpret_cast<int4 *>(static_cast<uint8_t *>(workspace) + kWorkHeaderBytes);
-    if (launch_prefill_worklist(cu_seqlens, num_seqs, total_tokens, max_seqlen, hdr, work, dev_status, stream) !=
-        cudaSuccess)
+    if (with_plan &&
+        launch_prefill_worklist(cu_seqlens, num_seqs, total_tokens, max_seqlen, hdr, work, dev_status, stream) !=
+            cudaSuccess)
         return BG_ERR_CUDA;
 
     AttnParams p;
@@ -239,6 +242,37 @@ bg_status_t bg_packed_prefill_attn(const void *q, const void *k, const void *v, 
 {
     return prefill_impl(q, k, v, cu_seqlens, num_seqs, total_tokens, max_seqlen, Hq, Hkv, head_dim, scale, out, lse,
                         workspace, workspace_bytes, dev_status, stream, false);
+}
+
+bg_status_t bg_packed_prefill_plan(const int32_t *cu_seqlens, int32_t num_seqs, int32_t total_tokens,
+                                   int32_t max_seqlen, void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                                   cudaStream_t stream)
+{
+    if (num_seqs < 0 || total_tokens < 0 || max_seqlen < 0) return BG_ERR_INVALID_ARG;
+    if (max_seqlen > BG_MAX_SEQLEN) return BG_ERR_UNSUPPORTED;
+    if (num_seqs == 0 || total_tokens == 0) return BG_OK;   // the planned run is a no-op as well
+    if (!cu_seqlens || !aligned(cu_seqlens, 4) || (dev_status && !aligned(dev_status, 4))) return BG_ERR_INVALID_ARG;
+    if (!workspace || !aligned(workspace, 256)) return BG_ERR_INVALID_ARG;
+    if (workspace_bytes < bg_packed_prefill_workspace_size(num_seqs, total_tokens, max_seqlen, 1, 1, 64))
+        return BG_ERR_INVALID_ARG;
+    if (overlap(cu_seqlens, (static_cast<size_t>(num_seqs) + 1) * 4, workspace, workspace_bytes))
+        return BG_ERR_INVALID_ARG;
+    int32_t *hdr = static_cast<int32_t *>(workspace);
+    int4 *work = reinterpret_cast<int4 *>(static_cast<uint8_t *>(workspace) + kWorkHeaderBytes);
+    return launch_prefill_worklist(cu_seqlens, num_seqs, total_tokens, max_seqlen, hdr, work, dev_status, stream) ==
+                   cudaSuccess
+               ? BG_OK
+               : BG_ERR_CUDA;
+}
+
+bg_status_t bg_packed_prefill_attn_planned(const void *q, const void *k, const void *v, const int32_t *cu_seqlens,
+                                           int32_t num_seqs, int32_t total_tokens, int32_t max_seqlen, int32_t Hq,
+                                           int32_t Hkv, int32_t head_dim, float scale, void *out, float *lse,
+                                           void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                                           cudaStream_t stream)
+{
+    return prefill_impl(q, k, v, cu_seqlens, num_seqs, total_tokens, max_seqlen, Hq, Hkv, head_dim, scale, out, lse,
+                        workspace, workspace_bytes, dev_status, stream, false, false);
 }
 
 bg_status_t bg_packed_prefill_attn_fp8(const void *q_codes, float q_scale, const void *k_codes, float k_scale,

@@ -134,6 +134,45 @@ bg_status_t bg_packed_prefill_attn(const void *q, const void *k, const void *v,
                                    int32_t *dev_status, cudaStream_t stream);
 
 /*
+ * The same prefill in two parts, for a batch whose layers share one packing
+ * (same cu_seqlens): plan once, then run every layer.  Source: as for
+ * bg_packed_prefill_attn; the work list depends on the packing alone.
+ *
+ * bg_packed_prefill_plan enqueues the work-list pre-pass: it checks
+ * cu_seqlens on the device (errors go to dev_status as for the one-call
+ * form) and writes the list into the workspace.  Arguments as for
+ * bg_packed_prefill_attn; the workspace needs
+ * bg_packed_prefill_workspace_size(num_seqs, total_tokens, ...) bytes (the
+ * head arguments of that function do not change the size).
+ *
+ * bg_packed_prefill_attn_planned enqueues only the attention.  Its arguments
+ * and result are those of bg_packed_prefill_attn, and it reads the list the
+ * last plan left in `workspace`.  That plan must have been enqueued before it,
+ * with the same cu_seqlens contents, num_seqs, total_tokens and max_seqlen.
+ * No other call may use the workspace in between (a planned run only reads
+ * it, so runs on the same stream may follow one plan).  A plan whose
+ * cu_seqlens failed the device checks makes every planned run a no-op that
+ * writes nothing, as the one-call form does.
+ *
+ * Errors: bg_packed_prefill_plan gives BG_ERR_INVALID_ARG for NULL/misaligned
+ * pointers, negative sizes, a too-small workspace or a workspace overlapping
+ * cu_seqlens, and BG_ERR_UNSUPPORTED for max_seqlen > BG_MAX_SEQLEN;
+ * num_seqs == 0 or total_tokens == 0 is a valid no-op.  The planned run gives
+ * the errors of bg_packed_prefill_attn.
+ */
+bg_status_t bg_packed_prefill_plan(const int32_t *cu_seqlens, int32_t num_seqs,
+                                   int32_t total_tokens, int32_t max_seqlen,
+                                   void *workspace, size_t workspace_bytes,
+                                   int32_t *dev_status, cudaStream_t stream);
+bg_status_t bg_packed_prefill_attn_planned(const void *q, const void *k, const void *v,
+                                           const int32_t *cu_seqlens, int32_t num_seqs,
+                                           int32_t total_tokens, int32_t max_seqlen,
+                                           int32_t Hq, int32_t Hkv, int32_t head_dim,
+                                           float scale, void *out, float *lse,
+                                           void *workspace, size_t workspace_bytes,
+                                           int32_t *dev_status, cudaStream_t stream);
+
+/*
  * Packed variable-length causal GQA prefill attention with FP8 (E4M3) Q and K.
  * Source: the abstract of the page above counts "selective FP8" among the
  * engine's mixed-precision choices without saying which matmuls use it; the

@@ -94,6 +94,33 @@ def test_prefill_host_validation(lib, kw, expect):
     assert prefill(lib, **kw) == expect
 
 
+@pytest.mark.parametrize("kw,expect", [
+    (dict(q=None), 1), (dict(cu=None), 1), (dict(out=None), 1), (dict(ws=None), 1), (dict(Hq=6, Hkv=4), 1),
+    (dict(d=96), 2), (dict(maxlen=70000), 2), (dict(wsb=64), 1), (dict(out=FAKE * 1 + 64), 1),
+    (dict(scale=0.0), 1), (dict(B=0, q=None), 0),
+])
+def test_prefill_planned_host_validation(lib, kw, expect):
+    a = dict(q=FAKE, k=FAKE * 2, v=FAKE * 3, cu=FAKE * 4, B=2, T=10, maxlen=8, Hq=4, Hkv=2, d=64, scale=0.125,
+             out=FAKE * 5, lse=None, ws=FAKE * 6, wsb=1 << 20, st=None, stream=None)
+    a.update(kw)
+    assert lib.bg_packed_prefill_attn_planned(a["q"], a["k"], a["v"], a["cu"], a["B"], a["T"], a["maxlen"], a["Hq"],
+                                              a["Hkv"], a["d"], a["scale"], a["out"], a["lse"], a["ws"], a["wsb"],
+                                              a["st"], a["stream"]) == expect
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(cu=None), 1), (dict(ws=None), 1), (dict(wsb=64), 1), (dict(maxlen=70000), 2), (dict(B=-1), 1),
+    (dict(T=-1), 1), (dict(cu=FAKE * 4 + 2), 1), (dict(ws=FAKE * 6 + 16), 1), (dict(st=FAKE * 7 + 2), 1),
+    (dict(cu=FAKE * 6 + 256), 1),               # cu_seqlens inside the workspace
+    (dict(B=0, cu=None), 0), (dict(T=0, cu=None), 0),   # empty packings are a no-op
+])
+def test_prefill_plan_host_validation(lib, kw, expect):
+    a = dict(cu=FAKE * 4, B=2, T=10, maxlen=8, ws=FAKE * 6, wsb=1 << 20, st=None, stream=None)
+    a.update(kw)
+    assert lib.bg_packed_prefill_plan(a["cu"], a["B"], a["T"], a["maxlen"], a["ws"], a["wsb"], a["st"],
+                                      a["stream"]) == expect
+
+
 def prefill_fp8(lib, **kw):
     a = dict(q=FAKE, qs=0.5, k=FAKE * 2, ks=0.25, v=FAKE * 3, cu=FAKE * 4, B=2, T=10, maxlen=8, Hq=4, Hkv=2, d=128,
              scale=0.125, out=FAKE * 5, lse=None, ws=FAKE * 6, wsb=1 << 20, st=None, stream=None)
