@@ -213,30 +213,29 @@ __device__ uint32_t radix_cut(Sh &sh, uint32_t need, uint32_t cap, VisitFn visit
 __device__ __forceinline__ void sort_in_registers(uint32_t &key, int32_t &tok, int P, uint32_t *xk, int32_t *xt)
 {
     const int t = threadIdx.x;
+    // one 64-bit value per entry, larger = better: the key, then the token inverted (smaller
+    // tokens first among equal keys)
+    uint64_t v = (static_cast<uint64_t>(key) << 32) | static_cast<uint32_t>(~tok);
     int buf = 0;
     for (int k = 2; k <= P; k <<= 1) {
         for (int j = k >> 1; j > 0; j >>= 1) {
-            uint32_t ok;
-            int32_t ot;
+            uint64_t o;
             if (j < 32) {
-                ok = __shfl_xor_sync(0xffffffffu, key, j);
-                ot = __shfl_xor_sync(0xffffffffu, tok, j);
+                o = __shfl_xor_sync(0xffffffffu, v, j);
             } else {
-                xk[buf * kSelThreads + t] = key;
-                xt[buf * kSelThreads + t] = tok;
+                xk[buf * kSelThreads + t] = static_cast<uint32_t>(v >> 32);
+                xt[buf * kSelThreads + t] = static_cast<int32_t>(static_cast<uint32_t>(v));
                 __syncthreads();
-                ok = xk[buf * kSelThreads + (t ^ j)];
-                ot = xt[buf * kSelThreads + (t ^ j)];
+                o = (static_cast<uint64_t>(xk[buf * kSelThreads + (t ^ j)]) << 32) |
+                    static_cast<uint32_t>(xt[buf * kSelThreads + (t ^ j)]);
                 buf ^= 1;
             }
-            const bool mine_better = key > ok || (key == ok && tok < ot);
             const bool keep_better = ((t & j) == 0) == ((t & k) == 0);
-            if (mine_better != keep_better) {
-                key = ok;
-                tok = ot;
-            }
+            if ((v > o) != keep_better) v = o;
         }
     }
+    key = static_cast<uint32_t>(v >> 32);
+    tok = static_cast<int32_t>(~static_cast<uint32_t>(v));
 }
 
 // Selection of the W highest keys of n elements (key(i) for element i; equal keys by
