@@ -14,11 +14,14 @@
 //      (from HBM) computes the row's logsumexp and the maximum of each of 2048
 //      interleaved groups of its logits; those maxima are 2048 distinct logits, so
 //      the W-th largest of them (narrowed by a radix selection on an order-preserving
-//      integer key) bounds the row's W-th best from below.  The second pass (the row
-//      is still in L2) gathers the few logits at or above the bound into shared
-//      memory, and a bitonic sort in registers orders them: the beam's W best
-//      (value, token) and its logsumexp go to the workspace.  A beam's W best tokens
-//      contain its whole share of the request's W best candidates.
+//      integer key) bounds the row's W-th best from below.  The first pass also keeps
+//      every float4's maximum, truncated to bf16, in shared memory; the second pass
+//      reads back from L2 only the float4s whose stored maximum reaches the bound
+//      (rows longer than 131,072 logits stream the whole row again), gathers the
+//      logits at or above the bound into shared memory, and a bitonic sort in
+//      registers orders them: the beam's W best (value, token) and its logsumexp go
+//      to the workspace.  A beam's W best tokens contain its whole share of the
+//      request's W best candidates.
 //   2. the merge, a radix selection over the W x W local candidates of a request keyed
 //      by their scores, in two levels so that more than R CTAs share it:
 //      merge_part_kernel selects the W best of each of S slices of beams, and

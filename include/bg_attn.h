@@ -375,7 +375,8 @@ bg_status_t bg_beam_decode_step(const void *q, const void *prompt_k, const void 
  *                intermediate survivors); contents on entry do not matter
  * Outputs must not overlap the inputs or the workspace.  Three launches on
  * `stream` (per-beam selection, then a two-level merge); the logits come from HBM
- * once (a second pass over each beam's row reads it back from L2).  NaN logits are
+ * once (a second pass over each beam's row reads back from L2 only the 16-byte
+ * groups that can hold one of its W best).  NaN logits are
  * not supported (the result is then unspecified).
  * Errors: BG_ERR_INVALID_ARG for NULL/misaligned pointers, R < 0, a too small
  * workspace or overlaps; BG_ERR_UNSUPPORTED unless 1 <= W <= BG_MAX_BEAM and
