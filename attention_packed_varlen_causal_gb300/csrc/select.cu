@@ -692,7 +692,8 @@ __global__ void __launch_bounds__(kSelThreads)
 __global__ void __launch_bounds__(kSelThreads)
     merge_part_kernel(const float *__restrict__ cand_val, const float *__restrict__ row_lse,
                       const float *__restrict__ cum, int32_t W, int32_t S, uint32_t *__restrict__ part_key,
-                      int32_t *__restrict__ part_idx)
+                      int32_t *__restrict__ part_idx, const int32_t *__restrict__ cand_tok,
+                      int32_t *__restrict__ token_out, int32_t *__restrict__ parent_out, float *__restrict__ score_out)
 {
     __shared__ SelShared sh;
     grid_dep_launch();
@@ -729,6 +730,16 @@ __global__ void __launch_bounds__(kSelThreads)
     // and a beam's candidates with equal scores have equal logits, kept in token order)
     select_top(sh, n, W, key, [&](auto &&body) { for_each_key(n, key, body); });
     const int64_t out = blockIdx.x * static_cast<int64_t>(W);
+    if (S == 1) {
+        // one slice holds the whole request: these are the request's W best
+        for (int k = tid; k < W; k += kSelThreads) {
+            const int i = base + sh.ci[k];
+            token_out[r * W + k] = cand_tok[r * W * W + i];
+            parent_out[r * W + k] = i / W;
+            score_out[r * W + k] = key2f(sh.ck[k]);
+        }
+        return;
+    }
     for (int k = tid; k < W; k += kSelThreads) {
         part_key[out + k] = sh.ck[k];
         part_idx[out + k] = base + sh.ci[k];
@@ -775,7 +786,9 @@ __global__ void __launch_bounds__(kSelThreads)
 
 int beam_select_slices(int32_t R, int32_t W)
 {
-    // about two level-1 CTAs per SM over the requests; every slice keeps at least one beam
+    // one level when a request's W x W candidates fit one CTA's key cache; otherwise about two
+    // level-1 CTAs per SM over the requests, every slice keeping at least one beam
+    if (static_cast<int64_t>(W) * W <= kMergeCacheKeys) return 1;
     int S = static_cast<int>((2 * 152 + R - 1) / (R > 0 ? R : 1));
     if (S > W) S = W;
     if (S > 16) S = 16;
@@ -812,8 +825,9 @@ cudaError_t launch_beam_select(const float *logits, const float *cum, int32_t R,
     const size_t final_smem = static_cast<size_t>(S) * W * 4;
     e = launch_dependent(merge_part_kernel, dim3(static_cast<unsigned>(static_cast<int64_t>(R) * S)),
                          dim3(kSelThreads), part_smem, stream, static_cast<const float *>(cand_val),
-                         static_cast<const float *>(row_lse), cum, W, S, part_key, part_idx);
-    if (e != cudaSuccess) return e;
+                         static_cast<const float *>(row_lse), cum, W, S, part_key, part_idx,
+                         static_cast<const int32_t *>(cand_tok), token_out, parent_out, score_out);
+    if (e != cudaSuccess || S == 1) return e;   // one slice: level 1 wrote the result
     return launch_dependent(merge_final_kernel, dim3(static_cast<unsigned>(R)), dim3(kSelThreads), final_smem, stream,
                             static_cast<const uint32_t *>(part_key), static_cast<const int32_t *>(part_idx),
                             static_cast<const int32_t *>(cand_tok), W, S, token_out, parent_out, score_out);
