@@ -9,7 +9,7 @@
 // the W best (b, v) of a request are kept, best first, equal scores by the
 // smaller b * V + v.
 //
-// Three launches on the caller's stream:
+// Two or three launches on the caller's stream:
 //   1. row_select_kernel, one CTA per beam row, two passes over the row.  The first
 //      (from HBM) computes the row's logsumexp and the maximum of each of 2048
 //      interleaved groups of its logits; those maxima are 2048 distinct logits, so
@@ -23,9 +23,10 @@
 //      to the workspace.  A beam's W best tokens contain its whole share of the
 //      request's W best candidates.
 //   2. the merge, a radix selection over the W x W local candidates of a request keyed
-//      by their scores, in two levels so that more than R CTAs share it:
-//      merge_part_kernel selects the W best of each of S slices of beams, and
-//   3. merge_final_kernel the W best of the S * W survivors of each request.
+//      by their scores: merge_part_kernel selects the W best of each of S slices of
+//      beams (S = 1 when all W x W fit one CTA's key cache: then it writes the result),
+//   3. and for S > 1, merge_final_kernel the W best of the S * W survivors of each
+//      request (two levels, so that more than R CTAs share the work).
 // HBM-bound: the logits come from HBM once; everything else stays on chip or in L2.
 #include "bg_internal.h"
 #include "bg_ptx.cuh"

@@ -373,8 +373,9 @@ bg_status_t bg_beam_decode_step(const void *q, const void *prompt_k, const void 
  *   workspace    device scratch of at least bg_beam_select_workspace_size(R, W, V)
  *                bytes, 256-byte aligned (per-beam candidates and the merge's
  *                intermediate survivors); contents on entry do not matter
- * Outputs must not overlap the inputs or the workspace.  Three launches on
- * `stream` (per-beam selection, then a two-level merge); the logits come from HBM
+ * Outputs must not overlap the inputs or the workspace.  Two or three launches
+ * on `stream` (per-beam selection, then a merge: one level when W * W <= 16384,
+ * else two); the logits come from HBM
  * once (a second pass over each beam's row reads back from L2 only the 16-byte
  * groups that can hold one of its W best).  NaN logits are
  * not supported (the result is then unspecified).
