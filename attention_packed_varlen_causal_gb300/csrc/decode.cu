@@ -47,7 +47,7 @@ cudaError_t launch_decode_attn(int head_dim, const CUtensorMap &tm_q, const CUte
                                const CUtensorMap &tm_v, const CUtensorMap &tm_sk, const CUtensorMap &tm_sv,
                                const CUtensorMap &tm_o, const AttnParams &p, int grid, cudaStream_t stream)
 {
-    if (head_dim == 64) return launch_one<64, 4, 4, 3>(tm_q, tm_k, tm_v, tm_sk, tm_sv, tm_o, p, grid, stream);
+    if (head_dim == 64) return launch_one<64, 6, 6, 3>(tm_q, tm_k, tm_v, tm_sk, tm_sv, tm_o, p, grid, stream);
     if (head_dim == 128) return launch_one<128, 3, 2, 2>(tm_q, tm_k, tm_v, tm_sk, tm_sv, tm_o, p, grid, stream);
     return cudaErrorInvalidValue;
 }
