@@ -25,6 +25,7 @@ BG_DEVSTAT_SEQ_TOO_LONG = 0x02
 BG_DEVSTAT_PARENT = 0x04
 BG_DEVSTAT_CU_PROMPT = 0x08
 BG_DEVSTAT_EMPTY_ROW = 0x10
+BG_DEVSTAT_PLAN = 0x20
 BG_DEVSTAT_TIMEOUT = 0x100
 BG_MAX_SUFFIX = 16
 BG_MAX_SEQLEN = 65536

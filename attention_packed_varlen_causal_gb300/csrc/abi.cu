@@ -225,6 +225,8 @@ bg_status_t prefill_impl(const void *q, const void *k, const void *v, const int3
     p.groups_per_kv = groups_per_kv;
     p.n_head_groups = Hkv * groups_per_kv;
     p.lse = lse;
+    p.total_prompt = total_tokens;   // the packing this call expects the work list to be for
+    p.R = num_seqs;
     const int grid = static_cast<int>(items_bound < nsm ? items_bound : nsm);
     const cudaError_t e = qk8 ? launch_prefill_attn_fp8(head_dim, tm_q, tm_k, tm_v, tm_o, p, grid, stream)
                               : launch_prefill_attn(head_dim, tm_q, tm_k, tm_v, tm_o, p, grid, stream);

@@ -88,7 +88,7 @@ struct AttnParams {
     const int32_t *cu_prompt;
     int32_t R, W, BT;              // BT = beams per query tile = 128 / g
     int32_t pairs_per_rk;          // ceil(ceil(W / BT) / NH)
-    int32_t max_prompt_len, total_prompt;
+    int32_t max_prompt_len, total_prompt;   // prefill: total_prompt = total tokens, R = sequences
     int32_t suffix_len;            // suffix slots per beam (t)
     int32_t suf_bpt;               // beams per suffix key tile (suf_bpt * t <= 64)
     int32_t suf_tx;                // bytes one suffix key tile brings (all column blocks)
@@ -392,7 +392,11 @@ __global__ void __maxnreg__((AttnCfg<D, NH, NK, NV, NS, QK8>::kRegsLaunch))
 
     int n_items;
     if constexpr (MODE == Mode::Prefill) {
-        n_items = (p.work_hdr[0] == 0) ? p.work_hdr[1] * p.n_head_groups : 0;
+        // a list the pre-pass accepted, for this call's packing (total tokens, sequences)
+        const bool planned_here = p.work_hdr[3] == p.total_prompt && p.work_hdr[4] == p.R;
+        n_items = (p.work_hdr[0] == 0 && planned_here) ? p.work_hdr[1] * p.n_head_groups : 0;
+        if (p.work_hdr[0] == 0 && !planned_here && blockIdx.x == 0 && threadIdx.x == 0 && p.dev_status)
+            atomicOr(p.dev_status, BG_DEVSTAT_PLAN);
     } else {
         n_items = p.n_items_decode;
     }

@@ -67,6 +67,8 @@ __global__ void __launch_bounds__(1024) worklist_kernel(const int32_t *__restric
             off += s_count[nt] * nt;
         }
         hdr[1] = off;
+        hdr[3] = T;      // the packing the list belongs to, checked by every run that reads it
+        hdr[4] = B;
         hdr[0] = 0;
     }
     __syncthreads();

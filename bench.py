@@ -48,7 +48,7 @@ SPEC_HBM_GBS = 8000.0   # nominal GB300 HBM3e bandwidth (~8 TB/s), reported besi
 # (dram__bytes_read.sum + dram__bytes_write.sum from one ncu capture of that launch).  It holds
 # only for the sources that launch is built from, identified by `sources`
 # (kernel_sources_hash); otherwise the bench reports null.
-PREFILL_TRAFFIC = {"sources": "6d5c13ae1a8f437b", "bytes": 649664512 + 243288064}
+PREFILL_TRAFFIC = {"sources": "13fe91063a561eee", "bytes": 649549824 + 243861504}
 # the files a bg_packed_prefill_attn launch is built from
 PREFILL_SOURCES = ["abi.cu", "prefill.cu", "bg_attn_kernel.cuh", "bg_ptx.cuh", "bg_internal.h"]
 

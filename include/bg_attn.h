@@ -58,6 +58,8 @@ typedef enum {
 #define BG_DEVSTAT_PARENT       0x04  /* a parent index is outside [0, W)           */
 #define BG_DEVSTAT_CU_PROMPT    0x08  /* cu_prompt invalid or prompt > max_prompt   */
 #define BG_DEVSTAT_EMPTY_ROW    0x10  /* prompt length 0 with suffix_len 0          */
+#define BG_DEVSTAT_PLAN         0x20  /* planned run: the workspace's work list is
+                                         for another packing (nothing written)     */
 #define BG_DEVSTAT_TIMEOUT      0x100 /* an internal pipeline wait ran out          */
 
 /* Supported shapes: head_dim in {64, 128}; Hq % Hkv == 0; for decode
@@ -152,7 +154,10 @@ bg_status_t bg_packed_prefill_attn(const void *q, const void *k, const void *v,
  * No other call may use the workspace in between (a planned run only reads
  * it, so runs on the same stream may follow one plan).  A plan whose
  * cu_seqlens failed the device checks makes every planned run a no-op that
- * writes nothing, as the one-call form does.
+ * writes nothing, as the one-call form does.  The plan records its
+ * total_tokens and num_seqs in the workspace; a planned run whose own differ
+ * writes nothing and raises BG_DEVSTAT_PLAN (the device cannot tell apart two
+ * packings with equal sizes: the caller keeps those matched).
  *
  * Errors: bg_packed_prefill_plan gives BG_ERR_INVALID_ARG for NULL/misaligned
  * pointers, negative sizes, a too-small workspace or a workspace overlapping

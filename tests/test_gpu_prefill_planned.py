@@ -77,3 +77,22 @@ def test_a_bad_plan_makes_the_planned_run_write_nothing():
     torch.cuda.synchronize()
     assert int(st.item()) & bg.BG_DEVSTAT_CU_SEQLENS
     assert torch.isnan(out.float()).all(), "a planned run after a failed plan wrote output"
+
+
+def test_a_plan_for_another_packing_is_refused():
+    # plan 2 sequences (300 tokens), then run on 3 sequences (500 tokens): the run writes nothing
+    # and raises BG_DEVSTAT_PLAN.  (The planned list only addresses rows below 300, inside the
+    # larger run's buffers, so even an unchecked run would stay in bounds.)
+    import torch
+    a = _layer_inputs([100, 200], 16, 8, 128, 0)
+    b = _layer_inputs([100, 200, 200], 16, 8, 128, 1)
+    Ta, Tb = int(a["cu_seqlens"][-1]), int(b["cu_seqlens"][-1])
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = torch.empty(bg.bg_packed_prefill_workspace_size(3, Tb, 200, 16, 8, 128), dtype=torch.uint8, device="cuda")
+    bg.bg_packed_prefill_plan(i32_dev(a["cu_seqlens"]), Ta, 200, workspace=ws, dev_status=st)
+    out = torch.full((Tb, 16, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    bg.bg_packed_prefill_attn_planned(to_dev(b["q"]), to_dev(b["k"]), to_dev(b["v"]), i32_dev(b["cu_seqlens"]), 200,
+                                      out, workspace=ws, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == bg.BG_DEVSTAT_PLAN
+    assert torch.isnan(out.float()).all(), "a run with another packing's plan wrote output"
