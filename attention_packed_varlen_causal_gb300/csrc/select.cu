@@ -83,7 +83,7 @@ __device__ __forceinline__ float key2f(uint32_t k)
     return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
 
-// Shared state of a selection; CAP = the candidates it can gather and sort.
+// Shared state of a selection; CAP = the entries ck/ci hold.
 template <int CAP>
 struct SelState {
     uint32_t hist[kBins];
@@ -314,9 +314,10 @@ __device__ void select_top(SelShared &sh, int n, int W, KeyFn key, VisitFn visit
 }
 
 // Gathers into sh.ck/ci (key, token) a superset, at most cap >= W entries, of the W best
-// of the n buffered entries (key descending, token ascending), and returns the bound that
-// every later logit of the row must pass to possibly join them: key >= lo, or key > lo
-// when `strict` (later logits have larger tokens, so they lose ties at lo).
+// of the n entries in bval/btok (key descending, token ascending; entries whose token is
+// V or more are padding and never count).  Returns the radix threshold lo of the gathered
+// set: it holds every entry with key >= lo, or, when `strict`, every entry with key > lo
+// and, of the entries tied at lo, those with the smallest tokens.
 template <class Sh>
 __device__ uint32_t row_reduce(Sh &sh, const float *bval, const int32_t *btok, int n, int V, int W, int cap,
                                bool &strict)
