@@ -461,7 +461,8 @@ __global__ void __launch_bounds__(kSelThreads)
     const bool stored = n4 <= kMaxStored;
     constexpr int kStep = kRowLoads * kSelThreads;
     const int kJ = kRowLoads * ((n4 + kStep - 1) / kStep);
-    uint32_t *smax = row_buf + 2 * kGather + tid * (kJ / 2);   // this thread's kJ halfwords
+    // this thread's kJ halfwords, past the gather buffer; allocated and touched only if stored
+    uint32_t *smax = row_buf + 2 * kGather + tid * (kJ / 2);
     // float4 group i of the row: logits 4i .. 4i+3 (-inf past V); VEC: V % 4 == 0, so the
     // rows start 16-byte aligned, as the logits do
     auto load_keep = [&](int i) -> float4 {      // first pass: the second reads it again (L2)
