@@ -6,7 +6,9 @@ One packing serves every layer of a batch, so its work list is built once.  Chec
     layer, over several layers that share one plan (and lse too);
   * a planned layer matches the fp64 oracle within the parity tolerance;
   * a plan whose cu_seqlens fail the device checks flags dev_status, and the planned run
-    after it writes nothing, as the one-call form does."""
+    after it writes nothing, as the one-call form does;
+  * a planned run given another packing's plan (other total tokens and sequence count)
+    writes nothing and raises BG_DEVSTAT_PLAN."""
 import math
 
 import numpy as np
